@@ -1,0 +1,151 @@
+/*
+ * pattn.h -- C ABI of libpattn: paged-KV varlen attention on GB300 (sm_103a).
+ *
+ * The operation (one call computes it for a whole batch):
+ *
+ *   for every sequence b, query token i < ql_b = cu_q[b+1] - cu_q[b], query head h:
+ *     hk  = h / (n_heads_q / n_heads_kv)             contiguous GQA groups
+ *     pos = L_b - ql_b + i                           queries are the last ql_b keys
+ *     J   = { j < L_b : !causal or j <= pos }
+ *     out[cu_q[b]+i][h] = sum_{j in J} softmax_j(scale * q . k_j) v_j   (0 if J is empty)
+ *
+ * with k_j, v_j row j % page_size of page block_table[b][j / page_size] of the
+ * pool. Sources: the trtllm-gen paged decode manifest (examples/decode.json:
+ * op "decode" parameters out, q, k, v, table, seq, cuq, seqs, tokens; the
+ * scratch buffers "partial" and "stats" of its split-KV launch; its Q and
+ * K/V tensor maps, which fix the GQA packing and the page geometry) and the
+ * FlashAttention-4 SM100MHA2Q kernel doc (paged KV lookup, causal or unmasked
+ * mask, ragged valid lengths, KV partitions). Q/K/V/out are bf16; scores,
+ * softmax and accumulation are fp32.
+ *
+ * Conventions for every call:
+ *   - Device pointers are owned by the caller; the library keeps none of them
+ *     past the call. Calls are asynchronous and ordered on `stream`; nothing
+ *     here synchronises the host except pattn_get_device_status,
+ *     pattn_profile_read and pattn_forward_host.
+ *   - Errors the host can see (null or misaligned pointers, sizes, unsupported
+ *     shapes) are returned before anything is launched.
+ *   - Errors only the data shows (a block-table entry outside the pool inside
+ *     a live range, lengths beyond the host bounds, cu_q out of order) set a
+ *     device error word and zero the affected sequence's output rows; no call
+ *     traps or reads outside the pool. pattn_get_device_status reports them.
+ *   - Every wait inside a kernel is bounded (about 2 s); a wait that runs out
+ *     sets the error word (PATTN_ERR_DEVICE_TIMEOUT) and the kernel returns.
+ *   - The library is not re-entrant across host threads for one device (one
+ *     workspace per device).
+ */
+#ifndef PATTN_H_
+#define PATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the two types are the same pointer); NULL = legacy default stream. */
+typedef struct CUstream_st *pattn_stream_t;
+
+typedef enum pattn_status {
+  PATTN_OK = 0,
+  PATTN_ERR_INVALID_ARG = 1,      /* null/misaligned pointer, bad size or bound */
+  PATTN_ERR_UNSUPPORTED = 2,      /* head_dim not 128/256, page_size not 64, group > 128, ... */
+  PATTN_ERR_CUDA = 3,             /* a CUDA runtime/driver call failed */
+  PATTN_ERR_NO_MEMORY = 4,        /* workspace allocation failed or caller workspace too small */
+  PATTN_ERR_DEVICE_BAD_INPUT = 5, /* device data rejected (page index, lengths, cu_q) */
+  PATTN_ERR_DEVICE_TIMEOUT = 6    /* a bounded wait inside a kernel ran out */
+} pattn_status;
+
+/*
+ * pattn_forward -- causal or full attention over a paged (or contiguous) KV cache.
+ *
+ *   out         bf16 [total_q][n_heads_q][head_dim], written in full.
+ *   q           bf16 [total_q][n_heads_q][head_dim].
+ *   kv_pool     paged:      bf16 [num_pages][2 (K, V)][page_size][n_heads_kv][head_dim];
+ *               contiguous: bf16 [2 (K, V)][num_pages][n_heads_kv][head_dim] when
+ *               block_table is NULL (num_pages then counts rows of each plane, and
+ *               sequence b's keys are rows sum(seq_lens[0..b)) onwards).
+ *   block_table int32 [num_seqs][ceil(max_kv / page_size)]: the page of each
+ *               logical slot; slots at or past ceil(L_b / page_size) are never
+ *               read (-1 by convention). NULL selects the contiguous cache.
+ *   seq_lens    int32 [num_seqs]: KV length L_b, the current queries included.
+ *   cu_q        int32 [num_seqs + 1]: query offsets, cu_q[0] = 0, non-decreasing,
+ *               cu_q[num_seqs] = total_q.
+ *   num_seqs, total_q   batch size and number of query tokens (the manifest's
+ *               "seqs" and "tokens" op parameters).
+ *   max_q, max_kv       host upper bounds of ql_b and L_b (size the plan and the
+ *               block-table row stride).
+ *   n_heads_q, n_heads_kv, head_dim, page_size   head_dim in {128, 256},
+ *               page_size 64, n_heads_q a multiple of n_heads_kv, group <= 128.
+ *   num_pages   pages in the pool (bounds every block-table entry).
+ *   scale       softmax scale, finite and >= 0.
+ *   causal      0: every key of the sequence; 1: keys up to the query position.
+ *   stream      stream the three launches (plan, attention, combine) go on.
+ *
+ * All pointers 16-byte aligned. The first call on a device allocates the
+ * library workspace (grow-only) unless pattn_set_workspace gave one.
+ */
+pattn_status pattn_forward(void *out, const void *q, const void *kv_pool,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           const int32_t *cu_q, int num_seqs, int total_q, int max_q,
+                           int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
+                           int page_size, int num_pages, float scale, int causal,
+                           pattn_stream_t stream);
+
+/*
+ * pattn_forward_host -- the same operation on HOST buffers, end to end: copies
+ * the inputs to device buffers the library keeps (grow-only, per device),
+ * runs pattn_forward on `stream`, copies `out` back and synchronises the
+ * stream. Layouts and arguments as for pattn_forward. Host buffers should be
+ * pinned for full copy bandwidth. kv_pool_bytes is the size of the pool buffer.
+ */
+pattn_status pattn_forward_host(void *out, const void *q, const void *kv_pool,
+                                size_t kv_pool_bytes, const int32_t *block_table,
+                                const int32_t *seq_lens, const int32_t *cu_q, int num_seqs,
+                                int total_q, int max_q, int max_kv, int n_heads_q,
+                                int n_heads_kv, int head_dim, int page_size, int num_pages,
+                                float scale, int causal, pattn_stream_t stream);
+
+/*
+ * Workspace bytes pattn_forward needs for these bounds: a header with the
+ * device error word, the planned work list, and the split-KV partial O and
+ * (max, sum) scratch (the manifest's "partial" and "stats" buffers).
+ */
+size_t pattn_workspace_size(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
+                            int n_heads_kv, int head_dim, int page_size);
+
+/*
+ * Use caller-owned device memory as the workspace of the current device
+ * (ptr 256-byte aligned; NULL returns to the library-owned one). The library
+ * clears its header once here; later calls need at least pattn_workspace_size
+ * bytes or return PATTN_ERR_NO_MEMORY.
+ */
+pattn_status pattn_set_workspace(void *ptr, size_t bytes);
+
+/*
+ * Synchronises `stream`, reads and clears the device error word of the
+ * current device. Returns PATTN_OK, PATTN_ERR_DEVICE_BAD_INPUT or
+ * PATTN_ERR_DEVICE_TIMEOUT (timeout wins if both are set).
+ */
+pattn_status pattn_get_device_status(pattn_stream_t stream);
+
+/* Static description of a status code. */
+const char *pattn_status_string(pattn_status status);
+
+/*
+ * Kernel timing: while enabled, pattn_forward records CUDA events around each
+ * of its launches on its stream (at most 4096 calls are kept).
+ * pattn_profile_read synchronises those events and returns the summed device
+ * time in milliseconds of the plan, attention and combine kernels and the
+ * number of calls recorded, then clears the record.
+ */
+pattn_status pattn_profile_enable(int on);
+pattn_status pattn_profile_read(double *ms_plan, double *ms_attention, double *ms_combine,
+                                int *calls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PATTN_H_ */

@@ -1,0 +1,145 @@
+"""paged_kv_flashattention_varlen_gb300 -- paged-KV varlen attention for GB300.
+
+Python face of ``libpattn.so``. The functions below check tensor types and
+pass raw pointers and the current CUDA stream to the C ABI (include/pattn.h);
+PyTorch only provides device memory and streams. There is no CPU path.
+
+    forward(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q, max_kv,
+            n_heads_kv, scale, causal, num_pages=None, stream=None)
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+from . import _lib
+
+__all__ = ["PattnError", "forward", "forward_host", "workspace_size", "set_workspace",
+           "device_status", "status_string", "profile_enable", "profile_read", "STATUS",
+           "library_path"]
+
+STATUS = {
+    0: "PATTN_OK", 1: "PATTN_ERR_INVALID_ARG", 2: "PATTN_ERR_UNSUPPORTED", 3: "PATTN_ERR_CUDA",
+    4: "PATTN_ERR_NO_MEMORY", 5: "PATTN_ERR_DEVICE_BAD_INPUT", 6: "PATTN_ERR_DEVICE_TIMEOUT",
+}
+
+
+class PattnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({status_string(code)})")
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def status_string(code: int) -> str:
+    return _lib.load().pattn_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise PattnError(code, where)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _shape_args(q, kv_pool, block_table, n_heads_kv: int, num_pages: Optional[int]):
+    total_q, n_heads_q, head_dim = (int(x) for x in q.shape)
+    if block_table is not None:
+        page_size = int(kv_pool.shape[2])
+        pages = int(kv_pool.shape[0]) if num_pages is None else int(num_pages)
+    else:
+        page_size = 64
+        pages = int(kv_pool.shape[1]) if num_pages is None else int(num_pages)
+    return total_q, n_heads_q, head_dim, page_size, pages
+
+
+def forward(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,
+            n_heads_kv: int, scale: float, causal: bool, num_pages: Optional[int] = None,
+            stream=None, check: bool = True) -> int:
+    """Attention over a paged KV cache on the GPU (``pattn_forward``).
+
+    ``q``/``out``: bf16 [total_q, Hq, D] on the device; ``kv_pool``: bf16
+    [pages, 2, 64, Hkv, D] (or [2, rows, Hkv, D] with ``block_table=None``);
+    ``block_table`` int32 [B, ceil(max_kv/64)]; ``seq_lens`` int32 [B];
+    ``cu_q`` int32 [B+1]. Returns the status code (raises if ``check``).
+    """
+    import torch
+    for name, t, dt in (("out", out, torch.bfloat16), ("q", q, torch.bfloat16),
+                        ("kv_pool", kv_pool, torch.bfloat16), ("seq_lens", seq_lens, torch.int32),
+                        ("cu_q", cu_q, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name}: expected a contiguous CUDA {dt} tensor")
+    if block_table is not None and (block_table.dtype != torch.int32 or not block_table.is_cuda
+                                    or not block_table.is_contiguous()):
+        raise TypeError("block_table: expected a contiguous CUDA int32 tensor or None")
+    total_q, hq, d, page, pages = _shape_args(q, kv_pool, block_table, n_heads_kv, num_pages)
+    rc = _lib.load().pattn_forward(
+        _ptr(out), _ptr(q), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens), _ptr(cu_q),
+        int(seq_lens.numel()), total_q, int(max_q), int(max_kv), hq, int(n_heads_kv), d, page,
+        pages, float(scale), int(bool(causal)), _stream_handle(stream))
+    if check:
+        _check(rc, "pattn_forward")
+    return rc
+
+
+def forward_host(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,
+                 n_heads_kv: int, scale: float, causal: bool, num_pages: Optional[int] = None,
+                 stream=None) -> None:
+    """End-to-end call on HOST tensors (``pattn_forward_host``): copies in, runs, copies out."""
+    import torch
+    for name, t in (("out", out), ("q", q), ("kv_pool", kv_pool), ("seq_lens", seq_lens),
+                    ("cu_q", cu_q)):
+        if t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name}: expected a contiguous host tensor")
+    total_q, hq, d, page, pages = _shape_args(q, kv_pool, block_table, n_heads_kv, num_pages)
+    rc = _lib.load().pattn_forward_host(
+        _ptr(out), _ptr(q), _ptr(kv_pool), kv_pool.numel() * kv_pool.element_size(),
+        _ptr(block_table), _ptr(seq_lens), _ptr(cu_q), int(seq_lens.numel()), total_q, int(max_q),
+        int(max_kv), hq, int(n_heads_kv), d, page, pages, float(scale), int(bool(causal)),
+        _stream_handle(stream))
+    _check(rc, "pattn_forward_host")
+
+
+def workspace_size(num_seqs: int, total_q: int, max_q: int, max_kv: int, n_heads_q: int,
+                   n_heads_kv: int, head_dim: int, page_size: int = 64) -> int:
+    return int(_lib.load().pattn_workspace_size(num_seqs, total_q, max_q, max_kv, n_heads_q,
+                                                n_heads_kv, head_dim, page_size))
+
+
+def set_workspace(buf=None) -> None:
+    """Use a caller-owned CUDA byte tensor as the workspace (None: library-owned)."""
+    if buf is None:
+        _check(_lib.load().pattn_set_workspace(None, 0), "pattn_set_workspace")
+    else:
+        _check(_lib.load().pattn_set_workspace(_ptr(buf), buf.numel() * buf.element_size()),
+               "pattn_set_workspace")
+
+
+def device_status(stream=None) -> int:
+    """Synchronise, read and clear the device error word (0 = fine)."""
+    return int(_lib.load().pattn_get_device_status(_stream_handle(stream)))
+
+
+def profile_enable(on: bool = True) -> None:
+    _check(_lib.load().pattn_profile_enable(int(bool(on))), "pattn_profile_enable")
+
+
+def profile_read() -> Tuple[float, float, float, int]:
+    """(ms plan, ms attention, ms combine, calls) summed since the last read."""
+    a, b, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    n = ctypes.c_int()
+    _check(_lib.load().pattn_profile_read(ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
+                                          ctypes.byref(n)), "pattn_profile_read")
+    return a.value, b.value, c.value, n.value

@@ -1,0 +1,508 @@
+// api.cu -- host side of libpattn: argument validation, per-device workspace,
+// TMA tensor-map encoding and the launch sequence plan -> attention -> combine.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/pattn.h"
+#include "kernels.cuh"
+
+namespace pattn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kTargetItemsPerSm = 4;
+constexpr int kTargetItemsCap = 1024;  // bound used when sizing the workspace
+constexpr int kMinChunk = 4;           // KV tiles per split, at least
+constexpr int kProfileCap = 4096;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct ProfileRec {
+  cudaEvent_t ev[4];
+};
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  bool ws_caller = false;
+  void* stage[6] = {};
+  size_t stage_bytes[6] = {};
+  std::vector<ProfileRec> prof;
+  std::vector<ProfileRec> prof_pool;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+bool g_profile = false;
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+struct Shape {
+  int group, tokens_per_tile, block_n;
+};
+
+pattn_status check_args(const void* out, const void* q, const void* kv, const int32_t* bt,
+                        const int32_t* seq_lens, const int32_t* cu_q, int num_seqs, int total_q,
+                        int max_q, int max_kv, int hq, int hkv, int d, int page, int num_pages,
+                        float scale, int causal, Shape* sh) {
+  if (!out || !q || !kv || !seq_lens || !cu_q) return PATTN_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(kv, 16)) return PATTN_ERR_INVALID_ARG;
+  if (!aligned(seq_lens, 4) || !aligned(cu_q, 4) || (bt && !aligned(bt, 4)))
+    return PATTN_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_q < 0 || max_q < 0 || max_kv < 0) return PATTN_ERR_INVALID_ARG;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return PATTN_ERR_INVALID_ARG;
+  if (num_pages <= 0) return PATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return PATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PATTN_ERR_INVALID_ARG;
+  if (scale < 0.f) return PATTN_ERR_UNSUPPORTED;
+  if (d != 128 && d != 256) return PATTN_ERR_UNSUPPORTED;
+  if (page != kPage) return PATTN_ERR_UNSUPPORTED;
+  const int g = hq / hkv;
+  if (g > kBM) return PATTN_ERR_UNSUPPORTED;
+  sh->group = g;
+  sh->tokens_per_tile = kBM / g;
+  sh->block_n = attention_block_n(d);
+  // item encoding keeps q tiles and KV tiles in 16 bits
+  if (cdiv(max_q, sh->tokens_per_tile) > 65535) return PATTN_ERR_UNSUPPORTED;
+  if (cdiv(max_kv, sh->block_n) > 65535) return PATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_pages) * 2 > 0x7fffffffLL) return PATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(total_q) * hq * d > (1LL << 40)) return PATTN_ERR_UNSUPPORTED;
+  return PATTN_OK;
+}
+
+struct WsLayout {
+  size_t hdr, seq_info, seq_plan, seq_part, items, units, part_ml, part_o, total;
+  int max_items, max_units, max_part_rows;
+};
+
+WsLayout ws_layout(int num_seqs, int total_q, int max_q, int hq, int hkv, int d) {
+  WsLayout w{};
+  const int g = hq / hkv;
+  const int T = kBM / g;
+  const long long units = static_cast<long long>(num_seqs) * hkv;
+  const long long qtiles = cdiv(total_q, T) + static_cast<long long>(num_seqs);
+  const long long items = static_cast<long long>(hkv) * qtiles + kTargetItemsCap + units + 64;
+  const long long rows_cap = std::min<long long>(kBM, static_cast<long long>(max_q) * g);
+  const long long part_rows = (kTargetItemsCap + units) * std::max<long long>(rows_cap, 1);
+  w.max_items = static_cast<int>(std::min<long long>(items, 0x7fffffffLL));
+  w.max_units = static_cast<int>(std::min<long long>(units, 0x7fffffffLL));
+  w.max_part_rows = static_cast<int>(std::min<long long>(part_rows, 0x7fffffffLL));
+  size_t off = 0;
+  w.hdr = off;
+  off += kHdrWords * sizeof(int);
+  w.seq_info = off = align_up(off, 256);
+  off += sizeof(int4) * static_cast<size_t>(num_seqs);
+  w.seq_plan = off = align_up(off, 256);
+  off += sizeof(int4) * static_cast<size_t>(num_seqs);
+  w.seq_part = off = align_up(off, 256);
+  off += sizeof(int) * static_cast<size_t>(num_seqs);
+  w.items = off = align_up(off, 256);
+  off += sizeof(int4) * static_cast<size_t>(w.max_items);
+  w.units = off = align_up(off, 256);
+  off += sizeof(int4) * static_cast<size_t>(w.max_units);
+  w.part_ml = off = align_up(off, 256);
+  off += sizeof(float2) * static_cast<size_t>(w.max_part_rows);
+  w.part_o = off = align_up(off, 256);
+  off += sizeof(float) * static_cast<size_t>(d) * static_cast<size_t>(w.max_part_rows);
+  w.total = align_up(off, 256);
+  return w;
+}
+
+pattn_status cuda_fail(cudaError_t e) {
+  if (e == cudaSuccess) return PATTN_OK;
+  if (e == cudaErrorMemoryAllocation) return PATTN_ERR_NO_MEMORY;
+  return PATTN_ERR_CUDA;
+}
+
+// Per-device one-time set-up; caller holds g_mu.
+pattn_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PATTN_ERR_UNSUPPORTED;
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PATTN_ERR_CUDA;
+    if (major != 10 || minor != 3) return PATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return PATTN_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    if (attention_set_attributes() != cudaSuccess) return PATTN_ERR_CUDA;
+    st.ready = true;
+  }
+  *out = &st;
+  return PATTN_OK;
+}
+
+pattn_status ensure_workspace(DeviceState& st, size_t need) {
+  if (st.ws_caller) return st.ws_bytes >= need ? PATTN_OK : PATTN_ERR_NO_MEMORY;
+  if (st.ws && st.ws_bytes >= need) return PATTN_OK;
+  if (st.ws) {
+    // grow: the old buffer may still be in use by queued work
+    cudaDeviceSynchronize();
+    cudaFree(st.ws);
+    st.ws = nullptr;
+    st.ws_bytes = 0;
+  }
+  size_t bytes = align_up(need + need / 4, 1 << 20);
+  cudaError_t e = cudaMalloc(&st.ws, bytes);
+  if (e != cudaSuccess) {
+    st.ws = nullptr;
+    return cuda_fail(e);
+  }
+  e = cudaMemset(st.ws, 0, kHdrWords * sizeof(int));
+  if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  st.ws_bytes = bytes;
+  return PATTN_OK;
+}
+
+pattn_status encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                    const cuuint64_t* strides, const cuuint32_t* box) {
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                        const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PATTN_OK : PATTN_ERR_CUDA;
+}
+
+ProfileRec take_events(DeviceState& st) {
+  ProfileRec r{};
+  if (!st.prof_pool.empty()) {
+    r = st.prof_pool.back();
+    st.prof_pool.pop_back();
+    return r;
+  }
+  for (auto& e : r.ev) cudaEventCreate(&e);
+  return r;
+}
+
+pattn_status forward_locked(void* out, const void* q, const void* kv, const int32_t* bt,
+                            const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
+                            int total_q, int max_q, int max_kv, int hq, int hkv, int d, int page,
+                            int num_pages, float scale, int causal, cudaStream_t stream,
+                            const Shape& sh) {
+  DeviceState* stp = nullptr;
+  pattn_status s = device_state(&stp);
+  if (s != PATTN_OK) return s;
+  DeviceState& st = *stp;
+  const WsLayout L = ws_layout(num_seqs, total_q, max_q, hq, hkv, d);
+  if ((s = ensure_workspace(st, L.total)) != PATTN_OK) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(st.ws);
+
+  Workspace ws{};
+  ws.hdr = reinterpret_cast<int*>(wsb + L.hdr);
+  ws.seq_info = reinterpret_cast<int4*>(wsb + L.seq_info);
+  ws.seq_plan = reinterpret_cast<int4*>(wsb + L.seq_plan);
+  ws.seq_part = reinterpret_cast<int*>(wsb + L.seq_part);
+  ws.items = reinterpret_cast<int4*>(wsb + L.items);
+  ws.units = reinterpret_cast<int4*>(wsb + L.units);
+  ws.part_ml = reinterpret_cast<float2*>(wsb + L.part_ml);
+  ws.part_o = reinterpret_cast<float*>(wsb + L.part_o);
+  ws.max_items = L.max_items;
+  ws.max_units = L.max_units;
+  ws.max_part_rows = L.max_part_rows;
+
+  // ---- tensor maps (bf16, 128-byte swizzle, 64-element inner boxes)
+  const int g = sh.group, T = sh.tokens_per_tile;
+  CUtensorMap tq, tkv;
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
+                                static_cast<cuuint64_t>(hkv),
+                                static_cast<cuuint64_t>(std::max(total_q, 1))};
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(g) * d * 2,
+                               static_cast<cuuint64_t>(hq) * d * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(T)};
+    if ((s = encode(&tq, q, 4, dims, str, box)) != PATTN_OK) return s;
+  }
+  if (bt) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kPage),
+                                static_cast<cuuint64_t>(hkv),
+                                static_cast<cuuint64_t>(num_pages) * 2};
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(hkv) * d * 2,
+                               static_cast<cuuint64_t>(d) * 2,
+                               static_cast<cuuint64_t>(kPage) * hkv * d * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kPage), 1, 1};
+    if ((s = encode(&tkv, kv, 4, dims, str, box)) != PATTN_OK) return s;
+  } else {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                                static_cast<cuuint64_t>(num_pages), 2};
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(d) * 2,
+                               static_cast<cuuint64_t>(hkv) * d * 2,
+                               static_cast<cuuint64_t>(num_pages) * hkv * d * 2};
+    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kPage), 1};
+    if ((s = encode(&tkv, kv, 4, dims, str, box)) != PATTN_OK) return s;
+  }
+
+  PlanParams pp{};
+  pp.cu_q = cu_q;
+  pp.seq_lens = seq_lens;
+  pp.block_table = bt;
+  pp.out = static_cast<__nv_bfloat16*>(out);
+  pp.ws = ws;
+  pp.num_seqs = num_seqs;
+  pp.total_q = total_q;
+  pp.max_q = max_q;
+  pp.max_kv = max_kv;
+  pp.n_heads_q = hq;
+  pp.n_heads_kv = hkv;
+  pp.group = g;
+  pp.head_dim = d;
+  pp.tokens_per_tile = T;
+  pp.block_n = sh.block_n;
+  pp.bt_stride = std::max(1, cdiv(max_kv, kPage));
+  pp.num_pages = num_pages;
+  pp.causal = causal;
+  pp.target_items = std::min(kTargetItemsPerSm * st.sms, kTargetItemsCap);
+  pp.min_chunk = kMinChunk;
+
+  AttnParams ap{};
+  ap.items = ws.items;
+  ap.hdr = ws.hdr;
+  ap.seq_info = ws.seq_info;
+  ap.block_table = bt;
+  ap.out = static_cast<__nv_bfloat16*>(out);
+  ap.part_o = ws.part_o;
+  ap.part_ml = ws.part_ml;
+  ap.err = ws.hdr + kHdrErr;
+  ap.bt_stride = pp.bt_stride;
+  ap.num_pages = num_pages;
+  ap.n_heads_q = hq;
+  ap.n_heads_kv = hkv;
+  ap.group = g;
+  ap.tokens_per_tile = T;
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.causal = causal;
+  ap.paged = bt ? 1 : 0;
+
+  CombineParams cp{};
+  cp.units = ws.units;
+  cp.hdr = ws.hdr;
+  cp.seq_info = ws.seq_info;
+  cp.part_o = ws.part_o;
+  cp.part_ml = ws.part_ml;
+  cp.out = static_cast<__nv_bfloat16*>(out);
+  cp.n_heads_q = hq;
+  cp.group = g;
+  cp.head_dim = d;
+
+  const bool prof = g_profile && st.prof.size() < static_cast<size_t>(kProfileCap);
+  ProfileRec rec{};
+  if (prof) {
+    rec = take_events(st);
+    cudaEventRecord(rec.ev[0], stream);
+  }
+  cudaError_t e = launch_plan(pp, stream);
+  if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  if (prof) cudaEventRecord(rec.ev[1], stream);
+  e = launch_attention(ap, tq, tkv, d, st.sms, stream);
+  if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  if (prof) cudaEventRecord(rec.ev[2], stream);
+  const int cgrid = std::min(ws.max_units, 2 * st.sms);
+  e = launch_combine(cp, cgrid, stream);
+  if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  if (prof) {
+    cudaEventRecord(rec.ev[3], stream);
+    st.prof.push_back(rec);
+  }
+  return PATTN_OK;
+}
+
+}  // namespace
+}  // namespace pattn
+
+using namespace pattn;
+
+extern "C" {
+
+pattn_status pattn_forward(void* out, const void* q, const void* kv_pool,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           const int32_t* cu_q, int num_seqs, int total_q, int max_q, int max_kv,
+                           int n_heads_q, int n_heads_kv, int head_dim, int page_size,
+                           int num_pages, float scale, int causal, pattn_stream_t stream) {
+  Shape sh{};
+  pattn_status s = check_args(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                              max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size,
+                              num_pages, scale, causal, &sh);
+  if (s != PATTN_OK) return s;
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return forward_locked(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
+                        max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, scale,
+                        causal, reinterpret_cast<cudaStream_t>(stream), sh);
+}
+
+pattn_status pattn_forward_host(void* out, const void* q, const void* kv_pool,
+                                size_t kv_pool_bytes, const int32_t* block_table,
+                                const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
+                                int total_q, int max_q, int max_kv, int n_heads_q, int n_heads_kv,
+                                int head_dim, int page_size, int num_pages, float scale,
+                                int causal, pattn_stream_t stream) {
+  Shape sh{};
+  pattn_status s = check_args(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                              max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size,
+                              num_pages, scale, causal, &sh);
+  if (s != PATTN_OK) return s;
+  if (kv_pool_bytes == 0) return PATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* stp = nullptr;
+  if ((s = device_state(&stp)) != PATTN_OK) return s;
+  DeviceState& st = *stp;
+  const size_t qo_bytes = static_cast<size_t>(total_q) * n_heads_q * head_dim * 2;
+  const size_t bt_bytes =
+      block_table ? static_cast<size_t>(num_seqs) * std::max(1, cdiv(max_kv, page_size)) * 4 : 0;
+  const size_t need[6] = {qo_bytes, kv_pool_bytes, std::max<size_t>(bt_bytes, 16),
+                          static_cast<size_t>(num_seqs) * 4, static_cast<size_t>(num_seqs + 1) * 4,
+                          qo_bytes};
+  for (int i = 0; i < 6; ++i) {
+    if (st.stage[i] && st.stage_bytes[i] >= need[i]) continue;
+    if (st.stage[i]) {
+      cudaDeviceSynchronize();
+      cudaFree(st.stage[i]);
+      st.stage[i] = nullptr;
+      st.stage_bytes[i] = 0;
+    }
+    cudaError_t e = cudaMalloc(&st.stage[i], need[i]);
+    if (e != cudaSuccess) {
+      st.stage[i] = nullptr;
+      return cuda_fail(e);
+    }
+    st.stage_bytes[i] = need[i];
+  }
+  cudaError_t e = cudaSuccess;
+  const void* src[5] = {q, kv_pool, block_table, seq_lens, cu_q};
+  const size_t n[5] = {qo_bytes, kv_pool_bytes, bt_bytes, static_cast<size_t>(num_seqs) * 4,
+                       static_cast<size_t>(num_seqs + 1) * 4};
+  for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+    if (src[i] && n[i]) e = cudaMemcpyAsync(st.stage[i], src[i], n[i], cudaMemcpyHostToDevice, st_);
+  if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  s = forward_locked(st.stage[5], st.stage[0], st.stage[1],
+                     block_table ? static_cast<const int32_t*>(st.stage[2]) : nullptr,
+                     static_cast<const int32_t*>(st.stage[3]), static_cast<const int32_t*>(st.stage[4]),
+                     num_seqs, total_q, max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size,
+                     num_pages, scale, causal, st_, sh);
+  if (s != PATTN_OK) return s;
+  e = cudaMemcpyAsync(out, st.stage[5], qo_bytes, cudaMemcpyDeviceToHost, st_);
+  if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  e = cudaStreamSynchronize(st_);
+  return e == cudaSuccess ? PATTN_OK : PATTN_ERR_CUDA;
+}
+
+size_t pattn_workspace_size(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
+                            int n_heads_kv, int head_dim, int page_size) {
+  (void)max_kv;
+  (void)page_size;
+  if (num_seqs < 0 || total_q < 0 || max_q < 0 || n_heads_q <= 0 || n_heads_kv <= 0 ||
+      n_heads_q % n_heads_kv != 0 || n_heads_q / n_heads_kv > kBM || (head_dim != 128 && head_dim != 256))
+    return 0;
+  return ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim).total;
+}
+
+pattn_status pattn_set_workspace(void* ptr, size_t bytes) {
+  if (ptr && (!aligned(ptr, 256) || bytes < kHdrWords * sizeof(int))) return PATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* stp = nullptr;
+  pattn_status s = device_state(&stp);
+  if (s != PATTN_OK) return s;
+  DeviceState& st = *stp;
+  if (!st.ws_caller && st.ws) {
+    cudaDeviceSynchronize();
+    cudaFree(st.ws);
+  }
+  st.ws = nullptr;
+  st.ws_bytes = 0;
+  st.ws_caller = false;
+  if (ptr) {
+    if (cudaMemset(ptr, 0, kHdrWords * sizeof(int)) != cudaSuccess) return PATTN_ERR_CUDA;
+    st.ws = ptr;
+    st.ws_bytes = bytes;
+    st.ws_caller = true;
+  }
+  return PATTN_OK;
+}
+
+pattn_status pattn_get_device_status(pattn_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* stp = nullptr;
+  pattn_status s = device_state(&stp);
+  if (s != PATTN_OK) return s;
+  cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st_) != cudaSuccess) return PATTN_ERR_CUDA;
+  if (!stp->ws) return PATTN_OK;
+  int err = 0;
+  if (cudaMemcpy(&err, stp->ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PATTN_ERR_CUDA;
+  if (cudaMemset(stp->ws, 0, sizeof(int)) != cudaSuccess) return PATTN_ERR_CUDA;
+  if (err & kErrTimeout) return PATTN_ERR_DEVICE_TIMEOUT;
+  if (err & kErrBadInput) return PATTN_ERR_DEVICE_BAD_INPUT;
+  return PATTN_OK;
+}
+
+const char* pattn_status_string(pattn_status status) {
+  switch (status) {
+    case PATTN_OK: return "ok";
+    case PATTN_ERR_INVALID_ARG: return "invalid argument";
+    case PATTN_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case PATTN_ERR_CUDA: return "CUDA call failed";
+    case PATTN_ERR_NO_MEMORY: return "out of device memory or workspace too small";
+    case PATTN_ERR_DEVICE_BAD_INPUT: return "device data rejected (page index, lengths or cu_q)";
+    case PATTN_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
+  }
+  return "unknown status";
+}
+
+pattn_status pattn_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_profile = on != 0;
+  return PATTN_OK;
+}
+
+pattn_status pattn_profile_read(double* ms_plan, double* ms_attention, double* ms_combine,
+                                int* calls) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* stp = nullptr;
+  pattn_status s = device_state(&stp);
+  if (s != PATTN_OK) return s;
+  DeviceState& st = *stp;
+  double t[3] = {0, 0, 0};
+  for (auto& r : st.prof) {
+    if (cudaEventSynchronize(r.ev[3]) != cudaSuccess) return PATTN_ERR_CUDA;
+    for (int k = 0; k < 3; ++k) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, r.ev[k], r.ev[k + 1]) != cudaSuccess) return PATTN_ERR_CUDA;
+      t[k] += ms;
+    }
+  }
+  if (ms_plan) *ms_plan = t[0];
+  if (ms_attention) *ms_attention = t[1];
+  if (ms_combine) *ms_combine = t[2];
+  if (calls) *calls = static_cast<int>(st.prof.size());
+  for (auto& r : st.prof) st.prof_pool.push_back(r);
+  st.prof.clear();
+  return PATTN_OK;
+}
+
+}  // extern "C"

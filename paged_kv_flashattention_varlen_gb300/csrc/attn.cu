@@ -1,0 +1,498 @@
+// attn.cu -- fused paged-KV attention for sm_103a (tcgen05 + TMA).
+//
+// One persistent CTA per SM walks the planned work list (longest first,
+// round robin over CTAs). A work item is (sequence, kv head, q tile, KV tile
+// range). For each item:
+//
+//   * the load warp TMA-loads the GQA-packed Q tile: the G query heads of one
+//     KV head for T = 128 / G tokens, as 128 rows of 128-byte-swizzled shared
+//     memory (the GQA-packed Q tensor map of the trtllm-gen paged decode
+//     manifest: dims [D, group, kv head, token]); then, per KV tile of BN keys,
+//     gathers the K and V rows page by page through one tensor map over the
+//     whole pool, [D, 64 rows, Hkv, 2 x pages] (the manifest's K and V tensor
+//     maps), each page read once per KV head for all G query heads;
+//   * the MMA thread issues S = Q K^T (tcgen05.mma kind::f16, M = 128,
+//     N = BN, K = D) into one of two TMEM S buffers, then O += P V (M = 128,
+//     N = D, K = BN) with V read MN-major from shared memory; commits signal
+//     mbarriers (the SM100MHA2Q "UMMA0" / "UMMA1" accumulators of the
+//     FlashAttention-4 doc);
+//   * the softmax warpgroup owns one query row per thread: it reads its S row
+//     from TMEM, masks keys past the end or (causal) past its position only on
+//     tiles that need it, keeps the running max m and sum l in log2 units
+//     (exp2 with the scale folded into log2 e, as the manifest's pack scalar
+//     does), rescales the O row in TMEM only when the max grew by more than
+//     2^8 (exact: O and l share the stale max), and writes P as bf16 into
+//     128-byte-swizzled shared memory for the PV MMA;
+//   * the tail warp zeroes V rows past the sequence end in the last tile, so
+//     that NaN or garbage there cannot reach O through 0 * NaN.
+//
+// At the end of an item the softmax warps divide by l and store bf16 rows, or
+// (split items) write the normalised partial O and (m, l) for the combine.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace pattn {
+namespace {
+
+template <int D, int BN>
+struct Cfg {
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kKVStage = BN * D * 2;
+  static constexpr int kPBytes = kBM * BN * 2;
+  static constexpr int kStages = 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kStages * kKVStage;
+  static constexpr int kOffP = kOffV + kStages * kKVStage;
+  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kOffMisc = kOffBar + kBarBytes;
+  static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
+  static constexpr int kColO = 0;                     // TMEM columns [0, D)
+  static constexpr int kColS = 256;                   // two S buffers of BN columns
+  static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns per row
+  static constexpr int kPagesPerTile = BN / kPage;
+  static_assert(kColS + 2 * BN <= kTmemCols, "TMEM budget");
+  static_assert(D <= kColS, "O columns");
+  static_assert(BN % kPage == 0 && BN % 32 == 0, "tile");
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+// mbarrier slots
+enum Bar {
+  kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVReady0,
+  kVReady1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull, kPVDone, kDrain,
+  kNumBars
+};
+
+struct Item {
+  int b, hk, qt, kt0, kt1, part;
+};
+
+__device__ __forceinline__ Item decode_item(int4 v) {
+  Item it;
+  it.b = v.x;
+  it.hk = v.y >> 16;
+  it.qt = v.y & 0xFFFF;
+  it.kt0 = (v.z >> 16) & 0xFFFF;
+  it.kt1 = v.z & 0xFFFF;
+  it.part = v.w;
+  return it;
+}
+
+template <int D, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
+            const AttnParams p) {
+  using C = Cfg<D, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_addr(smem);
+  const uint32_t sQ = s_base + C::kOffQ;
+  const uint32_t sK = s_base + C::kOffK;
+  const uint32_t sV = s_base + C::kOffV;
+  const uint32_t sP = s_base + C::kOffP;
+  const uint32_t sBar = s_base + C::kOffBar;
+  uint8_t* misc = smem + C::kOffMisc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 16);
+  auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitCtl ctl{abort_flag, p.err};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(kQFull), 1);
+    mbar_init(bar(kQEmpty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kKFull0 + s), 1);
+      mbar_init(bar(kKEmpty0 + s), 1);
+      mbar_init(bar(kVFull0 + s), 1);
+      mbar_init(bar(kVReady0 + s), 1);
+      mbar_init(bar(kVEmpty0 + s), 1);
+      mbar_init(bar(kSFull0 + s), 1);
+      mbar_init(bar(kSFree0 + s), 4);
+    }
+    mbar_init(bar(kPFull), 4);
+    mbar_init(bar(kPVDone), 1);
+    mbar_init(bar(kDrain), 1);
+    mbar_init_fence();
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_kv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int n_items = p.hdr[kHdrItems];
+  const int G = p.group;
+  const int T = p.tokens_per_tile;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ load warp
+    if (lane == 0) {
+      uint32_t n = 0, itl = 0;
+      bool ok = true;
+      const uint64_t pol_q = l2_policy_evict_last();
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+        const Item it = decode_item(p.items[idx]);
+        const int4 si = p.seq_info[it.b];
+        const int q0 = si.x, L = si.z, kv0 = si.w;
+        const bool decode_like = si.y <= T;
+        const uint64_t pol_kv = decode_like ? l2_policy_evict_first() : l2_policy_evict_last();
+        if (!(ok = wait_one(bar(kQEmpty), (itl & 1u) ^ 1u, ctl))) break;
+        mbar_arrive_expect_tx(bar(kQFull), static_cast<uint32_t>(C::kDBlocks * 128 * G * T));
+        for (int c = 0; c < C::kDBlocks; ++c)
+          tma_load_4d(sQ + c * (kBM * 128), &tmap_q, bar(kQFull), c * 64, 0, it.hk,
+                      q0 + it.qt * T, pol_q);
+        for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
+          const uint32_t s = n & 1u, ph = ((n >> 1) & 1u) ^ 1u;
+          // pages of this tile (the block table is read once for K and V)
+          int coord[C::kPagesPerTile];
+          int nload = 0;
+#pragma unroll
+          for (int pg = 0; pg < C::kPagesPerTile; ++pg) {
+            const int key = kt * BN + pg * kPage;
+            coord[pg] = -1;
+            if (key < L) {
+              if (p.paged) {
+                int page = p.block_table[static_cast<size_t>(it.b) * p.bt_stride + key / kPage];
+                if (page >= 0 && page < p.num_pages) {
+                  coord[pg] = page;
+                  ++nload;
+                } else {
+                  atomicOr(p.err, kErrBadInput);
+                }
+              } else {
+                coord[pg] = kv0 + key;
+                ++nload;
+              }
+            }
+          }
+          const uint32_t bytes = static_cast<uint32_t>(nload * C::kDBlocks * kPage * 128);
+          for (int kind = 0; kind < 2; ++kind) {
+            const int full = kind ? kVFull0 : kKFull0;
+            const int empty = kind ? kVEmpty0 : kKEmpty0;
+            const uint32_t dst0 = (kind ? sV : sK) + s * C::kKVStage;
+            if (!(ok = wait_one(bar(empty + s), ph, ctl))) break;
+            mbar_arrive_expect_tx(bar(full + s), bytes);
+#pragma unroll
+            for (int pg = 0; pg < C::kPagesPerTile; ++pg) {
+              if (coord[pg] < 0) continue;
+              for (int c = 0; c < C::kDBlocks; ++c) {
+                const uint32_t dst = dst0 + c * (BN * 128) + pg * (kPage * 128);
+                if (p.paged)
+                  tma_load_4d(dst, &tmap_kv, bar(full + s), c * 64, 0, it.hk, 2 * coord[pg] + kind,
+                              pol_kv);
+                else
+                  tma_load_4d(dst, &tmap_kv, bar(full + s), c * 64, it.hk, coord[pg], kind, pol_kv);
+              }
+            }
+          }
+          if (!ok) break;
+        }
+      }
+      // Drain: every copy this thread started must have landed before exit.
+      if (itl > 0 || n > 0) {
+        if (n > 0) {
+          for (uint32_t s = 0; s < 2; ++s) {
+            if (n <= s) continue;
+            const uint32_t last = ((n - 1 - s) & ~1u) + s;  // last fill index on stage s
+            wait_one(bar(kKFull0 + s), (last >> 1) & 1u, ctl);
+            wait_one(bar(kVFull0 + s), (last >> 1) & 1u, ctl);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA warp
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, BN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
+      uint32_t n = 0, itl = 0;
+      bool ok = true;
+      auto issue_pv = [&](uint32_t m, bool first) -> bool {
+        if (!wait_one(bar(kPFull), m & 1u, ctl)) return false;
+        if (!wait_one(bar(kVReady0 + (m & 1u)), (m >> 1) & 1u, ctl)) return false;
+        tc_fence_after();
+        const uint32_t v0 = sV + (m & 1u) * C::kKVStage;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t a = sw128_desc(sP + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = sw128_desc(v0 + kk * (16 * 128), BN * 128, 1024);
+          umma_f16(tmem + C::kColO, a, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(bar(kVEmpty0 + (m & 1u)));
+        umma_commit(bar(kPVDone));
+        return true;
+      };
+      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+        const Item it = decode_item(p.items[idx]);
+        if (!(ok = wait_one(bar(kQFull), itl & 1u, ctl))) break;
+        tc_fence_after();
+        for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
+          const uint32_t s = n & 1u;
+          if (!(ok = wait_one(bar(kKFull0 + s), (n >> 1) & 1u, ctl))) break;
+          if (!(ok = wait_one(bar(kSFree0 + s), ((n >> 1) & 1u) ^ 1u, ctl))) break;
+          tc_fence_after();
+          const uint32_t k0 = sK + s * C::kKVStage;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t a = sw128_desc(sQ + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = sw128_desc(k0 + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
+            umma_f16(tmem + C::kColS + s * BN, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar(kKEmpty0 + s));
+          umma_commit(bar(kSFull0 + s));
+          if (kt > it.kt0 && !(ok = issue_pv(n - 1, kt - 1 == it.kt0))) break;
+        }
+        if (!ok) break;
+        umma_commit(bar(kQEmpty));
+        if (!(ok = issue_pv(n - 1, it.kt1 - 1 == it.kt0))) break;
+      }
+      // Drain: all UMMAs issued by this thread complete before TMEM is freed.
+      umma_commit(bar(kDrain));
+      wait_one(bar(kDrain), 0, ctl);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ V tail warp
+    uint32_t n = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      const Item it = decode_item(p.items[idx]);
+      const int L = p.seq_info[it.b].z;
+      for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
+        const uint32_t s = n & 1u;
+        if (!(ok = wait_warp(bar(kVFull0 + s), (n >> 1) & 1u, ctl))) break;
+        const int live = L - kt * BN;
+        if (live < BN) {
+          // rows [live, BN) of every 64-column block: whole 128-byte rows, so the
+          // swizzle does not matter
+          uint8_t* v0 = smem + C::kOffV + s * C::kKVStage;
+          const int dead = BN - live;
+          const int chunks = dead * 8;  // 16-byte chunks per block
+          for (int c = 0; c < C::kDBlocks; ++c) {
+            uint4* blk = reinterpret_cast<uint4*>(v0 + c * (BN * 128) + live * 128);
+            for (int i = lane; i < chunks; i += 32) blk[i] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kVReady0 + s));
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax warpgroup
+    const int sw = warp - 4;              // TMEM lane quarter
+    const int r = threadIdx.x - 128;      // query row of this thread
+    const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
+    const int t_local = r / G;
+    const int g = r - t_local * G;
+    const float c = p.scale_log2;
+    uint32_t n = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      const Item it = decode_item(p.items[idx]);
+      const int4 si = p.seq_info[it.b];
+      const int q0 = si.x, ql = si.y, L = si.z;
+      const int tok = it.qt * T + t_local;
+      const bool valid = (t_local < T) && (tok < ql);
+      int lim = 0;  // keys [0, lim) visible to this row
+      if (valid) lim = p.causal ? min(L, L - ql + tok + 1) : L;
+      const bool warp_live = __any_sync(0xffffffffu, valid) != 0;
+      float m_used = -INFINITY, l = 0.f;
+      for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
+        const uint32_t s = n & 1u;
+        const bool first = kt == it.kt0;
+        if (!(ok = wait_warp(bar(kSFull0 + s), (n >> 1) & 1u, ctl))) break;
+        tc_fence_after();
+        uint32_t sr[BN / 32][32];
+        if (warp_live) {
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j)
+            tmem_ld32(tmem + lane_base + C::kColS + s * BN + j * 32, sr[j]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) reg_fence(sr[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kSFree0 + s));
+
+        bool pv_waited = false;
+        uint32_t pk[BN / 2];
+        if (warp_live) {
+          const int key0 = kt * BN;
+          const bool full_tile = key0 + BN <= lim;
+          float mx = -INFINITY;
+          if (full_tile) {
+#pragma unroll
+            for (int j = 0; j < BN / 32; ++j)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[j][i]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 32; ++j)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (key0 + j * 32 + i < lim) mx = fmaxf(mx, __uint_as_float(sr[j][i]));
+          }
+          const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
+          const float m_new = fmaxf(m_used, mx_s);
+          if (first) {
+            m_used = m_new;
+          } else {
+            const bool need = m_new > m_used + 8.0f;
+            if (__any_sync(0xffffffffu, need)) {
+              // O holds the previous tiles; rescale it once their PV is done.
+              if (!(ok = wait_warp(bar(kPVDone), (n - 1) & 1u, ctl))) break;
+              pv_waited = true;
+              tc_fence_after();
+              const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+              if (need) {
+                l *= alpha;
+                m_used = m_new;
+              }
+#pragma unroll 1
+              for (int j = 0; j < D / 32; ++j) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_base + C::kColO + j * 32, o);
+                tmem_wait_ld();
+                reg_fence(o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st32(tmem + lane_base + C::kColO + j * 32, o);
+              }
+              tmem_wait_st();
+            }
+          }
+          const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+          float sum = 0.f;
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int key = key0 + j * 32 + i;
+              float p0 = ex2(fmaf(__uint_as_float(sr[j][i]), c, -m_ref));
+              float p1 = ex2(fmaf(__uint_as_float(sr[j][i + 1]), c, -m_ref));
+              if (!full_tile) {
+                p0 = key < lim ? p0 : 0.f;
+                p1 = key + 1 < lim ? p1 : 0.f;
+              }
+              sum += p0 + p1;
+              __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+              pk[(j * 32 + i) >> 1] = *reinterpret_cast<uint32_t*>(&h);
+            }
+          }
+          l += sum;
+        }
+        if (!first && !pv_waited) {
+          // P shared memory is still read by the previous tile's PV MMA.
+          if (!(ok = wait_warp(bar(kPVDone), (n - 1) & 1u, ctl))) break;
+        }
+        if (warp_live) {
+          // row r of P, key blocks of 64 (128-byte rows), 16-byte chunks XOR-swizzled
+#pragma unroll
+          for (int kb = 0; kb < BN / 64; ++kb) {
+            uint8_t* rowp = smem + C::kOffP + kb * (kBM * 128) + r * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const int w0 = kb * 32 + ch * 4;
+              *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
+                  make_uint4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kPFull));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      if (!(ok = wait_warp(bar(kPVDone), (n - 1) & 1u, ctl))) break;
+      tc_fence_after();
+      if (warp_live) {
+        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+        const int h = it.hk * G + g;
+#pragma unroll 1
+        for (int j = 0; j < D / 32; ++j) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + C::kColO + j * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (!valid) continue;
+          if (it.part < 0) {
+            uint4* dst = reinterpret_cast<uint4*>(
+                p.out + (static_cast<size_t>(q0 + tok) * p.n_heads_q + h) * D + j * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(o[v * 8 + 2 * e]) * inv_l,
+                                                          __uint_as_float(o[v * 8 + 2 * e + 1]) * inv_l);
+                w[e] = *reinterpret_cast<uint32_t*>(&hh);
+              }
+              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(
+                p.part_o + static_cast<size_t>(it.part + r) * D + j * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(o[v * 4]) * inv_l, __uint_as_float(o[v * 4 + 1]) * inv_l,
+                                   __uint_as_float(o[v * 4 + 2]) * inv_l,
+                                   __uint_as_float(o[v * 4 + 3]) * inv_l);
+          }
+        }
+        if (valid && it.part >= 0) p.part_ml[it.part + r] = make_float2(l > 0.f ? m_used : -INFINITY, l);
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+int attention_block_n(int head_dim) { return head_dim == 128 ? 128 : 64; }
+
+size_t attention_smem_bytes(int head_dim) {
+  return head_dim == 128 ? static_cast<size_t>(Cfg<128, 128>::kSmem)
+                         : static_cast<size_t>(Cfg<256, 64>::kSmem);
+}
+
+cudaError_t attention_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<128, 128>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg<128, 128>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_kernel<256, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<256, 64>::kSmem);
+}
+
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
+                             int head_dim, int grid, cudaStream_t s) {
+  if (head_dim == 128)
+    attn_kernel<128, 128><<<grid, kThreads, Cfg<128, 128>::kSmem, s>>>(tq, tkv, p);
+  else
+    attn_kernel<256, 64><<<grid, kThreads, Cfg<256, 64>::kSmem, s>>>(tq, tkv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace pattn

@@ -1,0 +1,100 @@
+// kernels.cuh -- parameters shared by the host planner and the three device
+// kernels (plan, attention, combine) of the paged-KV varlen attention library.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace pattn {
+
+constexpr int kBM = 128;            // packed query rows per tile (tokens x GQA group)
+constexpr int kPage = 64;           // page size handled by the gather (rows per TMA box)
+constexpr int kThreads = 256;       // 8 warps: load, MMA, V tail fix, idle, 4 x softmax
+constexpr int kTmemCols = 512;
+constexpr int kHistBuckets = 4096;  // cost buckets of the longest-first item order
+constexpr int kMaxSplits = 64;
+
+// Bits of the device error word.
+constexpr int kErrBadInput = 1;
+constexpr int kErrTimeout = 2;
+
+// Device workspace header (int words).
+enum HdrWord { kHdrErr = 0, kHdrItems = 1, kHdrUnits = 2, kHdrPartRows = 3, kHdrOverflow = 4,
+               kHdrWords = 64 };
+
+// Work item, 16 bytes:
+//   x = sequence b
+//   y = kv head << 16 | q tile
+//   z = first kv tile << 16 | end kv tile
+//   w = first partial row of this split (-1: not split, write bf16 out directly)
+// Split unit (combine), 16 bytes: x = b, y = kv head, z = splits S, w = first partial row.
+// Sequence info, 16 bytes: x = first query token, y = query length (-1: rejected),
+//   z = KV length, w = first KV row (contiguous cache).
+
+struct Workspace {
+  int* hdr;
+  int4* seq_info;
+  int4* seq_plan;   // x = first global q tile, y = q tiles, z = splits, w = first split unit
+  int* seq_part;    // first partial row of the sequence's split units
+  int4* items;
+  int4* units;
+  float* part_o;    // [rows][D] split-normalised partial O
+  float2* part_ml;  // [rows] (running max in log2 units, sum of exp2)
+  int max_items;
+  int max_units;
+  int max_part_rows;
+};
+
+struct PlanParams {
+  const int32_t* cu_q;
+  const int32_t* seq_lens;
+  const int32_t* block_table;  // nullptr: contiguous cache
+  __nv_bfloat16* out;
+  Workspace ws;
+  int num_seqs, total_q, max_q, max_kv;
+  int n_heads_q, n_heads_kv, group, head_dim;
+  int tokens_per_tile;  // T = kBM / group
+  int block_n;          // keys per KV tile
+  int bt_stride, num_pages;
+  int causal;
+  int target_items;     // items the split heuristic aims at (a multiple of the SM count)
+  int min_chunk;        // fewest KV tiles per split
+};
+
+struct AttnParams {
+  const int4* items;
+  const int* hdr;
+  const int4* seq_info;
+  const int32_t* block_table;
+  __nv_bfloat16* out;
+  float* part_o;
+  float2* part_ml;
+  int* err;
+  int bt_stride, num_pages;
+  int n_heads_q, n_heads_kv, group, tokens_per_tile;
+  float scale_log2;  // softmax scale * log2(e)
+  int causal;
+  int paged;
+};
+
+struct CombineParams {
+  const int4* units;
+  const int* hdr;
+  const int4* seq_info;
+  const float* part_o;
+  const float2* part_ml;
+  __nv_bfloat16* out;
+  int n_heads_q, group, head_dim;
+};
+
+// Launchers (defined in the .cu files; return the launch error).
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
+cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
+                             int head_dim, int grid, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
+int attention_block_n(int head_dim);
+size_t attention_smem_bytes(int head_dim);
+cudaError_t attention_set_attributes();
+
+}  // namespace pattn

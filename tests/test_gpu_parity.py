@@ -1,0 +1,229 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Small cases are compared element by element over every output; the five named
+workloads at full size are compared over every decode row and over sampled
+prefill rows (first/last rows of each sequence, q-tile boundaries, seeded
+random rows), which the oracle computes one by one. Bar: max |err| <= 2e-2 and
+mean |err| <= 2e-3 on the bf16 outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from helpers import assert_parity, run_gpu, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU-only machines, never run there
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_flashattention_varlen_gb300 import build
+    build.build()
+    import paged_kv_flashattention_varlen_gb300 as pk
+    assert pk.device_status() == 0
+
+
+def _status():
+    import paged_kv_flashattention_varlen_gb300 as pk
+    return pk.device_status()
+
+
+# --------------------------------------------------------------- named workloads
+def test_tiny_paged_decode_full():
+    wl = workloads.named(1)
+    out = run_gpu(wl)
+    assert_parity(out, wl)
+    assert _status() == 0
+
+
+def test_decode_batch_full():
+    wl = workloads.named(2)
+    out = run_gpu(wl)
+    assert_parity(out, wl)
+    assert _status() == 0
+
+
+def test_causal_prefill_small_full():
+    wl = workloads.named(3, scale_down=16)      # 4 x 512 tokens, every row
+    out = run_gpu(wl)
+    assert_parity(out, wl)
+
+
+def test_causal_prefill_full_size_sampled():
+    wl = workloads.named(3)
+    out = run_gpu(wl)
+    assert_parity(out, wl, rows=sample_rows(wl, per_seq=8))
+    assert _status() == 0
+
+
+def test_noncausal_contiguous_small_full():
+    wl = workloads.named(4, scale_down=32)      # 1181 tokens, every row
+    out = run_gpu(wl)
+    assert_parity(out, wl)
+
+
+def test_noncausal_contiguous_full_size_sampled():
+    wl = workloads.named(4)
+    out = run_gpu(wl)
+    rows = sample_rows(wl, per_seq=4)
+    assert_parity(out, wl, rows=rows)
+    assert _status() == 0
+
+
+def test_mixed_batch_small_full():
+    wl = workloads.named(5, scale_down=8)
+    out = run_gpu(wl)
+    assert_parity(out, wl)
+
+
+def test_mixed_batch_full_size():
+    wl = workloads.named(5)
+    out = run_gpu(wl)
+    decode_rows = list(range(96))
+    assert_parity(out, wl, rows=decode_rows)
+    chunk_rows = [r for r in sample_rows(wl, per_seq=6) if r >= 96]
+    assert_parity(out, wl, rows=chunk_rows)
+    assert _status() == 0
+
+
+# --------------------------------------------------------------- edge sweep
+EDGES = [1, 63, 64, 65, 127, 128, 129]
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(128, 4, 1), (128, 8, 8), (256, 12, 2), (256, 16, 2)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_edge_lengths(d, hq, hkv, causal):
+    kv_lens, q_lens = [], []
+    for L in EDGES:
+        for ql in EDGES:
+            if causal and ql > L:
+                continue
+            kv_lens.append(L)
+            q_lens.append(ql)
+    wl = workloads.make_paged("edges", 500 + d + hq, q_lens, kv_lens, hq, hkv, d, 64,
+                              causal=causal, extra_pages=3)
+    out = run_gpu(wl)
+    assert_parity(out, wl)
+    assert _status() == 0
+
+
+def test_long_decode_splits_and_short_sequences_mixed():
+    rng = np.random.default_rng(7)
+    kv = [1, 2, 64, 65, 129, 4000, 20000, 300, 8191, 8192, 8193]
+    wl = workloads.make_paged("splits", 8, [1] * len(kv), kv, 32, 8, 128, 64, causal=True,
+                              extra_pages=2)
+    out = run_gpu(wl)
+    assert_parity(out, wl)
+    wl2 = workloads.make_paged("splits256", 9, [1, 3, 1] * 4, rng.integers(1, 9000, size=12),
+                               16, 2, 256, 64, causal=True)
+    assert_parity(run_gpu(wl2), wl2)
+
+
+# --------------------------------------------------------------- degenerate inputs
+def test_empty_and_queries_before_the_first_key():
+    # L = 0 (no key), ql = 0 (no query), and non-causal/causal ql > L rows
+    wl = workloads.make_paged("empty", 11, [3, 0, 5, 2], [0, 10, 3, 70], 8, 2, 128, 64,
+                              causal=True, extra_pages=1)
+    out = run_gpu(wl)
+    assert_parity(out, wl)
+    assert torch.all(out[:3] == 0)
+    assert torch.all(out[3:5] == 0)   # positions 3-5+i < 0 for i < 2
+    assert _status() == 0
+
+
+def test_bad_page_sets_error_and_zeroes_that_sequence():
+    wl = workloads.make_paged("bad", 12, [2, 2], [100, 100], 8, 2, 128, 64, causal=True)
+    d = to_device(wl)
+    bt = d["bt"].clone()
+    bt[1, 1] = wl.num_pages + 5
+    d["bt"] = bt
+    out = run_gpu(wl, d=d)
+    import paged_kv_flashattention_varlen_gb300 as pk
+    assert pk.device_status() == 5
+    assert torch.all(out[2:4] == 0)
+    assert_parity(out, wl, rows=[0, 1])
+    assert pk.device_status() == 0
+
+
+def test_lengths_beyond_host_bounds_are_rejected_on_device():
+    wl = workloads.make_paged("bounds", 13, [2, 1], [100, 50], 8, 2, 128, 64, causal=True)
+    d = to_device(wl)
+    d["bt"] = d["bt"][:, :1].contiguous()           # table stride ceil(max_kv / 64) = 1
+    import paged_kv_flashattention_varlen_gb300 as pk
+    out = torch.full_like(d["q"], float("nan"))
+    pk.forward(out, d["q"], d["kv"], d["bt"], d["sl"], d["cu"], max_q=2, max_kv=64,
+               n_heads_kv=2, scale=wl.scale, causal=True, num_pages=wl.num_pages)
+    assert pk.device_status() == 5
+    assert torch.all(out[:2] == 0)                  # L = 100 > max_kv: rejected
+    assert_parity(out, wl, rows=[2])
+
+
+# --------------------------------------------------------------- invariants on the GPU
+def test_repeatable_and_page_permutation_bitwise():
+    wl = workloads.named(2, scale_down=4)
+    d = to_device(wl)
+    a = run_gpu(wl, d=d)
+    b = run_gpu(wl, d=d)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(wl.num_pages))
+    pool2 = torch.empty_like(wl.kv_pool)
+    pool2[perm] = wl.kv_pool
+    bt = wl.block_table.clone()
+    m = bt >= 0
+    bt[m] = perm[bt[m].long()].to(torch.int32)
+    d2 = dict(d, kv=pool2.cuda(), bt=bt.cuda())
+    c = run_gpu(wl, d=d2)
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_contiguous_equals_paged_bitwise():
+    wl = workloads.make_contiguous("c", 14, [40, 1, 7], [300, 129, 64], 8, 2, 128, causal=True)
+    a = run_gpu(wl)
+    # same rows laid out as pages of 64
+    P = 64
+    pages, table, start = [], [], 0
+    for L in wl.seq_lens.tolist():
+        row = []
+        for s in range((L + P - 1) // P):
+            blk = torch.full((2, P, 2, 128), float("nan"), dtype=torch.bfloat16)
+            n = min(P, L - s * P)
+            blk[:, :n] = wl.kv_pool[:, start + s * P:start + s * P + n]
+            row.append(len(pages))
+            pages.append(blk)
+        start += L
+        table.append(row)
+    w = max(len(r) for r in table)
+    wl.block_table = torch.tensor([r + [-1] * (w - len(r)) for r in table], dtype=torch.int32)
+    wl.kv_pool = torch.stack(pages)
+    wl.num_pages = len(pages)
+    b = run_gpu(wl)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_host_entry_point_matches_device_entry_point():
+    import paged_kv_flashattention_varlen_gb300 as pk
+    wl = workloads.named(1)
+    a = run_gpu(wl)
+    out = torch.empty_like(wl.q).pin_memory()
+    pk.forward_host(out, wl.q.pin_memory(), wl.kv_pool.pin_memory(), wl.block_table.pin_memory(),
+                    wl.seq_lens, wl.cu_q, max_q=wl.max_q, max_kv=wl.max_kv,
+                    n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
+                    num_pages=wl.num_pages)
+    assert torch.equal(a.cpu().view(torch.int16), out.view(torch.int16))
+
+
+def test_profile_counts_launches():
+    import paged_kv_flashattention_varlen_gb300 as pk
+    wl = workloads.named(1)
+    d = to_device(wl)
+    pk.profile_read()
+    pk.profile_enable(True)
+    for _ in range(3):
+        run_gpu(wl, d=d)
+    pk.profile_enable(False)
+    plan, attn, comb, calls = pk.profile_read()
+    assert calls == 3 and attn > 0 and plan > 0
