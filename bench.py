@@ -36,7 +36,7 @@ PREFILL = 3
 NOMINAL_HBM_GBS = 7900.0
 NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["attn.cu", "ptx.cuh", "kernels.cuh"]
+KERNEL_SOURCES = ["attn.cu", "decode.cu", "ptx.cuh", "kernels.cuh"]
 
 
 def parse():
@@ -75,7 +75,7 @@ def kernel_source_hash() -> str:
 def ncu_traffic(kind: str):
     """DRAM bytes per launch of the attention kernel from the committed ncu summary,
     if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"attn_kernel_{kind}_traffic.md")
+    path = os.path.join(ROOT, "profiles", f"{kind}_attention_kernel_traffic.md")
     try:
         text = open(path).read()
     except OSError:
@@ -204,7 +204,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs", "nominal_frac": round(achieved / NOMINAL_HBM_GBS, 4),
-                "kernel": "attn_kernel<128,128>", "kernel_ms": round(attn_ms, 5),
+                "kernel": "decode_kernel<128> (swap-AB)", "kernel_ms": round(attn_ms, 5),
                 "share": {"plan": round(t_plan / max(t_plan + t_attn + t_comb, 1e-9), 4),
                           "attention": round(t_attn / max(t_plan + t_attn + t_comb, 1e-9), 4),
                           "combine": round(t_comb / max(t_plan + t_attn + t_comb, 1e-9), 4)},

@@ -15,7 +15,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kTargetItemsPerSm = 4;
 constexpr int kTargetItemsCap = 1024;  // bound used when sizing the workspace
-constexpr int kMinChunk = 4;           // KV tiles per split, at least
+constexpr int kMinChunk = 8;           // 64-key blocks per split, at least
 constexpr int kProfileCap = 4096;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -23,8 +23,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Events around plan | decode kernel | prefill kernel | combine.
 struct ProfileRec {
-  cudaEvent_t ev[4];
+  cudaEvent_t ev[5];
 };
 
 struct DeviceState {
@@ -41,6 +42,7 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+double g_last_split[2] = {0, 0};  // decode-kernel and prefill-kernel ms of the last profile read
 EncodeTiledFn g_encode = nullptr;
 bool g_profile = false;
 
@@ -82,7 +84,7 @@ pattn_status check_args(const void* out, const void* q, const void* kv, const in
 }
 
 struct WsLayout {
-  size_t hdr, seq_info, seq_plan, seq_part, items, units, part_ml, part_o, total;
+  size_t hdr, seq_info, seq_plan, seq_part, items, dec_items, units, part_ml, part_o, total;
   int max_items, max_units, max_part_rows;
 };
 
@@ -108,6 +110,8 @@ WsLayout ws_layout(int num_seqs, int total_q, int max_q, int hq, int hkv, int d)
   w.seq_part = off = align_up(off, 256);
   off += sizeof(int) * static_cast<size_t>(num_seqs);
   w.items = off = align_up(off, 256);
+  off += sizeof(int4) * static_cast<size_t>(w.max_items);
+  w.dec_items = off = align_up(off, 256);
   off += sizeof(int4) * static_cast<size_t>(w.max_items);
   w.units = off = align_up(off, 256);
   off += sizeof(int4) * static_cast<size_t>(w.max_units);
@@ -149,6 +153,7 @@ pattn_status device_state(DeviceState** out) {
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
     if (attention_set_attributes() != cudaSuccess) return PATTN_ERR_CUDA;
+    if (decode_set_attributes() != cudaSuccess) return PATTN_ERR_CUDA;
     st.ready = true;
   }
   *out = &st;
@@ -217,6 +222,7 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
   ws.seq_plan = reinterpret_cast<int4*>(wsb + L.seq_plan);
   ws.seq_part = reinterpret_cast<int*>(wsb + L.seq_part);
   ws.items = reinterpret_cast<int4*>(wsb + L.items);
+  ws.dec_items = reinterpret_cast<int4*>(wsb + L.dec_items);
   ws.units = reinterpret_cast<int4*>(wsb + L.units);
   ws.part_ml = reinterpret_cast<float2*>(wsb + L.part_ml);
   ws.part_o = reinterpret_cast<float*>(wsb + L.part_o);
@@ -226,7 +232,20 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
 
   // ---- tensor maps (bf16, 128-byte swizzle, 64-element inner boxes)
   const int g = sh.group, T = sh.tokens_per_tile;
-  CUtensorMap tq, tkv;
+  const bool dec_enabled = g <= kDecRows;
+  const bool run_prefill = !dec_enabled || static_cast<long long>(max_q) * g > kDecRows;
+  CUtensorMap tq, tq_dec, tkv;
+  if (dec_enabled) {
+    // decode items: the G heads of one KV head for kDecRows / G tokens
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
+                                static_cast<cuuint64_t>(hkv),
+                                static_cast<cuuint64_t>(std::max(total_q, 1))};
+    const cuuint64_t str[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(g) * d * 2,
+                               static_cast<cuuint64_t>(hq) * d * 2};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g), 1,
+                               static_cast<cuuint32_t>(kDecRows / g)};
+    if ((s = encode(&tq_dec, q, 4, dims, str, box)) != PATTN_OK) return s;
+  }
   {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
                                 static_cast<cuuint64_t>(hkv),
@@ -274,6 +293,7 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
   pp.bt_stride = std::max(1, cdiv(max_kv, kPage));
   pp.num_pages = num_pages;
   pp.causal = causal;
+  pp.dec_enabled = dec_enabled ? 1 : 0;
   pp.target_items = std::min(kTargetItemsPerSm * st.sms, kTargetItemsCap);
   pp.min_chunk = kMinChunk;
 
@@ -307,6 +327,10 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
   cp.group = g;
   cp.head_dim = d;
 
+  AttnParams dp = ap;
+  dp.items = ws.dec_items;
+  dp.tokens_per_tile = dec_enabled ? kDecRows / g : 0;
+
   const bool prof = g_profile && st.prof.size() < static_cast<size_t>(kProfileCap);
   ProfileRec rec{};
   if (prof) {
@@ -316,14 +340,21 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
   cudaError_t e = launch_plan(pp, stream);
   if (e != cudaSuccess) return PATTN_ERR_CUDA;
   if (prof) cudaEventRecord(rec.ev[1], stream);
-  e = launch_attention(ap, tq, tkv, d, st.sms, stream);
-  if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  if (dec_enabled) {
+    e = launch_decode(dp, tq_dec, tkv, d, st.sms, stream);
+    if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  }
   if (prof) cudaEventRecord(rec.ev[2], stream);
+  if (run_prefill) {
+    e = launch_attention(ap, tq, tkv, d, st.sms, stream);
+    if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  }
+  if (prof) cudaEventRecord(rec.ev[3], stream);
   const int cgrid = std::min(ws.max_units, 2 * st.sms);
   e = launch_combine(cp, cgrid, stream);
   if (e != cudaSuccess) return PATTN_ERR_CUDA;
   if (prof) {
-    cudaEventRecord(rec.ev[3], stream);
+    cudaEventRecord(rec.ev[4], stream);
     st.prof.push_back(rec);
   }
   return PATTN_OK;
@@ -487,18 +518,20 @@ pattn_status pattn_profile_read(double* ms_plan, double* ms_attention, double* m
   pattn_status s = device_state(&stp);
   if (s != PATTN_OK) return s;
   DeviceState& st = *stp;
-  double t[3] = {0, 0, 0};
+  double t[4] = {0, 0, 0, 0};
   for (auto& r : st.prof) {
-    if (cudaEventSynchronize(r.ev[3]) != cudaSuccess) return PATTN_ERR_CUDA;
-    for (int k = 0; k < 3; ++k) {
+    if (cudaEventSynchronize(r.ev[4]) != cudaSuccess) return PATTN_ERR_CUDA;
+    for (int k = 0; k < 4; ++k) {
       float ms = 0.f;
       if (cudaEventElapsedTime(&ms, r.ev[k], r.ev[k + 1]) != cudaSuccess) return PATTN_ERR_CUDA;
       t[k] += ms;
     }
   }
+  g_last_split[0] = t[1];
+  g_last_split[1] = t[2];
   if (ms_plan) *ms_plan = t[0];
-  if (ms_attention) *ms_attention = t[1];
-  if (ms_combine) *ms_combine = t[2];
+  if (ms_attention) *ms_attention = t[1] + t[2];
+  if (ms_combine) *ms_combine = t[3];
   if (calls) *calls = static_cast<int>(st.prof.size());
   for (auto& r : st.prof) st.prof_pool.push_back(r);
   st.prof.clear();

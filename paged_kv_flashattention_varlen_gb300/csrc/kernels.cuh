@@ -12,7 +12,9 @@ constexpr int kBM = 128;            // packed query rows per tile (tokens x GQA 
 constexpr int kPage = 64;           // page size handled by the gather (rows per TMA box)
 constexpr int kThreads = 256;       // 8 warps: load, MMA, V tail fix, idle, 4 x softmax
 constexpr int kTmemCols = 512;
-constexpr int kHistBuckets = 4096;  // cost buckets of the longest-first item order
+constexpr int kHistBuckets = 2048;  // cost buckets of the longest-first order, per item list
+constexpr int kDecRows = 16;        // packed query rows a swap-AB decode item holds
+constexpr int kDecBlockN = 128;     // keys per KV tile of the decode kernel
 constexpr int kMaxSplits = 64;
 
 // Bits of the device error word.
@@ -21,7 +23,7 @@ constexpr int kErrTimeout = 2;
 
 // Device workspace header (int words).
 enum HdrWord { kHdrErr = 0, kHdrItems = 1, kHdrUnits = 2, kHdrPartRows = 3, kHdrOverflow = 4,
-               kHdrWords = 64 };
+               kHdrDecItems = 5, kHdrWords = 64 };
 
 // Work item, 16 bytes:
 //   x = sequence b
@@ -37,7 +39,8 @@ struct Workspace {
   int4* seq_info;
   int4* seq_plan;   // x = first global q tile, y = q tiles, z = splits, w = first split unit
   int* seq_part;    // first partial row of the sequence's split units
-  int4* items;
+  int4* items;      // prefill kernel items
+  int4* dec_items;  // swap-AB decode kernel items
   int4* units;
   float* part_o;    // [rows][D] split-normalised partial O
   float2* part_ml;  // [rows] (running max in log2 units, sum of exp2)
@@ -55,7 +58,8 @@ struct PlanParams {
   int num_seqs, total_q, max_q, max_kv;
   int n_heads_q, n_heads_kv, group, head_dim;
   int tokens_per_tile;  // T = kBM / group
-  int block_n;          // keys per KV tile
+  int block_n;          // keys per KV tile of the prefill kernel
+  int dec_enabled;      // group <= kDecRows: units of <= kDecRows packed rows go to the decode kernel
   int bt_stride, num_pages;
   int causal;
   int target_items;     // items the split heuristic aims at (a multiple of the SM count)
@@ -93,6 +97,10 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                              int head_dim, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
+cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
+                          int head_dim, int grid, cudaStream_t s);
+size_t decode_smem_bytes(int head_dim);
+cudaError_t decode_set_attributes();
 int attention_block_n(int head_dim);
 size_t attention_smem_bytes(int head_dim);
 cudaError_t attention_set_attributes();

@@ -59,6 +59,11 @@ __device__ int block_exclusive_scan(int v, int* out_excl, int* warp_sums) {
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
+// Units of at most kDecRows packed rows run on the swap-AB decode kernel.
+__device__ __forceinline__ bool is_decode(const PlanParams& p, int ql) {
+  return p.dec_enabled && ql >= 1 && ql * p.group <= kDecRows;
+}
+
 // Visible KV tiles of q tile qt: keys [0, kv_hi), kv_hi the largest limit of its rows.
 __device__ __forceinline__ int qtile_kv_tiles(const PlanParams& p, int ql, int L, int qt) {
   int hi = L;
@@ -66,14 +71,21 @@ __device__ __forceinline__ int qtile_kv_tiles(const PlanParams& p, int ql, int L
     const int last_tok = min(ql, (qt + 1) * p.tokens_per_tile);
     hi = min(L, L - ql + last_tok);
   }
-  return hi > 0 ? cdiv(hi, p.block_n) : 0;
+  const int bn = is_decode(p, ql) ? kDecBlockN : p.block_n;
+  return hi > 0 ? cdiv(hi, bn) : 0;
+}
+
+// Work of a q tile in 64-key blocks (comparable across the two kernels' tile sizes).
+__device__ __forceinline__ int qtile_blocks(const PlanParams& p, int ql, int L, int qt) {
+  const int bn = is_decode(p, ql) ? kDecBlockN : p.block_n;
+  return qtile_kv_tiles(p, ql, L, qt) * (bn / kPage);
 }
 
 constexpr int kSmemSeqs = 4096;  // sequences whose q-tile prefix is kept in shared memory
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams p) {
   __shared__ int warp_sums[32];
-  __shared__ int hist[kHistBuckets];
+  __shared__ int hist[2][kHistBuckets];  // [0] prefill items, [1] decode items
   __shared__ int s_qt_prefix[kSmemSeqs];
   __shared__ int s_carry[4];
   __shared__ unsigned long long s_tiles;
@@ -106,7 +118,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       if (ok) {
         nqt = cdiv(ql, p.tokens_per_tile);
         for (int qt = 0; qt < nqt; ++qt)
-          my_tiles += static_cast<unsigned long long>(qtile_kv_tiles(p, ql, L, qt));
+          my_tiles += static_cast<unsigned long long>(qtile_blocks(p, ql, L, qt));
       }
     }
     int kv_excl, qt_excl;
@@ -170,7 +182,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       const int nqt = ws.seq_plan[b].y;
       if (si.y > 0 && nqt == 1) {
         const int tiles = qtile_kv_tiles(p, si.y, si.z, 0);
-        if (tiles >= 2) S = min(min(cdiv(tiles, chunk), kMaxSplits), tiles);
+        const int per_tile = qtile_blocks(p, si.y, si.z, 0) / max(tiles, 1);  // 64-key blocks
+        const int chunk_tiles = max(1, cdiv(chunk, max(per_tile, 1)));
+        if (tiles >= 2) S = min(min(cdiv(tiles, chunk_tiles), kMaxSplits), tiles);
         rows = si.y * G;
       }
     }
@@ -208,8 +222,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     return lo;
   };
 
-  // ---- pass 3: histogram of item costs (KV tiles per item)
-  for (int i = threadIdx.x; i < kHistBuckets; i += kPlanThreads) hist[i] = 0;
+  // ---- pass 3: histogram of item costs (KV tiles per item), one per kernel
+  for (int i = threadIdx.x; i < 2 * kHistBuckets; i += kPlanThreads) (&hist[0][0])[i] = 0;
   __syncthreads();
   if (!overflow) {
     for (int gq = threadIdx.x; gq < total_qt; gq += kPlanThreads) {
@@ -219,34 +233,38 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       if (si.y <= 0) continue;
       const int tiles = qtile_kv_tiles(p, si.y, si.z, gq - sp.x);
       if (tiles == 0) continue;
+      const int list = is_decode(p, si.y) ? 1 : 0;
       for (int s = 0; s < sp.z; ++s) {
         const int k0 = static_cast<int>(static_cast<long long>(s) * tiles / sp.z);
         const int k1 = static_cast<int>(static_cast<long long>(s + 1) * tiles / sp.z);
-        atomicAdd(&hist[min(k1 - k0, kHistBuckets - 1)], p.n_heads_kv);
+        atomicAdd(&hist[list][min(k1 - k0, kHistBuckets - 1)], p.n_heads_kv);
       }
     }
   }
   __syncthreads();
-  // exclusive scan from the most expensive bucket down
-  {
+  // exclusive scan of each list from the most expensive bucket down
+  __shared__ int s_list_items[2];
+  for (int list = 0; list < 2; ++list) {
     constexpr int kPer = kHistBuckets / kPlanThreads;
     int local[kPer];
     int sum = 0;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      local[k] = hist[kHistBuckets - 1 - (threadIdx.x * kPer + k)];
+      local[k] = hist[list][kHistBuckets - 1 - (threadIdx.x * kPer + k)];
       sum += local[k];
     }
     int excl;
     const int tot = block_exclusive_scan(sum, &excl, warp_sums);
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      hist[kHistBuckets - 1 - (threadIdx.x * kPer + k)] = excl;
+      hist[list][kHistBuckets - 1 - (threadIdx.x * kPer + k)] = excl;
       excl += local[k];
     }
-    if (threadIdx.x == 0) s_total_items = tot;
+    if (threadIdx.x == 0) s_list_items[list] = tot;
     __syncthreads();
   }
+  if (threadIdx.x == 0) s_total_items = max(s_list_items[0], s_list_items[1]);
+  __syncthreads();
   const bool item_overflow = s_total_items > ws.max_items;
   const bool bad_plan = overflow || item_overflow;
 
@@ -262,13 +280,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       if (tiles == 0) continue;
       const int S = sp.z;
       const int rows = si.y * G;
+      const int list = is_decode(p, si.y) ? 1 : 0;
+      int4* dst = list ? ws.dec_items : ws.items;
       for (int s = 0; s < S; ++s) {
         const int k0 = static_cast<int>(static_cast<long long>(s) * tiles / S);
         const int k1 = static_cast<int>(static_cast<long long>(s + 1) * tiles / S);
-        const int pos = atomicAdd(&hist[min(k1 - k0, kHistBuckets - 1)], p.n_heads_kv);
+        const int pos = atomicAdd(&hist[list][min(k1 - k0, kHistBuckets - 1)], p.n_heads_kv);
         for (int hk = 0; hk < p.n_heads_kv; ++hk) {
           const int part = S >= 2 ? ws.seq_part[b] + (hk * S + s) * rows : -1;
-          ws.items[pos + hk] = make_int4(b, (hk << 16) | qt, (k0 << 16) | k1, part);
+          dst[pos + hk] = make_int4(b, (hk << 16) | qt, (k0 << 16) | k1, part);
         }
       }
     }
@@ -305,7 +325,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     }
   }
   if (threadIdx.x == 0) {
-    ws.hdr[kHdrItems] = bad_plan ? 0 : s_total_items;
+    ws.hdr[kHdrItems] = bad_plan ? 0 : s_list_items[0];
+    ws.hdr[kHdrDecItems] = bad_plan ? 0 : s_list_items[1];
     ws.hdr[kHdrUnits] = bad_plan ? 0 : total_units;
     ws.hdr[kHdrPartRows] = total_part_rows;
     ws.hdr[kHdrOverflow] = bad_plan ? 1 : 0;
