@@ -37,7 +37,7 @@ struct DCfg {
   static constexpr int kOffRing = 0;
   static constexpr int kOffQ = kOffRing + kRing * kStage;
   static constexpr int kOffP = kOffQ + kQBytes;
-  static constexpr int kOffRed = kOffP + kPBytes;           // 3 x 4 warps x 16 floats
+  static constexpr int kOffRed = kOffP + 2 * kPBytes;       // 3 x 4 warps x 16 floats
   static constexpr int kOffBar = kOffRed + 3 * 4 * kNQ * 4;
   static constexpr int kOffMisc = kOffBar + 512;
   static constexpr int kSmem = kOffMisc + 64 + 1024;
@@ -50,9 +50,183 @@ struct DCfg {
   static_assert(kSmem <= 232448, "shared memory");
 };
 
-enum DBar { kDQFull = 0, kDQEmpty, kDSFull0, kDSFull1, kDSFree0, kDSFree1, kDPFull, kDPVDone,
-            kDDrain, kDRedMax0, kDRedMax1, kDRedSum,
-            kDRingFull0 = 12 };  // then ring full [R], ring ready [R], ring empty [R]
+// P is double-buffered: p_full[b] / pv_done[b] complete once per use of P buffer b.
+enum DBar { kDQFull = 0, kDQEmpty, kDSFull0, kDSFull1, kDSFree0, kDSFree1, kDPFull0, kDPFull1,
+            kDPVDone0, kDPVDone1, kDDrain, kDRedMax0, kDRedMax1, kDRedSum,
+            kDRingFull0 = 14 };  // then ring full [R], ring ready [R], ring empty [R]
+
+struct SoftCtx {
+  uint8_t* smem;
+  uint32_t sBar, tmem, lane_base;
+  int sw, t, lane;
+  WaitCtl ctl;
+};
+
+// One decode item on the softmax warpgroup. NR >= the item's packed query
+// rows: only NR columns of S^T, P and O^T are touched. Returns false when a
+// bounded wait gave up.
+template <int D, int NR>
+__device__ __forceinline__ bool softmax_item(const SoftCtx& x, const AttnParams& p, int4 iv,
+                                             int4 si, uint32_t& n, uint32_t& itl) {
+  using C = DCfg<D>;
+  const unsigned full = 0xffffffffu;
+  auto bar = [&](int i) { return x.sBar + 8u * static_cast<uint32_t>(i); };
+  float* red = reinterpret_cast<float*>(x.smem + C::kOffRed);
+  float* red_max = red;                 // [2][4][16]
+  float* red_sum = red + 2 * 4 * kNQ;   // [4][16]
+  const int G = p.group;
+  const int hk = iv.y >> 16;
+  const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
+  const int part = iv.w;
+  const int q0 = si.x, ql = si.y, L = si.z;
+  const int rows = ql * G;
+  const float c = p.scale_log2;
+  const int t = x.t, lane = x.lane, sw = x.sw;
+  int lim[NR];
+  float m[NR], lp[NR];
+#pragma unroll
+  for (int j = 0; j < NR; ++j) {
+    const int tok = j / G;
+    lim[j] = j < rows ? (p.causal ? min(L, L - ql + tok + 1) : L) : 0;
+    m[j] = -INFINITY;
+    lp[j] = 0.f;
+  }
+  for (int kt = kt0; kt < kt1; ++kt, ++n) {
+    const uint32_t sb = n & 1u;
+    const bool first = kt == kt0;
+    if (!wait_warp(bar(kDSFull0 + sb), (n >> 1) & 1u, x.ctl)) return false;
+    tc_fence_after();
+    uint32_t sr[NR];
+    tmem_ld(x.tmem + x.lane_base + C::kColS + sb * kNQ, sr);
+    tmem_wait_ld();
+    reg_fence(sr);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kDSFree0 + sb));
+
+    const int key = kt * kDBN + t;
+    float s[NR];
+#pragma unroll
+    for (int j = 0; j < NR; ++j) s[j] = key < lim[j] ? __uint_as_float(sr[j]) : -INFINITY;
+    // tile max per query row: warp shuffles, then the four warps through shared memory
+    float* rb = red_max + sb * (4 * kNQ);
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+      float v = s[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(full, v, o));
+      if (lane == 0) rb[sw * kNQ + j] = v;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kDRedMax0 + sb));
+    if (!wait_warp(bar(kDRedMax0 + sb), (n >> 1) & 1u, x.ctl)) return false;
+    bool any_need = false;
+    float alpha[NR];
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+      alpha[j] = 1.f;
+      const float tm = fmaxf(fmaxf(rb[j], rb[kNQ + j]), fmaxf(rb[2 * kNQ + j], rb[3 * kNQ + j]));
+      const float tms = tm == -INFINITY ? -INFINITY : tm * c;
+      const float mn = fmaxf(m[j], tms);
+      if (first) {
+        m[j] = mn;
+      } else if (mn > m[j] + 8.0f) {
+        alpha[j] = ex2(m[j] - mn);
+        m[j] = mn;
+        any_need = true;
+      }
+    }
+    if (any_need) {
+      // rescale the O^T columns of the rows whose max grew, once the previous PV is done
+      const uint32_t pm = n - 1;
+      if (!wait_warp(bar(kDPVDone0 + (pm & 1u)), (pm >> 1) & 1u, x.ctl)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < C::kHalves; ++h) {
+        uint32_t o[NR];
+        tmem_ld(x.tmem + x.lane_base + C::kColO + h * kNQ, o);
+        tmem_wait_ld();
+        reg_fence(o);
+#pragma unroll
+        for (int j = 0; j < NR; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
+        tmem_st(x.tmem + x.lane_base + C::kColO + h * kNQ, o);
+      }
+      tmem_wait_st();
+#pragma unroll
+      for (int j = 0; j < NR; ++j) lp[j] *= alpha[j];
+    }
+    float pr[NR];
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+      const float mref = m[j] == -INFINITY ? 0.f : m[j];
+      pr[j] = s[j] == -INFINITY ? 0.f : ex2(fmaf(s[j], c, -mref));
+      lp[j] += pr[j];
+    }
+    // P buffer sb was last read by the PV of tile n - 2
+    if (n >= 2) {
+      const uint32_t pm = n - 2;
+      if (!wait_warp(bar(kDPVDone0 + (pm & 1u)), (pm >> 1) & 1u, x.ctl)) return false;
+    }
+    // P [16 rows][128 keys], K-major B operand: key block t/64, 128-byte rows
+    {
+      uint8_t* pb = x.smem + C::kOffP + sb * C::kPBytes + (t >> 6) * (kNQ * 128);
+      const int k = t & 63;
+#pragma unroll
+      for (int j = 0; j < NR; ++j) {
+        __nv_bfloat16 h = __float2bfloat16_rn(pr[j]);
+        *reinterpret_cast<__nv_bfloat16*>(pb + j * 128 + (((k >> 3) ^ (j & 7)) << 4) + (k & 7) * 2) = h;
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kDPFull0 + sb));
+  }
+  // ------------------------------------------------------------ epilogue
+#pragma unroll
+  for (int j = 0; j < NR; ++j) {
+    float v = lp[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(full, v, o);
+    if (lane == 0) red_sum[sw * kNQ + j] = v;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar(kDRedSum));
+  if (!wait_warp(bar(kDRedSum), itl & 1u, x.ctl)) return false;
+  ++itl;
+  float inv[NR];
+#pragma unroll
+  for (int j = 0; j < NR; ++j) {
+    const float l = (red_sum[j] + red_sum[kNQ + j]) + (red_sum[2 * kNQ + j] + red_sum[3 * kNQ + j]);
+    inv[j] = l > 0.f ? 1.f / l : 0.f;
+    if (part >= 0 && t == 0 && j < rows) p.part_ml[part + j] = make_float2(l > 0.f ? m[j] : -INFINITY, l);
+  }
+  const uint32_t pm = n - 1;
+  if (!wait_warp(bar(kDPVDone0 + (pm & 1u)), (pm >> 1) & 1u, x.ctl)) return false;
+  tc_fence_after();
+#pragma unroll
+  for (int h = 0; h < C::kHalves; ++h) {
+    uint32_t o[NR];
+    tmem_ld(x.tmem + x.lane_base + C::kColO + h * kNQ, o);
+    tmem_wait_ld();
+    reg_fence(o);
+    const int d = h * 128 + t;
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+      if (j >= rows) continue;
+      const float v = __uint_as_float(o[j]) * inv[j];
+      if (part < 0) {
+        const int tok = j / G, g = j - tok * G;
+        p.out[(static_cast<size_t>(q0 + tok) * p.n_heads_q + hk * G + g) * D + d] = __float2bfloat16_rn(v);
+      } else {
+        p.part_o[static_cast<size_t>(part + j) * D + d] = v;
+      }
+    }
+  }
+  tc_fence_before();
+  return true;
+}
+
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -89,8 +263,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       mbar_init(bar(kDSFull0 + s), 1);
       mbar_init(bar(kDSFree0 + s), 4);
     }
-    mbar_init(bar(kDPFull), 4);
-    mbar_init(bar(kDPVDone), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kDPFull0 + s), 4);
+      mbar_init(bar(kDPVDone0 + s), 1);
+    }
     mbar_init(bar(kDDrain), 1);
     mbar_init(bar(kDRedMax0), 4);
     mbar_init(bar(kDRedMax1), 4);
@@ -206,13 +382,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       bool ok = true;
       auto issue_pv = [&](uint32_t m, bool first) -> bool {
         const uint32_t fv = 2 * m + 1, s = fv % R, ph = (fv / R) & 1u;
-        if (!wait_one(bar(kDPFull), m & 1u, ctl)) return false;
+        if (!wait_one(bar(kDPFull0 + (m & 1u)), (m >> 1) & 1u, ctl)) return false;
         if (!wait_one(ring_ready(s), ph, ctl)) return false;
         tc_fence_after();
         const uint32_t v0 = sRing + s * C::kStage;
 #pragma unroll
         for (int kk = 0; kk < kDBN / 16; ++kk) {
-          const uint64_t b = sw128_desc(sP + (kk >> 2) * (kNQ * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = sw128_desc(sP + (m & 1u) * C::kPBytes + (kk >> 2) * (kNQ * 128) + (kk & 3) * 32,
+                                        16, 1024);
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h) {
             const uint64_t a = sw128_desc(v0 + (2 * h) * (kDBN * 128) + kk * (16 * 128), kDBN * 128, 1024);
@@ -220,7 +397,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           }
         }
         umma_commit(ring_empty(s));
-        umma_commit(bar(kDPVDone));
+        umma_commit(bar(kDPVDone0 + (m & 1u)));
         return true;
       };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
@@ -283,172 +460,27 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax: one key per thread
-    const int sw = warp - 4;
-    const int t = threadIdx.x - 128;  // key within the tile, and d within an O^T slice
-    const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
-    const float c = p.scale_log2;
-    float* red_max = red;              // [2][4][16]
-    float* red_sum = red + 2 * 4 * kNQ; // [4][16]
+    SoftCtx x;
+    x.smem = smem;
+    x.sBar = sBar;
+    x.sw = warp - 4;
+    x.t = threadIdx.x - 128;
+    x.lane = lane;
+    x.lane_base = static_cast<uint32_t>(x.sw * 32) << 16;
+    x.tmem = tmem;
+    x.ctl = ctl;
     uint32_t n = 0, itl = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
       const int4 iv = p.items[idx];
-      const int b = iv.x, hk = iv.y >> 16;
-      const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
-      const int part = iv.w;
-      const int4 si = p.seq_info[b];
-      const int q0 = si.x, ql = si.y, L = si.z;
-      const int rows = ql * G;  // <= 16
-      int lim[kNQ];
-      float m[kNQ], lp[kNQ];
-#pragma unroll
-      for (int j = 0; j < kNQ; ++j) {
-        const int tok = j / G;
-        lim[j] = j < rows ? (p.causal ? min(L, L - ql + tok + 1) : L) : 0;
-        m[j] = -INFINITY;
-        lp[j] = 0.f;
-      }
-      for (int kt = kt0; kt < kt1; ++kt, ++n) {
-        const uint32_t sb = n & 1u;
-        const bool first = kt == kt0;
-        if (!(ok = wait_warp(bar(kDSFull0 + sb), (n >> 1) & 1u, ctl))) break;
-        tc_fence_after();
-        uint32_t sr[kNQ];
-        tmem_ld16(tmem + lane_base + C::kColS + sb * kNQ, sr);
-        tmem_wait_ld();
-        reg_fence(sr);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kDSFree0 + sb));
-
-        const int key = kt * kDBN + t;
-        float s[kNQ];
-#pragma unroll
-        for (int j = 0; j < kNQ; ++j) s[j] = key < lim[j] ? __uint_as_float(sr[j]) : -INFINITY;
-        // tile max per query row: warp shuffles, then the four warps through shared memory
-        float* rb = red_max + sb * (4 * kNQ);
-#pragma unroll
-        for (int j = 0; j < kNQ; ++j) {
-          if (j < rows) {
-            float v = s[j];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(full, v, o));
-            if (lane == 0) rb[sw * kNQ + j] = v;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kDRedMax0 + sb));
-        if (!(ok = wait_warp(bar(kDRedMax0 + sb), (n >> 1) & 1u, ctl))) break;
-        bool any_need = false;
-        float alpha[kNQ];
-#pragma unroll
-        for (int j = 0; j < kNQ; ++j) {
-          alpha[j] = 1.f;
-          if (j < rows) {
-            const float tm = fmaxf(fmaxf(rb[j], rb[kNQ + j]), fmaxf(rb[2 * kNQ + j], rb[3 * kNQ + j]));
-            const float tms = tm == -INFINITY ? -INFINITY : tm * c;
-            const float mn = fmaxf(m[j], tms);
-            if (first) {
-              m[j] = mn;
-            } else if (mn > m[j] + 8.0f) {
-              alpha[j] = ex2(m[j] - mn);
-              m[j] = mn;
-              any_need = true;
-            }
-          }
-        }
-        bool pv_waited = false;
-        if (any_need) {
-          // O^T columns of the rows whose max grew: rescale once the previous PV is done
-          if (!(ok = wait_warp(bar(kDPVDone), (n - 1) & 1u, ctl))) break;
-          pv_waited = true;
-          tc_fence_after();
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) {
-            uint32_t o[kNQ];
-            tmem_ld16(tmem + lane_base + C::kColO + h * kNQ, o);
-            tmem_wait_ld();
-            reg_fence(o);
-#pragma unroll
-            for (int j = 0; j < kNQ; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j]);
-            tmem_st16(tmem + lane_base + C::kColO + h * kNQ, o);
-            tmem_wait_st();
-          }
-#pragma unroll
-          for (int j = 0; j < kNQ; ++j) lp[j] *= alpha[j];
-        }
-        float pr[kNQ];
-#pragma unroll
-        for (int j = 0; j < kNQ; ++j) {
-          const float mref = m[j] == -INFINITY ? 0.f : m[j];
-          pr[j] = s[j] == -INFINITY ? 0.f : ex2(fmaf(s[j], c, -mref));
-          lp[j] += pr[j];
-        }
-        if (!first && !pv_waited) {
-          if (!(ok = wait_warp(bar(kDPVDone), (n - 1) & 1u, ctl))) break;
-        }
-        // P [16 rows][128 keys], K-major for the B operand: key block t/64, 128-byte rows
-        {
-          uint8_t* pb = smem + C::kOffP + (t >> 6) * (kNQ * 128);
-          const int k = t & 63;
-#pragma unroll
-          for (int j = 0; j < kNQ; ++j) {
-            __nv_bfloat16 h = __float2bfloat16_rn(pr[j]);
-            *reinterpret_cast<__nv_bfloat16*>(pb + j * 128 + ((((k >> 3) ^ (j & 7))) << 4) + (k & 7) * 2) = h;
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kDPFull));
-      }
-      if (!ok) break;
-      // ---------------------------------------------------------- epilogue
-#pragma unroll
-      for (int j = 0; j < kNQ; ++j) {
-        if (j < rows) {
-          float v = lp[j];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(full, v, o);
-          if (lane == 0) red_sum[sw * kNQ + j] = v;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDRedSum));
-      if (!(ok = wait_warp(bar(kDRedSum), itl & 1u, ctl))) break;
-      ++itl;
-      float l[kNQ];
-#pragma unroll
-      for (int j = 0; j < kNQ; ++j)
-        l[j] = j < rows ? (red_sum[j] + red_sum[kNQ + j]) + (red_sum[2 * kNQ + j] + red_sum[3 * kNQ + j]) : 0.f;
-      if (!(ok = wait_warp(bar(kDPVDone), (n - 1) & 1u, ctl))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < C::kHalves; ++h) {
-        uint32_t o[kNQ];
-        tmem_ld16(tmem + lane_base + C::kColO + h * kNQ, o);
-        tmem_wait_ld();
-        reg_fence(o);
-        const int d = h * 128 + t;
-#pragma unroll
-        for (int j = 0; j < kNQ; ++j) {
-          if (j >= rows) continue;
-          const float inv = l[j] > 0.f ? 1.f / l[j] : 0.f;
-          const float v = __uint_as_float(o[j]) * inv;
-          if (part < 0) {
-            const int tok = j / G, g = j - tok * G;
-            p.out[(static_cast<size_t>(q0 + tok) * p.n_heads_q + hk * G + g) * D + d] = __float2bfloat16_rn(v);
-          } else {
-            p.part_o[static_cast<size_t>(part + j) * D + d] = v;
-          }
-        }
-      }
-      if (part >= 0 && t == 0) {
-#pragma unroll
-        for (int j = 0; j < kNQ; ++j)
-          if (j < rows) p.part_ml[part + j] = make_float2(l[j] > 0.f ? m[j] : -INFINITY, l[j]);
-      }
-      tc_fence_before();
+      const int4 si = p.seq_info[iv.x];
+      const int rows = si.y * G;
+      if (rows <= 4)
+        ok = softmax_item<D, 4>(x, p, iv, si, n, itl);
+      else if (rows <= 8)
+        ok = softmax_item<D, 8>(x, p, iv, si, n, itl);
+      else
+        ok = softmax_item<D, 16>(x, p, iv, si, n, itl);
     }
   }
 
