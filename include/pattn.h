@@ -93,6 +93,41 @@ pattn_status pattn_forward(void *out, const void *q, const void *kv_pool,
                            int page_size, int num_pages, float scale, int causal,
                            pattn_stream_t stream);
 
+/* Bytes of the fixed device scratch behind pattn_forward_noalloc. */
+#define PATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * pattn_forward_noalloc -- pattn_forward without any allocation. The pages
+ * have no counterpart of this entry point; it exists for callers that must
+ * not allocate device memory: a serving process whose caching allocator has
+ * already reserved nearly all of the GPU (a fresh cudaMalloc would fail or
+ * force the cache to be emptied), a decode loop that cannot afford the device
+ * synchronisation cudaMalloc/cudaFree imply, or a host application that owns
+ * every device buffer itself.
+ *
+ * Same arguments, layouts and results as pattn_forward. Instead of the
+ * library workspace it uses one fixed device array of
+ * PATTN_NOALLOC_SCRATCH_BYTES, compiled into the library: every GPU that
+ * loads the library holds it until the process exits. Batches whose
+ * workspace (pattn_workspace_size) exceeds it are rejected with
+ * PATTN_ERR_NO_MEMORY before anything is launched. Nothing here calls
+ * cudaMalloc, cudaFree or any allocating routine.
+ *
+ * The first call on a device sets the scratch up (looks up its device
+ * address and clears its header, a synchronous step), so make that first call
+ * before any stream capture. All calls share the one array and it keeps the
+ * previous call's contents: calls that overlap on the GPU (other streams,
+ * other host threads) race on it and must be serialised by the caller.
+ * Device-side data errors are recorded in the scratch's own error word, which
+ * pattn_get_device_status does not read; rejected rows are still zero-filled.
+ */
+pattn_status pattn_forward_noalloc(void *out, const void *q, const void *kv_pool,
+                                   const int32_t *block_table, const int32_t *seq_lens,
+                                   const int32_t *cu_q, int num_seqs, int total_q, int max_q,
+                                   int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
+                                   int page_size, int num_pages, float scale, int causal,
+                                   pattn_stream_t stream);
+
 /*
  * pattn_forward_host -- the same operation on HOST buffers, end to end: copies
  * the inputs to device buffers the library keeps (grow-only, per device),

@@ -14,7 +14,7 @@ from typing import Optional, Tuple
 
 from . import _lib
 
-__all__ = ["PattnError", "forward", "forward_host", "workspace_size", "set_workspace",
+__all__ = ["PattnError", "forward", "forward_noalloc", "forward_host", "workspace_size", "set_workspace",
            "device_status", "status_string", "profile_enable", "profile_read", "STATUS",
            "library_path"]
 
@@ -91,6 +91,28 @@ def forward(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv:
         pages, float(scale), int(bool(causal)), _stream_handle(stream))
     if check:
         _check(rc, "pattn_forward")
+    return rc
+
+
+def forward_noalloc(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,
+                    n_heads_kv: int, scale: float, causal: bool, num_pages: Optional[int] = None,
+                    stream=None, check: bool = True) -> int:
+    """As :func:`forward`, through ``pattn_forward_noalloc``: no device allocation, the
+    library's fixed scratch instead of its workspace (for callers that must not
+    allocate; calls sharing the scratch must not overlap on the GPU)."""
+    import torch
+    for name, t, dt in (("out", out, torch.bfloat16), ("q", q, torch.bfloat16),
+                        ("kv_pool", kv_pool, torch.bfloat16), ("seq_lens", seq_lens, torch.int32),
+                        ("cu_q", cu_q, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name}: expected a contiguous CUDA {dt} tensor")
+    total_q, hq, d, page, pages = _shape_args(q, kv_pool, block_table, n_heads_kv, num_pages)
+    rc = _lib.load().pattn_forward_noalloc(
+        _ptr(out), _ptr(q), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens), _ptr(cu_q),
+        int(seq_lens.numel()), total_q, int(max_q), int(max_kv), hq, int(n_heads_kv), d, page,
+        pages, float(scale), int(bool(causal)), _stream_handle(stream))
+    if check:
+        _check(rc, "pattn_forward_noalloc")
     return rc
 
 

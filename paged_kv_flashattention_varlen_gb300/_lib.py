@@ -18,6 +18,8 @@ _dp = ctypes.POINTER(ctypes.c_double)
 _ip = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "pattn_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "pattn_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
+                                   _vp]),
     "pattn_forward_host": (_i, [_vp, _vp, _vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                 _f, _i, _vp]),
     "pattn_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),

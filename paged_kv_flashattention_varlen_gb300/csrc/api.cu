@@ -88,15 +88,25 @@ struct WsLayout {
   int max_items, max_units, max_part_rows;
 };
 
-WsLayout ws_layout(int num_seqs, int total_q, int max_q, int hq, int hkv, int d) {
+// Workspace layout for these bounds. With max_kv >= 0 the split bound also
+// uses the planner's per-unit limit (at most min(kMaxSplits, ceil(max_kv/64))
+// splits per unit) and `target` the planner's own item target; without it,
+// the bound assumes kTargetItemsCap items and no length limit.
+WsLayout ws_layout(int num_seqs, int total_q, int max_q, int hq, int hkv, int d, int max_kv = -1,
+                   int target = kTargetItemsCap) {
   WsLayout w{};
   const int g = hq / hkv;
   const int T = kBM / g;
   const long long units = static_cast<long long>(num_seqs) * hkv;
   const long long qtiles = cdiv(total_q, T) + static_cast<long long>(num_seqs);
-  const long long items = static_cast<long long>(hkv) * qtiles + kTargetItemsCap + units + 64;
+  const long long items = static_cast<long long>(hkv) * qtiles + target + units + 64;
   const long long rows_cap = std::min<long long>(kBM, static_cast<long long>(max_q) * g);
-  const long long part_rows = (kTargetItemsCap + units) * std::max<long long>(rows_cap, 1);
+  long long splits = target + units;
+  if (max_kv >= 0) {
+    const long long per_unit = std::min<long long>(kMaxSplits, std::max(1, cdiv(max_kv, kPage)));
+    splits = std::min(splits, units * per_unit);
+  }
+  const long long part_rows = splits * std::max<long long>(rows_cap, 1);
   w.max_items = static_cast<int>(std::min<long long>(items, 0x7fffffffLL));
   w.max_units = static_cast<int>(std::min<long long>(units, 0x7fffffffLL));
   w.max_part_rows = static_cast<int>(std::min<long long>(part_rows, 0x7fffffffLL));
@@ -203,18 +213,14 @@ ProfileRec take_events(DeviceState& st) {
   return r;
 }
 
-pattn_status forward_locked(void* out, const void* q, const void* kv, const int32_t* bt,
-                            const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
-                            int total_q, int max_q, int max_kv, int hq, int hkv, int d, int page,
-                            int num_pages, float scale, int causal, cudaStream_t stream,
-                            const Shape& sh) {
-  DeviceState* stp = nullptr;
-  pattn_status s = device_state(&stp);
-  if (s != PATTN_OK) return s;
-  DeviceState& st = *stp;
-  const WsLayout L = ws_layout(num_seqs, total_q, max_q, hq, hkv, d);
-  if ((s = ensure_workspace(st, L.total)) != PATTN_OK) return s;
-  uint8_t* wsb = static_cast<uint8_t*>(st.ws);
+// Encodes the tensor maps and launches plan -> decode -> prefill -> combine with
+// the workspace at `wsb` (laid out as L). Caller holds g_mu.
+pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* out, const void* q,
+                        const void* kv, const int32_t* bt, const int32_t* seq_lens,
+                        const int32_t* cu_q, int num_seqs, int total_q, int max_q, int max_kv,
+                        int hq, int hkv, int d, int num_pages, float scale, int causal,
+                        cudaStream_t stream, const Shape& sh) {
+  pattn_status s = PATTN_OK;
 
   Workspace ws{};
   ws.hdr = reinterpret_cast<int*>(wsb + L.hdr);
@@ -360,6 +366,44 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
   return PATTN_OK;
 }
 
+pattn_status forward_locked(void* out, const void* q, const void* kv, const int32_t* bt,
+                            const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
+                            int total_q, int max_q, int max_kv, int hq, int hkv, int d, int page,
+                            int num_pages, float scale, int causal, cudaStream_t stream,
+                            const Shape& sh) {
+  (void)page;
+  DeviceState* stp = nullptr;
+  pattn_status s = device_state(&stp);
+  if (s != PATTN_OK) return s;
+  DeviceState& st = *stp;
+  const WsLayout L = ws_layout(num_seqs, total_q, max_q, hq, hkv, d);
+  if ((s = ensure_workspace(st, L.total)) != PATTN_OK) return s;
+  return launch_all(st, static_cast<uint8_t*>(st.ws), L, out, q, kv, bt, seq_lens, cu_q, num_seqs,
+                    total_q, max_q, max_kv, hq, hkv, d, num_pages, scale, causal, stream, sh);
+}
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for pattn_forward_noalloc: one file-scope device array that
+// every GPU loading the library holds until the process exits. Host code only
+// sees a stand-in symbol; the device address comes from cudaGetSymbolAddress,
+// taken once per device at set-up with that device current.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[PATTN_NOALLOC_SCRATCH_BYTES];
+uint8_t* g_noalloc_ptr[kMaxDevices] = {};
+
+// Caller holds g_mu; `dev` is the current device.
+pattn_status noalloc_scratch(int dev, uint8_t** out) {
+  if (dev < 0 || dev >= kMaxDevices) return PATTN_ERR_UNSUPPORTED;
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return PATTN_ERR_CUDA;
+    // the device error word and counters of the header start at zero
+    if (cudaMemset(ptr, 0, kHdrWords * sizeof(int)) != cudaSuccess) return PATTN_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<uint8_t*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return PATTN_OK;
+}
+
 }  // namespace
 }  // namespace pattn
 
@@ -382,6 +426,34 @@ pattn_status pattn_forward(void* out, const void* q, const void* kv_pool,
   return forward_locked(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
                         max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, scale,
                         causal, reinterpret_cast<cudaStream_t>(stream), sh);
+}
+
+pattn_status pattn_forward_noalloc(void* out, const void* q, const void* kv_pool,
+                                   const int32_t* block_table, const int32_t* seq_lens,
+                                   const int32_t* cu_q, int num_seqs, int total_q, int max_q,
+                                   int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
+                                   int page_size, int num_pages, float scale, int causal,
+                                   pattn_stream_t stream) {
+  Shape sh{};
+  pattn_status s = check_args(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                              max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size,
+                              num_pages, scale, causal, &sh);
+  if (s != PATTN_OK) return s;
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* stp = nullptr;
+  if ((s = device_state(&stp)) != PATTN_OK) return s;
+  const int target = std::min(kTargetItemsPerSm * stp->sms, kTargetItemsCap);
+  const WsLayout L =
+      ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim, max_kv, target);
+  if (L.total > static_cast<size_t>(PATTN_NOALLOC_SCRATCH_BYTES)) return PATTN_ERR_NO_MEMORY;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PATTN_ERR_CUDA;
+  uint8_t* scratch = nullptr;
+  if ((s = noalloc_scratch(dev, &scratch)) != PATTN_OK) return s;
+  return launch_all(*stp, scratch, L, out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs,
+                    total_q, max_q, max_kv, n_heads_q, n_heads_kv, head_dim, num_pages, scale,
+                    causal, reinterpret_cast<cudaStream_t>(stream), sh);
 }
 
 pattn_status pattn_forward_host(void* out, const void* q, const void* kv_pool,
