@@ -16,8 +16,10 @@
 //     N = D, K = BN) with V read MN-major from shared memory; commits signal
 //     mbarriers (the SM100MHA2Q "UMMA0" / "UMMA1" accumulators of the
 //     FlashAttention-4 doc);
-//   * the softmax warpgroup owns one query row per thread: it reads its S row
-//     from TMEM, masks keys past the end or (causal) past its position only on
+//   * two softmax warpgroups share the 128 query rows, one row per thread in
+//     each, and split the keys of every tile between them (exchanging the
+//     partial row max once per tile): each reads its half of the S row from
+//     TMEM, masks keys past the end or (causal) past its position only on
 //     tiles that need it, keeps the running max m and sum l in log2 units
 //     (exp2 with the scale folded into log2 e, as the manifest's pack scalar
 //     does), rescales the O row in TMEM only when the max grew by more than
@@ -44,7 +46,9 @@ struct Cfg {
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVStage;
   static constexpr int kOffP = kOffV + kStages * kKVStage;
-  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kOffX = kOffP + kPBytes;             // row max / sum exchange
+  static constexpr int kXBytes = (2 * 2 + 2) * kBM * 4;
+  static constexpr int kOffBar = kOffX + kXBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kOffMisc = kOffBar + kBarBytes;
   static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
@@ -62,8 +66,10 @@ struct Cfg {
 enum Bar {
   kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVReady0,
   kVReady1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull, kPVDone, kDrain,
-  kNumBars
+  kXMax0, kXMax1, kXSum, kNumBars
 };
+constexpr int kAttnThreads = 384;  // 4 role warps + 2 softmax warpgroups
+constexpr int kSoftmaxWarps = 8;
 
 struct Item {
   int b, hk, qt, kt0, kt1, part;
@@ -81,7 +87,7 @@ __device__ __forceinline__ Item decode_item(int4 v) {
 }
 
 template <int D, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
             const AttnParams p) {
   using C = Cfg<D, BN>;
@@ -114,11 +120,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       mbar_init(bar(kVReady0 + s), 1);
       mbar_init(bar(kVEmpty0 + s), 1);
       mbar_init(bar(kSFull0 + s), 1);
-      mbar_init(bar(kSFree0 + s), 4);
+      mbar_init(bar(kSFree0 + s), kSoftmaxWarps);
+      mbar_init(bar(kXMax0 + s), kSoftmaxWarps);
     }
-    mbar_init(bar(kPFull), 4);
+    mbar_init(bar(kPFull), kSoftmaxWarps);
     mbar_init(bar(kPVDone), 1);
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kXSum), kSoftmaxWarps);
     mbar_init_fence();
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_kv);
@@ -292,16 +300,25 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       }
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax warpgroup
-    const int sw = warp - 4;              // TMEM lane quarter
-    const int r = threadIdx.x - 128;      // query row of this thread
+    // ------------------------------------------------------------ softmax: two warpgroups
+    // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) takes keys [h*KH, h*KH + KH)
+    // of every tile and O columns [h*DH, h*DH + DH) for the same 128 rows; the two
+    // threads of a row exchange their partial max once per tile and their partial
+    // sums once per item.
+    constexpr int KH = BN / 2;
+    constexpr int DH = D / 2;
+    const int h = (warp - 4) >> 2;
+    const int sw = (warp - 4) & 3;        // TMEM lane quarter
+    const int r = sw * 32 + lane;         // query row of this thread
     const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
+    float* xmax = reinterpret_cast<float*>(smem + C::kOffX);  // [2 parity][2 wg][128]
+    float* xsum = xmax + 2 * 2 * kBM;                           // [2 wg][128]
     const int t_local = r / G;
     const int g = r - t_local * G;
     const float c = p.scale_log2;
-    uint32_t n = 0;
+    uint32_t n = 0, itl = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
       const Item it = decode_item(p.items[idx]);
       const int4 si = p.seq_info[it.b];
       const int q0 = si.x, ql = si.y, L = si.z;
@@ -316,37 +333,52 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         const bool first = kt == it.kt0;
         if (!(ok = wait_warp(bar(kSFull0 + s), (n >> 1) & 1u, ctl))) break;
         tc_fence_after();
-        uint32_t sr[BN / 32][32];
+        uint32_t sr[KH / 32][32];
         if (warp_live) {
 #pragma unroll
-          for (int j = 0; j < BN / 32; ++j)
-            tmem_ld32(tmem + lane_base + C::kColS + s * BN + j * 32, sr[j]);
+          for (int j = 0; j < KH / 32; ++j)
+            tmem_ld32(tmem + lane_base + C::kColS + s * BN + h * KH + j * 32, sr[j]);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < BN / 32; ++j) reg_fence(sr[j]);
+          for (int j = 0; j < KH / 32; ++j) reg_fence(sr[j]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kSFree0 + s));
 
-        bool pv_waited = false;
-        uint32_t pk[BN / 2];
+        const int key0 = kt * BN + h * KH;
+        const bool full_tile = key0 + KH <= lim;
+        float mx = -INFINITY;
         if (warp_live) {
-          const int key0 = kt * BN;
-          const bool full_tile = key0 + BN <= lim;
-          float mx = -INFINITY;
+          float acc[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] = -INFINITY;
           if (full_tile) {
 #pragma unroll
-            for (int j = 0; j < BN / 32; ++j)
+            for (int j = 0; j < KH / 32; ++j)
 #pragma unroll
-              for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[j][i]));
+              for (int i = 0; i < 32; ++i) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 32; ++j)
+            for (int j = 0; j < KH / 32; ++j)
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                if (key0 + j * 32 + i < lim) mx = fmaxf(mx, __uint_as_float(sr[j][i]));
+                if (key0 + j * 32 + i < lim) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
           }
+          mx = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
+                     fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
+        }
+        // exchange the partial row max with the other warpgroup
+        float* xb = xmax + s * (2 * kBM);
+        xb[h * kBM + r] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kXMax0 + s));
+        if (!(ok = wait_warp(bar(kXMax0 + s), (n >> 1) & 1u, ctl))) break;
+        mx = fmaxf(mx, xb[(1 - h) * kBM + r]);
+
+        bool pv_waited = false;
+        uint32_t pk[KH / 2];
+        if (warp_live) {
           const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
           const float m_new = fmaxf(m_used, mx_s);
           if (first) {
@@ -354,7 +386,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           } else {
             const bool need = m_new > m_used + 8.0f;
             if (__any_sync(0xffffffffu, need)) {
-              // O holds the previous tiles; rescale it once their PV is done.
+              // O holds the previous tiles; rescale this warpgroup's half once their PV is done.
               if (!(ok = wait_warp(bar(kPVDone), (n - 1) & 1u, ctl))) break;
               pv_waited = true;
               tc_fence_after();
@@ -364,22 +396,22 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
                 m_used = m_new;
               }
 #pragma unroll 1
-              for (int j = 0; j < D / 32; ++j) {
+              for (int j = 0; j < DH / 32; ++j) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_base + C::kColO + j * 32, o);
+                tmem_ld32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
                 tmem_wait_ld();
                 reg_fence(o);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st32(tmem + lane_base + C::kColO + j * 32, o);
+                tmem_st32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
               }
               tmem_wait_st();
             }
           }
           const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-          float sum = 0.f;
+          float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < BN / 32; ++j) {
+          for (int j = 0; j < KH / 32; ++j) {
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
               const int key = key0 + j * 32 + i;
@@ -389,28 +421,27 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
                 p0 = key < lim ? p0 : 0.f;
                 p1 = key + 1 < lim ? p1 : 0.f;
               }
-              sum += p0 + p1;
-              __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-              pk[(j * 32 + i) >> 1] = *reinterpret_cast<uint32_t*>(&h);
+              sum[(i >> 1) & 3] += p0 + p1;
+              __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+              pk[(j * 32 + i) >> 1] = *reinterpret_cast<uint32_t*>(&hh);
             }
           }
-          l += sum;
+          l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
         }
         if (!first && !pv_waited) {
           // P shared memory is still read by the previous tile's PV MMA.
           if (!(ok = wait_warp(bar(kPVDone), (n - 1) & 1u, ctl))) break;
         }
         if (warp_live) {
-          // row r of P, key blocks of 64 (128-byte rows), 16-byte chunks XOR-swizzled
+          // row r of P: this warpgroup's KH keys as 16-byte chunks, XOR-swizzled in
+          // 128-byte rows of 64-key blocks
 #pragma unroll
-          for (int kb = 0; kb < BN / 64; ++kb) {
-            uint8_t* rowp = smem + C::kOffP + kb * (kBM * 128) + r * 128;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-              const int w0 = kb * 32 + ch * 4;
-              *reinterpret_cast<uint4*>(rowp + ((ch ^ (r & 7)) << 4)) =
-                  make_uint4(pk[w0], pk[w0 + 1], pk[w0 + 2], pk[w0 + 3]);
-            }
+          for (int ch = 0; ch < KH / 8; ++ch) {
+            const int kg = h * KH + ch * 8;  // first key of the chunk within the tile
+            uint8_t* rowp = smem + C::kOffP + (kg >> 6) * (kBM * 128) + r * 128;
+            const int cc = (kg & 63) >> 3;
+            *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) =
+                make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
           }
           fence_proxy_async_smem();
         }
@@ -420,21 +451,27 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
+      xsum[h * kBM + r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kXSum));
+      if (!(ok = wait_warp(bar(kXSum), itl & 1u, ctl))) break;
+      const float l_all = l + xsum[(1 - h) * kBM + r];
       if (!(ok = wait_warp(bar(kPVDone), (n - 1) & 1u, ctl))) break;
       tc_fence_after();
       if (warp_live) {
-        const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-        const int h = it.hk * G + g;
+        const float inv_l = l_all > 0.f ? 1.0f / l_all : 0.f;
+        const int hq = it.hk * G + g;
 #pragma unroll 1
-        for (int j = 0; j < D / 32; ++j) {
+        for (int j = 0; j < DH / 32; ++j) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_base + C::kColO + j * 32, o);
+          tmem_ld32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
           tmem_wait_ld();
           reg_fence(o);
           if (!valid) continue;
+          const int col = h * DH + j * 32;
           if (it.part < 0) {
             uint4* dst = reinterpret_cast<uint4*>(
-                p.out + (static_cast<size_t>(q0 + tok) * p.n_heads_q + h) * D + j * 32);
+                p.out + (static_cast<size_t>(q0 + tok) * p.n_heads_q + hq) * D + col);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint32_t w[4];
@@ -448,7 +485,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             }
           } else {
             float4* dst = reinterpret_cast<float4*>(
-                p.part_o + static_cast<size_t>(it.part + r) * D + j * 32);
+                p.part_o + static_cast<size_t>(it.part + r) * D + col);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               dst[v] = make_float4(__uint_as_float(o[v * 4]) * inv_l, __uint_as_float(o[v * 4 + 1]) * inv_l,
@@ -456,7 +493,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
                                    __uint_as_float(o[v * 4 + 3]) * inv_l);
           }
         }
-        if (valid && it.part >= 0) p.part_ml[it.part + r] = make_float2(l > 0.f ? m_used : -INFINITY, l);
+        if (valid && it.part >= 0 && h == 0)
+          p.part_ml[it.part + r] = make_float2(l_all > 0.f ? m_used : -INFINITY, l_all);
       }
       tc_fence_before();
     }
@@ -489,9 +527,9 @@ cudaError_t attention_set_attributes() {
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                              int head_dim, int grid, cudaStream_t s) {
   if (head_dim == 128)
-    attn_kernel<128, 128><<<grid, kThreads, Cfg<128, 128>::kSmem, s>>>(tq, tkv, p);
+    attn_kernel<128, 128><<<grid, kAttnThreads, Cfg<128, 128>::kSmem, s>>>(tq, tkv, p);
   else
-    attn_kernel<256, 64><<<grid, kThreads, Cfg<256, 64>::kSmem, s>>>(tq, tkv, p);
+    attn_kernel<256, 64><<<grid, kAttnThreads, Cfg<256, 64>::kSmem, s>>>(tq, tkv, p);
   return cudaGetLastError();
 }
 
