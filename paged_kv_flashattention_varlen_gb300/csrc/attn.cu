@@ -13,7 +13,8 @@
 //     maps), each page read once per KV head for all G query heads;
 //   * the MMA thread issues S = Q K^T (tcgen05.mma kind::f16, M = 128,
 //     N = BN, K = D) into one of two TMEM S buffers, then O += P V (M = 128,
-//     N = D, K = BN) with V read MN-major from shared memory; commits signal
+//     N = D, K = BN) with P from TMEM and V read MN-major from shared memory;
+//     commits signal
 //     mbarriers (the SM100MHA2Q "UMMA0" / "UMMA1" accumulators of the
 //     FlashAttention-4 doc);
 //   * two softmax warpgroups share the 128 query rows, one row per thread in
@@ -23,8 +24,8 @@
 //     tiles that need it, keeps the running max m and sum l in log2 units
 //     (exp2 with the scale folded into log2 e, as the manifest's pack scalar
 //     does), rescales the O row in TMEM only when the max grew by more than
-//     2^8 (exact: O and l share the stale max), and writes P as bf16 into
-//     128-byte-swizzled shared memory for the PV MMA;
+//     2^8 (exact: O and l share the stale max), and writes P as bf16 pairs
+//     into TMEM (two buffers), where the PV MMA reads its A operand;
 //   * the tail warp zeroes V rows past the sequence end in the last tile, so
 //     that NaN or garbage there cannot reach O through 0 * NaN.
 //
@@ -40,13 +41,11 @@ template <int D, int BN>
 struct Cfg {
   static constexpr int kQBytes = kBM * D * 2;
   static constexpr int kKVStage = BN * D * 2;
-  static constexpr int kPBytes = kBM * BN * 2;
   static constexpr int kStages = 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVStage;
-  static constexpr int kOffP = kOffV + kStages * kKVStage;
-  static constexpr int kOffX = kOffP + kPBytes;             // row max / sum exchange
+  static constexpr int kOffX = kOffV + kStages * kKVStage;  // row max / sum exchange
   static constexpr int kXBytes = (2 * 2 + 2) * kBM * 4;
   static constexpr int kOffBar = kOffX + kXBytes;
   static constexpr int kBarBytes = 256;
@@ -54,9 +53,13 @@ struct Cfg {
   static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
   static constexpr int kColO = 0;                     // TMEM columns [0, D)
   static constexpr int kColS = 256;                   // two S buffers of BN columns
+  static constexpr int kPCols = BN / 2;               // P as bf16 pairs: BN keys in BN/2 columns
+  static constexpr int kColP = D == 128 ? 128 : kColS + 2 * BN;  // two P buffers
   static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns per row
   static constexpr int kPagesPerTile = BN / kPage;
   static_assert(kColS + 2 * BN <= kTmemCols, "TMEM budget");
+  static_assert(kColP + 2 * kPCols <= kTmemCols && (kColP >= kColS + 2 * BN || kColP + 2 * kPCols <= kColS),
+                "P columns");
   static_assert(D <= kColS, "O columns");
   static_assert(BN % kPage == 0 && BN % 32 == 0, "tile");
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -65,8 +68,8 @@ struct Cfg {
 // mbarrier slots
 enum Bar {
   kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVReady0,
-  kVReady1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull, kPVDone, kDrain,
-  kXMax0, kXMax1, kXSum, kNumBars
+  kVReady1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1,
+  kPVDone0, kPVDone1, kDrain, kXMax0, kXMax1, kXSum, kNumBars
 };
 constexpr int kAttnThreads = 384;  // 4 role warps + 2 softmax warpgroups
 constexpr int kSoftmaxWarps = 8;
@@ -98,7 +101,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   const uint32_t sQ = s_base + C::kOffQ;
   const uint32_t sK = s_base + C::kOffK;
   const uint32_t sV = s_base + C::kOffV;
-  const uint32_t sP = s_base + C::kOffP;
   const uint32_t sBar = s_base + C::kOffBar;
   uint8_t* misc = smem + C::kOffMisc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
@@ -123,8 +125,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       mbar_init(bar(kSFree0 + s), kSoftmaxWarps);
       mbar_init(bar(kXMax0 + s), kSoftmaxWarps);
     }
-    mbar_init(bar(kPFull), kSoftmaxWarps);
-    mbar_init(bar(kPVDone), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kPFull0 + s), kSoftmaxWarps);
+      mbar_init(bar(kPVDone0 + s), 1);
+    }
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kXSum), kSoftmaxWarps);
     mbar_init_fence();
@@ -229,18 +233,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       uint32_t n = 0, itl = 0;
       bool ok = true;
       auto issue_pv = [&](uint32_t m, bool first) -> bool {
-        if (!wait_one(bar(kPFull), m & 1u, ctl)) return false;
+        const uint32_t pb = m & 1u;
+        if (!wait_one(bar(kPFull0 + pb), (m >> 1) & 1u, ctl)) return false;
         if (!wait_one(bar(kVReady0 + (m & 1u)), (m >> 1) & 1u, ctl)) return false;
         tc_fence_after();
         const uint32_t v0 = sV + (m & 1u) * C::kKVStage;
+        const uint32_t a0 = tmem + C::kColP + pb * C::kPCols;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a = sw128_desc(sP + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
           const uint64_t b = sw128_desc(v0 + kk * (16 * 128), BN * 128, 1024);
-          umma_f16(tmem + C::kColO, a, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+          umma_f16_tmem_a(tmem + C::kColO, a0 + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
         }
         umma_commit(bar(kVEmpty0 + (m & 1u)));
-        umma_commit(bar(kPVDone));
+        umma_commit(bar(kPVDone0 + pb));
         return true;
       };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
@@ -368,47 +373,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           mx = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
                      fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
         }
-        // exchange the partial row max with the other warpgroup
+        // exchange the partial row max with the other warpgroup; while it is in
+        // flight, compute P against the running max both warpgroups already share
         float* xb = xmax + s * (2 * kBM);
         xb[h * kBM + r] = mx;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kXMax0 + s));
-        if (!(ok = wait_warp(bar(kXMax0 + s), (n >> 1) & 1u, ctl))) break;
-        mx = fmaxf(mx, xb[(1 - h) * kBM + r]);
 
-        bool pv_waited = false;
         uint32_t pk[KH / 2];
-        if (warp_live) {
-          const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
-          const float m_new = fmaxf(m_used, mx_s);
-          if (first) {
-            m_used = m_new;
-          } else {
-            const bool need = m_new > m_used + 8.0f;
-            if (__any_sync(0xffffffffu, need)) {
-              // O holds the previous tiles; rescale this warpgroup's half once their PV is done.
-              if (!(ok = wait_warp(bar(kPVDone), (n - 1) & 1u, ctl))) break;
-              pv_waited = true;
-              tc_fence_after();
-              const float alpha = need ? ex2(m_used - m_new) : 1.0f;
-              if (need) {
-                l *= alpha;
-                m_used = m_new;
-              }
-#pragma unroll 1
-              for (int j = 0; j < DH / 32; ++j) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
-                tmem_wait_ld();
-                reg_fence(o);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
-              }
-              tmem_wait_st();
-            }
-          }
-          const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+        float l_tile = 0.f;
+        auto exps = [&](float m_ref) {
           float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int j = 0; j < KH / 32; ++j) {
@@ -426,28 +400,61 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
               pk[(j * 32 + i) >> 1] = *reinterpret_cast<uint32_t*>(&hh);
             }
           }
-          l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+          l_tile = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        };
+        const bool speculate = warp_live && !first && m_used != -INFINITY;
+        if (speculate) exps(m_used);
+        if (!(ok = wait_warp(bar(kXMax0 + s), (n >> 1) & 1u, ctl))) break;
+        mx = fmaxf(mx, xb[(1 - h) * kBM + r]);
+
+        if (warp_live) {
+          const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
+          const float m_new = fmaxf(m_used, mx_s);
+          bool redo = !speculate;
+          if (first) {
+            m_used = m_new;
+          } else {
+            const bool need = m_new > m_used + 8.0f;
+            if (__any_sync(0xffffffffu, need)) {
+              // O holds the previous tiles; rescale this warpgroup's half once their PV is done.
+              const uint32_t pm = n - 1;
+              if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+              tc_fence_after();
+              const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+              if (need) {
+                l *= alpha;
+                m_used = m_new;
+              }
+#pragma unroll 1
+              for (int j = 0; j < DH / 32; ++j) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
+                tmem_wait_ld();
+                reg_fence(o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
+              }
+              tmem_wait_st();
+              redo = true;  // the speculative P used the old max for some rows of this warp
+            }
+          }
+          if (redo) exps((m_used == -INFINITY) ? 0.f : m_used);
+          l += l_tile;
         }
-        if (!first && !pv_waited) {
-          // P shared memory is still read by the previous tile's PV MMA.
-          if (!(ok = wait_warp(bar(kPVDone), (n - 1) & 1u, ctl))) break;
+        // P buffer s was last read by the PV of tile n - 2
+        if (n >= 2) {
+          const uint32_t pm = n - 2;
+          if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
         }
         if (warp_live) {
-          // row r of P: this warpgroup's KH keys as 16-byte chunks, XOR-swizzled in
-          // 128-byte rows of 64-key blocks
-#pragma unroll
-          for (int ch = 0; ch < KH / 8; ++ch) {
-            const int kg = h * KH + ch * 8;  // first key of the chunk within the tile
-            uint8_t* rowp = smem + C::kOffP + (kg >> 6) * (kBM * 128) + r * 128;
-            const int cc = (kg & 63) >> 3;
-            *reinterpret_cast<uint4*>(rowp + ((cc ^ (r & 7)) << 4)) =
-                make_uint4(pk[ch * 4], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-          }
-          fence_proxy_async_smem();
+          // row r of P as bf16 pairs: this warpgroup's KH keys -> KH/2 TMEM columns
+          tmem_st_cols<KH / 2>(tmem + lane_base + C::kColP + s * C::kPCols + h * (KH / 2), pk);
+          tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kPFull));
+        if (lane == 0) mbar_arrive(bar(kPFull0 + s));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -456,7 +463,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       if (lane == 0) mbar_arrive(bar(kXSum));
       if (!(ok = wait_warp(bar(kXSum), itl & 1u, ctl))) break;
       const float l_all = l + xsum[(1 - h) * kBM + r];
-      if (!(ok = wait_warp(bar(kPVDone), (n - 1) & 1u, ctl))) break;
+      {
+        const uint32_t pm = n - 1;
+        if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+      }
       tc_fence_after();
       if (warp_live) {
         const float inv_l = l_all > 0.f ? 1.0f / l_all : 0.f;

@@ -159,6 +159,18 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A is M x 16 bf16 held as 8 TMEM
+// columns of packed pairs (lane = row, low half = even k), B from shared memory.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on an mbarrier once every UMMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
@@ -283,6 +295,17 @@ __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&v)[8]) 
                : "memory");
 }
 __device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t (&v)[16]) { tmem_st16(taddr, v); }
+
+// Store N in {16, 32} columns from a register array (32x32b shape).
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
+  if constexpr (N == 32) {
+    tmem_st32(taddr, v);
+  } else {
+    static_assert(N == 16, "16 or 32 columns");
+    tmem_st16(taddr, v);
+  }
+}
 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
