@@ -4,7 +4,7 @@
 // round robin over CTAs). A work item is (sequence, kv head, q tile, KV tile
 // range). For each item:
 //
-//   * the load warp TMA-loads the GQA-packed Q tile: the G query heads of one
+//   * two load warps (Q and K; V) TMA-load the GQA-packed Q tile: the G query heads of one
 //     KV head for T = 128 / G tokens, as 128 rows of 128-byte-swizzled shared
 //     memory (the GQA-packed Q tensor map of the trtllm-gen paged decode
 //     manifest: dims [D, group, kv head, token]); then, per KV tile of BN keys,
@@ -71,7 +71,7 @@ enum Bar {
   kVReady1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1,
   kPVDone0, kPVDone1, kDrain, kXMax0, kXMax1, kXSum, kNumBars
 };
-constexpr int kAttnThreads = 384;  // 4 role warps + 2 softmax warpgroups
+constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
 constexpr int kSoftmaxWarps = 8;
 
 struct Item {
@@ -148,81 +148,96 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   const int G = p.group;
   const int T = p.tokens_per_tile;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ load warp
-    if (lane == 0) {
-      uint32_t n = 0, itl = 0;
-      bool ok = true;
-      const uint64_t pol_q = l2_policy_evict_last();
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
-        const Item it = decode_item(p.items[idx]);
-        const int4 si = p.seq_info[it.b];
-        const int q0 = si.x, L = si.z, kv0 = si.w;
-        const bool decode_like = si.y <= T;
-        const uint64_t pol_kv = decode_like ? l2_policy_evict_first() : l2_policy_evict_last();
-        if (!(ok = wait_one(bar(kQEmpty), (itl & 1u) ^ 1u, ctl))) break;
-        mbar_arrive_expect_tx(bar(kQFull), static_cast<uint32_t>(C::kDBlocks * 128 * G * T));
-        for (int c = 0; c < C::kDBlocks; ++c)
-          tma_load_4d(sQ + c * (kBM * 128), &tmap_q, bar(kQFull), c * 64, 0, it.hk,
-                      q0 + it.qt * T, pol_q);
-        for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
-          const uint32_t s = n & 1u, ph = ((n >> 1) & 1u) ^ 1u;
-          // pages of this tile (the block table is read once for K and V)
-          int coord[C::kPagesPerTile];
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ load warps
+    // warp 0 loads Q and the K tiles, warp 3 the V tiles, so that a K load never
+    // queues behind the release of a V stage. Each warp reads the block table
+    // 32 tiles at a time across its lanes; lane 0 issues the copies.
+    const int kind = warp == 0 ? 0 : 1;
+    const int full = kind ? kVFull0 : kKFull0;
+    const int empty = kind ? kVEmpty0 : kKEmpty0;
+    const uint32_t ring = kind ? sV : sK;
+    const unsigned fullmask = 0xffffffffu;
+    uint32_t n = 0, itl = 0;
+    bool ok = true;
+    const uint64_t pol_q = l2_policy_evict_last();
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+      const Item it = decode_item(p.items[idx]);
+      const int4 si = p.seq_info[it.b];
+      const int q0 = si.x, L = si.z, kv0 = si.w;
+      const bool decode_like = si.y <= T;
+      const uint64_t pol_kv = decode_like ? l2_policy_evict_first() : l2_policy_evict_last();
+      if (kind == 0 && lane == 0) {
+        ok = wait_one(bar(kQEmpty), (itl & 1u) ^ 1u, ctl);
+        if (ok) {
+          mbar_arrive_expect_tx(bar(kQFull), static_cast<uint32_t>(C::kDBlocks * 128 * G * T));
+          for (int c = 0; c < C::kDBlocks; ++c)
+            tma_load_4d(sQ + c * (kBM * 128), &tmap_q, bar(kQFull), c * 64, 0, it.hk,
+                        q0 + it.qt * T, pol_q);
+        }
+      }
+      ok = __shfl_sync(fullmask, ok, 0);
+      const int ntiles = it.kt1 - it.kt0;
+      for (int t0 = 0; t0 < ntiles && ok; t0 += 32) {
+        // lane l looks up the pages of tile t0 + l
+        int pg[C::kPagesPerTile];
+#pragma unroll
+        for (int j = 0; j < C::kPagesPerTile; ++j) {
+          pg[j] = -1;
+          const int key = (it.kt0 + t0 + lane) * BN + j * kPage;
+          if (t0 + lane < ntiles && key < L) {
+            if (p.paged) {
+              const int page = p.block_table[static_cast<size_t>(it.b) * p.bt_stride + key / kPage];
+              if (page >= 0 && page < p.num_pages)
+                pg[j] = page;
+              else
+                atomicOr(p.err, kErrBadInput);
+            } else {
+              pg[j] = kv0 + key;
+            }
+          }
+        }
+        const int nb = min(32, ntiles - t0);
+        for (int i = 0; i < nb; ++i, ++n) {
+          int a[C::kPagesPerTile];
           int nload = 0;
 #pragma unroll
-          for (int pg = 0; pg < C::kPagesPerTile; ++pg) {
-            const int key = kt * BN + pg * kPage;
-            coord[pg] = -1;
-            if (key < L) {
-              if (p.paged) {
-                int page = p.block_table[static_cast<size_t>(it.b) * p.bt_stride + key / kPage];
-                if (page >= 0 && page < p.num_pages) {
-                  coord[pg] = page;
-                  ++nload;
-                } else {
-                  atomicOr(p.err, kErrBadInput);
-                }
-              } else {
-                coord[pg] = kv0 + key;
-                ++nload;
-              }
-            }
+          for (int j = 0; j < C::kPagesPerTile; ++j) {
+            a[j] = __shfl_sync(fullmask, pg[j], i);
+            nload += a[j] >= 0;
           }
-          const uint32_t bytes = static_cast<uint32_t>(nload * C::kDBlocks * kPage * 128);
-          for (int kind = 0; kind < 2; ++kind) {
-            const int full = kind ? kVFull0 : kKFull0;
-            const int empty = kind ? kVEmpty0 : kKEmpty0;
-            const uint32_t dst0 = (kind ? sV : sK) + s * C::kKVStage;
-            if (!(ok = wait_one(bar(empty + s), ph, ctl))) break;
-            mbar_arrive_expect_tx(bar(full + s), bytes);
+          if (lane == 0) {
+            const uint32_t st = n & 1u, ph = ((n >> 1) & 1u) ^ 1u;
+            ok = wait_one(bar(empty + st), ph, ctl);
+            if (ok) {
+              mbar_arrive_expect_tx(bar(full + st), static_cast<uint32_t>(nload * C::kDBlocks * kPage * 128));
+              const uint32_t dst0 = ring + st * C::kKVStage;
 #pragma unroll
-            for (int pg = 0; pg < C::kPagesPerTile; ++pg) {
-              if (coord[pg] < 0) continue;
-              for (int c = 0; c < C::kDBlocks; ++c) {
-                const uint32_t dst = dst0 + c * (BN * 128) + pg * (kPage * 128);
-                if (p.paged)
-                  tma_load_4d(dst, &tmap_kv, bar(full + s), c * 64, 0, it.hk, 2 * coord[pg] + kind,
-                              pol_kv);
-                else
-                  tma_load_4d(dst, &tmap_kv, bar(full + s), c * 64, it.hk, coord[pg], kind, pol_kv);
+              for (int j = 0; j < C::kPagesPerTile; ++j) {
+                if (a[j] < 0) continue;
+                for (int c = 0; c < C::kDBlocks; ++c) {
+                  const uint32_t dst = dst0 + c * (BN * 128) + j * (kPage * 128);
+                  if (p.paged)
+                    tma_load_4d(dst, &tmap_kv, bar(full + st), c * 64, 0, it.hk, 2 * a[j] + kind, pol_kv);
+                  else
+                    tma_load_4d(dst, &tmap_kv, bar(full + st), c * 64, it.hk, a[j], kind, pol_kv);
+                }
               }
             }
           }
-          if (!ok) break;
+          ok = __shfl_sync(fullmask, ok, 0);
+          if (!ok) break;  // n counts only the fills that were issued
         }
       }
-      // Drain: every copy this thread started must have landed before exit.
-      if (itl > 0 || n > 0) {
-        if (n > 0) {
-          for (uint32_t s = 0; s < 2; ++s) {
-            if (n <= s) continue;
-            const uint32_t last = ((n - 1 - s) & ~1u) + s;  // last fill index on stage s
-            wait_one(bar(kKFull0 + s), (last >> 1) & 1u, ctl);
-            wait_one(bar(kVFull0 + s), (last >> 1) & 1u, ctl);
-          }
-        }
+    }
+    // Drain: every copy this warp started must have landed before exit.
+    if (lane == 0) {
+      for (uint32_t st = 0; st < 2; ++st) {
+        if (n <= st) continue;
+        const uint32_t last = ((n - 1 - st) & ~1u) + st;  // last fill index on stage st
+        wait_one(bar(full + st), (last >> 1) & 1u, WaitCtl{abort_flag, p.err});
       }
+      if (kind == 0 && itl > 0) wait_one(bar(kQFull), (itl - 1) & 1u, WaitCtl{abort_flag, p.err});
     }
     __syncwarp();
   } else if (warp == 1) {
