@@ -41,36 +41,42 @@ template <int D, int BN>
 struct Cfg {
   static constexpr int kQBytes = kBM * D * 2;
   static constexpr int kKVStage = BN * D * 2;
-  static constexpr int kStages = 2;
+  static constexpr int kKStages = D == 128 ? 3 : 2;        // K runs a tile further ahead
+  static constexpr int kVStages = 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKVStage;
-  static constexpr int kOffX = kOffV + kStages * kKVStage;  // row max / sum exchange
+  static constexpr int kOffV = kOffK + kKStages * kKVStage;
+  static constexpr int kOffX = kOffV + kVStages * kKVStage;  // row max / sum exchange
   static constexpr int kXBytes = (2 * 2 + 2) * kBM * 4;
   static constexpr int kOffBar = kOffX + kXBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kOffMisc = kOffBar + kBarBytes;
   static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
-  static constexpr int kColO = 0;                     // TMEM columns [0, D)
-  static constexpr int kColS = 256;                   // two S buffers of BN columns
+  // D = 128: each softmax warpgroup accumulates its key half into its own O
+  // (columns 0-127 and 128-255) against its own running max, with one S buffer
+  // (256-383) and two P buffers (384-511). D = 256: one shared O (0-255), two S
+  // buffers (256-383) and two P buffers (384-447).
+  static constexpr bool kSplitO = D == 128;
+  static constexpr int kSBufs = kSplitO ? 1 : 2;
+  static constexpr int kColO = 0;
+  static constexpr int kColS = 256;
   static constexpr int kPCols = BN / 2;               // P as bf16 pairs: BN keys in BN/2 columns
-  static constexpr int kColP = D == 128 ? 128 : kColS + 2 * BN;  // two P buffers
+  static constexpr int kColP = kColS + kSBufs * BN;
   static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns per row
   static constexpr int kPagesPerTile = BN / kPage;
-  static_assert(kColS + 2 * BN <= kTmemCols, "TMEM budget");
-  static_assert(kColP + 2 * kPCols <= kTmemCols && (kColP >= kColS + 2 * BN || kColP + 2 * kPCols <= kColS),
-                "P columns");
-  static_assert(D <= kColS, "O columns");
+  static_assert(kColP + 2 * kPCols <= kTmemCols, "TMEM budget");
+  static_assert((kSplitO ? 2 * D : D) <= kColS, "O columns");
   static_assert(BN % kPage == 0 && BN % 32 == 0, "tile");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 // mbarrier slots
 enum Bar {
-  kQFull = 0, kQEmpty, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVReady0,
+  kQFull = 0, kQEmpty, kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2, kVFull0, kVFull1, kVReady0,
   kVReady1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1,
-  kPVDone0, kPVDone1, kDrain, kXMax0, kXMax1, kXSum, kNumBars
+  kPFull2, kPFull3, kPVDone0, kPVDone1, kDrain, kXMax0, kXMax1, kXSum, kNumBars
 };
+static_assert(kNumBars * 8 <= 256, "mbarrier area");
 constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
 constexpr int kSoftmaxWarps = 8;
 
@@ -115,9 +121,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     *abort_flag = 0;
     mbar_init(bar(kQFull), 1);
     mbar_init(bar(kQEmpty), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(kKFull0 + s), 1);
       mbar_init(bar(kKEmpty0 + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kVFull0 + s), 1);
       mbar_init(bar(kVReady0 + s), 1);
       mbar_init(bar(kVEmpty0 + s), 1);
@@ -125,10 +133,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       mbar_init(bar(kSFree0 + s), kSoftmaxWarps);
       mbar_init(bar(kXMax0 + s), kSoftmaxWarps);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kPFull0 + s), kSoftmaxWarps);
-      mbar_init(bar(kPVDone0 + s), 1);
-    }
+    // P buffer b, key half h: p_full[2 * b + h], one arrival per warp of warpgroup h
+    for (int s = 0; s < 4; ++s) mbar_init(bar(kPFull0 + s), kSoftmaxWarps / 2);
+    for (int s = 0; s < 2; ++s) mbar_init(bar(kPVDone0 + s), 1);
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kXSum), kSoftmaxWarps);
     mbar_init_fence();
@@ -154,6 +161,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     // queues behind the release of a V stage. Each warp reads the block table
     // 32 tiles at a time across its lanes; lane 0 issues the copies.
     const int kind = warp == 0 ? 0 : 1;
+    const uint32_t stages = kind ? C::kVStages : C::kKStages;
     const int full = kind ? kVFull0 : kKFull0;
     const int empty = kind ? kVEmpty0 : kKEmpty0;
     const uint32_t ring = kind ? sV : sK;
@@ -207,7 +215,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             nload += a[j] >= 0;
           }
           if (lane == 0) {
-            const uint32_t st = n & 1u, ph = ((n >> 1) & 1u) ^ 1u;
+            const uint32_t st = n % stages, ph = ((n / stages) & 1u) ^ 1u;
             ok = wait_one(bar(empty + st), ph, ctl);
             if (ok) {
               mbar_arrive_expect_tx(bar(full + st), static_cast<uint32_t>(nload * C::kDBlocks * kPage * 128));
@@ -232,10 +240,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     }
     // Drain: every copy this warp started must have landed before exit.
     if (lane == 0) {
-      for (uint32_t st = 0; st < 2; ++st) {
+      for (uint32_t st = 0; st < stages; ++st) {
         if (n <= st) continue;
-        const uint32_t last = ((n - 1 - st) & ~1u) + st;  // last fill index on stage st
-        wait_one(bar(full + st), (last >> 1) & 1u, WaitCtl{abort_flag, p.err});
+        const uint32_t last = ((n - 1 - st) / stages) * stages + st;  // last fill on stage st
+        wait_one(bar(full + st), (last / stages) & 1u, WaitCtl{abort_flag, p.err});
       }
       if (kind == 0 && itl > 0) wait_one(bar(kQFull), (itl - 1) & 1u, WaitCtl{abort_flag, p.err});
     }
@@ -249,15 +257,25 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       bool ok = true;
       auto issue_pv = [&](uint32_t m, bool first) -> bool {
         const uint32_t pb = m & 1u;
-        if (!wait_one(bar(kPFull0 + pb), (m >> 1) & 1u, ctl)) return false;
         if (!wait_one(bar(kVReady0 + (m & 1u)), (m >> 1) & 1u, ctl)) return false;
-        tc_fence_after();
         const uint32_t v0 = sV + (m & 1u) * C::kKVStage;
         const uint32_t a0 = tmem + C::kColP + pb * C::kPCols;
+        // the key halves in a fixed order, each as soon as its warpgroup's P is in
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t b = sw128_desc(v0 + kk * (16 * 128), BN * 128, 1024);
-          umma_f16_tmem_a(tmem + C::kColO, a0 + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!wait_one(bar(kPFull0 + 2 * pb + hh), (m >> 1) & 1u, ctl)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = hh * (BN / 32); kk < (hh + 1) * (BN / 32); ++kk) {
+            const uint64_t b = sw128_desc(v0 + kk * (16 * 128), BN * 128, 1024);
+            if constexpr (C::kSplitO) {
+              // key half hh accumulates into its own O (columns hh * D ...)
+              umma_f16_tmem_a(tmem + C::kColO + hh * D, a0 + kk * 8, b, idesc_pv,
+                              (first && kk == hh * (BN / 32)) ? 0u : 1u);
+            } else {
+              umma_f16_tmem_a(tmem + C::kColO, a0 + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+            }
+          }
         }
         umma_commit(bar(kVEmpty0 + (m & 1u)));
         umma_commit(bar(kPVDone0 + pb));
@@ -268,18 +286,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         if (!(ok = wait_one(bar(kQFull), itl & 1u, ctl))) break;
         tc_fence_after();
         for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
-          const uint32_t s = n & 1u;
-          if (!(ok = wait_one(bar(kKFull0 + s), (n >> 1) & 1u, ctl))) break;
-          if (!(ok = wait_one(bar(kSFree0 + s), ((n >> 1) & 1u) ^ 1u, ctl))) break;
+          const uint32_t s = n % C::kSBufs, su = n / C::kSBufs;
+          const uint32_t ks = n % C::kKStages;
+          if (!(ok = wait_one(bar(kKFull0 + ks), (n / C::kKStages) & 1u, ctl))) break;
+          if (!(ok = wait_one(bar(kSFree0 + s), (su & 1u) ^ 1u, ctl))) break;
           tc_fence_after();
-          const uint32_t k0 = sK + s * C::kKVStage;
+          const uint32_t k0 = sK + ks * C::kKVStage;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t a = sw128_desc(sQ + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
             const uint64_t b = sw128_desc(k0 + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
             umma_f16(tmem + C::kColS + s * BN, a, b, idesc_qk, kk > 0 ? 1u : 0u);
           }
-          umma_commit(bar(kKEmpty0 + s));
+          umma_commit(bar(kKEmpty0 + ks));
           umma_commit(bar(kSFull0 + s));
           if (kt > it.kt0 && !(ok = issue_pv(n - 1, kt - 1 == it.kt0))) break;
         }
@@ -320,6 +339,193 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       }
     }
   } else if (warp >= 4) {
+    if constexpr (C::kSplitO) {
+    // ------------------------------------------------------------ softmax, D = 128
+    // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) takes keys [h*KH, h*KH + KH)
+    // of every tile for all 128 rows, with its own running max, sum and O; the two
+    // halves are merged once per item.
+    constexpr int KH = BN / 2;
+    const int h = (warp - 4) >> 2;
+    const int sw = (warp - 4) & 3;        // TMEM lane quarter
+    const int r = sw * 32 + lane;         // query row of this thread
+    const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
+    float2* xml = reinterpret_cast<float2*>(smem + C::kOffX);  // [2 wg][128] (m, l)
+    const uint32_t o_own = tmem + lane_base + C::kColO + h * D;
+    const int t_local = r / G;
+    const int g = r - t_local * G;
+    const float c = p.scale_log2;
+    uint32_t n = 0, itl = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+      const Item it = decode_item(p.items[idx]);
+      const int4 si = p.seq_info[it.b];
+      const int q0 = si.x, ql = si.y, L = si.z;
+      const int tok = it.qt * T + t_local;
+      const bool valid = (t_local < T) && (tok < ql);
+      int lim = 0;  // keys [0, lim) visible to this row
+      if (valid) lim = p.causal ? min(L, L - ql + tok + 1) : L;
+      const bool warp_live = __any_sync(0xffffffffu, valid) != 0;
+      float m_used = -INFINITY, l = 0.f;
+      for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
+        const uint32_t pb = n & 1u;
+        const bool first = kt == it.kt0;
+        if (!(ok = wait_warp(bar(kSFull0), n & 1u, ctl))) break;
+        tc_fence_after();
+        uint32_t sr[KH / 32][32];
+        if (warp_live) {
+#pragma unroll
+          for (int j = 0; j < KH / 32; ++j)
+            tmem_ld32(tmem + lane_base + C::kColS + h * KH + j * 32, sr[j]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < KH / 32; ++j) reg_fence(sr[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kSFree0));
+
+        const int key0 = kt * BN + h * KH;
+        const bool full_tile = key0 + KH <= lim;
+        uint32_t pk[KH / 2];
+        if (warp_live) {
+          float acc[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) acc[u] = -INFINITY;
+          if (full_tile) {
+#pragma unroll
+            for (int j = 0; j < KH / 32; ++j)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < KH / 32; ++j)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (key0 + j * 32 + i < lim) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
+          }
+          const float mx = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
+                                 fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
+          const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
+          const float m_new = fmaxf(m_used, mx_s);
+          if (first) {
+            m_used = m_new;
+          } else {
+            const bool need = m_new > m_used + 8.0f;
+            if (__any_sync(0xffffffffu, need)) {
+              // this half's O holds the previous tiles; rescale it once their PV is done
+              const uint32_t pm = n - 1;
+              if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+              tc_fence_after();
+              const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+              if (need) {
+                l *= alpha;
+                m_used = m_new;
+              }
+#pragma unroll 1
+              for (int j = 0; j < D / 32; ++j) {
+                uint32_t o[32];
+                tmem_ld32(o_own + j * 32, o);
+                tmem_wait_ld();
+                reg_fence(o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                tmem_st32(o_own + j * 32, o);
+              }
+              tmem_wait_st();
+            }
+          }
+          const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+          float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < KH / 32; ++j) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int key = key0 + j * 32 + i;
+              float p0 = ex2(fmaf(__uint_as_float(sr[j][i]), c, -m_ref));
+              float p1 = ex2(fmaf(__uint_as_float(sr[j][i + 1]), c, -m_ref));
+              if (!full_tile) {
+                p0 = key < lim ? p0 : 0.f;
+                p1 = key + 1 < lim ? p1 : 0.f;
+              }
+              sum[(i >> 1) & 3] += p0 + p1;
+              __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+              pk[(j * 32 + i) >> 1] = *reinterpret_cast<uint32_t*>(&hh);
+            }
+          }
+          l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        }
+        // P buffer pb was last read by the PV of tile n - 2
+        if (n >= 2) {
+          const uint32_t pm = n - 2;
+          if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+        }
+        if (warp_live) {
+          tmem_st_cols<KH / 2>(tmem + lane_base + C::kColP + pb * C::kPCols + h * (KH / 2), pk);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kPFull0 + 2 * pb + h));
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue: merge the halves
+      xml[h * kBM + r] = make_float2(m_used, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kXSum));
+      if (!(ok = wait_warp(bar(kXSum), itl & 1u, ctl))) break;
+      const float2 a0 = xml[r], a1 = xml[kBM + r];
+      const float M = fmaxf(a0.x, a1.x);
+      const float w0 = a0.y > 0.f ? ex2(a0.x - M) : 0.f;
+      const float w1 = a1.y > 0.f ? ex2(a1.x - M) : 0.f;
+      const float den = w0 * a0.y + w1 * a1.y;
+      const float inv = den > 0.f ? 1.0f / den : 0.f;
+      const float c0 = w0 * inv, c1 = w1 * inv;
+      {
+        const uint32_t pm = n - 1;
+        if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+      }
+      tc_fence_after();
+      if (warp_live) {
+        const int hq = it.hk * G + g;
+#pragma unroll 1
+        for (int j = 0; j < (D / 2) / 16; ++j) {
+          const int col = h * (D / 2) + j * 16;  // this warpgroup writes half of the columns
+          uint32_t o0[16], o1[16];
+          tmem_ld16(tmem + lane_base + C::kColO + col, o0);
+          tmem_ld16(tmem + lane_base + C::kColO + D + col, o1);
+          tmem_wait_ld();
+          reg_fence(o0);
+          reg_fence(o1);
+          if (!valid) continue;
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(o0[i]) * c0 + __uint_as_float(o1[i]) * c1;
+          if (it.part < 0) {
+            uint4* dst = reinterpret_cast<uint4*>(
+                p.out + (static_cast<size_t>(q0 + tok) * p.n_heads_q + hq) * D + col);
+#pragma unroll
+            for (int q4 = 0; q4 < 2; ++q4) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 hh = __floats2bfloat162_rn(v[q4 * 8 + 2 * e], v[q4 * 8 + 2 * e + 1]);
+                w[e] = *reinterpret_cast<uint32_t*>(&hh);
+              }
+              dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(p.part_o + static_cast<size_t>(it.part + r) * D + col);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_float4(v[q4 * 4], v[q4 * 4 + 1], v[q4 * 4 + 2], v[q4 * 4 + 3]);
+          }
+        }
+        if (valid && it.part >= 0 && h == 0)
+          p.part_ml[it.part + r] = make_float2(den > 0.f ? M : -INFINITY, den);
+      }
+      tc_fence_before();
+    }
+    } else {
     // ------------------------------------------------------------ softmax: two warpgroups
     // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) takes keys [h*KH, h*KH + KH)
     // of every tile and O columns [h*DH, h*DH + DH) for the same 128 rows; the two
@@ -469,7 +675,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kPFull0 + s));
+        if (lane == 0) mbar_arrive(bar(kPFull0 + 2 * s + h));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -522,6 +728,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           p.part_ml[it.part + r] = make_float2(l_all > 0.f ? m_used : -INFINITY, l_all);
       }
       tc_fence_before();
+    }
     }
   }
 
