@@ -253,12 +253,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
+      // operand descriptors built once; each MMA adds a compile-time offset
+      const SmemDesc dq = sw128_desc_split(sQ, 16, 1024);
+      const SmemDesc dk = sw128_desc_split(sK, 16, 1024);
+      const SmemDesc dv = sw128_desc_split(sV, BN * 128, 1024);
       uint32_t n = 0, itl = 0;
       bool ok = true;
       auto issue_pv = [&](uint32_t m, bool first) -> bool {
         const uint32_t pb = m & 1u;
         if (!wait_one(bar(kVReady0 + (m & 1u)), (m >> 1) & 1u, ctl)) return false;
-        const uint32_t v0 = sV + (m & 1u) * C::kKVStage;
+        const uint32_t v_lo = desc_lo_at(dv, (m & 1u) * C::kKVStage);
         const uint32_t a0 = tmem + C::kColP + pb * C::kPCols;
         // the key halves in a fixed order, each as soon as its warpgroup's P is in
 #pragma unroll
@@ -267,13 +271,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           tc_fence_after();
 #pragma unroll
           for (int kk = hh * (BN / 32); kk < (hh + 1) * (BN / 32); ++kk) {
-            const uint64_t b = sw128_desc(v0 + kk * (16 * 128), BN * 128, 1024);
+            const uint32_t b_lo = v_lo + ((kk * (16 * 128)) >> 4);
             if constexpr (C::kSplitO) {
               // key half hh accumulates into its own O (columns hh * D ...)
-              umma_f16_tmem_a(tmem + C::kColO + hh * D, a0 + kk * 8, b, idesc_pv,
-                              (first && kk == hh * (BN / 32)) ? 0u : 1u);
+              umma_f16_ts(tmem + C::kColO + hh * D, a0 + kk * 8, b_lo, dv.hi, idesc_pv,
+                          (first && kk == hh * (BN / 32)) ? 0u : 1u);
             } else {
-              umma_f16_tmem_a(tmem + C::kColO, a0 + kk * 8, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+              umma_f16_ts(tmem + C::kColO, a0 + kk * 8, b_lo, dv.hi, idesc_pv,
+                          (first && kk == 0) ? 0u : 1u);
             }
           }
         }
@@ -291,12 +296,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           if (!(ok = wait_one(bar(kKFull0 + ks), (n / C::kKStages) & 1u, ctl))) break;
           if (!(ok = wait_one(bar(kSFree0 + s), (su & 1u) ^ 1u, ctl))) break;
           tc_fence_after();
-          const uint32_t k0 = sK + ks * C::kKVStage;
+          const uint32_t k_lo = desc_lo_at(dk, ks * C::kKVStage);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = sw128_desc(sQ + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = sw128_desc(k0 + (kk >> 2) * (BN * 128) + (kk & 3) * 32, 16, 1024);
-            umma_f16(tmem + C::kColS + s * BN, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+            const uint32_t a_lo = dq.lo + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+            const uint32_t b_lo = k_lo + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
+            umma_f16_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(kKEmpty0 + ks));
           umma_commit(bar(kSFull0 + s));

@@ -378,6 +378,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kNQ, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kNQ, true, false);
+      const SmemDesc dring_k = sw128_desc_split(sRing, 16, 1024);          // K tiles, K-major
+      const SmemDesc dring_v = sw128_desc_split(sRing, kDBN * 128, 1024);  // V tiles, MN-major
+      const SmemDesc dq = sw128_desc_split(sQ, 16, 1024);
+      const SmemDesc dp = sw128_desc_split(sP, 16, 1024);
       uint32_t n = 0, itl = 0;
       bool ok = true;
       auto issue_pv = [&](uint32_t m, bool first) -> bool {
@@ -385,15 +389,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         if (!wait_one(bar(kDPFull0 + (m & 1u)), (m >> 1) & 1u, ctl)) return false;
         if (!wait_one(ring_ready(s), ph, ctl)) return false;
         tc_fence_after();
-        const uint32_t v0 = sRing + s * C::kStage;
+        const uint32_t v_lo = desc_lo_at(dring_v, s * C::kStage);
+        const uint32_t p_lo = desc_lo_at(dp, (m & 1u) * C::kPBytes);
 #pragma unroll
         for (int kk = 0; kk < kDBN / 16; ++kk) {
-          const uint64_t b = sw128_desc(sP + (m & 1u) * C::kPBytes + (kk >> 2) * (kNQ * 128) + (kk & 3) * 32,
-                                        16, 1024);
+          const uint32_t b_lo = p_lo + (((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4);
 #pragma unroll
           for (int h = 0; h < C::kHalves; ++h) {
-            const uint64_t a = sw128_desc(v0 + (2 * h) * (kDBN * 128) + kk * (16 * 128), kDBN * 128, 1024);
-            umma_f16(tmem + C::kColO + h * kNQ, a, b, idesc_pv, (first && kk == 0) ? 0u : 1u);
+            const uint32_t a_lo = v_lo + (((2 * h) * (kDBN * 128) + kk * (16 * 128)) >> 4);
+            umma_f16_ss(tmem + C::kColO + h * kNQ, a_lo, dring_v.hi, b_lo, dp.hi, idesc_pv,
+                        (first && kk == 0) ? 0u : 1u);
           }
         }
         umma_commit(ring_empty(s));
@@ -411,12 +416,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           if (!(ok = wait_one(ring_ready(s), ph, ctl))) break;
           if (!(ok = wait_one(bar(kDSFree0 + sb), ((n >> 1) & 1u) ^ 1u, ctl))) break;
           tc_fence_after();
-          const uint32_t k0 = sRing + s * C::kStage;
+          const uint32_t k_lo = desc_lo_at(dring_k, s * C::kStage);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = sw128_desc(k0 + (kk >> 2) * (kDBN * 128) + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = sw128_desc(sQ + (kk >> 2) * (kNQ * 128) + (kk & 3) * 32, 16, 1024);
-            umma_f16(tmem + C::kColS + sb * kNQ, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+            const uint32_t a_lo = k_lo + (((kk >> 2) * (kDBN * 128) + (kk & 3) * 32) >> 4);
+            const uint32_t b_lo = dq.lo + (((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4);
+            umma_f16_ss(tmem + C::kColS + sb * kNQ, a_lo, dring_k.hi, b_lo, dq.hi, idesc_qk,
+                        kk > 0 ? 1u : 0u);
           }
           umma_commit(ring_empty(s));
           umma_commit(bar(kDSFull0 + sb));

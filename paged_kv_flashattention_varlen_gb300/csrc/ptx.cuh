@@ -198,6 +198,49 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
+// A descriptor split into its two 32-bit words. Offsets of an operand inside
+// shared memory change only the start-address field of the low word, and
+// never carry out of it (shared addresses stay below 256 KB), so a per-MMA
+// descriptor is one 32-bit add on a base built once.
+struct SmemDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SmemDesc sw128_desc_split(uint32_t saddr, uint32_t lbo_bytes,
+                                                     uint32_t sbo_bytes) {
+  const uint64_t d = sw128_desc(saddr, lbo_bytes, sbo_bytes);
+  return SmemDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+// Descriptor of the operand `byte_offset` bytes further (a multiple of 16).
+__device__ __forceinline__ uint32_t desc_lo_at(const SmemDesc& d, uint32_t byte_offset) {
+  return d.lo + (byte_offset >> 4);
+}
+
+// D[tmem] (+)= A[smem] * B[smem] with the descriptors given as 32-bit words.
+__device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                            uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem] with B's descriptor as 32-bit words.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16)
 //   bit 15 A major (0 = K-major), bit 16 B major (1 = MN-major)
