@@ -54,17 +54,21 @@ struct Cfg {
   static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
   // D = 128: each softmax warpgroup accumulates its key half into its own O
   // (columns 0-127 and 128-255) against its own running max, with one S buffer
-  // (256-383) and two P buffers (384-511). D = 256: one shared O (0-255), two S
-  // buffers (256-383) and two P buffers (384-447).
+  // (256-383), one P buffer (384-447) and the Q tile (448-511), so that QK reads
+  // only K from shared memory. D = 256: one shared O (0-255), two S buffers
+  // (256-383) and two P buffers (384-447), Q from shared memory.
   static constexpr bool kSplitO = D == 128;
+  static constexpr bool kQTmem = kSplitO;             // Q also in TMEM: QK reads only K from smem
   static constexpr int kSBufs = kSplitO ? 1 : 2;
+  static constexpr int kPBufs = kSplitO ? 1 : 2;
   static constexpr int kColO = 0;
   static constexpr int kColS = 256;
   static constexpr int kPCols = BN / 2;               // P as bf16 pairs: BN keys in BN/2 columns
   static constexpr int kColP = kColS + kSBufs * BN;
+  static constexpr int kColQ = kColP + kPBufs * kPCols;  // Q as bf16 pairs (D/2 columns)
   static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns per row
   static constexpr int kPagesPerTile = BN / kPage;
-  static_assert(kColP + 2 * kPCols <= kTmemCols, "TMEM budget");
+  static_assert(kColQ + (kQTmem ? D / 2 : 0) <= kTmemCols, "TMEM budget");
   static_assert((kSplitO ? 2 * D : D) <= kColS, "O columns");
   static_assert(BN % kPage == 0 && BN % 32 == 0, "tile");
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -74,7 +78,7 @@ struct Cfg {
 enum Bar {
   kQFull = 0, kQEmpty, kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2, kVFull0, kVFull1, kVReady0,
   kVReady1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1,
-  kPFull2, kPFull3, kPVDone0, kPVDone1, kDrain, kXMax0, kXMax1, kXSum, kNumBars
+  kPFull2, kPFull3, kPVDone0, kPVDone1, kDrain, kXMax0, kXMax1, kXSum, kQTReady, kQTFree, kNumBars
 };
 static_assert(kNumBars * 8 <= 256, "mbarrier area");
 constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
@@ -120,7 +124,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar(kQFull), 1);
-    mbar_init(bar(kQEmpty), 1);
+    // Q shared memory is released by the QK MMAs, or (Q in TMEM) by the softmax
+    // warps once they copied it into TMEM
+    mbar_init(bar(kQEmpty), C::kQTmem ? kSoftmaxWarps : 1);
+    mbar_init(bar(kQTReady), kSoftmaxWarps);
+    mbar_init(bar(kQTFree), 1);
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(kKFull0 + s), 1);
       mbar_init(bar(kKEmpty0 + s), 1);
@@ -260,14 +268,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       uint32_t n = 0, itl = 0;
       bool ok = true;
       auto issue_pv = [&](uint32_t m, bool first) -> bool {
-        const uint32_t pb = m & 1u;
+        const uint32_t pb = m % C::kPBufs, pu = m / C::kPBufs;
         if (!wait_one(bar(kVReady0 + (m & 1u)), (m >> 1) & 1u, ctl)) return false;
         const uint32_t v_lo = desc_lo_at(dv, (m & 1u) * C::kKVStage);
         const uint32_t a0 = tmem + C::kColP + pb * C::kPCols;
         // the key halves in a fixed order, each as soon as its warpgroup's P is in
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          if (!wait_one(bar(kPFull0 + 2 * pb + hh), (m >> 1) & 1u, ctl)) return false;
+          if (!wait_one(bar(kPFull0 + 2 * pb + hh), pu & 1u, ctl)) return false;
           tc_fence_after();
 #pragma unroll
           for (int kk = hh * (BN / 32); kk < (hh + 1) * (BN / 32); ++kk) {
@@ -288,7 +296,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       };
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
         const Item it = decode_item(p.items[idx]);
-        if (!(ok = wait_one(bar(kQFull), itl & 1u, ctl))) break;
+        if (!(ok = wait_one(bar(C::kQTmem ? kQTReady : kQFull), itl & 1u, ctl))) break;
         tc_fence_after();
         for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
           const uint32_t s = n % C::kSBufs, su = n / C::kSBufs;
@@ -299,16 +307,21 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           const uint32_t k_lo = desc_lo_at(dk, ks * C::kKVStage);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t a_lo = dq.lo + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
             const uint32_t b_lo = k_lo + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
-            umma_f16_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
+            if constexpr (C::kQTmem) {
+              umma_f16_ts(tmem + C::kColS + s * BN, tmem + C::kColQ + kk * 8, b_lo, dk.hi, idesc_qk,
+                          kk > 0 ? 1u : 0u);
+            } else {
+              const uint32_t a_lo = dq.lo + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+              umma_f16_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
+            }
           }
           umma_commit(bar(kKEmpty0 + ks));
           umma_commit(bar(kSFull0 + s));
           if (kt > it.kt0 && !(ok = issue_pv(n - 1, kt - 1 == it.kt0))) break;
         }
         if (!ok) break;
-        umma_commit(bar(kQEmpty));
+        umma_commit(bar(C::kQTmem ? kQTFree : kQEmpty));
         if (!(ok = issue_pv(n - 1, it.kt1 - 1 == it.kt0))) break;
       }
       // Drain: all UMMAs issued by this thread complete before TMEM is freed.
@@ -370,9 +383,34 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       int lim = 0;  // keys [0, lim) visible to this row
       if (valid) lim = p.causal ? min(L, L - ql + tok + 1) : L;
       const bool warp_live = __any_sync(0xffffffffu, valid) != 0;
+      {
+        // Q tile -> TMEM: this thread's row, this warpgroup's 64 columns of d,
+        // once the TMA landed it and the previous item's QK MMAs are done
+        if (!(ok = wait_warp(bar(kQFull), itl & 1u, ctl))) break;
+        if (!(ok = wait_warp(bar(kQTFree), (itl & 1u) ^ 1u, ctl))) break;
+        tc_fence_after();
+        const uint8_t* qrow = smem + C::kOffQ + h * (kBM * 128) + r * 128;
+        uint32_t qv[32];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v4 = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) << 4));
+          qv[ch * 4] = v4.x;
+          qv[ch * 4 + 1] = v4.y;
+          qv[ch * 4 + 2] = v4.z;
+          qv[ch * 4 + 3] = v4.w;
+        }
+        tmem_st32(tmem + lane_base + C::kColQ + h * 32, qv);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(kQTReady));
+          mbar_arrive(bar(kQEmpty));
+        }
+      }
       float m_used = -INFINITY, l = 0.f;
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
-        const uint32_t pb = n & 1u;
+        const uint32_t pb = n % C::kPBufs;
         const bool first = kt == it.kt0;
         if (!(ok = wait_warp(bar(kSFull0), n & 1u, ctl))) break;
         tc_fence_after();
@@ -419,7 +457,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             if (__any_sync(0xffffffffu, need)) {
               // this half's O holds the previous tiles; rescale it once their PV is done
               const uint32_t pm = n - 1;
-              if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+              if (!(ok = wait_warp(bar(kPVDone0 + pm % C::kPBufs), (pm / C::kPBufs) & 1u, ctl))) break;
               tc_fence_after();
               const float alpha = need ? ex2(m_used - m_new) : 1.0f;
               if (need) {
@@ -459,10 +497,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           }
           l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
         }
-        // P buffer pb was last read by the PV of tile n - 2
-        if (n >= 2) {
-          const uint32_t pm = n - 2;
-          if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+        // P buffer pb was last read by the PV of tile n - kPBufs
+        if (n >= static_cast<uint32_t>(C::kPBufs)) {
+          const uint32_t pm = n - C::kPBufs;
+          if (!(ok = wait_warp(bar(kPVDone0 + pm % C::kPBufs), (pm / C::kPBufs) & 1u, ctl))) break;
         }
         if (warp_live) {
           tmem_st_cols<KH / 2>(tmem + lane_base + C::kColP + pb * C::kPCols + h * (KH / 2), pk);
@@ -487,7 +525,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       const float c0 = w0 * inv, c1 = w1 * inv;
       {
         const uint32_t pm = n - 1;
-        if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+        if (!(ok = wait_warp(bar(kPVDone0 + pm % C::kPBufs), (pm / C::kPBufs) & 1u, ctl))) break;
       }
       tc_fence_after();
       if (warp_live) {
