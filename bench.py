@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["decode", "prefill"], default=None,
                     help="profiling runs: time one workload only")
+    ap.add_argument("--workload", default=None,
+                    help="time named workload(s) 1-5 (comma list or 'all'): one JSON line each")
     return ap.parse_args()
 
 
@@ -389,8 +391,72 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_workloads(args):
+    """One JSON line per named workload: step time, KV GB/s, attention TFLOP/s and the
+    attention kernels' fractions of the HBM and bf16 rooflines."""
+    import torch
+
+    import paged_kv_flashattention_varlen_gb300 as pk
+    from paged_kv_flashattention_varlen_gb300 import build as pkbuild
+    import workloads
+
+    pkbuild.build()
+    pk_peaks, peak_kind = peaks()
+    hbm, tc = float(pk_peaks["hbm_gbs"]), float(pk_peaks["bf16_tflops"])
+    idxs = [1, 2, 3, 4, 5] if args.workload == "all" else [int(x) for x in args.workload.split(",")]
+    dev = torch.device("cuda", 0)
+    for i in idxs:
+        wl = workloads.named(i)
+        q, kv = wl.q.to(dev), wl.kv_pool.to(dev)
+        bt = None if wl.block_table is None else wl.block_table.to(dev)
+        sl, cu = wl.seq_lens.to(dev), wl.cu_q.to(dev)
+        out = torch.empty_like(q)
+
+        def step():
+            pk.forward(out, q, kv, bt, sl, cu, max_q=wl.max_q, max_kv=wl.max_kv,
+                       n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
+                       num_pages=wl.num_pages, check=False)
+
+        flops = 4.0 * wl.head_dim * wl.n_heads_q * wl.visible_pairs()
+        nbytes = wl.kv_bytes() + wl.qo_bytes()
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        est = 1e-3 * max(flops / 9e14, nbytes / 6e12, 2e-5) * 1e3
+        steps = max(5, min(2000, int(1.0 / max(est, 1e-6))))
+        pk.profile_read()
+        pk.profile_enable(True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        pk.profile_enable(False)
+        t_plan, t_attn, t_comb, calls = pk.profile_read()
+        ms = e0.elapsed_time(e1) / steps
+        attn_ms = t_attn / max(calls, 1)
+        line = {
+            "workload": workloads.NAMES[i - 1], "steps": steps, "ms_per_step": round(ms, 5),
+            "kv_gbs_step": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "tflops_step": round(flops / (ms * 1e-3) / 1e12, 1),
+            "attention_kernels_ms": round(attn_ms, 5),
+            "hbm_frac_attention": round(nbytes / (attn_ms * 1e-3) / 1e9 / hbm, 4),
+            "tensor_frac_attention": round(flops / (attn_ms * 1e-3) / 1e12 / tc, 4),
+            "plan_ms": round(t_plan / max(calls, 1), 5), "combine_ms": round(t_comb / max(calls, 1), 5),
+            "bytes": nbytes, "flops": flops, "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 {tc} TFLOP/s",
+            "device_status": pk.device_status(),
+        }
+        print(json.dumps(line), flush=True)
+        del q, kv, bt, sl, cu, out
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
+    if args.workload:
+        run_workloads(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
