@@ -81,7 +81,7 @@ typedef enum pattn_status {
  *   num_pages   pages in the pool (bounds every block-table entry).
  *   scale       softmax scale, finite and >= 0.
  *   causal      0: every key of the sequence; 1: keys up to the query position.
- *   stream      stream the three launches (plan, attention, combine) go on.
+ *   stream      stream the launches (plan, decode and/or prefill attention) go on.
  *
  * All pointers 16-byte aligned. The first call on a device allocates the
  * library workspace (grow-only) unless pattn_set_workspace gave one.
@@ -144,8 +144,9 @@ pattn_status pattn_forward_host(void *out, const void *q, const void *kv_pool,
 
 /*
  * Workspace bytes pattn_forward needs for these bounds: a header with the
- * device error word, the planned work list, and the split-KV partial O and
- * (max, sum) scratch (the manifest's "partial" and "stats" buffers).
+ * device error word, the planned work list, the split-KV partial O and
+ * (max, sum) scratch and the per-unit finished-split counters (the manifest's
+ * "partial", "stats" and "counter" buffers).
  */
 size_t pattn_workspace_size(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
                             int n_heads_kv, int head_dim, int page_size);
@@ -172,8 +173,10 @@ const char *pattn_status_string(pattn_status status);
  * Kernel timing: while enabled, pattn_forward records CUDA events around each
  * of its launches on its stream (at most 4096 calls are kept).
  * pattn_profile_read synchronises those events and returns the summed device
- * time in milliseconds of the plan, attention and combine kernels and the
- * number of calls recorded, then clears the record.
+ * time in milliseconds of the plan kernel and of the attention kernels
+ * (decode and prefill) and the number of calls recorded, then clears the
+ * record. ms_combine is the time after the attention kernels; split-KV
+ * partials are merged inside them, so it is close to zero.
  */
 pattn_status pattn_profile_enable(int on);
 pattn_status pattn_profile_read(double *ms_plan, double *ms_attention, double *ms_combine,

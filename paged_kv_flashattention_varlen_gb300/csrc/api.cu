@@ -1,5 +1,6 @@
 // api.cu -- host side of libpattn: argument validation, per-device workspace,
-// TMA tensor-map encoding and the launch sequence plan -> attention -> combine.
+// TMA tensor-map encoding and the launch sequence plan -> decode -> prefill ->
+// merge (the decode kernel merges its own split-KV partials).
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -23,7 +24,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Events around plan | decode kernel | prefill kernel | combine.
+// Events around plan | decode kernel | prefill kernel | merge of prefill splits.
 struct ProfileRec {
   cudaEvent_t ev[5];
 };
@@ -79,12 +80,13 @@ pattn_status check_args(const void* out, const void* q, const void* kv, const in
   if (cdiv(max_q, sh->tokens_per_tile) > 65535) return PATTN_ERR_UNSUPPORTED;
   if (cdiv(max_kv, sh->block_n) > 65535) return PATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_pages) * 2 > 0x7fffffffLL) return PATTN_ERR_UNSUPPORTED;
+  if (num_seqs > kSeqMask) return PATTN_ERR_UNSUPPORTED;  // item encoding: 24-bit sequence index
   if (static_cast<long long>(total_q) * hq * d > (1LL << 40)) return PATTN_ERR_UNSUPPORTED;
   return PATTN_OK;
 }
 
 struct WsLayout {
-  size_t hdr, seq_info, seq_plan, seq_part, items, dec_items, units, part_ml, part_o, total;
+  size_t hdr, seq_info, seq_plan, seq_part, items, dec_items, unit_cnt, part_ml, part_o, total;
   int max_items, max_units, max_part_rows;
 };
 
@@ -123,8 +125,8 @@ WsLayout ws_layout(int num_seqs, int total_q, int max_q, int hq, int hkv, int d,
   off += sizeof(int4) * static_cast<size_t>(w.max_items);
   w.dec_items = off = align_up(off, 256);
   off += sizeof(int4) * static_cast<size_t>(w.max_items);
-  w.units = off = align_up(off, 256);
-  off += sizeof(int4) * static_cast<size_t>(w.max_units);
+  w.unit_cnt = off = align_up(off, 256);
+  off += sizeof(int) * static_cast<size_t>(w.max_units);
   w.part_ml = off = align_up(off, 256);
   off += sizeof(float2) * static_cast<size_t>(w.max_part_rows);
   w.part_o = off = align_up(off, 256);
@@ -229,7 +231,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   ws.seq_part = reinterpret_cast<int*>(wsb + L.seq_part);
   ws.items = reinterpret_cast<int4*>(wsb + L.items);
   ws.dec_items = reinterpret_cast<int4*>(wsb + L.dec_items);
-  ws.units = reinterpret_cast<int4*>(wsb + L.units);
+  ws.unit_cnt = reinterpret_cast<int*>(wsb + L.unit_cnt);
   ws.part_ml = reinterpret_cast<float2*>(wsb + L.part_ml);
   ws.part_o = reinterpret_cast<float*>(wsb + L.part_o);
   ws.max_items = L.max_items;
@@ -307,6 +309,8 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   ap.items = ws.items;
   ap.hdr = ws.hdr;
   ap.seq_info = ws.seq_info;
+  ap.seq_plan = ws.seq_plan;
+  ap.unit_cnt = ws.unit_cnt;
   ap.block_table = bt;
   ap.out = static_cast<__nv_bfloat16*>(out);
   ap.part_o = ws.part_o;
@@ -321,17 +325,6 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   ap.scale_log2 = scale * 1.4426950408889634f;
   ap.causal = causal;
   ap.paged = bt ? 1 : 0;
-
-  CombineParams cp{};
-  cp.units = ws.units;
-  cp.hdr = ws.hdr;
-  cp.seq_info = ws.seq_info;
-  cp.part_o = ws.part_o;
-  cp.part_ml = ws.part_ml;
-  cp.out = static_cast<__nv_bfloat16*>(out);
-  cp.n_heads_q = hq;
-  cp.group = g;
-  cp.head_dim = d;
 
   AttnParams dp = ap;
   dp.items = ws.dec_items;
@@ -356,9 +349,12 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (prof) cudaEventRecord(rec.ev[3], stream);
-  const int cgrid = std::min(ws.max_units, 2 * st.sms);
-  e = launch_combine(cp, cgrid, stream);
-  if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  if (run_prefill) {
+    // split units of the prefill kernel (single-q-tile units of more than
+    // kDecRows rows) are merged by a separate pass; the decode kernel merges its own
+    e = launch_merge(ap, d, std::min(ws.max_items, 2 * st.sms), stream);
+    if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  }
   if (prof) {
     cudaEventRecord(rec.ev[4], stream);
     st.prof.push_back(rec);

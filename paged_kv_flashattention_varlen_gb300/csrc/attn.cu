@@ -30,7 +30,8 @@
 //     that NaN or garbage there cannot reach O through 0 * NaN.
 //
 // At the end of an item the softmax warps divide by l and store bf16 rows, or
-// (split items) write the normalised partial O and (m, l) for the combine.
+// (split items) write the normalised partial O and (m, l); merge_kernel then
+// merges each split unit.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -84,13 +85,14 @@ static_assert(kNumBars * 8 <= 256, "mbarrier area");
 constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
 constexpr int kSoftmaxWarps = 8;
 
+// part: first partial row of this split, -1 if the item is not split.
 struct Item {
   int b, hk, qt, kt0, kt1, part;
 };
 
 __device__ __forceinline__ Item decode_item(int4 v) {
   Item it;
-  it.b = v.x;
+  it.b = v.x & kSeqMask;
   it.hk = v.y >> 16;
   it.qt = v.y & 0xFFFF;
   it.kt0 = (v.z >> 16) & 0xFFFF;
@@ -129,6 +131,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     mbar_init(bar(kQEmpty), C::kQTmem ? kSoftmaxWarps : 1);
     mbar_init(bar(kQTReady), kSoftmaxWarps);
     mbar_init(bar(kQTFree), 1);
+
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(kKFull0 + s), 1);
       mbar_init(bar(kKEmpty0 + s), 1);

@@ -20,6 +20,7 @@
 // on a global load. The tail warp forwards every filled stage, zeroing V rows
 // past the sequence end first (so 0 * NaN cannot reach O).
 #include "kernels.cuh"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace pattn {
@@ -52,14 +53,15 @@ struct DCfg {
 
 // P is double-buffered: p_full[b] / pv_done[b] complete once per use of P buffer b.
 enum DBar { kDQFull = 0, kDQEmpty, kDSFull0, kDSFull1, kDSFree0, kDSFree1, kDPFull0, kDPFull1,
-            kDPVDone0, kDPVDone1, kDDrain, kDRedMax0, kDRedMax1, kDRedSum,
-            kDRingFull0 = 14 };  // then ring full [R], ring ready [R], ring empty [R]
+            kDPVDone0, kDPVDone1, kDDrain, kDRedMax0, kDRedMax1, kDRedSum, kDMerge0, kDMerge1,
+            kDRingFull0 = 16 };  // then ring full [R], ring ready [R], ring empty [R]
 
 struct SoftCtx {
   uint8_t* smem;
   uint32_t sBar, tmem, lane_base;
   int sw, t, lane;
   WaitCtl ctl;
+  volatile int* merge_flag;  // shared: this CTA finished a split unit last
 };
 
 // One decode item on the softmax warpgroup. NR >= the item's packed query
@@ -67,7 +69,7 @@ struct SoftCtx {
 // bounded wait gave up.
 template <int D, int NR>
 __device__ __forceinline__ bool softmax_item(const SoftCtx& x, const AttnParams& p, int4 iv,
-                                             int4 si, uint32_t& n, uint32_t& itl) {
+                                             int4 si, uint32_t& n, uint32_t& itl, uint32_t& nsp) {
   using C = DCfg<D>;
   const unsigned full = 0xffffffffu;
   auto bar = [&](int i) { return x.sBar + 8u * static_cast<uint32_t>(i); };
@@ -77,9 +79,9 @@ __device__ __forceinline__ bool softmax_item(const SoftCtx& x, const AttnParams&
   const int G = p.group;
   const int hk = iv.y >> 16;
   const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
-  const int part = iv.w;
   const int q0 = si.x, ql = si.y, L = si.z;
   const int rows = ql * G;
+  const int part = iv.w;  // first partial row of this split, -1 if not split
   const float c = p.scale_log2;
   const int t = x.t, lane = x.lane, sw = x.sw;
   int lim[NR];
@@ -224,6 +226,13 @@ __device__ __forceinline__ bool softmax_item(const SoftCtx& x, const AttnParams&
     }
   }
   tc_fence_before();
+  if (part >= 0) {
+    // hand the written partials to the merge warp (which took the previous split item)
+    if (!wait_warp(bar(kDMerge1), (nsp & 1u) ^ 1u, x.ctl)) return false;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kDMerge0));
+    ++nsp;
+  }
   return true;
 }
 
@@ -271,6 +280,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     mbar_init(bar(kDRedMax0), 4);
     mbar_init(bar(kDRedMax1), 4);
     mbar_init(bar(kDRedSum), 4);
+    mbar_init(bar(kDMerge0), 4);  // a split item's partial rows are written (softmax warps)
+    mbar_init(bar(kDMerge1), 1);  // the merge warp has taken that item
     for (int s = 0; s < R; ++s) {
       mbar_init(ring_full(s), 1);
       mbar_init(ring_ready(s), 1);
@@ -302,7 +313,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     const uint64_t pol_q = l2_policy_evict_last();
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
       const int4 iv = p.items[idx];
-      const int b = iv.x, hk = iv.y >> 16;
+      const int b = iv.x & kSeqMask, hk = iv.y >> 16;
       const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
       const int4 si = p.seq_info[b];
       const int q0 = si.x, L = si.z, kv0 = si.w;
@@ -443,7 +454,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
       const int4 iv = p.items[idx];
       const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
-      const int L = p.seq_info[iv.x].z;
+      const int L = p.seq_info[iv.x & kSeqMask].z;
       for (int kt = kt0; kt < kt1; ++kt, ++n) {
         for (uint32_t kind = 0; kind < 2; ++kind) {
           const uint32_t fi = 2 * n + kind, s = fi % R, ph = (fi / R) & 1u;
@@ -464,6 +475,34 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         if (!ok) break;
       }
     }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ split merge warp
+    // For every split item: once its partials are written, count it; the CTA
+    // that finished the unit's last split merges the unit here, off the softmax
+    // warps' path.
+    uint32_t nsp = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+      const int4 iv = p.items[idx];
+      if (iv.w < 0) continue;
+      if (!(ok = wait_warp(bar(kDMerge0), nsp & 1u, ctl))) break;
+      const int4 sp = p.seq_plan[iv.x & kSeqMask];
+      int last = 0;
+      if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(&p.unit_cnt[sp.w + (iv.y >> 16)], 1) == sp.z - 1;
+        if (last) __threadfence();
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDMerge1));
+      ++nsp;
+      if (last) {
+        const int4 si = p.seq_info[iv.x & kSeqMask];
+        const int rows = si.y * G;
+        merge_unit<D>(p, si.x, iv.y >> 16, sp.z, iv.w - (iv.x >> kSeqBits) * rows, rows, 0, 1);
+      }
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax: one key per thread
     SoftCtx x;
@@ -475,18 +514,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     x.lane_base = static_cast<uint32_t>(x.sw * 32) << 16;
     x.tmem = tmem;
     x.ctl = ctl;
-    uint32_t n = 0, itl = 0;
+    x.merge_flag = reinterpret_cast<volatile int*>(misc + 32);
+    uint32_t n = 0, itl = 0, nsp = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
       const int4 iv = p.items[idx];
-      const int4 si = p.seq_info[iv.x];
+      const int4 si = p.seq_info[iv.x & kSeqMask];
       const int rows = si.y * G;
       if (rows <= 4)
-        ok = softmax_item<D, 4>(x, p, iv, si, n, itl);
+        ok = softmax_item<D, 4>(x, p, iv, si, n, itl, nsp);
       else if (rows <= 8)
-        ok = softmax_item<D, 8>(x, p, iv, si, n, itl);
+        ok = softmax_item<D, 8>(x, p, iv, si, n, itl, nsp);
       else
-        ok = softmax_item<D, 16>(x, p, iv, si, n, itl);
+        ok = softmax_item<D, 16>(x, p, iv, si, n, itl, nsp);
     }
   }
 

@@ -26,11 +26,14 @@ enum HdrWord { kHdrErr = 0, kHdrItems = 1, kHdrUnits = 2, kHdrPartRows = 3, kHdr
                kHdrDecItems = 5, kHdrWords = 64 };
 
 // Work item, 16 bytes:
-//   x = sequence b
-//   y = kv head << 16 | q tile
+//   x = sequence b (bits 0-23) | split index << 24 (split items)
+//   y = kv head << 16 | q tile (0 for split items: their unit has one q tile)
 //   z = first kv tile << 16 | end kv tile
-//   w = first partial row of this split (-1: not split, write bf16 out directly)
-// Split unit (combine), 16 bytes: x = b, y = kv head, z = splits S, w = first partial row.
+//   w = -1: not split, the item writes bf16 out directly;
+//       >= 0: first partial row of this split (split s of a unit with `rows`
+//       packed rows; the unit's partials start at w - s * rows)
+constexpr int kSeqBits = 24;
+constexpr int kSeqMask = (1 << kSeqBits) - 1;
 // Sequence info, 16 bytes: x = first query token, y = query length (-1: rejected),
 //   z = KV length, w = first KV row (contiguous cache).
 
@@ -38,10 +41,10 @@ struct Workspace {
   int* hdr;
   int4* seq_info;
   int4* seq_plan;   // x = first global q tile, y = q tiles, z = splits, w = first split unit
+  int* unit_cnt;    // finished splits per split unit (zeroed by the plan)
   int* seq_part;    // first partial row of the sequence's split units
   int4* items;      // prefill kernel items
   int4* dec_items;  // swap-AB decode kernel items
-  int4* units;
   float* part_o;    // [rows][D] split-normalised partial O
   float2* part_ml;  // [rows] (running max in log2 units, sum of exp2)
   int max_items;
@@ -80,23 +83,16 @@ struct AttnParams {
   float scale_log2;  // softmax scale * log2(e)
   int causal;
   int paged;
+  const int4* seq_plan;  // z = splits, w = first split unit of the sequence
+  int* unit_cnt;         // finished splits per split unit
 };
 
-struct CombineParams {
-  const int4* units;
-  const int* hdr;
-  const int4* seq_info;
-  const float* part_o;
-  const float2* part_ml;
-  __nv_bfloat16* out;
-  int n_heads_q, group, head_dim;
-};
 
 // Launchers (defined in the .cu files; return the launch error).
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                              int head_dim, int grid, cudaStream_t s);
-cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
+cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                           int head_dim, int grid, cudaStream_t s);
 size_t decode_smem_bytes(int head_dim);

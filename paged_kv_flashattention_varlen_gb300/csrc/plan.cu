@@ -1,4 +1,4 @@
-// plan.cu -- device-side varlen tile scheduler and split-KV combine.
+// plan.cu -- device-side varlen tile scheduler.
 //
 // plan_kernel (one CTA) turns (cu_q, seq_lens, block_table) into the work list
 // the attention kernel walks, without a host round trip:
@@ -15,13 +15,14 @@
 //      head, with partial O and (max, sum) statistics in scratch);
 //   4. orders the items longest first (counting sort on the number of KV
 //      tiles) so that round-robin assignment to persistent CTAs balances;
-//   5. zero-fills the output rows of q tiles that see no key at all.
+//   5. zero-fills the output rows of q tiles that see no key at all, and
+//      zeroes the finished-split counter of every split unit (the decode
+//      kernel merges a unit's partials in the CTA that finishes it last).
 //
-// combine_kernel merges the split partials of a unit: with m_s the running
-// max (log2 units) and l_s the sum of a split, w_s = l_s * 2^(m_s - M),
-// M = max_s m_s, and out = sum_s w_s O_s / sum_s w_s (O_s already divided by
-// l_s). Splits that saw no key carry m = -inf, l = 0 and weigh nothing.
+// merge_kernel merges the split units of the prefill kernel's items (one per
+// unit, found at its split-0 item), after that kernel.
 #include "kernels.cuh"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace pattn {
@@ -287,18 +288,19 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
         const int k1 = static_cast<int>(static_cast<long long>(s + 1) * tiles / S);
         const int pos = atomicAdd(&hist[list][min(k1 - k0, kHistBuckets - 1)], p.n_heads_kv);
         for (int hk = 0; hk < p.n_heads_kv; ++hk) {
-          const int part = S >= 2 ? ws.seq_part[b] + (hk * S + s) * rows : -1;
-          dst[pos + hk] = make_int4(b, (hk << 16) | qt, (k0 << 16) | k1, part);
+          if (S >= 2)  // split s of the (b, hk) unit (q tile 0)
+            dst[pos + hk] = make_int4(b | (s << kSeqBits), hk << 16, (k0 << 16) | k1,
+                                      ws.seq_part[b] + (hk * S + s) * rows);
+          else
+            dst[pos + hk] = make_int4(b, (hk << 16) | qt, (k0 << 16) | k1, -1);
         }
       }
     }
-    // split units for the combine
+    // finished-split counters of the split units start at zero
     for (int b = threadIdx.x; b < B; b += kPlanThreads) {
       const int4 sp = ws.seq_plan[b];
       if (sp.z < 2) continue;
-      const int rows = ws.seq_info[b].y * G;
-      for (int hk = 0; hk < p.n_heads_kv; ++hk)
-        ws.units[sp.w + hk] = make_int4(b, hk, sp.z, ws.seq_part[b] + hk * sp.z * rows);
+      for (int hk = 0; hk < p.n_heads_kv; ++hk) ws.unit_cnt[sp.w + hk] = 0;
     }
   }
 
@@ -335,65 +337,31 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
-  const int n_units = p.hdr[kHdrUnits];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kPer = D / 32;  // elements per lane
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int4 un = p.units[u];
-    const int b = un.x, hk = un.y, S = un.z, base = un.w;
+__global__ void __launch_bounds__(256) merge_kernel(const AttnParams p) {
+  const int n_items = p.hdr[kHdrItems];
+  const int warp = threadIdx.x >> 5;
+  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
+    const int4 iv = p.items[idx];
+    if (iv.w < 0 || (iv.x >> kSeqBits) != 0) continue;  // one CTA per unit: its split 0
+    const int b = iv.x & kSeqMask;
     const int4 si = p.seq_info[b];
-    const int rows = si.y * p.group;
-    for (int r = warp; r < rows; r += 8) {
-      float M = -INFINITY;
-      for (int s = 0; s < S; ++s) M = fmaxf(M, p.part_ml[base + s * rows + r].x);
-      float acc[kPer];
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-      float den = 0.f;
-      if (M != -INFINITY) {
-        for (int s = 0; s < S; ++s) {
-          const float2 ml = p.part_ml[base + s * rows + r];
-          if (ml.y <= 0.f) continue;
-          const float w = ml.y * ex2(ml.x - M);
-          den += w;
-          const float* o = p.part_o + static_cast<size_t>(base + s * rows + r) * D + lane * kPer;
-#pragma unroll
-          for (int e = 0; e < kPer; e += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(o + e);
-            acc[e] += w * v.x;
-            acc[e + 1] += w * v.y;
-            acc[e + 2] += w * v.z;
-            acc[e + 3] += w * v.w;
-          }
-        }
-      }
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      const int tok = si.x + r / p.group;
-      const int h = hk * p.group + r % p.group;
-      __nv_bfloat16* dst = p.out + (static_cast<size_t>(tok) * p.n_heads_q + h) * D + lane * kPer;
-#pragma unroll
-      for (int e = 0; e < kPer; e += 2) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-        *reinterpret_cast<__nv_bfloat162*>(dst + e) = v;
-      }
-    }
+    const int4 sp = p.seq_plan[b];
+    merge_unit<D>(p, si.x, iv.y >> 16, sp.z, iv.w, si.y * p.group, warp, 8);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s) {
+  if (head_dim == 128)
+    merge_kernel<128><<<grid, 256, 0, s>>>(p);
+  else
+    merge_kernel<256><<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s) {
-  if (grid <= 0) return cudaSuccess;
-  if (p.head_dim == 128)
-    combine_kernel<128><<<grid, 256, 0, s>>>(p);
-  else
-    combine_kernel<256><<<grid, 256, 0, s>>>(p);
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
