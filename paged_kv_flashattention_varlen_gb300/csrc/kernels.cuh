@@ -12,7 +12,7 @@ constexpr int kBM = 128;            // packed query rows per tile (tokens x GQA 
 constexpr int kPage = 64;           // page size handled by the gather (rows per TMA box)
 constexpr int kThreads = 256;       // 8 warps: load, MMA, V tail fix, idle, 4 x softmax
 constexpr int kTmemCols = 512;
-constexpr int kHistBuckets = 2048;  // cost buckets of the longest-first order, per item list
+constexpr int kHistBuckets = 1024;  // cost buckets of the longest-first order, per item list
 constexpr int kDecRows = 16;        // packed query rows a swap-AB decode item holds
 constexpr int kDecBlockN = 128;     // keys per KV tile of the decode kernel
 constexpr int kMaxSplits = 64;

@@ -30,34 +30,6 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-// Block-wide exclusive scan of one int per thread; returns the block total.
-__device__ int block_exclusive_scan(int v, int* out_excl, int* warp_sums) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_sums[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = warp_sums[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    warp_sums[lane] = w;  // inclusive
-  }
-  __syncthreads();
-  const int before = warp ? warp_sums[warp - 1] : 0;
-  *out_excl = before + x - v;
-  const int total = warp_sums[31];
-  __syncthreads();
-  return total;
-}
-
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 // Units of at most kDecRows packed rows run on the swap-AB decode kernel.
@@ -82,28 +54,92 @@ __device__ __forceinline__ int qtile_blocks(const PlanParams& p, int ql, int L, 
   return qtile_kv_tiles(p, ql, L, qt) * (bn / kPage);
 }
 
-constexpr int kSmemSeqs = 4096;  // sequences whose q-tile prefix is kept in shared memory
+// Block-wide exclusive scan of two ints per thread; returns both block totals.
+__device__ int2 block_exclusive_scan2(int v0, int v1, int* e0, int* e1, int2* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x0 = v0, x1 = v1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y0 = __shfl_up_sync(0xffffffffu, x0, o);
+    const int y1 = __shfl_up_sync(0xffffffffu, x1, o);
+    if (lane >= o) {
+      x0 += y0;
+      x1 += y1;
+    }
+  }
+  if (lane == 31) warp_sums[warp] = make_int2(x0, x1);
+  __syncthreads();
+  if (warp == 0) {
+    int2 w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y0 = __shfl_up_sync(0xffffffffu, w.x, o);
+      const int y1 = __shfl_up_sync(0xffffffffu, w.y, o);
+      if (lane >= o) {
+        w.x += y0;
+        w.y += y1;
+      }
+    }
+    warp_sums[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  const int2 before = warp ? warp_sums[warp - 1] : make_int2(0, 0);
+  *e0 = before.x + x0 - v0;
+  *e1 = before.y + x1 - v1;
+  const int2 total = warp_sums[31];
+  __syncthreads();
+  return total;
+}
+
+// Work of all q tiles of a sequence in 64-key blocks, for the split heuristic
+// only: exact for short sequences, an arithmetic-series estimate for long ones.
+__device__ __forceinline__ unsigned long long seq_blocks(const PlanParams& p, int ql, int L, int nqt) {
+  if (nqt <= 8) {
+    unsigned long long t = 0;
+    for (int qt = 0; qt < nqt; ++qt) t += static_cast<unsigned long long>(qtile_blocks(p, ql, L, qt));
+    return t;
+  }
+  const int bn = is_decode(p, ql) ? kDecBlockN : p.block_n;
+  if (!p.causal) return static_cast<unsigned long long>(nqt) * cdiv(L, bn) * (bn / kPage);
+  // keys [0, L - ql + (qt + 1) T) for qt < nqt - 1, keys [0, L) for the last q tile
+  const long long T = p.tokens_per_tile;
+  const long long n1 = nqt - 1;
+  const long long keys = max(n1 * (static_cast<long long>(L) - ql) + T * n1 * (n1 + 1) / 2 + L, 0ll);
+  return static_cast<unsigned long long>(keys / kPage + static_cast<long long>(nqt) * (bn / kPage) / 2 + 1);
+}
+
+constexpr int kSmemSeqs = 4096;   // sequences whose q-tile prefix is kept in shared memory
+constexpr int kCacheSeqs = 1024;  // sequences whose plan is kept in shared memory
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams p) {
-  __shared__ int warp_sums[32];
+  __shared__ int2 warp_sums[32];
   __shared__ int hist[2][kHistBuckets];  // [0] prefill items, [1] decode items
   __shared__ int s_qt_prefix[kSmemSeqs];
+  __shared__ int4 s_seq[kCacheSeqs];     // x = first token, y = query length (-1 rejected), z = L, w = splits
+  __shared__ int s_part[kCacheSeqs];     // first partial row of the sequence's split units
   __shared__ int s_carry[4];
   __shared__ unsigned long long s_tiles;
   __shared__ int s_chunk;
-  __shared__ int s_total_items;
+  __shared__ int s_list_items[2];
   const Workspace& ws = p.ws;
   const int B = p.num_seqs;
   const int G = p.group;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto seq_at = [&](int b) -> int4 {
+    if (b < kCacheSeqs) return s_seq[b];
+    const int4 si = ws.seq_info[b];
+    return make_int4(si.x, si.y, si.z, ws.seq_plan[b].z);
+  };
+  auto part_at = [&](int b) -> int { return b < kCacheSeqs ? s_part[b] : ws.seq_part[b]; };
 
   if (threadIdx.x == 0) {
     s_tiles = 0ull;
     s_carry[0] = s_carry[1] = s_carry[2] = s_carry[3] = 0;
   }
+  for (int i = threadIdx.x; i < 2 * kHistBuckets; i += kPlanThreads) (&hist[0][0])[i] = 0;
   __syncthreads();
 
-  // ---- pass 1: lengths, KV prefix (contiguous cache), q tile prefix, total tiles
+  // ---- pass 1: lengths, KV prefix (contiguous cache), q tile prefix, total work
   unsigned long long my_tiles = 0;
   for (int base = 0; base < B; base += kPlanThreads) {
     const int b = base + threadIdx.x;
@@ -118,13 +154,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       if (!ok) atomicOr(ws.hdr + kHdrErr, kErrBadInput);
       if (ok) {
         nqt = cdiv(ql, p.tokens_per_tile);
-        for (int qt = 0; qt < nqt; ++qt)
-          my_tiles += static_cast<unsigned long long>(qtile_blocks(p, ql, L, qt));
+        my_tiles += seq_blocks(p, ql, L, nqt);
       }
     }
     int kv_excl, qt_excl;
-    const int kv_tot = block_exclusive_scan(b < B ? max(L, 0) : 0, &kv_excl, warp_sums);
-    const int qt_tot = block_exclusive_scan(nqt, &qt_excl, warp_sums);
+    const int2 tot = block_exclusive_scan2(b < B ? max(L, 0) : 0, nqt, &kv_excl, &qt_excl, warp_sums);
     if (b < B) {
       // contiguous cache: the sequence's rows must lie inside the K/V planes
       if (ok && !p.block_table &&
@@ -132,32 +166,43 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
         ok = false;
         atomicOr(ws.hdr + kHdrErr, kErrBadInput);
       }
-      ws.seq_info[b] = make_int4(q0, ok ? ql : -1, L, s_carry[0] + kv_excl);
+      const int4 si = make_int4(q0, ok ? ql : -1, L, s_carry[0] + kv_excl);
+      ws.seq_info[b] = si;
       ws.seq_plan[b] = make_int4(s_carry[1] + qt_excl, nqt, 1, 0);
       if (b < kSmemSeqs) s_qt_prefix[b] = s_carry[1] + qt_excl;
+      if (b < kCacheSeqs) s_seq[b] = make_int4(q0, si.y, L, 1);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      s_carry[0] += kv_tot;
-      s_carry[1] += qt_tot;
+      s_carry[0] += tot.x;
+      s_carry[1] += tot.y;
     }
     __syncthreads();
   }
   atomicAdd(&s_tiles, my_tiles * static_cast<unsigned long long>(p.n_heads_kv));
 
-  // ---- pass 1b: every live block-table entry must name a pool page (warp per sequence)
+  // ---- pass 1b: every live block-table entry must name a pool page (a warp per
+  // sequence, four independent loads per lane in flight)
   if (p.block_table) {
     for (int b = warp; b < B; b += kPlanThreads / 32) {
-      const int4 si = ws.seq_info[b];
-      if (si.y < 0) continue;
-      const int np = cdiv(si.z, kPage);
+      const int4 sq = seq_at(b);
+      if (sq.y < 0) continue;
+      const int np = cdiv(sq.z, kPage);
+      const int32_t* row = p.block_table + static_cast<size_t>(b) * p.bt_stride;
       bool bad = false;
-      for (int s = lane; s < np; s += 32) {
-        const int pg = p.block_table[static_cast<size_t>(b) * p.bt_stride + s];
-        bad |= pg < 0 || pg >= p.num_pages;
+      for (int s0 = 0; s0 < np; s0 += 128) {
+        int pg[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int s = s0 + u * 32 + lane;
+          pg[u] = s < np ? row[s] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) bad |= pg[u] < 0 || pg[u] >= p.num_pages;
       }
       if (__any_sync(0xffffffffu, bad) && lane == 0) {
         ws.seq_info[b].y = -1;
+        if (b < kCacheSeqs) s_seq[b].y = -1;
         atomicOr(ws.hdr + kHdrErr, kErrBadInput);
       }
     }
@@ -179,32 +224,38 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     const int b = base + threadIdx.x;
     int S = 1, rows = 0;
     if (b < B) {
-      const int4 si = ws.seq_info[b];
-      const int nqt = ws.seq_plan[b].y;
-      if (si.y > 0 && nqt == 1) {
-        const int tiles = qtile_kv_tiles(p, si.y, si.z, 0);
-        const int per_tile = qtile_blocks(p, si.y, si.z, 0) / max(tiles, 1);  // 64-key blocks
-        const int chunk_tiles = max(1, cdiv(chunk, max(per_tile, 1)));
+      const int4 sq = seq_at(b);
+      if (sq.y > 0 && cdiv(sq.y, p.tokens_per_tile) == 1) {
+        const int tiles = qtile_kv_tiles(p, sq.y, sq.z, 0);
+        const int per_tile = is_decode(p, sq.y) ? kDecBlockN / kPage : p.block_n / kPage;
+        const int chunk_tiles = max(1, cdiv(chunk, per_tile));
         if (tiles >= 2) S = min(min(cdiv(tiles, chunk_tiles), kMaxSplits), tiles);
-        rows = si.y * G;
+        rows = sq.y * G;
       }
     }
     const int part_rows = S >= 2 ? p.n_heads_kv * S * rows : 0;
     const int units = S >= 2 ? p.n_heads_kv : 0;
     int part_excl, unit_excl;
-    const int part_tot = block_exclusive_scan(part_rows, &part_excl, warp_sums);
-    const int unit_tot = block_exclusive_scan(units, &unit_excl, warp_sums);
+    const int2 tot = block_exclusive_scan2(part_rows, units, &part_excl, &unit_excl, warp_sums);
     if (b < B) {
       int4 sp = ws.seq_plan[b];
       sp.z = S;
       sp.w = s_carry[3] + unit_excl;
       ws.seq_plan[b] = sp;
       ws.seq_part[b] = s_carry[2] + part_excl;
+      if (b < kCacheSeqs) {
+        s_seq[b].w = S;
+        s_part[b] = s_carry[2] + part_excl;
+      }
+      // the finished-split counters of the unit's KV heads start at zero (a plan
+      // with more units than the workspace holds is rejected below)
+      if (S >= 2 && sp.w + p.n_heads_kv <= ws.max_units)
+        for (int hk = 0; hk < p.n_heads_kv; ++hk) ws.unit_cnt[sp.w + hk] = 0;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      s_carry[2] += part_tot;
-      s_carry[3] += unit_tot;
+      s_carry[2] += tot.x;
+      s_carry[3] += tot.y;
     }
     __syncthreads();
   }
@@ -222,67 +273,56 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     }
     return lo;
   };
+  auto qtile_first = [&](int b) { return b < kSmemSeqs ? s_qt_prefix[b] : ws.seq_plan[b].x; };
 
   // ---- pass 3: histogram of item costs (KV tiles per item), one per kernel
-  for (int i = threadIdx.x; i < 2 * kHistBuckets; i += kPlanThreads) (&hist[0][0])[i] = 0;
-  __syncthreads();
   if (!overflow) {
     for (int gq = threadIdx.x; gq < total_qt; gq += kPlanThreads) {
       const int b = seq_of_qtile(gq);
-      const int4 sp = ws.seq_plan[b];
-      const int4 si = ws.seq_info[b];
-      if (si.y <= 0) continue;
-      const int tiles = qtile_kv_tiles(p, si.y, si.z, gq - sp.x);
+      const int4 sq = seq_at(b);
+      if (sq.y <= 0) continue;
+      const int tiles = qtile_kv_tiles(p, sq.y, sq.z, gq - qtile_first(b));
       if (tiles == 0) continue;
-      const int list = is_decode(p, si.y) ? 1 : 0;
-      for (int s = 0; s < sp.z; ++s) {
-        const int k0 = static_cast<int>(static_cast<long long>(s) * tiles / sp.z);
-        const int k1 = static_cast<int>(static_cast<long long>(s + 1) * tiles / sp.z);
+      const int list = is_decode(p, sq.y) ? 1 : 0;
+      for (int s = 0; s < sq.w; ++s) {
+        const int k0 = static_cast<int>(static_cast<long long>(s) * tiles / sq.w);
+        const int k1 = static_cast<int>(static_cast<long long>(s + 1) * tiles / sq.w);
         atomicAdd(&hist[list][min(k1 - k0, kHistBuckets - 1)], p.n_heads_kv);
       }
     }
   }
   __syncthreads();
   // exclusive scan of each list from the most expensive bucket down
-  __shared__ int s_list_items[2];
-  for (int list = 0; list < 2; ++list) {
-    constexpr int kPer = kHistBuckets / kPlanThreads;
-    int local[kPer];
-    int sum = 0;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      local[k] = hist[list][kHistBuckets - 1 - (threadIdx.x * kPer + k)];
-      sum += local[k];
+  {
+    static_assert(kHistBuckets == kPlanThreads, "one bucket per thread");
+    const int c = kHistBuckets - 1 - threadIdx.x;
+    int e0, e1;
+    const int2 tot = block_exclusive_scan2(hist[0][c], hist[1][c], &e0, &e1, warp_sums);
+    hist[0][c] = e0;
+    hist[1][c] = e1;
+    if (threadIdx.x == 0) {
+      s_list_items[0] = tot.x;
+      s_list_items[1] = tot.y;
     }
-    int excl;
-    const int tot = block_exclusive_scan(sum, &excl, warp_sums);
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      hist[list][kHistBuckets - 1 - (threadIdx.x * kPer + k)] = excl;
-      excl += local[k];
-    }
-    if (threadIdx.x == 0) s_list_items[list] = tot;
     __syncthreads();
   }
-  if (threadIdx.x == 0) s_total_items = max(s_list_items[0], s_list_items[1]);
-  __syncthreads();
-  const bool item_overflow = s_total_items > ws.max_items;
+  const bool item_overflow = s_list_items[0] > ws.max_items || s_list_items[1] > ws.max_items;
   const bool bad_plan = overflow || item_overflow;
 
   // ---- pass 4: emit items, longest first
   if (!bad_plan) {
     for (int gq = threadIdx.x; gq < total_qt; gq += kPlanThreads) {
       const int b = seq_of_qtile(gq);
-      const int4 sp = ws.seq_plan[b];
-      const int4 si = ws.seq_info[b];
-      if (si.y <= 0) continue;
-      const int qt = gq - sp.x;
-      const int tiles = qtile_kv_tiles(p, si.y, si.z, qt);
+      const int4 sq = seq_at(b);
+      if (sq.y <= 0) continue;
+      const int qt = gq - qtile_first(b);
+      const int tiles = qtile_kv_tiles(p, sq.y, sq.z, qt);
       if (tiles == 0) continue;
-      const int S = sp.z;
-      const int rows = si.y * G;
-      const int list = is_decode(p, si.y) ? 1 : 0;
+      const int S = sq.w;
+      const int rows = sq.y * G;
+      const int list = is_decode(p, sq.y) ? 1 : 0;
       int4* dst = list ? ws.dec_items : ws.items;
+      const int part0 = S >= 2 ? part_at(b) : 0;
       for (int s = 0; s < S; ++s) {
         const int k0 = static_cast<int>(static_cast<long long>(s) * tiles / S);
         const int k1 = static_cast<int>(static_cast<long long>(s + 1) * tiles / S);
@@ -290,17 +330,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
         for (int hk = 0; hk < p.n_heads_kv; ++hk) {
           if (S >= 2)  // split s of the (b, hk) unit (q tile 0)
             dst[pos + hk] = make_int4(b | (s << kSeqBits), hk << 16, (k0 << 16) | k1,
-                                      ws.seq_part[b] + (hk * S + s) * rows);
+                                      part0 + (hk * S + s) * rows);
           else
             dst[pos + hk] = make_int4(b, (hk << 16) | qt, (k0 << 16) | k1, -1);
         }
       }
-    }
-    // finished-split counters of the split units start at zero
-    for (int b = threadIdx.x; b < B; b += kPlanThreads) {
-      const int4 sp = ws.seq_plan[b];
-      if (sp.z < 2) continue;
-      for (int hk = 0; hk < p.n_heads_kv; ++hk) ws.unit_cnt[sp.w + hk] = 0;
     }
   }
 
@@ -310,14 +344,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   for (int b = threadIdx.x; b < B; b += kPlanThreads) {
     const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
     if (!(q0 >= 0 && q1 >= q0 && q1 <= p.total_q) || q1 == q0) continue;
-    const int4 si = ws.seq_info[b];
+    const int4 sq = seq_at(b);
     int z1 = q0;  // rows [q0, z1) get zeros
-    if (si.y < 0 || bad_plan) {
+    if (sq.y < 0 || bad_plan) {
       z1 = q1;
     } else {
-      const int nqt = ws.seq_plan[b].y;
-      for (int qt = 0; qt < nqt && qtile_kv_tiles(p, si.y, si.z, qt) == 0; ++qt)
-        z1 = q0 + min(si.y, (qt + 1) * p.tokens_per_tile);
+      const int nqt = cdiv(sq.y, p.tokens_per_tile);
+      for (int qt = 0; qt < nqt && qtile_kv_tiles(p, sq.y, sq.z, qt) == 0; ++qt)
+        z1 = q0 + min(sq.y, (qt + 1) * p.tokens_per_tile);
     }
     if (z1 > q0) {
       const size_t row = static_cast<size_t>(p.n_heads_q) * p.head_dim;
