@@ -336,23 +336,28 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     rec = take_events(st);
     cudaEventRecord(rec.ev[0], stream);
   }
+  // The plan is launched in stream order (it rewrites the workspace that the
+  // previous call's kernels read); each later kernel is a dependent launch that
+  // sets itself up while its predecessor finishes and waits for it on the device.
+  // Profiling events between the launches turn that overlap off.
+  const bool dep = !prof;
   cudaError_t e = launch_plan(pp, stream);
   if (e != cudaSuccess) return PATTN_ERR_CUDA;
   if (prof) cudaEventRecord(rec.ev[1], stream);
   if (dec_enabled) {
-    e = launch_decode(dp, tq_dec, tkv, d, st.sms, stream);
+    e = launch_decode(dp, tq_dec, tkv, d, st.sms, stream, dep);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (prof) cudaEventRecord(rec.ev[2], stream);
   if (run_prefill) {
-    e = launch_attention(ap, tq, tkv, d, st.sms, stream);
+    e = launch_attention(ap, tq, tkv, d, st.sms, stream, dep);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (prof) cudaEventRecord(rec.ev[3], stream);
   if (run_prefill) {
     // split units of the prefill kernel (single-q-tile units of more than
     // kDecRows rows) are merged by a separate pass; the decode kernel merges its own
-    e = launch_merge(ap, d, std::min(ws.max_items, 2 * st.sms), stream);
+    e = launch_merge(ap, d, std::min(ws.max_items, 2 * st.sms), stream, dep);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (prof) {

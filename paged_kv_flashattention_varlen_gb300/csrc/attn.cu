@@ -101,6 +101,39 @@ __device__ __forceinline__ Item decode_item(int4 v) {
   return it;
 }
 
+// One row's probabilities for KH keys: p_i = 2^(S_i c - m_ref) as bf16 pairs in
+// pk, returning the fp32 sum of the p_i. With kMasked only the first nv keys
+// count (the others give 0 whatever their score); full tiles take the unmasked
+// body, so they carry no per-key compare. Scale and sum use packed fp32x2 ops.
+template <int KH, bool kMasked>
+__device__ __forceinline__ float exp_row(const uint32_t (&sr)[KH / 32][32], float c, float m_ref,
+                                         int nv, uint32_t (&pk)[KH / 2]) {
+  const float2 c2 = make_float2(c, c);
+  const float2 nm2 = make_float2(-m_ref, -m_ref);
+  float2 acc[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) acc[u] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < KH / 32; ++j) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float2 x =
+          __ffma2_rn(make_float2(__uint_as_float(sr[j][i]), __uint_as_float(sr[j][i + 1])), c2, nm2);
+      float p0 = ex2(x.x);
+      float p1 = ex2(x.y);
+      if constexpr (kMasked) {
+        p0 = j * 32 + i < nv ? p0 : 0.f;
+        p1 = j * 32 + i + 1 < nv ? p1 : 0.f;
+      }
+      acc[(i >> 1) & 3] = __fadd2_rn(acc[(i >> 1) & 3], make_float2(p0, p1));
+      __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+      pk[(j * 32 + i) >> 1] = *reinterpret_cast<uint32_t*>(&hh);
+    }
+  }
+  const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  return a.x + a.y;
+}
+
 template <int D, int BN>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
@@ -161,6 +194,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();    // the plan (and whatever ran before) is complete from here on
+  grid_dep_launch();  // the merge pass may take SMs as this grid's CTAs leave
 
   const int n_items = p.hdr[kHdrItems];
   const int G = p.group;
@@ -432,6 +467,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
 
         const int key0 = kt * BN + h * KH;
         const bool full_tile = key0 + KH <= lim;
+        const int nv = lim - key0;  // visible keys of this row in the chunk (any sign)
         uint32_t pk[KH / 2];
         if (warp_live) {
           float acc[8];
@@ -447,7 +483,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             for (int j = 0; j < KH / 32; ++j)
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                if (key0 + j * 32 + i < lim) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
+                if (j * 32 + i < nv) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
           }
           const float mx = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
                                  fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
@@ -481,24 +517,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             }
           }
           const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-          float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < KH / 32; ++j) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int key = key0 + j * 32 + i;
-              float p0 = ex2(fmaf(__uint_as_float(sr[j][i]), c, -m_ref));
-              float p1 = ex2(fmaf(__uint_as_float(sr[j][i + 1]), c, -m_ref));
-              if (!full_tile) {
-                p0 = key < lim ? p0 : 0.f;
-                p1 = key + 1 < lim ? p1 : 0.f;
-              }
-              sum[(i >> 1) & 3] += p0 + p1;
-              __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-              pk[(j * 32 + i) >> 1] = *reinterpret_cast<uint32_t*>(&hh);
-            }
-          }
-          l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+          if (full_tile)
+            l += exp_row<KH, false>(sr, c, m_ref, KH, pk);
+          else
+            l += exp_row<KH, true>(sr, c, m_ref, lim - key0, pk);
         }
         // P buffer pb was last read by the PV of tile n - kPBufs
         if (n >= static_cast<uint32_t>(C::kPBufs)) {
@@ -620,6 +642,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
 
         const int key0 = kt * BN + h * KH;
         const bool full_tile = key0 + KH <= lim;
+        const int nv = lim - key0;  // visible keys of this row in the chunk (any sign)
         float mx = -INFINITY;
         if (warp_live) {
           float acc[8];
@@ -635,7 +658,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             for (int j = 0; j < KH / 32; ++j)
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                if (key0 + j * 32 + i < lim) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
+                if (j * 32 + i < nv) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
           }
           mx = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
                      fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
@@ -650,24 +673,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         uint32_t pk[KH / 2];
         float l_tile = 0.f;
         auto exps = [&](float m_ref) {
-          float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int j = 0; j < KH / 32; ++j) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int key = key0 + j * 32 + i;
-              float p0 = ex2(fmaf(__uint_as_float(sr[j][i]), c, -m_ref));
-              float p1 = ex2(fmaf(__uint_as_float(sr[j][i + 1]), c, -m_ref));
-              if (!full_tile) {
-                p0 = key < lim ? p0 : 0.f;
-                p1 = key + 1 < lim ? p1 : 0.f;
-              }
-              sum[(i >> 1) & 3] += p0 + p1;
-              __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-              pk[(j * 32 + i) >> 1] = *reinterpret_cast<uint32_t*>(&hh);
-            }
-          }
-          l_tile = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+          l_tile = full_tile ? exp_row<KH, false>(sr, c, m_ref, KH, pk)
+                             : exp_row<KH, true>(sr, c, m_ref, lim - key0, pk);
         };
         const bool speculate = warp_live && !first && m_used != -INFINITY;
         if (speculate) exps(m_used);
@@ -803,12 +810,12 @@ cudaError_t attention_set_attributes() {
 }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
-                             int head_dim, int grid, cudaStream_t s) {
+                             int head_dim, int grid, cudaStream_t s, bool dependent) {
   if (head_dim == 128)
-    attn_kernel<128, 128><<<grid, kAttnThreads, Cfg<128, 128>::kSmem, s>>>(tq, tkv, p);
-  else
-    attn_kernel<256, 64><<<grid, kAttnThreads, Cfg<256, 64>::kSmem, s>>>(tq, tkv, p);
-  return cudaGetLastError();
+    return launch_kernel(attn_kernel<128, 128>, grid, kAttnThreads, Cfg<128, 128>::kSmem, s,
+                         dependent, tq, tkv, p);
+  return launch_kernel(attn_kernel<256, 64>, grid, kAttnThreads, Cfg<256, 64>::kSmem, s, dependent,
+                       tq, tkv, p);
 }
 
 }  // namespace pattn

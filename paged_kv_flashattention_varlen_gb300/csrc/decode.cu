@@ -299,6 +299,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();    // the plan is complete from here on
+  grid_dep_launch();  // the prefill kernel may take SMs as this grid's CTAs leave
 
   const int n_items = p.hdr[kHdrDecItems];
   const int G = p.group;
@@ -551,12 +553,10 @@ cudaError_t decode_set_attributes() {
 }
 
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
-                          int head_dim, int grid, cudaStream_t s) {
+                          int head_dim, int grid, cudaStream_t s, bool dependent) {
   if (head_dim == 128)
-    decode_kernel<128><<<grid, kThreads, DCfg<128>::kSmem, s>>>(tq, tkv, p);
-  else
-    decode_kernel<256><<<grid, kThreads, DCfg<256>::kSmem, s>>>(tq, tkv, p);
-  return cudaGetLastError();
+    return launch_kernel(decode_kernel<128>, grid, kThreads, DCfg<128>::kSmem, s, dependent, tq, tkv, p);
+  return launch_kernel(decode_kernel<256>, grid, kThreads, DCfg<256>::kSmem, s, dependent, tq, tkv, p);
 }
 
 }  // namespace pattn

@@ -89,12 +89,30 @@ struct AttnParams {
 
 
 // Launchers (defined in the .cu files; return the launch error).
+// Kernel launch; with `dependent` the grid may begin (up to its grid_dep_wait)
+// while the previous grid in the stream finishes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, bool dependent, const Args&... args) {
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = &attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
-                             int head_dim, int grid, cudaStream_t s);
-cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s);
+                             int head_dim, int grid, cudaStream_t s, bool dependent);
+cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
-                          int head_dim, int grid, cudaStream_t s);
+                          int head_dim, int grid, cudaStream_t s, bool dependent);
 size_t decode_smem_bytes(int head_dim);
 cudaError_t decode_set_attributes();
 int attention_block_n(int head_dim);

@@ -132,6 +132,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   };
   auto part_at = [&](int b) -> int { return b < kCacheSeqs ? s_part[b] : ws.seq_part[b]; };
 
+  // The attention kernels launched after this one may set themselves up now;
+  // they read nothing of the plan before the plan grid has completed.
+  grid_dep_launch();
   if (threadIdx.x == 0) {
     s_tiles = 0ull;
     s_carry[0] = s_carry[1] = s_carry[2] = s_carry[3] = 0;
@@ -372,6 +375,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
 
 template <int D>
 __global__ void __launch_bounds__(256) merge_kernel(const AttnParams p) {
+  grid_dep_wait();  // every split of the prefill kernel is written
   const int n_items = p.hdr[kHdrItems];
   const int warp = threadIdx.x >> 5;
   for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
@@ -386,12 +390,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const AttnParams p) {
 
 }  // namespace
 
-cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s) {
-  if (head_dim == 128)
-    merge_kernel<128><<<grid, 256, 0, s>>>(p);
-  else
-    merge_kernel<256><<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s, bool dependent) {
+  if (head_dim == 128) return launch_kernel(merge_kernel<128>, grid, 256, 0, s, dependent, p);
+  return launch_kernel(merge_kernel<256>, grid, 256, 0, s, dependent, p);
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {

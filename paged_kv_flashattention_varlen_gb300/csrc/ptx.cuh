@@ -123,6 +123,16 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A grid launched with programmatic stream serialisation may start while the
+// grid before it in the stream still runs. grid_dep_wait blocks until that grid
+// has completed and its memory writes are visible (it returns at once for a grid
+// launched the ordinary way); grid_dep_launch lets the next such grid start.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (UMMA, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
