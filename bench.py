@@ -36,7 +36,7 @@ PREFILL = 3
 NOMINAL_HBM_GBS = 7900.0
 NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["attn.cu", "decode.cu", "ptx.cuh", "kernels.cuh"]
+KERNEL_SOURCES = ["attn.cu", "decode.cu", "ptx.cuh", "kernels.cuh", "merge.cuh"]
 
 
 def parse():

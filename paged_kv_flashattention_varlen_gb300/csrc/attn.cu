@@ -1,33 +1,37 @@
-// attn.cu -- fused paged-KV attention for sm_103a (tcgen05 + TMA).
+// attn.cu -- fused paged-KV attention for sm_103a (tcgen05 + TMA): the prefill
+// kernel, for work units of more than 16 packed query rows.
 //
 // One persistent CTA per SM walks the planned work list (longest first,
 // round robin over CTAs). A work item is (sequence, kv head, q tile, KV tile
-// range). For each item:
+// range). Warp roles:
 //
-//   * two load warps (Q and K; V) TMA-load the GQA-packed Q tile: the G query heads of one
-//     KV head for T = 128 / G tokens, as 128 rows of 128-byte-swizzled shared
-//     memory (the GQA-packed Q tensor map of the trtllm-gen paged decode
-//     manifest: dims [D, group, kv head, token]); then, per KV tile of BN keys,
-//     gathers the K and V rows page by page through one tensor map over the
-//     whole pool, [D, 64 rows, Hkv, 2 x pages] (the manifest's K and V tensor
+//   * warps 0 and 3 TMA-load the GQA-packed Q tile (the G query heads of one KV
+//     head for T = 128 / G tokens, as 128 rows of 128-byte-swizzled shared
+//     memory: the GQA-packed Q tensor map of the trtllm-gen paged decode
+//     manifest, dims [D, group, kv head, token]) and, per KV tile of BN keys,
+//     the K (warp 0) and V (warp 3) rows page by page through one tensor map
+//     over the whole pool, [D, 64 rows, Hkv, 2 x pages] (the manifest's K and V
 //     maps), each page read once per KV head for all G query heads;
-//   * the MMA thread issues S = Q K^T (tcgen05.mma kind::f16, M = 128,
-//     N = BN, K = D) into one of two TMEM S buffers, then O += P V (M = 128,
-//     N = D, K = BN) with P from TMEM and V read MN-major from shared memory;
-//     commits signal
-//     mbarriers (the SM100MHA2Q "UMMA0" / "UMMA1" accumulators of the
-//     FlashAttention-4 doc);
-//   * two softmax warpgroups share the 128 query rows, one row per thread in
-//     each, and split the keys of every tile between them (exchanging the
-//     partial row max once per tile): each reads its half of the S row from
-//     TMEM, masks keys past the end or (causal) past its position only on
-//     tiles that need it, keeps the running max m and sum l in log2 units
-//     (exp2 with the scale folded into log2 e, as the manifest's pack scalar
-//     does), rescales the O row in TMEM only when the max grew by more than
-//     2^8 (exact: O and l share the stale max), and writes P as bf16 pairs
-//     into TMEM (two buffers), where the PV MMA reads its A operand;
-//   * the tail warp zeroes V rows past the sequence end in the last tile, so
-//     that NaN or garbage there cannot reach O through 0 * NaN.
+//   * warp 1 issues S = Q K^T (tcgen05.mma kind::f16, M = 128, N = BN, K = D)
+//     from one thread, with Q from TMEM (D = 128) or shared memory (D = 256);
+//   * warp 2 zeroes V rows past the sequence end (so that NaN or garbage there
+//     cannot reach O through 0 * NaN) and issues O += P V (M = 128, N = D,
+//     K = BN) with P from TMEM and V read MN-major from shared memory. QK and
+//     PV come from different threads so that each stream's waits overlap the
+//     other's MMAs; commits signal mbarriers (the SM100MHA2Q "UMMA0" / "UMMA1"
+//     accumulators of the FlashAttention-4 doc);
+//   * warps 4-11 are two softmax warpgroups over the same 128 query rows, one
+//     row per thread in each, splitting the keys of every tile between them.
+//     Each reads its half of the S row from TMEM, masks keys past the end or
+//     (causal) past its position only on tiles that need it, keeps the running
+//     max m and sum l in log2 units (exp2 with the scale folded into log2 e, as
+//     the manifest's pack scalar does), rescales O in TMEM only when the max grew
+//     by more than 2^8 (exact: O and l share the stale max), and writes P as
+//     bf16 pairs into TMEM, where the PV MMA reads its A operand. D = 128: each
+//     warpgroup has its own O and running max (merged once per item), and
+//     copies the next item's Q into TMEM as soon as the current item's last S
+//     has been read. D = 256: one shared O; the partial row max is exchanged
+//     once per tile.
 //
 // At the end of an item the softmax warps divide by l and store bf16 rows, or
 // (split items) write the normalised partial O and (m, l); merge_kernel then
@@ -77,9 +81,9 @@ struct Cfg {
 
 // mbarrier slots
 enum Bar {
-  kQFull = 0, kQEmpty, kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2, kVFull0, kVFull1, kVReady0,
-  kVReady1, kVEmpty0, kVEmpty1, kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1,
-  kPFull2, kPFull3, kPVDone0, kPVDone1, kDrain, kXMax0, kXMax1, kXSum, kQTReady, kQTFree, kNumBars
+  kQFull = 0, kQEmpty, kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2, kVFull0, kVFull1,
+  kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPVDone0, kPVDone1, kDrain, kDrainPV, kXMax0,
+  kXMax1, kXSum, kQTReady, kQTFree, kNumBars
 };
 static_assert(kNumBars * 8 <= 256, "mbarrier area");
 constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
@@ -171,16 +175,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kVFull0 + s), 1);
-      mbar_init(bar(kVReady0 + s), 1);
-      mbar_init(bar(kVEmpty0 + s), 1);
       mbar_init(bar(kSFull0 + s), 1);
       mbar_init(bar(kSFree0 + s), kSoftmaxWarps);
       mbar_init(bar(kXMax0 + s), kSoftmaxWarps);
     }
-    // P buffer b, key half h: p_full[2 * b + h], one arrival per warp of warpgroup h
-    for (int s = 0; s < 4; ++s) mbar_init(bar(kPFull0 + s), kSoftmaxWarps / 2);
+    // P buffer b: p_full[b], one arrival per softmax warp (both key halves written).
+    // pv_done[t & 1]: the PV of tile t has completed, which also frees V stage t & 1.
+    for (int s = 0; s < 2; ++s) mbar_init(bar(kPFull0 + s), kSoftmaxWarps);
     for (int s = 0; s < 2; ++s) mbar_init(bar(kPVDone0 + s), 1);
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kDrainPV), 1);
     mbar_init(bar(kXSum), kSoftmaxWarps);
     mbar_init_fence();
     tma_prefetch_desc(&tmap_q);
@@ -209,7 +213,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     const int kind = warp == 0 ? 0 : 1;
     const uint32_t stages = kind ? C::kVStages : C::kKStages;
     const int full = kind ? kVFull0 : kKFull0;
-    const int empty = kind ? kVEmpty0 : kKEmpty0;
+    const int empty = kind ? kPVDone0 : kKEmpty0;  // a V stage is free once its PV is done
     const uint32_t ring = kind ? sV : sK;
     const unsigned fullmask = 0xffffffffu;
     uint32_t n = 0, itl = 0;
@@ -295,52 +299,29 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA warp
+    // ------------------------------------------------------------ QK MMA warp
+    // S = Q K^T for every tile, issued by one thread. The PV MMAs come from warp 2:
+    // the two streams touch disjoint TMEM (S, Q / P, O) and feed the tensor pipe
+    // independently, so that neither one's waits leave the pipe idle.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
       // operand descriptors built once; each MMA adds a compile-time offset
       const SmemDesc dq = sw128_desc_split(sQ, 16, 1024);
       const SmemDesc dk = sw128_desc_split(sK, 16, 1024);
-      const SmemDesc dv = sw128_desc_split(sV, BN * 128, 1024);
       uint32_t n = 0, itl = 0;
       bool ok = true;
-      auto issue_pv = [&](uint32_t m, bool first) -> bool {
-        const uint32_t pb = m % C::kPBufs, pu = m / C::kPBufs;
-        if (!wait_one(bar(kVReady0 + (m & 1u)), (m >> 1) & 1u, ctl)) return false;
-        const uint32_t v_lo = desc_lo_at(dv, (m & 1u) * C::kKVStage);
-        const uint32_t a0 = tmem + C::kColP + pb * C::kPCols;
-        // the key halves in a fixed order, each as soon as its warpgroup's P is in
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!wait_one(bar(kPFull0 + 2 * pb + hh), pu & 1u, ctl)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = hh * (BN / 32); kk < (hh + 1) * (BN / 32); ++kk) {
-            const uint32_t b_lo = v_lo + ((kk * (16 * 128)) >> 4);
-            if constexpr (C::kSplitO) {
-              // key half hh accumulates into its own O (columns hh * D ...)
-              umma_f16_ts(tmem + C::kColO + hh * D, a0 + kk * 8, b_lo, dv.hi, idesc_pv,
-                          (first && kk == hh * (BN / 32)) ? 0u : 1u);
-            } else {
-              umma_f16_ts(tmem + C::kColO, a0 + kk * 8, b_lo, dv.hi, idesc_pv,
-                          (first && kk == 0) ? 0u : 1u);
-            }
-          }
-        }
-        umma_commit(bar(kVEmpty0 + (m & 1u)));
-        umma_commit(bar(kPVDone0 + pb));
-        return true;
-      };
+      int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
-        const Item it = decode_item(p.items[idx]);
+        const Item it = decode_item(iv_next);
+        if (idx + static_cast<int>(gridDim.x) < n_items) iv_next = p.items[idx + gridDim.x];
         if (!(ok = wait_one(bar(C::kQTmem ? kQTReady : kQFull), itl & 1u, ctl))) break;
         tc_fence_after();
         for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
           const uint32_t s = n % C::kSBufs, su = n / C::kSBufs;
           const uint32_t ks = n % C::kKStages;
-          if (!(ok = wait_one(bar(kKFull0 + ks), (n / C::kKStages) & 1u, ctl))) break;
-          if (!(ok = wait_one(bar(kSFree0 + s), (su & 1u) ^ 1u, ctl))) break;
+          if (!(ok = wait_two(bar(kKFull0 + ks), (n / C::kKStages) & 1u, bar(kSFree0 + s), (su & 1u) ^ 1u,
+                              ctl)))
+            break;
           tc_fence_after();
           const uint32_t k_lo = desc_lo_at(dk, ks * C::kKVStage);
 #pragma unroll
@@ -356,11 +337,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           }
           umma_commit(bar(kKEmpty0 + ks));
           umma_commit(bar(kSFull0 + s));
-          if (kt > it.kt0 && !(ok = issue_pv(n - 1, kt - 1 == it.kt0))) break;
+          if (kt + 1 == it.kt1) umma_commit(bar(C::kQTmem ? kQTFree : kQEmpty));  // item's last QK
         }
-        if (!ok) break;
-        umma_commit(bar(C::kQTmem ? kQTFree : kQEmpty));
-        if (!(ok = issue_pv(n - 1, it.kt1 - 1 == it.kt0))) break;
       }
       // Drain: all UMMAs issued by this thread complete before TMEM is freed.
       umma_commit(bar(kDrain));
@@ -368,19 +346,28 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     }
     __syncwarp();
   } else if (warp == 2) {
-    // ------------------------------------------------------------ V tail warp
+    // ------------------------------------------------------------ V tail + PV MMA warp
+    // Zeroes the V rows past the sequence end in a stage (whole 128-byte rows, so
+    // the swizzle does not matter), then one thread issues O += P V for the tile.
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
+    const SmemDesc dv = sw128_desc_split(sV, BN * 128, 1024);
+    const unsigned fullmask = 0xffffffffu;
     uint32_t n = 0;
     bool ok = true;
+    int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+    int L_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask].z : 0;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-      const Item it = decode_item(p.items[idx]);
-      const int L = p.seq_info[it.b].z;
+      const Item it = decode_item(iv_next);
+      const int L = L_next;
+      if (idx + static_cast<int>(gridDim.x) < n_items) {
+        iv_next = p.items[idx + gridDim.x];
+        L_next = p.seq_info[iv_next.x & kSeqMask].z;
+      }
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
         const uint32_t s = n & 1u;
         if (!(ok = wait_warp(bar(kVFull0 + s), (n >> 1) & 1u, ctl))) break;
         const int live = L - kt * BN;
         if (live < BN) {
-          // rows [live, BN) of every 64-column block: whole 128-byte rows, so the
-          // swizzle does not matter
           uint8_t* v0 = smem + C::kOffV + s * C::kKVStage;
           const int dead = BN - live;
           const int chunks = dead * 8;  // 16-byte chunks per block
@@ -391,9 +378,39 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kVReady0 + s));
+        if (lane == 0) {
+          const uint32_t pb = n % C::kPBufs, pu = n / C::kPBufs;
+          ok = wait_one(bar(kPFull0 + pb), pu & 1u, ctl);
+          if (ok) {
+            tc_fence_after();
+            const bool first = kt == it.kt0;
+            const uint32_t v_lo = desc_lo_at(dv, s * C::kKVStage);
+            const uint32_t a0 = tmem + C::kColP + pb * C::kPCols;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint32_t b_lo = v_lo + ((kk * (16 * 128)) >> 4);
+              if constexpr (C::kSplitO) {
+                // key half hh accumulates into its own O (columns hh * D ...)
+                const int hh = kk / (BN / 32);
+                umma_f16_ts(tmem + C::kColO + hh * D, a0 + kk * 8, b_lo, dv.hi, idesc_pv,
+                            (first && kk == hh * (BN / 32)) ? 0u : 1u);
+              } else {
+                umma_f16_ts(tmem + C::kColO, a0 + kk * 8, b_lo, dv.hi, idesc_pv,
+                            (first && kk == 0) ? 0u : 1u);
+              }
+            }
+            umma_commit(bar(kPVDone0 + s));  // PV of tile n done; V stage s free
+          }
+        }
+        ok = __shfl_sync(fullmask, ok, 0);
+        if (!ok) break;
       }
     }
+    if (lane == 0) {
+      umma_commit(bar(kDrainPV));
+      wait_one(bar(kDrainPV), 0, ctl);
+    }
+    __syncwarp();
   } else if (warp >= 4) {
     if constexpr (C::kSplitO) {
     // ------------------------------------------------------------ softmax, D = 128
@@ -410,42 +427,53 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     const int t_local = r / G;
     const int g = r - t_local * G;
     const float c = p.scale_log2;
+    // Q tile of the j-th item of this CTA -> TMEM: this thread's row, this
+    // warpgroup's 64 columns of d, once the TMA landed it and the QK MMAs of
+    // item j - 1 are done.
+    auto copy_q = [&](uint32_t j) -> bool {
+      if (!wait_warp(bar(kQFull), j & 1u, ctl)) return false;
+      if (!wait_warp(bar(kQTFree), (j & 1u) ^ 1u, ctl)) return false;
+      tc_fence_after();
+      const uint8_t* qrow = smem + C::kOffQ + h * (kBM * 128) + r * 128;
+      uint32_t qv[32];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 v4 = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) << 4));
+        qv[ch * 4] = v4.x;
+        qv[ch * 4 + 1] = v4.y;
+        qv[ch * 4 + 2] = v4.z;
+        qv[ch * 4 + 3] = v4.w;
+      }
+      tmem_st32(tmem + lane_base + C::kColQ + h * 32, qv);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(kQTReady));
+        mbar_arrive(bar(kQEmpty));
+      }
+      return true;
+    };
     uint32_t n = 0, itl = 0;
     bool ok = true;
+    // The next item's descriptor and sequence are loaded one item ahead, and its
+    // Q is copied into TMEM as soon as the last S tile of the current item has
+    // been read (the QK MMAs of the current item are then done), so that the
+    // next item's first QK overlaps this item's last softmax tile and epilogue.
+    int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+    int4 si_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
+    if (blockIdx.x < n_items) ok = copy_q(0);
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
-      const Item it = decode_item(p.items[idx]);
-      const int4 si = p.seq_info[it.b];
+      const Item it = decode_item(iv_next);
+      const int4 si = si_next;
+      const bool has_next = idx + static_cast<int>(gridDim.x) < n_items;
+      if (has_next) iv_next = p.items[idx + gridDim.x];
       const int q0 = si.x, ql = si.y, L = si.z;
       const int tok = it.qt * T + t_local;
       const bool valid = (t_local < T) && (tok < ql);
       int lim = 0;  // keys [0, lim) visible to this row
       if (valid) lim = p.causal ? min(L, L - ql + tok + 1) : L;
       const bool warp_live = __any_sync(0xffffffffu, valid) != 0;
-      {
-        // Q tile -> TMEM: this thread's row, this warpgroup's 64 columns of d,
-        // once the TMA landed it and the previous item's QK MMAs are done
-        if (!(ok = wait_warp(bar(kQFull), itl & 1u, ctl))) break;
-        if (!(ok = wait_warp(bar(kQTFree), (itl & 1u) ^ 1u, ctl))) break;
-        tc_fence_after();
-        const uint8_t* qrow = smem + C::kOffQ + h * (kBM * 128) + r * 128;
-        uint32_t qv[32];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 v4 = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) << 4));
-          qv[ch * 4] = v4.x;
-          qv[ch * 4 + 1] = v4.y;
-          qv[ch * 4 + 2] = v4.z;
-          qv[ch * 4 + 3] = v4.w;
-        }
-        tmem_st32(tmem + lane_base + C::kColQ + h * 32, qv);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(kQTReady));
-          mbar_arrive(bar(kQEmpty));
-        }
-      }
       float m_used = -INFINITY, l = 0.f;
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
         const uint32_t pb = n % C::kPBufs;
@@ -464,6 +492,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kSFree0));
+        if (kt + 1 == it.kt1 && has_next) {
+          if (!(ok = copy_q(itl + 1))) break;
+          si_next = p.seq_info[iv_next.x & kSeqMask];
+        }
 
         const int key0 = kt * BN + h * KH;
         const bool full_tile = key0 + KH <= lim;
@@ -496,7 +528,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             if (__any_sync(0xffffffffu, need)) {
               // this half's O holds the previous tiles; rescale it once their PV is done
               const uint32_t pm = n - 1;
-              if (!(ok = wait_warp(bar(kPVDone0 + pm % C::kPBufs), (pm / C::kPBufs) & 1u, ctl))) break;
+              if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
               tc_fence_after();
               const float alpha = need ? ex2(m_used - m_new) : 1.0f;
               if (need) {
@@ -525,7 +557,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         // P buffer pb was last read by the PV of tile n - kPBufs
         if (n >= static_cast<uint32_t>(C::kPBufs)) {
           const uint32_t pm = n - C::kPBufs;
-          if (!(ok = wait_warp(bar(kPVDone0 + pm % C::kPBufs), (pm / C::kPBufs) & 1u, ctl))) break;
+          if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
         }
         if (warp_live) {
           tmem_st_cols<KH / 2>(tmem + lane_base + C::kColP + pb * C::kPCols + h * (KH / 2), pk);
@@ -533,7 +565,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kPFull0 + 2 * pb + h));
+        if (lane == 0) mbar_arrive(bar(kPFull0 + pb));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue: merge the halves
@@ -550,7 +582,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       const float c0 = w0 * inv, c1 = w1 * inv;
       {
         const uint32_t pm = n - 1;
-        if (!(ok = wait_warp(bar(kPVDone0 + pm % C::kPBufs), (pm / C::kPBufs) & 1u, ctl))) break;
+        if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
       }
       tc_fence_after();
       if (warp_live) {
@@ -728,7 +760,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kPFull0 + 2 * s + h));
+        if (lane == 0) mbar_arrive(bar(kPFull0 + s));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue

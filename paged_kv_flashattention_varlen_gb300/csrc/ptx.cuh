@@ -72,6 +72,24 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Wa
   }
 }
 
+// Single-thread bounded wait for two barriers: both are tested by one pair of
+// concurrent try_waits (one round trip when both phases are already complete).
+__device__ __forceinline__ bool wait_two(uint32_t bar_a, uint32_t parity_a, uint32_t bar_b,
+                                         uint32_t parity_b, const WaitCtl& c) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred pa, pb;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 pa, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 pb, [%3], %4;\n\t"
+      "and.pred pa, pa, pb;\n\t"
+      "selp.u32 %0, 1, 0, pa;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_a), "r"(parity_a), "r"(bar_b), "r"(parity_b)
+      : "memory");
+  if (ok) return true;
+  return wait_one(bar_a, parity_a, c) && wait_one(bar_b, parity_b, c);
+}
+
 // Warp-uniform bounded wait: every lane polls (so every lane acquires), the
 // warp leaves together.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c) {
