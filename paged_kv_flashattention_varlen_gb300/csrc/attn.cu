@@ -46,10 +46,20 @@ template <int D, int BN>
 struct Cfg {
   static constexpr int kQBytes = kBM * D * 2;
   static constexpr int kKVStage = BN * D * 2;
-  static constexpr int kKStages = D == 128 ? 3 : 2;        // K runs a tile further ahead
+  // D = 128: each softmax warpgroup accumulates its key half into its own O
+  // (columns 0-127 and 128-255); two S buffers (256-383, 384-511), and each
+  // warpgroup writes its P (bf16 pairs) over the S columns it has just read, so
+  // that QK of tile n needs only the PV of tile n - 2, not the softmax of n - 1.
+  // Q is read from shared memory (two buffers, so the next item's Q lands early).
+  // D = 256: one shared O (0-255), two S buffers (256-383) and two P buffers
+  // (384-447), Q from shared memory.
+  static constexpr bool kSplitO = D == 128;
+  static constexpr bool kAliasP = kSplitO;
+  static constexpr int kQBufs = kAliasP ? 2 : 1;
+  static constexpr int kKStages = 2;
   static constexpr int kVStages = 2;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffK = kOffQ + kQBufs * kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKVStage;
   static constexpr int kOffX = kOffV + kVStages * kKVStage;  // row max / sum exchange
   static constexpr int kXBytes = (2 * 2 + 2) * kBM * 4;
@@ -57,23 +67,24 @@ struct Cfg {
   static constexpr int kBarBytes = 256;
   static constexpr int kOffMisc = kOffBar + kBarBytes;
   static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
-  // D = 128: each softmax warpgroup accumulates its key half into its own O
-  // (columns 0-127 and 128-255) against its own running max, with one S buffer
-  // (256-383), one P buffer (384-447) and the Q tile (448-511), so that QK reads
-  // only K from shared memory. D = 256: one shared O (0-255), two S buffers
-  // (256-383) and two P buffers (384-447), Q from shared memory.
-  static constexpr bool kSplitO = D == 128;
-  static constexpr bool kQTmem = kSplitO;             // Q also in TMEM: QK reads only K from smem
-  static constexpr int kSBufs = kSplitO ? 1 : 2;
-  static constexpr int kPBufs = kSplitO ? 1 : 2;
+  static constexpr bool kQTmem = false;               // Q copied into TMEM (A from TMEM for QK)
+  static constexpr int kSBufs = (kSplitO && !kAliasP) ? 1 : 2;
+  static constexpr int kPBufs = kAliasP ? 2 : ((kSplitO || kQTmem) ? 1 : 2);
   static constexpr int kColO = 0;
-  static constexpr int kColS = 256;
+  static constexpr int kColS = kSplitO ? 2 * D : D;
   static constexpr int kPCols = BN / 2;               // P as bf16 pairs: BN keys in BN/2 columns
   static constexpr int kColP = kColS + kSBufs * BN;
-  static constexpr int kColQ = kColP + kPBufs * kPCols;  // Q as bf16 pairs (D/2 columns)
+  static constexpr int kColQ = kColP + (kAliasP ? 0 : kPBufs * kPCols);  // Q as bf16 pairs (D/2 columns)
+  // TMEM column of P buffer b for keys [16 kk, 16 kk + 16): in its own S buffer
+  // (each warpgroup's half at the start of the half it read) or a P buffer.
+  __device__ static constexpr int p_col(int b, int kk) {
+    return kAliasP ? kColS + b * BN + (kk / (BN / 32)) * (BN / 2) + (kk % (BN / 32)) * 8
+                   : kColP + b * kPCols + kk * 8;
+  }
   static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns per row
   static constexpr int kPagesPerTile = BN / kPage;
   static_assert(kColQ + (kQTmem ? D / 2 : 0) <= kTmemCols, "TMEM budget");
+  static_assert(kColS + kSBufs * BN <= kTmemCols, "TMEM budget (S)");
   static_assert((kSplitO ? 2 * D : D) <= kColS, "O columns");
   static_assert(BN % kPage == 0 && BN % 32 == 0, "tile");
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -83,7 +94,7 @@ struct Cfg {
 enum Bar {
   kQFull = 0, kQEmpty, kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2, kVFull0, kVFull1,
   kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPVDone0, kPVDone1, kDrain, kDrainPV, kXMax0,
-  kXMax1, kXSum, kQTReady, kQTFree, kNumBars
+  kXMax1, kXSum, kQTReady, kQTFree, kQFull1, kQEmpty1, kNumBars
 };
 static_assert(kNumBars * 8 <= 256, "mbarrier area");
 constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
@@ -155,6 +166,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 16);
   auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
+  auto qfull = [&](uint32_t b) { return bar(b ? kQFull1 : kQFull); };
+  auto qempty = [&](uint32_t b) { return bar(b ? kQEmpty1 : kQEmpty); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -163,6 +176,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar(kQFull), 1);
+    mbar_init(bar(kQFull1), 1);
+    mbar_init(bar(kQEmpty1), 1);
     // Q shared memory is released by the QK MMAs, or (Q in TMEM) by the softmax
     // warps once they copied it into TMEM
     mbar_init(bar(kQEmpty), C::kQTmem ? kSoftmaxWarps : 1);
@@ -226,11 +241,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       const bool decode_like = si.y <= T;
       const uint64_t pol_kv = decode_like ? l2_policy_evict_first() : l2_policy_evict_last();
       if (kind == 0 && lane == 0) {
-        ok = wait_one(bar(kQEmpty), (itl & 1u) ^ 1u, ctl);
+        const uint32_t qb = itl % C::kQBufs, qu = itl / C::kQBufs;
+        ok = wait_one(qempty(qb), (qu & 1u) ^ 1u, ctl);
         if (ok) {
-          mbar_arrive_expect_tx(bar(kQFull), static_cast<uint32_t>(C::kDBlocks * 128 * G * T));
+          mbar_arrive_expect_tx(qfull(qb), static_cast<uint32_t>(C::kDBlocks * 128 * G * T));
           for (int c = 0; c < C::kDBlocks; ++c)
-            tma_load_4d(sQ + c * (kBM * 128), &tmap_q, bar(kQFull), c * 64, 0, it.hk,
+            tma_load_4d(sQ + qb * C::kQBytes + c * (kBM * 128), &tmap_q, qfull(qb), c * 64, 0, it.hk,
                         q0 + it.qt * T, pol_q);
         }
       }
@@ -295,7 +311,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         const uint32_t last = ((n - 1 - st) / stages) * stages + st;  // last fill on stage st
         wait_one(bar(full + st), (last / stages) & 1u, WaitCtl{abort_flag, p.err});
       }
-      if (kind == 0 && itl > 0) wait_one(bar(kQFull), (itl - 1) & 1u, WaitCtl{abort_flag, p.err});
+      if (kind == 0) {
+        for (uint32_t b = 0; b < static_cast<uint32_t>(C::kQBufs); ++b) {
+          if (itl <= b) continue;
+          const uint32_t last = ((itl - 1 - b) / C::kQBufs) * C::kQBufs + b;  // last Q fill of buffer b
+          wait_one(qfull(b), (last / C::kQBufs) & 1u, WaitCtl{abort_flag, p.err});
+        }
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -314,14 +336,22 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
         const Item it = decode_item(iv_next);
         if (idx + static_cast<int>(gridDim.x) < n_items) iv_next = p.items[idx + gridDim.x];
-        if (!(ok = wait_one(bar(C::kQTmem ? kQTReady : kQFull), itl & 1u, ctl))) break;
+        const uint32_t qb = itl % C::kQBufs, qu = itl / C::kQBufs;
+        if constexpr (C::kQTmem) {
+          if (!(ok = wait_one(bar(kQTReady), itl & 1u, ctl))) break;
+        } else {
+          if (!(ok = wait_one(qfull(qb), qu & 1u, ctl))) break;
+        }
         tc_fence_after();
+        const uint32_t q_lo = desc_lo_at(dq, qb * C::kQBytes);
         for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
           const uint32_t s = n % C::kSBufs, su = n / C::kSBufs;
           const uint32_t ks = n % C::kKStages;
-          if (!(ok = wait_two(bar(kKFull0 + ks), (n / C::kKStages) & 1u, bar(kSFree0 + s), (su & 1u) ^ 1u,
-                              ctl)))
-            break;
+          // S buffer s is free once the softmax read it (or, with P written over
+          // it, once the PV of tile n - 2 has consumed that P)
+          const uint32_t free_bar = C::kAliasP ? bar(kPVDone0 + (n & 1u)) : bar(kSFree0 + s);
+          const uint32_t free_par = C::kAliasP ? ((n >> 1) & 1u) ^ 1u : (su & 1u) ^ 1u;
+          if (!(ok = wait_two(bar(kKFull0 + ks), (n / C::kKStages) & 1u, free_bar, free_par, ctl))) break;
           tc_fence_after();
           const uint32_t k_lo = desc_lo_at(dk, ks * C::kKVStage);
 #pragma unroll
@@ -331,13 +361,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
               umma_f16_ts(tmem + C::kColS + s * BN, tmem + C::kColQ + kk * 8, b_lo, dk.hi, idesc_qk,
                           kk > 0 ? 1u : 0u);
             } else {
-              const uint32_t a_lo = dq.lo + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+              const uint32_t a_lo = q_lo + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
               umma_f16_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
             }
           }
           umma_commit(bar(kKEmpty0 + ks));
           umma_commit(bar(kSFull0 + s));
-          if (kt + 1 == it.kt1) umma_commit(bar(C::kQTmem ? kQTFree : kQEmpty));  // item's last QK
+          if (kt + 1 == it.kt1) umma_commit(C::kQTmem ? bar(kQTFree) : qempty(qb));  // item's last QK
         }
       }
       // Drain: all UMMAs issued by this thread complete before TMEM is freed.
@@ -385,18 +415,17 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             tc_fence_after();
             const bool first = kt == it.kt0;
             const uint32_t v_lo = desc_lo_at(dv, s * C::kKVStage);
-            const uint32_t a0 = tmem + C::kColP + pb * C::kPCols;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
               const uint32_t b_lo = v_lo + ((kk * (16 * 128)) >> 4);
+              const uint32_t a = tmem + C::p_col(static_cast<int>(pb), kk);
               if constexpr (C::kSplitO) {
                 // key half hh accumulates into its own O (columns hh * D ...)
                 const int hh = kk / (BN / 32);
-                umma_f16_ts(tmem + C::kColO + hh * D, a0 + kk * 8, b_lo, dv.hi, idesc_pv,
+                umma_f16_ts(tmem + C::kColO + hh * D, a, b_lo, dv.hi, idesc_pv,
                             (first && kk == hh * (BN / 32)) ? 0u : 1u);
               } else {
-                umma_f16_ts(tmem + C::kColO, a0 + kk * 8, b_lo, dv.hi, idesc_pv,
-                            (first && kk == 0) ? 0u : 1u);
+                umma_f16_ts(tmem + C::kColO, a, b_lo, dv.hi, idesc_pv, (first && kk == 0) ? 0u : 1u);
               }
             }
             umma_commit(bar(kPVDone0 + s));  // PV of tile n done; V stage s free
@@ -462,7 +491,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     // next item's first QK overlaps this item's last softmax tile and epilogue.
     int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
     int4 si_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
-    if (blockIdx.x < n_items) ok = copy_q(0);
+    if constexpr (C::kQTmem) {
+      if (blockIdx.x < n_items) ok = copy_q(0);
+    }
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
       const Item it = decode_item(iv_next);
       const int4 si = si_next;
@@ -476,24 +507,29 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       const bool warp_live = __any_sync(0xffffffffu, valid) != 0;
       float m_used = -INFINITY, l = 0.f;
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
+        const uint32_t sb = n % C::kSBufs, su = n / C::kSBufs;
         const uint32_t pb = n % C::kPBufs;
         const bool first = kt == it.kt0;
-        if (!(ok = wait_warp(bar(kSFull0), n & 1u, ctl))) break;
+        if (!(ok = wait_warp(bar(kSFull0 + sb), su & 1u, ctl))) break;
         tc_fence_after();
         uint32_t sr[KH / 32][32];
         if (warp_live) {
 #pragma unroll
           for (int j = 0; j < KH / 32; ++j)
-            tmem_ld32(tmem + lane_base + C::kColS + h * KH + j * 32, sr[j]);
+            tmem_ld32(tmem + lane_base + C::kColS + sb * BN + h * KH + j * 32, sr[j]);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < KH / 32; ++j) reg_fence(sr[j]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kSFree0));
+        if constexpr (!C::kAliasP) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kSFree0 + sb));
+        }
         if (kt + 1 == it.kt1 && has_next) {
-          if (!(ok = copy_q(itl + 1))) break;
+          if constexpr (C::kQTmem) {
+            if (!(ok = copy_q(itl + 1))) break;
+          }
           si_next = p.seq_info[iv_next.x & kSeqMask];
         }
 
@@ -554,13 +590,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           else
             l += exp_row<KH, true>(sr, c, m_ref, lim - key0, pk);
         }
-        // P buffer pb was last read by the PV of tile n - kPBufs
-        if (n >= static_cast<uint32_t>(C::kPBufs)) {
+        // P buffer pb was last read by the PV of tile n - kPBufs (written over S:
+        // the columns this warp has just read, nothing to wait for)
+        if (!C::kAliasP && n >= static_cast<uint32_t>(C::kPBufs)) {
           const uint32_t pm = n - C::kPBufs;
           if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
         }
         if (warp_live) {
-          tmem_st_cols<KH / 2>(tmem + lane_base + C::kColP + pb * C::kPCols + h * (KH / 2), pk);
+          tmem_st_cols<KH / 2>(tmem + lane_base + C::p_col(static_cast<int>(pb), h * (BN / 32)), pk);
           tmem_wait_st();
         }
         tc_fence_before();
@@ -642,11 +679,45 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     const int t_local = r / G;
     const int g = r - t_local * G;
     const float c = p.scale_log2;
+    // Q in TMEM: as for the split-O warpgroups, each copies its 64 columns of d
+    // of the j-th item's Q tile, the next one as soon as the last S of the
+    // current item has been read.
+    auto copy_q = [&](uint32_t j) -> bool {
+      if (!wait_warp(bar(kQFull), j & 1u, ctl)) return false;
+      if (!wait_warp(bar(kQTFree), (j & 1u) ^ 1u, ctl)) return false;
+      tc_fence_after();
+      const uint8_t* qrow = smem + C::kOffQ + h * (kBM * 128) + r * 128;
+      uint32_t qv[32];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 v4 = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) << 4));
+        qv[ch * 4] = v4.x;
+        qv[ch * 4 + 1] = v4.y;
+        qv[ch * 4 + 2] = v4.z;
+        qv[ch * 4 + 3] = v4.w;
+      }
+      tmem_st32(tmem + lane_base + C::kColQ + h * 32, qv);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(kQTReady));
+        mbar_arrive(bar(kQEmpty));
+      }
+      return true;
+    };
     uint32_t n = 0, itl = 0;
     bool ok = true;
+    int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
+    int4 si_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
+    if constexpr (C::kQTmem) {
+      if (blockIdx.x < n_items) ok = copy_q(0);
+    }
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
-      const Item it = decode_item(p.items[idx]);
-      const int4 si = p.seq_info[it.b];
+      const Item it = decode_item(iv_next);
+      const int4 si = si_next;
+      const bool has_next = idx + static_cast<int>(gridDim.x) < n_items;
+      if (has_next) iv_next = p.items[idx + gridDim.x];
       const int q0 = si.x, ql = si.y, L = si.z;
       const int tok = it.qt * T + t_local;
       const bool valid = (t_local < T) && (tok < ql);
@@ -656,6 +727,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       float m_used = -INFINITY, l = 0.f;
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
         const uint32_t s = n & 1u;
+        const uint32_t pb = n % C::kPBufs;
         const bool first = kt == it.kt0;
         if (!(ok = wait_warp(bar(kSFull0 + s), (n >> 1) & 1u, ctl))) break;
         tc_fence_after();
@@ -671,6 +743,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kSFree0 + s));
+        if (kt + 1 == it.kt1 && has_next) {
+          if constexpr (C::kQTmem) {
+            if (!(ok = copy_q(itl + 1))) break;
+          }
+          si_next = p.seq_info[iv_next.x & kSeqMask];
+        }
 
         const int key0 = kt * BN + h * KH;
         const bool full_tile = key0 + KH <= lim;
@@ -748,19 +826,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           if (redo) exps((m_used == -INFINITY) ? 0.f : m_used);
           l += l_tile;
         }
-        // P buffer s was last read by the PV of tile n - 2
-        if (n >= 2) {
-          const uint32_t pm = n - 2;
+        // P buffer pb was last read by the PV of tile n - kPBufs
+        if (n >= static_cast<uint32_t>(C::kPBufs)) {
+          const uint32_t pm = n - C::kPBufs;
           if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
         }
         if (warp_live) {
           // row r of P as bf16 pairs: this warpgroup's KH keys -> KH/2 TMEM columns
-          tmem_st_cols<KH / 2>(tmem + lane_base + C::kColP + s * C::kPCols + h * (KH / 2), pk);
+          tmem_st_cols<KH / 2>(tmem + lane_base + C::p_col(static_cast<int>(pb), h * (BN / 32)), pk);
           tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kPFull0 + s));
+        if (lane == 0) mbar_arrive(bar(kPFull0 + pb));
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
