@@ -538,57 +538,71 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         const int nv = lim - key0;  // visible keys of this row in the chunk (any sign)
         uint32_t pk[KH / 2];
         if (warp_live) {
-          float acc[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) acc[u] = -INFINITY;
-          if (full_tile) {
-#pragma unroll
-            for (int j = 0; j < KH / 32; ++j)
-#pragma unroll
-              for (int i = 0; i < 32; ++i) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < KH / 32; ++j)
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (j * 32 + i < nv) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
+          // Probabilities against the running max first. Their sum bounds every
+          // one of them, so a sum of at most 2^8 shows that the tile max exceeds
+          // the running max by at most 8 (log2 units): exactly the case in which
+          // the running max is kept, and nothing more is needed. Otherwise (and
+          // on an item's first tile) the tile max decides, as it always would.
+          const float kSumLimit = 256.0f;
+          float lt = 0.f;
+          bool exact = first || m_used == -INFINITY;
+          if (!exact) {
+            lt = full_tile ? exp_row<KH, false>(sr, c, m_used, KH, pk)
+                           : exp_row<KH, true>(sr, c, m_used, nv, pk);
+            exact = !(lt <= kSumLimit);  // also true for inf / NaN
           }
-          const float mx = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
-                                 fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
-          const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
-          const float m_new = fmaxf(m_used, mx_s);
-          if (first) {
-            m_used = m_new;
-          } else {
-            const bool need = m_new > m_used + 8.0f;
-            if (__any_sync(0xffffffffu, need)) {
-              // this half's O holds the previous tiles; rescale it once their PV is done
-              const uint32_t pm = n - 1;
-              if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
-              tc_fence_after();
-              const float alpha = need ? ex2(m_used - m_new) : 1.0f;
-              if (need) {
-                l *= alpha;
-                m_used = m_new;
-              }
-#pragma unroll 1
-              for (int j = 0; j < D / 32; ++j) {
-                uint32_t o[32];
-                tmem_ld32(o_own + j * 32, o);
-                tmem_wait_ld();
-                reg_fence(o);
+          if (__any_sync(0xffffffffu, exact)) {
+            float acc[8];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st32(o_own + j * 32, o);
-              }
-              tmem_wait_st();
+            for (int u = 0; u < 8; ++u) acc[u] = -INFINITY;
+            if (full_tile) {
+#pragma unroll
+              for (int j = 0; j < KH / 32; ++j)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < KH / 32; ++j)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (j * 32 + i < nv) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
             }
+            const float mx = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
+                                   fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
+            const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
+            const float m_new = fmaxf(m_used, mx_s);
+            if (first) {
+              m_used = m_new;
+            } else {
+              const bool need = m_new > m_used + 8.0f;
+              if (__any_sync(0xffffffffu, need)) {
+                // this half's O holds the previous tiles; rescale it once their PV is done
+                const uint32_t pm = n - 1;
+                if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+                tc_fence_after();
+                const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                if (need) {
+                  l *= alpha;
+                  m_used = m_new;
+                }
+#pragma unroll 1
+                for (int j = 0; j < D / 32; ++j) {
+                  uint32_t o[32];
+                  tmem_ld32(o_own + j * 32, o);
+                  tmem_wait_ld();
+                  reg_fence(o);
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                  tmem_st32(o_own + j * 32, o);
+                }
+                tmem_wait_st();
+              }
+            }
+            const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+            lt = full_tile ? exp_row<KH, false>(sr, c, m_ref, KH, pk)
+                           : exp_row<KH, true>(sr, c, m_ref, nv, pk);
           }
-          const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-          if (full_tile)
-            l += exp_row<KH, false>(sr, c, m_ref, KH, pk);
-          else
-            l += exp_row<KH, true>(sr, c, m_ref, lim - key0, pk);
+          l += lt;
         }
         // P buffer pb was last read by the PV of tile n - kPBufs (written over S:
         // the columns this warp has just read, nothing to wait for)
