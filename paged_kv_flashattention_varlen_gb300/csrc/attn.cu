@@ -13,7 +13,7 @@
 //     over the whole pool, [D, 64 rows, Hkv, 2 x pages] (the manifest's K and V
 //     maps), each page read once per KV head for all G query heads;
 //   * warp 1 issues S = Q K^T (tcgen05.mma kind::f16, M = 128, N = BN, K = D)
-//     from one thread, with Q from TMEM (D = 128) or shared memory (D = 256);
+//     from one thread, both operands from shared memory;
 //   * warp 2 zeroes V rows past the sequence end (so that NaN or garbage there
 //     cannot reach O through 0 * NaN) and issues O += P V (M = 128, N = D,
 //     K = BN) with P from TMEM and V read MN-major from shared memory. QK and
@@ -21,17 +21,25 @@
 //     other's MMAs; commits signal mbarriers (the SM100MHA2Q "UMMA0" / "UMMA1"
 //     accumulators of the FlashAttention-4 doc);
 //   * warps 4-11 are two softmax warpgroups over the same 128 query rows, one
-//     row per thread in each, splitting the keys of every tile between them.
-//     Each reads its half of the S row from TMEM, masks keys past the end or
-//     (causal) past its position only on tiles that need it, keeps the running
-//     max m and sum l in log2 units (exp2 with the scale folded into log2 e, as
-//     the manifest's pack scalar does), rescales O in TMEM only when the max grew
-//     by more than 2^8 (exact: O and l share the stale max), and writes P as
-//     bf16 pairs into TMEM, where the PV MMA reads its A operand. D = 128: each
-//     warpgroup has its own O and running max (merged once per item), and
-//     copies the next item's Q into TMEM as soon as the current item's last S
-//     has been read. D = 256: one shared O; the partial row max is exchanged
-//     once per tile.
+//     row per thread in each, splitting the keys of every tile between them
+//     (D = 256: sharing one O accumulator in TMEM). Each reads its half of the S row,
+//     computes P = 2^(S c - m) against the running max m (log2 units, the scale
+//     folded into log2 e, as the manifest's pack scalar does) and writes P as
+//     bf16 pairs into TMEM, where the PV MMA reads its A operand. The two warps
+//     of a row pair then add up their halves of the row sum: a sum of at most
+//     2^8 bounds every p by 2^8, which is exactly when the running max is kept.
+//     Otherwise (and on an item's first tile) they exchange the tile max, O is
+//     rescaled in TMEM if the max grew by more than 2^8 (exact: O and l share
+//     the stale max), and P is recomputed.
+//
+// D = 128 keeps one O per warpgroup instead (each over its own key half, with
+// its own running max, merged once per item), so that the warpgroups need not
+// agree on anything per tile; each skips the tile max while the sum of its
+// probabilities against its running max stays at most 2^8.
+//
+// TMEM (512 columns): D = 128: O0 | O1 | S0 | S1, P written over the S columns
+// each warp has just read, so that QK of tile n waits only for the PV of tile
+// n - 2. D = 256: O | S0 | S1 | P0 | P1.
 //
 // At the end of an item the softmax warps divide by l and store bf16 rows, or
 // (split items) write the normalised partial O and (m, l); merge_kernel then
@@ -46,45 +54,40 @@ template <int D, int BN>
 struct Cfg {
   static constexpr int kQBytes = kBM * D * 2;
   static constexpr int kKVStage = BN * D * 2;
-  // D = 128: each softmax warpgroup accumulates its key half into its own O
-  // (columns 0-127 and 128-255); two S buffers (256-383, 384-511), and each
-  // warpgroup writes its P (bf16 pairs) over the S columns it has just read, so
-  // that QK of tile n needs only the PV of tile n - 2, not the softmax of n - 1.
-  // Q is read from shared memory (two buffers, so the next item's Q lands early).
-  // D = 256: one shared O (0-255), two S buffers (256-383) and two P buffers
-  // (384-447), Q from shared memory.
-  static constexpr bool kSplitO = D == 128;
-  static constexpr bool kAliasP = kSplitO;
-  static constexpr int kQBufs = kAliasP ? 2 : 1;
+  static constexpr bool kSplitO = D == 128;          // one O per softmax warpgroup
+  static constexpr bool kAliasP = D == 128;          // P over its S buffer
+  static constexpr int kSBufs = 2;
+  static constexpr int kPBufs = kAliasP ? kSBufs : 2;
+  static constexpr int kPVBars = kAliasP ? kSBufs : 2;  // pv_done barriers, by tile index
+  static constexpr int kQBufs = D == 128 ? 2 : 1;    // D = 128: the next item's Q lands early
   static constexpr int kKStages = 2;
   static constexpr int kVStages = 2;
+  // shared memory
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBufs * kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKVStage;
-  static constexpr int kOffX = kOffV + kVStages * kKVStage;  // row max / sum exchange
-  static constexpr int kXBytes = (2 * 2 + 2) * kBM * 4;
+  static constexpr int kOffX = kOffV + kVStages * kKVStage;  // row sum / max / l exchange
+  static constexpr int kXBytes = (2 * 2 + 2 * 2 + 2) * kBM * 4;
   static constexpr int kOffBar = kOffX + kXBytes;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kOffMisc = kOffBar + kBarBytes;
   static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
-  static constexpr bool kQTmem = false;               // Q copied into TMEM (A from TMEM for QK)
-  static constexpr int kSBufs = (kSplitO && !kAliasP) ? 1 : 2;
-  static constexpr int kPBufs = kAliasP ? 2 : ((kSplitO || kQTmem) ? 1 : 2);
+  // tensor memory
   static constexpr int kColO = 0;
   static constexpr int kColS = kSplitO ? 2 * D : D;
   static constexpr int kPCols = BN / 2;               // P as bf16 pairs: BN keys in BN/2 columns
-  static constexpr int kColP = kColS + kSBufs * BN;
-  static constexpr int kColQ = kColP + (kAliasP ? 0 : kPBufs * kPCols);  // Q as bf16 pairs (D/2 columns)
-  // TMEM column of P buffer b for keys [16 kk, 16 kk + 16): in its own S buffer
-  // (each warpgroup's half at the start of the half it read) or a P buffer.
+  static constexpr int kColP = kColS + kSBufs * BN;   // separate P buffers (not aliased)
+  // TMEM column of P buffer b for keys [16 kk, 16 kk + 16): over its own S
+  // buffer (each warpgroup's half at the start of the half it read), or in a P
+  // buffer.
   __device__ static constexpr int p_col(int b, int kk) {
     return kAliasP ? kColS + b * BN + (kk / (BN / 32)) * (BN / 2) + (kk % (BN / 32)) * 8
                    : kColP + b * kPCols + kk * 8;
   }
   static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns per row
   static constexpr int kPagesPerTile = BN / kPage;
-  static_assert(kColQ + (kQTmem ? D / 2 : 0) <= kTmemCols, "TMEM budget");
-  static_assert(kColS + kSBufs * BN <= kTmemCols, "TMEM budget (S)");
+  static_assert(kColS + kSBufs * BN + (kAliasP ? 0 : kPBufs * kPCols) <= kTmemCols, "TMEM budget");
+  static_assert(kSBufs <= 3 && kPBufs <= 3 && kPVBars <= 3 && kQBufs <= 2, "barrier slots");
   static_assert((kSplitO ? 2 * D : D) <= kColS, "O columns");
   static_assert(BN % kPage == 0 && BN % 32 == 0, "tile");
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -92,11 +95,12 @@ struct Cfg {
 
 // mbarrier slots
 enum Bar {
-  kQFull = 0, kQEmpty, kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2, kVFull0, kVFull1,
-  kSFull0, kSFull1, kSFree0, kSFree1, kPFull0, kPFull1, kPVDone0, kPVDone1, kDrain, kDrainPV, kXMax0,
-  kXMax1, kXSum, kQTReady, kQTFree, kQFull1, kQEmpty1, kNumBars
+  kQFull0 = 0, kQFull1, kQEmpty0, kQEmpty1, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1,
+  kSFull0, kSFull1, kSFull2, kSFree0, kSFree1, kSFree2, kPFull0, kPFull1, kPFull2, kPVDone0,
+  kPVDone1, kPVDone2, kDrain, kDrainPV, kPairA0, kPairA1, kPairA2, kPairA3, kPairB0, kPairB1,
+  kPairB2, kPairB3, kXSum, kNumBars
 };
-static_assert(kNumBars * 8 <= 256, "mbarrier area");
+static_assert(kNumBars * 8 <= 512, "mbarrier area");
 constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
 constexpr int kSoftmaxWarps = 8;
 
@@ -149,6 +153,21 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[KH / 32][32], floa
   return a.x + a.y;
 }
 
+// Max of the first nv of a row's KH scores (all of them when !kMasked).
+template <int KH, bool kMasked>
+__device__ __forceinline__ float max_row(const uint32_t (&sr)[KH / 32][32], int nv) {
+  float acc[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) acc[u] = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < KH / 32; ++j)
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (!kMasked || j * 32 + i < nv) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
+  return fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
+               fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
+}
+
 template <int D, int BN>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
@@ -166,8 +185,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 16);
   auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
-  auto qfull = [&](uint32_t b) { return bar(b ? kQFull1 : kQFull); };
-  auto qempty = [&](uint32_t b) { return bar(b ? kQEmpty1 : kQEmpty); };
+  // pv_done of tile m: barrier m % kPVBars, phase m / kPVBars
+  auto pv_bar = [&](uint32_t m) { return bar(kPVDone0 + static_cast<int>(m % C::kPVBars)); };
+  auto pv_par = [&](uint32_t m) { return (m / C::kPVBars) & 1u; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -175,29 +195,23 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(bar(kQFull), 1);
-    mbar_init(bar(kQFull1), 1);
-    mbar_init(bar(kQEmpty1), 1);
-    // Q shared memory is released by the QK MMAs, or (Q in TMEM) by the softmax
-    // warps once they copied it into TMEM
-    mbar_init(bar(kQEmpty), C::kQTmem ? kSoftmaxWarps : 1);
-    mbar_init(bar(kQTReady), kSoftmaxWarps);
-    mbar_init(bar(kQTFree), 1);
-
-    for (int s = 0; s < C::kKStages; ++s) {
-      mbar_init(bar(kKFull0 + s), 1);
-      mbar_init(bar(kKEmpty0 + s), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kQFull0 + b), 1);
+      mbar_init(bar(kQEmpty0 + b), 1);  // the item's last QK MMA releases the buffer
+      mbar_init(bar(kKFull0 + b), 1);
+      mbar_init(bar(kKEmpty0 + b), 1);
+      mbar_init(bar(kVFull0 + b), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kVFull0 + s), 1);
-      mbar_init(bar(kSFull0 + s), 1);
-      mbar_init(bar(kSFree0 + s), kSoftmaxWarps);
-      mbar_init(bar(kXMax0 + s), kSoftmaxWarps);
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(bar(kSFull0 + b), 1);
+      mbar_init(bar(kSFree0 + b), kSoftmaxWarps);
+      mbar_init(bar(kPFull0 + b), kSoftmaxWarps);  // both key halves of P written
+      mbar_init(bar(kPVDone0 + b), 1);             // also frees that tile's V stage
     }
-    // P buffer b: p_full[b], one arrival per softmax warp (both key halves written).
-    // pv_done[t & 1]: the PV of tile t has completed, which also frees V stage t & 1.
-    for (int s = 0; s < 2; ++s) mbar_init(bar(kPFull0 + s), kSoftmaxWarps);
-    for (int s = 0; s < 2; ++s) mbar_init(bar(kPVDone0 + s), 1);
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(bar(kPairA0 + b), 2);  // the two warps of a row quarter: row sums
+      mbar_init(bar(kPairB0 + b), 2);  // and, when needed, row maxes
+    }
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kDrainPV), 1);
     mbar_init(bar(kXSum), kSoftmaxWarps);
@@ -228,8 +242,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     const int kind = warp == 0 ? 0 : 1;
     const uint32_t stages = kind ? C::kVStages : C::kKStages;
     const int full = kind ? kVFull0 : kKFull0;
-    const int empty = kind ? kPVDone0 : kKEmpty0;  // a V stage is free once its PV is done
-    const uint32_t ring = kind ? sV : sK;
     const unsigned fullmask = 0xffffffffu;
     uint32_t n = 0, itl = 0;
     bool ok = true;
@@ -242,12 +254,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       const uint64_t pol_kv = decode_like ? l2_policy_evict_first() : l2_policy_evict_last();
       if (kind == 0 && lane == 0) {
         const uint32_t qb = itl % C::kQBufs, qu = itl / C::kQBufs;
-        ok = wait_one(qempty(qb), (qu & 1u) ^ 1u, ctl);
+        ok = wait_one(bar(kQEmpty0 + qb), (qu & 1u) ^ 1u, ctl);
         if (ok) {
-          mbar_arrive_expect_tx(qfull(qb), static_cast<uint32_t>(C::kDBlocks * 128 * G * T));
+          mbar_arrive_expect_tx(bar(kQFull0 + qb), static_cast<uint32_t>(C::kDBlocks * 128 * G * T));
           for (int c = 0; c < C::kDBlocks; ++c)
-            tma_load_4d(sQ + qb * C::kQBytes + c * (kBM * 128), &tmap_q, qfull(qb), c * 64, 0, it.hk,
-                        q0 + it.qt * T, pol_q);
+            tma_load_4d(sQ + qb * C::kQBytes + c * (kBM * 128), &tmap_q, bar(kQFull0 + qb), c * 64, 0,
+                        it.hk, q0 + it.qt * T, pol_q);
         }
       }
       ok = __shfl_sync(fullmask, ok, 0);
@@ -281,11 +293,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             nload += a[j] >= 0;
           }
           if (lane == 0) {
-            const uint32_t st = n % stages, ph = ((n / stages) & 1u) ^ 1u;
-            ok = wait_one(bar(empty + st), ph, ctl);
+            const uint32_t st = n % stages;
+            if (kind == 0) {
+              ok = wait_one(bar(kKEmpty0 + st), ((n / stages) & 1u) ^ 1u, ctl);
+            } else if (n >= stages) {
+              // a V stage is free once the PV of the tile it held is done
+              ok = wait_one(pv_bar(n - stages), pv_par(n - stages), ctl);
+            }
             if (ok) {
               mbar_arrive_expect_tx(bar(full + st), static_cast<uint32_t>(nload * C::kDBlocks * kPage * 128));
-              const uint32_t dst0 = ring + st * C::kKVStage;
+              const uint32_t dst0 = (kind ? sV : sK) + st * C::kKVStage;
 #pragma unroll
               for (int j = 0; j < C::kPagesPerTile; ++j) {
                 if (a[j] < 0) continue;
@@ -315,7 +332,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         for (uint32_t b = 0; b < static_cast<uint32_t>(C::kQBufs); ++b) {
           if (itl <= b) continue;
           const uint32_t last = ((itl - 1 - b) / C::kQBufs) * C::kQBufs + b;  // last Q fill of buffer b
-          wait_one(qfull(b), (last / C::kQBufs) & 1u, WaitCtl{abort_flag, p.err});
+          wait_one(bar(kQFull0 + b), (last / C::kQBufs) & 1u, WaitCtl{abort_flag, p.err});
         }
       }
     }
@@ -323,7 +340,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   } else if (warp == 1) {
     // ------------------------------------------------------------ QK MMA warp
     // S = Q K^T for every tile, issued by one thread. The PV MMAs come from warp 2:
-    // the two streams touch disjoint TMEM (S, Q / P, O) and feed the tensor pipe
+    // the two streams touch disjoint TMEM (S / P, O) and feed the tensor pipe
     // independently, so that neither one's waits leave the pipe idle.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, BN, false, false);
@@ -337,37 +354,28 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         const Item it = decode_item(iv_next);
         if (idx + static_cast<int>(gridDim.x) < n_items) iv_next = p.items[idx + gridDim.x];
         const uint32_t qb = itl % C::kQBufs, qu = itl / C::kQBufs;
-        if constexpr (C::kQTmem) {
-          if (!(ok = wait_one(bar(kQTReady), itl & 1u, ctl))) break;
-        } else {
-          if (!(ok = wait_one(qfull(qb), qu & 1u, ctl))) break;
-        }
+        if (!(ok = wait_one(bar(kQFull0 + qb), qu & 1u, ctl))) break;
         tc_fence_after();
         const uint32_t q_lo = desc_lo_at(dq, qb * C::kQBytes);
         for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
-          const uint32_t s = n % C::kSBufs, su = n / C::kSBufs;
+          const uint32_t s = n % C::kSBufs;
           const uint32_t ks = n % C::kKStages;
-          // S buffer s is free once the softmax read it (or, with P written over
-          // it, once the PV of tile n - 2 has consumed that P)
-          const uint32_t free_bar = C::kAliasP ? bar(kPVDone0 + (n & 1u)) : bar(kSFree0 + s);
-          const uint32_t free_par = C::kAliasP ? ((n >> 1) & 1u) ^ 1u : (su & 1u) ^ 1u;
+          // S buffer s is free once the softmax has read it, or (P written over
+          // it) once the PV of tile n - kSBufs has consumed that P
+          const uint32_t free_bar = C::kAliasP ? pv_bar(n) : bar(kSFree0 + static_cast<int>(s));
+          const uint32_t free_par = ((n / C::kSBufs) & 1u) ^ 1u;
           if (!(ok = wait_two(bar(kKFull0 + ks), (n / C::kKStages) & 1u, free_bar, free_par, ctl))) break;
           tc_fence_after();
           const uint32_t k_lo = desc_lo_at(dk, ks * C::kKVStage);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t b_lo = k_lo + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
-            if constexpr (C::kQTmem) {
-              umma_f16_ts(tmem + C::kColS + s * BN, tmem + C::kColQ + kk * 8, b_lo, dk.hi, idesc_qk,
-                          kk > 0 ? 1u : 0u);
-            } else {
-              const uint32_t a_lo = q_lo + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
-              umma_f16_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
-            }
+            const uint32_t a_lo = q_lo + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+            umma_f16_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(kKEmpty0 + ks));
           umma_commit(bar(kSFull0 + s));
-          if (kt + 1 == it.kt1) umma_commit(C::kQTmem ? bar(kQTFree) : qempty(qb));  // item's last QK
+          if (kt + 1 == it.kt1) umma_commit(bar(kQEmpty0 + qb));  // item's last QK
         }
       }
       // Drain: all UMMAs issued by this thread complete before TMEM is freed.
@@ -394,8 +402,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         L_next = p.seq_info[iv_next.x & kSeqMask].z;
       }
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
-        const uint32_t s = n & 1u;
-        if (!(ok = wait_warp(bar(kVFull0 + s), (n >> 1) & 1u, ctl))) break;
+        const uint32_t s = n % C::kVStages;
+        if (!(ok = wait_warp(bar(kVFull0 + s), (n / C::kVStages) & 1u, ctl))) break;
         const int live = L - kt * BN;
         if (live < BN) {
           uint8_t* v0 = smem + C::kOffV + s * C::kKVStage;
@@ -428,7 +436,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
                 umma_f16_ts(tmem + C::kColO, a, b_lo, dv.hi, idesc_pv, (first && kk == 0) ? 0u : 1u);
               }
             }
-            umma_commit(bar(kPVDone0 + s));  // PV of tile n done; V stage s free
+            umma_commit(pv_bar(n));  // PV of tile n done; its P and V stage are free
           }
         }
         ok = __shfl_sync(fullmask, ok, 0);
@@ -456,44 +464,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     const int t_local = r / G;
     const int g = r - t_local * G;
     const float c = p.scale_log2;
-    // Q tile of the j-th item of this CTA -> TMEM: this thread's row, this
-    // warpgroup's 64 columns of d, once the TMA landed it and the QK MMAs of
-    // item j - 1 are done.
-    auto copy_q = [&](uint32_t j) -> bool {
-      if (!wait_warp(bar(kQFull), j & 1u, ctl)) return false;
-      if (!wait_warp(bar(kQTFree), (j & 1u) ^ 1u, ctl)) return false;
-      tc_fence_after();
-      const uint8_t* qrow = smem + C::kOffQ + h * (kBM * 128) + r * 128;
-      uint32_t qv[32];
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) << 4));
-        qv[ch * 4] = v4.x;
-        qv[ch * 4 + 1] = v4.y;
-        qv[ch * 4 + 2] = v4.z;
-        qv[ch * 4 + 3] = v4.w;
-      }
-      tmem_st32(tmem + lane_base + C::kColQ + h * 32, qv);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(kQTReady));
-        mbar_arrive(bar(kQEmpty));
-      }
-      return true;
-    };
     uint32_t n = 0, itl = 0;
     bool ok = true;
-    // The next item's descriptor and sequence are loaded one item ahead, and its
-    // Q is copied into TMEM as soon as the last S tile of the current item has
-    // been read (the QK MMAs of the current item are then done), so that the
-    // next item's first QK overlaps this item's last softmax tile and epilogue.
+    // The next item's descriptor and sequence are loaded one item ahead.
     int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
     int4 si_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
-    if constexpr (C::kQTmem) {
-      if (blockIdx.x < n_items) ok = copy_q(0);
-    }
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
       const Item it = decode_item(iv_next);
       const int4 si = si_next;
@@ -526,12 +501,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kSFree0 + sb));
         }
-        if (kt + 1 == it.kt1 && has_next) {
-          if constexpr (C::kQTmem) {
-            if (!(ok = copy_q(itl + 1))) break;
-          }
-          si_next = p.seq_info[iv_next.x & kSeqMask];
-        }
+        if (kt + 1 == it.kt1 && has_next) si_next = p.seq_info[iv_next.x & kSeqMask];
 
         const int key0 = kt * BN + h * KH;
         const bool full_tile = key0 + KH <= lim;
@@ -578,7 +548,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
               if (__any_sync(0xffffffffu, need)) {
                 // this half's O holds the previous tiles; rescale it once their PV is done
                 const uint32_t pm = n - 1;
-                if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+                if (!(ok = wait_warp(pv_bar(pm), pv_par(pm), ctl))) break;
                 tc_fence_after();
                 const float alpha = need ? ex2(m_used - m_new) : 1.0f;
                 if (need) {
@@ -608,7 +578,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         // the columns this warp has just read, nothing to wait for)
         if (!C::kAliasP && n >= static_cast<uint32_t>(C::kPBufs)) {
           const uint32_t pm = n - C::kPBufs;
-          if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+          if (!(ok = wait_warp(pv_bar(pm), pv_par(pm), ctl))) break;
         }
         if (warp_live) {
           tmem_st_cols<KH / 2>(tmem + lane_base + C::p_col(static_cast<int>(pb), h * (BN / 32)), pk);
@@ -633,7 +603,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       const float c0 = w0 * inv, c1 = w1 * inv;
       {
         const uint32_t pm = n - 1;
-        if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
+        if (!(ok = wait_warp(pv_bar(pm), pv_par(pm), ctl))) break;
       }
       tc_fence_after();
       if (warp_live) {
@@ -679,54 +649,29 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     } else {
     // ------------------------------------------------------------ softmax: two warpgroups
     // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) takes keys [h*KH, h*KH + KH)
-    // of every tile and O columns [h*DH, h*DH + DH) for the same 128 rows; the two
-    // threads of a row exchange their partial max once per tile and their partial
-    // sums once per item.
+    // of every tile and O columns [h*DH, h*DH + DH) for the same 128 rows. Warp w
+    // and warp w + 4 hold the same 32 rows: they exchange their partial row sums
+    // once per tile (and their partial row maxes when those are needed).
     constexpr int KH = BN / 2;
     constexpr int DH = D / 2;
     const int h = (warp - 4) >> 2;
     const int sw = (warp - 4) & 3;        // TMEM lane quarter
     const int r = sw * 32 + lane;         // query row of this thread
     const uint32_t lane_base = static_cast<uint32_t>(sw * 32) << 16;
-    float* xmax = reinterpret_cast<float*>(smem + C::kOffX);  // [2 parity][2 wg][128]
-    float* xsum = xmax + 2 * 2 * kBM;                           // [2 wg][128]
+    float* xsum_t = reinterpret_cast<float*>(smem + C::kOffX);  // [2 parity][2 wg][128]
+    float* xmax_t = xsum_t + 2 * 2 * kBM;                         // [2 parity][2 wg][128]
+    float* xl = xmax_t + 2 * 2 * kBM;                             // [2 wg][128]
+    const uint32_t pair_a = bar(kPairA0 + sw), pair_b = bar(kPairB0 + sw);
     const int t_local = r / G;
     const int g = r - t_local * G;
     const float c = p.scale_log2;
-    // Q in TMEM: as for the split-O warpgroups, each copies its 64 columns of d
-    // of the j-th item's Q tile, the next one as soon as the last S of the
-    // current item has been read.
-    auto copy_q = [&](uint32_t j) -> bool {
-      if (!wait_warp(bar(kQFull), j & 1u, ctl)) return false;
-      if (!wait_warp(bar(kQTFree), (j & 1u) ^ 1u, ctl)) return false;
-      tc_fence_after();
-      const uint8_t* qrow = smem + C::kOffQ + h * (kBM * 128) + r * 128;
-      uint32_t qv[32];
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) << 4));
-        qv[ch * 4] = v4.x;
-        qv[ch * 4 + 1] = v4.y;
-        qv[ch * 4 + 2] = v4.z;
-        qv[ch * 4 + 3] = v4.w;
-      }
-      tmem_st32(tmem + lane_base + C::kColQ + h * 32, qv);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(kQTReady));
-        mbar_arrive(bar(kQEmpty));
-      }
-      return true;
-    };
+    const float kSumLimit = 256.0f;  // 2^8: the running max is kept while every p <= 2^8
+    const unsigned full = 0xffffffffu;
     uint32_t n = 0, itl = 0;
+    uint32_t na = 0, nb = 0;  // row-sum / row-max exchanges of this warp pair
     bool ok = true;
     int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
     int4 si_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
-    if constexpr (C::kQTmem) {
-      if (blockIdx.x < n_items) ok = copy_q(0);
-    }
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
       const Item it = decode_item(iv_next);
       const int4 si = si_next;
@@ -737,117 +682,103 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       const bool valid = (t_local < T) && (tok < ql);
       int lim = 0;  // keys [0, lim) visible to this row
       if (valid) lim = p.causal ? min(L, L - ql + tok + 1) : L;
-      const bool warp_live = __any_sync(0xffffffffu, valid) != 0;
+      // the same for both warps of a pair (same rows)
+      const bool warp_live = __any_sync(full, valid) != 0;
       float m_used = -INFINITY, l = 0.f;
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
-        const uint32_t s = n & 1u;
-        const uint32_t pb = n % C::kPBufs;
+        const uint32_t sb = n % C::kSBufs, pb = n % C::kPBufs;
         const bool first = kt == it.kt0;
-        if (!(ok = wait_warp(bar(kSFull0 + s), (n >> 1) & 1u, ctl))) break;
+        if (!(ok = wait_warp(bar(kSFull0 + sb), (n / C::kSBufs) & 1u, ctl))) break;
         tc_fence_after();
         uint32_t sr[KH / 32][32];
         if (warp_live) {
 #pragma unroll
           for (int j = 0; j < KH / 32; ++j)
-            tmem_ld32(tmem + lane_base + C::kColS + s * BN + h * KH + j * 32, sr[j]);
+            tmem_ld32(tmem + lane_base + C::kColS + sb * BN + h * KH + j * 32, sr[j]);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < KH / 32; ++j) reg_fence(sr[j]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kSFree0 + s));
-        if (kt + 1 == it.kt1 && has_next) {
-          if constexpr (C::kQTmem) {
-            if (!(ok = copy_q(itl + 1))) break;
-          }
-          si_next = p.seq_info[iv_next.x & kSeqMask];
+        if constexpr (!C::kAliasP) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kSFree0 + sb));
         }
-
+        if (kt + 1 == it.kt1 && has_next) si_next = p.seq_info[iv_next.x & kSeqMask];
+        // a separate P buffer was last read by the PV of tile n - kPBufs; over S,
+        // P goes into the columns this warp has just read
+        if (!C::kAliasP && n >= static_cast<uint32_t>(C::kPBufs)) {
+          if (!(ok = wait_warp(pv_bar(n - C::kPBufs), pv_par(n - C::kPBufs), ctl))) break;
+        }
         const int key0 = kt * BN + h * KH;
         const bool full_tile = key0 + KH <= lim;
         const int nv = lim - key0;  // visible keys of this row in the chunk (any sign)
-        float mx = -INFINITY;
-        if (warp_live) {
-          float acc[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) acc[u] = -INFINITY;
-          if (full_tile) {
-#pragma unroll
-            for (int j = 0; j < KH / 32; ++j)
-#pragma unroll
-              for (int i = 0; i < 32; ++i) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < KH / 32; ++j)
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (j * 32 + i < nv) acc[i & 7] = fmaxf(acc[i & 7], __uint_as_float(sr[j][i]));
-          }
-          mx = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
-                     fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
-        }
-        // exchange the partial row max with the other warpgroup; while it is in
-        // flight, compute P against the running max both warpgroups already share
-        float* xb = xmax + s * (2 * kBM);
-        xb[h * kBM + r] = mx;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kXMax0 + s));
-
+        const uint32_t p_addr = tmem + lane_base + C::p_col(static_cast<int>(pb), h * (BN / 32));
         uint32_t pk[KH / 2];
-        float l_tile = 0.f;
-        auto exps = [&](float m_ref) {
-          l_tile = full_tile ? exp_row<KH, false>(sr, c, m_ref, KH, pk)
-                             : exp_row<KH, true>(sr, c, m_ref, lim - key0, pk);
-        };
-        const bool speculate = warp_live && !first && m_used != -INFINITY;
-        if (speculate) exps(m_used);
-        if (!(ok = wait_warp(bar(kXMax0 + s), (n >> 1) & 1u, ctl))) break;
-        mx = fmaxf(mx, xb[(1 - h) * kBM + r]);
-
+        float lt = 0.f;
         if (warp_live) {
-          const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
-          const float m_new = fmaxf(m_used, mx_s);
-          bool redo = !speculate;
-          if (first) {
-            m_used = m_new;
-          } else {
-            const bool need = m_new > m_used + 8.0f;
-            if (__any_sync(0xffffffffu, need)) {
-              // O holds the previous tiles; rescale this warpgroup's half once their PV is done.
-              const uint32_t pm = n - 1;
-              if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
-              tc_fence_after();
-              const float alpha = need ? ex2(m_used - m_new) : 1.0f;
-              if (need) {
-                l *= alpha;
-                m_used = m_new;
-              }
-#pragma unroll 1
-              for (int j = 0; j < DH / 32; ++j) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
-                tmem_wait_ld();
-                reg_fence(o);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                tmem_st32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
-              }
-              tmem_wait_st();
-              redo = true;  // the speculative P used the old max for some rows of this warp
-            }
+          bool exact = first;
+          if (!first) {
+            // P against the running max; a row that has seen no key yet (m = -inf)
+            // takes the exact path if it sees one now
+            const float m_spec = m_used == -INFINITY ? 0.f : m_used;
+            lt = full_tile ? exp_row<KH, false>(sr, c, m_spec, KH, pk)
+                           : exp_row<KH, true>(sr, c, m_spec, nv, pk);
+            tmem_st_cols<KH / 2>(p_addr, pk);
+            // round A: the row's two half sums (+inf forces the exact path)
+            xsum_t[((na & 1u) * 2 + h) * kBM + r] = (m_used == -INFINITY && nv > 0) ? INFINITY : lt;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pair_a);
+            if (!(ok = wait_warp(pair_a, na & 1u, ctl))) break;
+            const float mine = xsum_t[((na & 1u) * 2 + h) * kBM + r];
+            const float tot = mine + xsum_t[((na & 1u) * 2 + (1 - h)) * kBM + r];
+            ++na;
+            exact = !(tot <= kSumLimit);  // also true for inf / NaN
           }
-          if (redo) exps((m_used == -INFINITY) ? 0.f : m_used);
-          l += l_tile;
-        }
-        // P buffer pb was last read by the PV of tile n - kPBufs
-        if (n >= static_cast<uint32_t>(C::kPBufs)) {
-          const uint32_t pm = n - C::kPBufs;
-          if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
-        }
-        if (warp_live) {
-          // row r of P as bf16 pairs: this warpgroup's KH keys -> KH/2 TMEM columns
-          tmem_st_cols<KH / 2>(tmem + lane_base + C::p_col(static_cast<int>(pb), h * (BN / 32)), pk);
+          if (__any_sync(full, exact)) {
+            // round B: the tile max of the row over both halves
+            float mx = full_tile ? max_row<KH, false>(sr, nv) : max_row<KH, true>(sr, nv);
+            xmax_t[((nb & 1u) * 2 + h) * kBM + r] = mx;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pair_b);
+            if (!(ok = wait_warp(pair_b, nb & 1u, ctl))) break;
+            mx = fmaxf(mx, xmax_t[((nb & 1u) * 2 + (1 - h)) * kBM + r]);
+            ++nb;
+            const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
+            const float m_new = fmaxf(m_used, mx_s);
+            if (first) {
+              m_used = m_new;
+            } else {
+              const bool need = m_new > m_used + 8.0f;
+              if (__any_sync(full, need)) {
+                // O holds the previous tiles; rescale this warpgroup's half of the
+                // columns once their PV is done
+                if (!(ok = wait_warp(pv_bar(n - 1), pv_par(n - 1), ctl))) break;
+                tc_fence_after();
+                const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                if (need) {
+                  l *= alpha;
+                  m_used = m_new;
+                }
+#pragma unroll 1
+                for (int j = 0; j < DH / 32; ++j) {
+                  uint32_t o[32];
+                  tmem_ld32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
+                  tmem_wait_ld();
+                  reg_fence(o);
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                  tmem_st32(tmem + lane_base + C::kColO + h * DH + j * 32, o);
+                }
+              }
+            }
+            const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+            lt = full_tile ? exp_row<KH, false>(sr, c, m_ref, KH, pk)
+                           : exp_row<KH, true>(sr, c, m_ref, nv, pk);
+            tmem_wait_st();  // the speculative P (if any) lands before it is overwritten
+            tmem_st_cols<KH / 2>(p_addr, pk);
+          }
+          l += lt;
           tmem_wait_st();
         }
         tc_fence_before();
@@ -856,15 +787,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      xsum[h * kBM + r] = l;
+      xl[h * kBM + r] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kXSum));
       if (!(ok = wait_warp(bar(kXSum), itl & 1u, ctl))) break;
-      const float l_all = l + xsum[(1 - h) * kBM + r];
-      {
-        const uint32_t pm = n - 1;
-        if (!(ok = wait_warp(bar(kPVDone0 + (pm & 1u)), (pm >> 1) & 1u, ctl))) break;
-      }
+      const float l_all = l + xl[(1 - h) * kBM + r];
+      if (!(ok = wait_warp(pv_bar(n - 1), pv_par(n - 1), ctl))) break;
       tc_fence_after();
       if (warp_live) {
         const float inv_l = l_all > 0.f ? 1.0f / l_all : 0.f;
