@@ -22,7 +22,7 @@
  *   - Device pointers are owned by the caller; the library keeps none of them
  *     past the call. Calls are asynchronous and ordered on `stream`; nothing
  *     here synchronises the host except pattn_get_device_status,
- *     pattn_profile_read and pattn_forward_host.
+ *     pattn_profile_read, pattn_profile_read_kernels and pattn_forward_host.
  *   - Errors the host can see (null or misaligned pointers, sizes, unsupported
  *     shapes) are returned before anything is launched.
  *   - Errors only the data shows (a block-table entry outside the pool inside
@@ -92,6 +92,33 @@ pattn_status pattn_forward(void *out, const void *q, const void *kv_pool,
                            int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
                            int page_size, int num_pages, float scale, int causal,
                            pattn_stream_t stream);
+
+/*
+ * pattn_forward_append -- the cache write in front of attention, then
+ * pattn_forward: the `reshape_and_cache_flash` (kv_write) node that comes right
+ * before `attend` in the GB10 model graph, in the same stream-ordered call.
+ *
+ *   k_new, v_new  bf16 [total_q][n_heads_kv][head_dim]: the K and V rows of the
+ *                 query tokens, in the token order of q.
+ *   kv_pool       as for pattn_forward, written: token i of sequence b
+ *                 (i < ql_b) goes to cache position L_b - ql_b + i, i.e. row
+ *                 (pos mod page_size) of page block_table[b][pos / page_size]
+ *                 (contiguous cache: row sum(seq_lens[0..b)) + pos of the K and
+ *                 V planes). Nothing else in the pool is written.
+ *   other arguments as for pattn_forward; seq_lens count the new tokens.
+ *
+ * The attention then reads the updated cache. Tokens at positions < 0 (more
+ * queries than keys) are not written. Sequences rejected on the device
+ * (PATTN_ERR_DEVICE_BAD_INPUT) are neither written nor attended (rows zero).
+ * k_new and v_new are caller-owned device buffers, 16-byte aligned; they must
+ * not overlap kv_pool.
+ */
+pattn_status pattn_forward_append(void *out, const void *q, const void *k_new, const void *v_new,
+                                  void *kv_pool, const int32_t *block_table,
+                                  const int32_t *seq_lens, const int32_t *cu_q, int num_seqs,
+                                  int total_q, int max_q, int max_kv, int n_heads_q,
+                                  int n_heads_kv, int head_dim, int page_size, int num_pages,
+                                  float scale, int causal, pattn_stream_t stream);
 
 /* Bytes of the fixed device scratch behind pattn_forward_noalloc. */
 #define PATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -181,6 +208,14 @@ const char *pattn_status_string(pattn_status status);
 pattn_status pattn_profile_enable(int on);
 pattn_status pattn_profile_read(double *ms_plan, double *ms_attention, double *ms_combine,
                                 int *calls);
+
+/*
+ * The same record split by kernel: ms[0] plan, ms[1] cache write
+ * (pattn_forward_append), ms[2] decode kernel, ms[3] prefill kernel, ms[4] time
+ * after the attention kernels (the prefill split merge). ms holds 5 doubles.
+ * Clears the record like pattn_profile_read.
+ */
+pattn_status pattn_profile_read_kernels(double *ms, int *calls);
 
 #ifdef __cplusplus
 }

@@ -10,6 +10,9 @@ Functions:
 * :func:`forward` -- attention output and log-sum-exp for every query token
   (or a chosen subset of tokens), for a key window if asked.
 * :func:`combine` -- log-sum-exp merge of results over disjoint key sets.
+* :func:`append_kv` -- the cache write in front of attention (the GB10 model
+  graph's ``kv_write`` node, ``reshape_and_cache_flash``): the new tokens' K and
+  V rows into their cache slots, as a fresh pool. Plain numpy indexing.
 
 Both are pinned by the ``-m "not gpu"`` tests against closed forms, a dense
 brute force written separately in numpy, and invariants (page permutation,
@@ -169,3 +172,52 @@ def combine(out_parts: np.ndarray, lse_parts: np.ndarray):
     lib.pattn_oracle_combine(out.ctypes.data, lse.ctypes.data, op.ctypes.data, lp.ctypes.data,
                              int(S), int(n), int(d))
     return out, lse
+
+
+def append_kv(kv_pool, block_table, seq_lens, cu_q, k_new, v_new, page_size: int = 64):
+    """The cache write of the GB10 model graph's ``kv_write`` node
+    (``reshape_and_cache_flash``, "k:write,v:write", "cache bf16"), on a copy.
+
+    Token i of sequence b (``i < ql_b = cu_q[b+1] - cu_q[b]``) is the key at
+    logical position ``pos = seq_lens[b] - ql_b + i`` (the new tokens are the
+    last ``ql_b`` keys, the same bottom-right alignment as the attention); its
+    K and V rows ``k_new[t]``, ``v_new[t]`` (``t = cu_q[b] + i``, shape
+    ``[Hkv, D]``) go to row ``pos % P`` of page ``block_table[b][pos // P]``,
+    or, with ``block_table = None``, to row ``sum(seq_lens[:b]) + pos`` of the
+    K and V planes. Tokens with ``pos < 0`` have no slot and are skipped.
+    Returns the new pool (bf16 tensor on the CPU); the input is not modified.
+    """
+    import torch
+    pool = kv_pool.detach().cpu().clone()
+    kn = k_new.detach().cpu()
+    vn = v_new.detach().cpu()
+    sl = _i32(seq_lens)
+    cq = _i32(cu_q)
+    bt = _i32(block_table)
+    start = 0
+    for b in range(sl.shape[0]):
+        L = int(sl[b])
+        q0, q1 = int(cq[b]), int(cq[b + 1])
+        ql = q1 - q0
+        for i in range(ql):
+            pos = L - ql + i
+            if pos < 0:
+                continue
+            t = q0 + i
+            if bt is None:
+                pool[0, start + pos] = kn[t]
+                pool[1, start + pos] = vn[t]
+            else:
+                page = int(bt[b, pos // page_size])
+                pool[page, 0, pos % page_size] = kn[t]
+                pool[page, 1, pos % page_size] = vn[t]
+        start += L
+    return pool
+
+
+def append_workload(wl, k_new, v_new):
+    """:func:`append_kv` on a :class:`workloads.Workload`: the same workload with
+    the updated pool."""
+    import dataclasses
+    pool = append_kv(wl.kv_pool, wl.block_table, wl.seq_lens, wl.cu_q, k_new, v_new, wl.page_size)
+    return dataclasses.replace(wl, kv_pool=pool)

@@ -14,9 +14,9 @@ from typing import Optional, Tuple
 
 from . import _lib
 
-__all__ = ["PattnError", "forward", "forward_noalloc", "forward_host", "workspace_size", "set_workspace",
-           "device_status", "status_string", "profile_enable", "profile_read", "STATUS",
-           "library_path"]
+__all__ = ["PattnError", "forward", "forward_append", "forward_noalloc", "forward_host", "workspace_size",
+           "set_workspace", "device_status", "status_string", "profile_enable", "profile_read",
+           "profile_read_kernels", "STATUS", "library_path"]
 
 STATUS = {
     0: "PATTN_OK", 1: "PATTN_ERR_INVALID_ARG", 2: "PATTN_ERR_UNSUPPORTED", 3: "PATTN_ERR_CUDA",
@@ -94,6 +94,39 @@ def forward(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv:
     return rc
 
 
+def forward_append(out, q, k_new, v_new, kv_pool, block_table, seq_lens, cu_q, *, max_q: int,
+                   max_kv: int, n_heads_kv: int, scale: float, causal: bool,
+                   num_pages: Optional[int] = None, stream=None, check: bool = True) -> int:
+    """Cache write of the new tokens, then attention (``pattn_forward_append``).
+
+    ``k_new``/``v_new``: bf16 [total_q, Hkv, D] on the device, the K and V rows of
+    the query tokens; token i of sequence b is written to cache position
+    ``seq_lens[b] - ql_b + i`` of ``kv_pool`` (in place), then the attention reads
+    the updated cache. Other arguments as for :func:`forward`.
+    """
+    import torch
+    for name, t, dt in (("out", out, torch.bfloat16), ("q", q, torch.bfloat16),
+                        ("k_new", k_new, torch.bfloat16), ("v_new", v_new, torch.bfloat16),
+                        ("kv_pool", kv_pool, torch.bfloat16), ("seq_lens", seq_lens, torch.int32),
+                        ("cu_q", cu_q, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name}: expected a contiguous CUDA {dt} tensor")
+    if block_table is not None and (block_table.dtype != torch.int32 or not block_table.is_cuda
+                                    or not block_table.is_contiguous()):
+        raise TypeError("block_table: expected a contiguous CUDA int32 tensor or None")
+    total_q, hq, d, page, pages = _shape_args(q, kv_pool, block_table, n_heads_kv, num_pages)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if tuple(t.shape) != (total_q, int(n_heads_kv), d):
+            raise ValueError(f"{name}: expected shape {(total_q, int(n_heads_kv), d)}, got {tuple(t.shape)}")
+    rc = _lib.load().pattn_forward_append(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens),
+        _ptr(cu_q), int(seq_lens.numel()), total_q, int(max_q), int(max_kv), hq, int(n_heads_kv), d,
+        page, pages, float(scale), int(bool(causal)), _stream_handle(stream))
+    if check:
+        _check(rc, "pattn_forward_append")
+    return rc
+
+
 def forward_noalloc(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,
                     n_heads_kv: int, scale: float, causal: bool, num_pages: Optional[int] = None,
                     stream=None, check: bool = True) -> int:
@@ -156,6 +189,14 @@ def device_status(stream=None) -> int:
 
 def profile_enable(on: bool = True) -> None:
     _check(_lib.load().pattn_profile_enable(int(bool(on))), "pattn_profile_enable")
+
+
+def profile_read_kernels() -> Tuple[Tuple[float, float, float, float, float], int]:
+    """((ms plan, ms cache write, ms decode kernel, ms prefill kernel, ms after), calls)."""
+    ms = (ctypes.c_double * 5)()
+    n = ctypes.c_int()
+    _check(_lib.load().pattn_profile_read_kernels(ms, ctypes.byref(n)), "pattn_profile_read_kernels")
+    return tuple(ms[i] for i in range(5)), n.value
 
 
 def profile_read() -> Tuple[float, float, float, int]:

@@ -18,6 +18,8 @@ _dp = ctypes.POINTER(ctypes.c_double)
 _ip = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "pattn_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "pattn_forward_append": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                  _f, _i, _vp]),
     "pattn_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
                                    _vp]),
     "pattn_forward_host": (_i, [_vp, _vp, _vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
@@ -28,6 +30,7 @@ SIGNATURES = {
     "pattn_status_string": (ctypes.c_char_p, [_i]),
     "pattn_profile_enable": (_i, [_i]),
     "pattn_profile_read": (_i, [_dp, _dp, _dp, _ip]),
+    "pattn_profile_read_kernels": (_i, [_dp, _ip]),
 }
 
 _lock = threading.Lock()

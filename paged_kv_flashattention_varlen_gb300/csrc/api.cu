@@ -26,7 +26,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 // Events around plan | decode kernel | prefill kernel | merge of prefill splits.
 struct ProfileRec {
-  cudaEvent_t ev[5];
+  cudaEvent_t ev[6];  // plan | cache write | decode | prefill | merge
 };
 
 struct DeviceState {
@@ -43,7 +43,6 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
-double g_last_split[2] = {0, 0};  // decode-kernel and prefill-kernel ms of the last profile read
 EncodeTiledFn g_encode = nullptr;
 bool g_profile = false;
 
@@ -221,7 +220,8 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
                         const void* kv, const int32_t* bt, const int32_t* seq_lens,
                         const int32_t* cu_q, int num_seqs, int total_q, int max_q, int max_kv,
                         int hq, int hkv, int d, int num_pages, float scale, int causal,
-                        cudaStream_t stream, const Shape& sh) {
+                        cudaStream_t stream, const Shape& sh, const void* k_new = nullptr,
+                        const void* v_new = nullptr) {
   pattn_status s = PATTN_OK;
 
   Workspace ws{};
@@ -344,16 +344,36 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   cudaError_t e = launch_plan(pp, stream);
   if (e != cudaSuccess) return PATTN_ERR_CUDA;
   if (prof) cudaEventRecord(rec.ev[1], stream);
+  if (k_new) {
+    // the new tokens' K and V rows into their cache slots, before any attention
+    // kernel reads the cache (which waits for this grid on the device)
+    KvWriteParams wp{};
+    wp.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    wp.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    wp.kv_pool = static_cast<__nv_bfloat16*>(const_cast<void*>(kv));
+    wp.block_table = bt;
+    wp.cu_q = cu_q;
+    wp.seq_info = ws.seq_info;
+    wp.err = ws.hdr + kHdrErr;
+    wp.num_seqs = num_seqs;
+    wp.total_q = total_q;
+    wp.bt_stride = pp.bt_stride;
+    wp.num_pages = num_pages;
+    wp.row_elems = hkv * d;
+    e = launch_kv_write(wp, st.sms, stream);
+    if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  }
+  if (prof) cudaEventRecord(rec.ev[2], stream);
   if (dec_enabled) {
     e = launch_decode(dp, tq_dec, tkv, d, st.sms, stream, dep);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
-  if (prof) cudaEventRecord(rec.ev[2], stream);
+  if (prof) cudaEventRecord(rec.ev[3], stream);
   if (run_prefill) {
     e = launch_attention(ap, tq, tkv, d, st.sms, stream, dep);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
-  if (prof) cudaEventRecord(rec.ev[3], stream);
+  if (prof) cudaEventRecord(rec.ev[4], stream);
   if (run_prefill) {
     // split units of the prefill kernel (single-q-tile units of more than
     // kDecRows rows) are merged by a separate pass; the decode kernel merges its own
@@ -361,7 +381,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (prof) {
-    cudaEventRecord(rec.ev[4], stream);
+    cudaEventRecord(rec.ev[5], stream);
     st.prof.push_back(rec);
   }
   return PATTN_OK;
@@ -371,7 +391,8 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
                             const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
                             int total_q, int max_q, int max_kv, int hq, int hkv, int d, int page,
                             int num_pages, float scale, int causal, cudaStream_t stream,
-                            const Shape& sh) {
+                            const Shape& sh, const void* k_new = nullptr,
+                            const void* v_new = nullptr) {
   (void)page;
   DeviceState* stp = nullptr;
   pattn_status s = device_state(&stp);
@@ -380,7 +401,8 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
   const WsLayout L = ws_layout(num_seqs, total_q, max_q, hq, hkv, d);
   if ((s = ensure_workspace(st, L.total)) != PATTN_OK) return s;
   return launch_all(st, static_cast<uint8_t*>(st.ws), L, out, q, kv, bt, seq_lens, cu_q, num_seqs,
-                    total_q, max_q, max_kv, hq, hkv, d, num_pages, scale, causal, stream, sh);
+                    total_q, max_q, max_kv, hq, hkv, d, num_pages, scale, causal, stream, sh, k_new,
+                    v_new);
 }
 
 // ---------------------------------------------------------------------------
@@ -427,6 +449,26 @@ pattn_status pattn_forward(void* out, const void* q, const void* kv_pool,
   return forward_locked(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
                         max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, scale,
                         causal, reinterpret_cast<cudaStream_t>(stream), sh);
+}
+
+pattn_status pattn_forward_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                  void* kv_pool, const int32_t* block_table,
+                                  const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
+                                  int total_q, int max_q, int max_kv, int n_heads_q,
+                                  int n_heads_kv, int head_dim, int page_size, int num_pages,
+                                  float scale, int causal, pattn_stream_t stream) {
+  Shape sh{};
+  pattn_status s = check_args(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                              max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size,
+                              num_pages, scale, causal, &sh);
+  if (s != PATTN_OK) return s;
+  if (total_q > 0 && (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)))
+    return PATTN_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return forward_locked(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
+                        max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, scale,
+                        causal, reinterpret_cast<cudaStream_t>(stream), sh, k_new, v_new);
 }
 
 pattn_status pattn_forward_noalloc(void* out, const void* q, const void* kv_pool,
@@ -584,31 +626,44 @@ pattn_status pattn_profile_enable(int on) {
   return PATTN_OK;
 }
 
-pattn_status pattn_profile_read(double* ms_plan, double* ms_attention, double* ms_combine,
-                                int* calls) {
-  std::lock_guard<std::mutex> lk(g_mu);
+// Sums the recorded calls' per-kernel device time: plan, cache write, decode
+// kernel, prefill kernel, after the attention kernels. Caller holds g_mu.
+pattn_status profile_sum(double t[5], int* calls) {
   DeviceState* stp = nullptr;
   pattn_status s = device_state(&stp);
   if (s != PATTN_OK) return s;
   DeviceState& st = *stp;
-  double t[4] = {0, 0, 0, 0};
+  for (int k = 0; k < 5; ++k) t[k] = 0.0;
   for (auto& r : st.prof) {
-    if (cudaEventSynchronize(r.ev[4]) != cudaSuccess) return PATTN_ERR_CUDA;
-    for (int k = 0; k < 4; ++k) {
+    if (cudaEventSynchronize(r.ev[5]) != cudaSuccess) return PATTN_ERR_CUDA;
+    for (int k = 0; k < 5; ++k) {
       float ms = 0.f;
       if (cudaEventElapsedTime(&ms, r.ev[k], r.ev[k + 1]) != cudaSuccess) return PATTN_ERR_CUDA;
       t[k] += ms;
     }
   }
-  g_last_split[0] = t[1];
-  g_last_split[1] = t[2];
-  if (ms_plan) *ms_plan = t[0];
-  if (ms_attention) *ms_attention = t[1] + t[2];
-  if (ms_combine) *ms_combine = t[3];
   if (calls) *calls = static_cast<int>(st.prof.size());
   for (auto& r : st.prof) st.prof_pool.push_back(r);
   st.prof.clear();
   return PATTN_OK;
+}
+
+pattn_status pattn_profile_read(double* ms_plan, double* ms_attention, double* ms_combine,
+                                int* calls) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  double t[5];
+  const pattn_status s = profile_sum(t, calls);
+  if (s != PATTN_OK) return s;
+  if (ms_plan) *ms_plan = t[0];
+  if (ms_attention) *ms_attention = t[2] + t[3];
+  if (ms_combine) *ms_combine = t[4];
+  return PATTN_OK;
+}
+
+pattn_status pattn_profile_read_kernels(double* ms, int* calls) {
+  if (!ms) return PATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return profile_sum(ms, calls);
 }
 
 }  // extern "C"

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cstdint>
 
 namespace pattn {
@@ -69,6 +70,19 @@ struct PlanParams {
   int min_chunk;        // fewest KV tiles per split
 };
 
+// Cache write of the new tokens' K and V rows (kvwrite.cu).
+struct KvWriteParams {
+  const __nv_bfloat16* k_new;   // [total_q][n_heads_kv][head_dim]
+  const __nv_bfloat16* v_new;   // [total_q][n_heads_kv][head_dim]
+  __nv_bfloat16* kv_pool;       // the cache (paged or contiguous layout)
+  const int32_t* block_table;   // nullptr: contiguous cache
+  const int32_t* cu_q;
+  const int4* seq_info;         // from the plan: (first token, ql or -1, L, first contiguous row)
+  int* err;
+  int num_seqs, total_q, bt_stride, num_pages;
+  int row_elems;                // n_heads_kv * head_dim
+};
+
 struct AttnParams {
   const int4* items;
   const int* hdr;
@@ -108,6 +122,7 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
+cudaError_t launch_kv_write(const KvWriteParams& p, int sms, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                              int head_dim, int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s, bool dependent);

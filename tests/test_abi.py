@@ -69,9 +69,29 @@ def test_host_validation(lib):
     assert fwd(lib, B=0) == 0 and fwd(lib, tq=0) == 0   # nothing to do
 
 
+def append(lib, k=ALIGNED, v=ALIGNED, **kw):
+    a = dict(out=ALIGNED, q=ALIGNED, kv=ALIGNED, bt=ALIGNED, sl=ALIGNED, cu=ALIGNED, B=2, tq=16,
+             mq=8, mkv=650, hq=24, hkv=4, d=256, P=64, pages=22, scale=0.0625, causal=1)
+    a.update(kw)
+    return lib.pattn_forward_append(a["out"], a["q"], k, v, a["kv"], a["bt"], a["sl"], a["cu"], a["B"],
+                                    a["tq"], a["mq"], a["mkv"], a["hq"], a["hkv"], a["d"], a["P"],
+                                    a["pages"], a["scale"], a["causal"], None)
+
+
+def test_append_host_validation(lib):
+    INVALID = 1
+    assert append(lib, k=None) == INVALID
+    assert append(lib, v=None) == INVALID
+    assert append(lib, k=ALIGNED + 4) == INVALID        # not 16-byte aligned
+    assert append(lib, kv=None) == INVALID
+    assert append(lib, hq=25) == INVALID
+    assert append(lib, k=None, tq=0) == 0               # nothing to write or attend
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers must not reach a GPU")
 def test_valid_call_without_a_gpu_reports_cuda_error(lib):
     assert fwd(lib) == 3
+    assert append(lib) == 3
 
 
 def test_workspace_size(lib):

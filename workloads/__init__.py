@@ -31,7 +31,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
-from typing import List, Optional, Sequence
+from typing import List, Optional, Sequence, Tuple
 
 import numpy as np
 import torch
@@ -206,6 +206,16 @@ def make_contiguous(
         num_pages=max(rows, 1), scale=float(scale), causal=bool(causal),
         max_q=max(q_lens) if q_lens else 0, max_kv=max(kv_lens) if kv_lens else 0,
     )
+
+
+def new_kv_rows(wl: Workload, seed: int) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Seeded K and V rows of the query tokens, bf16 ``[total_q, Hkv, D]`` each
+    (standard normal, like the pool), for the cache write in front of attention."""
+    rng = np.random.default_rng(seed)
+    shape = (int(wl.q.shape[0]), wl.n_heads_kv, wl.head_dim)
+    k = rng.standard_normal(shape, dtype=np.float32)
+    v = rng.standard_normal(shape, dtype=np.float32)
+    return _bf16(k), _bf16(v)
 
 
 NAMES: List[str] = [
