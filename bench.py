@@ -53,6 +53,9 @@ def parse():
                     help="profiling runs: time one workload only")
     ap.add_argument("--workload", default=None,
                     help="time named workload(s) 1-5 (comma list or 'all'): one JSON line each")
+    ap.add_argument("--append", action="store_true",
+                    help="with --workload: each step first writes the query tokens' K/V rows into "
+                         "their cache slots (pattn_forward_append)")
     return ap.parse_args()
 
 
@@ -148,6 +151,20 @@ def profiled_pass(pk, step, steps):
     torch.cuda.synchronize()
     pk.profile_enable(False)
     return pk.profile_read()
+
+
+def profiled_kernels(pk, step, steps):
+    """As :func:`profiled_pass`, split by kernel: ((plan, cache write, decode,
+    prefill, after) ms summed over the calls, calls)."""
+    import torch
+    torch.cuda.synchronize()
+    pk.profile_read()
+    pk.profile_enable(True)
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    pk.profile_enable(False)
+    return pk.profile_read_kernels()
 
 
 def run_ours(args):
@@ -419,11 +436,19 @@ def run_workloads(args):
         bt = None if wl.block_table is None else wl.block_table.to(dev)
         sl, cu = wl.seq_lens.to(dev), wl.cu_q.to(dev)
         out = torch.empty_like(q)
+        k_new = v_new = None
+        if args.append:
+            k_new, v_new = (t.to(dev) for t in workloads.new_kv_rows(wl, 900 + i))
 
         def step():
-            pk.forward(out, q, kv, bt, sl, cu, max_q=wl.max_q, max_kv=wl.max_kv,
-                       n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
-                       num_pages=wl.num_pages, check=False)
+            if args.append:
+                pk.forward_append(out, q, k_new, v_new, kv, bt, sl, cu, max_q=wl.max_q,
+                                  max_kv=wl.max_kv, n_heads_kv=wl.n_heads_kv, scale=wl.scale,
+                                  causal=wl.causal, num_pages=wl.num_pages, check=False)
+            else:
+                pk.forward(out, q, kv, bt, sl, cu, max_q=wl.max_q, max_kv=wl.max_kv,
+                           n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
+                           num_pages=wl.num_pages, check=False)
 
         flops = 4.0 * wl.head_dim * wl.n_heads_q * wl.visible_pairs()
         nbytes = wl.kv_bytes() + wl.qo_bytes()
@@ -438,7 +463,8 @@ def run_workloads(args):
             step()
         e1.record()
         torch.cuda.synchronize()
-        t_plan, t_attn, t_comb, calls = profiled_pass(pk, step, min(steps, 500))
+        kt, calls = profiled_kernels(pk, step, min(steps, 500))
+        t_plan, t_write, t_attn, t_comb = kt[0], kt[1], kt[2] + kt[3], kt[4]
         ms = e0.elapsed_time(e1) / steps
         attn_ms = t_attn / max(calls, 1)
         line = {
@@ -449,9 +475,19 @@ def run_workloads(args):
             "hbm_frac_attention": round(nbytes / (attn_ms * 1e-3) / 1e9 / hbm, 4),
             "tensor_frac_attention": round(flops / (attn_ms * 1e-3) / 1e12 / tc, 4),
             "plan_ms": round(t_plan / max(calls, 1), 5), "combine_ms": round(t_comb / max(calls, 1), 5),
+            "decode_kernel_ms": round(kt[2] / max(calls, 1), 5),
+            "prefill_kernel_ms": round(kt[3] / max(calls, 1), 5),
             "bytes": nbytes, "flops": flops, "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 {tc} TFLOP/s",
             "device_status": pk.device_status(),
         }
+        if args.append:
+            # K and V rows of every query token read once and written once
+            wbytes = 4 * int(wl.q.shape[0]) * wl.n_heads_kv * wl.head_dim * 2
+            write_ms = t_write / max(calls, 1)
+            line["workload"] += "+kv_write"
+            line["kv_write_ms"] = round(write_ms, 5)
+            line["kv_write_bytes"] = wbytes
+            line["kv_write_hbm_frac"] = round(wbytes / (write_ms * 1e-3) / 1e9 / hbm, 4)
         print(json.dumps(line), flush=True)
         del q, kv, bt, sl, cu, out
         torch.cuda.empty_cache()

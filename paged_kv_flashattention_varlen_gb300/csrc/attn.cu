@@ -246,7 +246,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     uint32_t n = 0, itl = 0;
     bool ok = true;
     const uint64_t pol_q = l2_policy_evict_last();
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
+         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
       const Item it = decode_item(p.items[idx]);
       const int4 si = p.seq_info[it.b];
       const int q0 = si.x, L = si.z, kv0 = si.w;
@@ -350,9 +351,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       uint32_t n = 0, itl = 0;
       bool ok = true;
       int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+      for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
+         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
         const Item it = decode_item(iv_next);
-        if (idx + static_cast<int>(gridDim.x) < n_items) iv_next = p.items[idx + gridDim.x];
+        if (cta_item(kq + 1, blockIdx.x, gridDim.x) < n_items)
+          iv_next = p.items[cta_item(kq + 1, blockIdx.x, gridDim.x)];
         const uint32_t qb = itl % C::kQBufs, qu = itl / C::kQBufs;
         if (!(ok = wait_one(bar(kQFull0 + qb), qu & 1u, ctl))) break;
         tc_fence_after();
@@ -394,11 +397,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     bool ok = true;
     int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
     int L_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask].z : 0;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok; idx = cta_item(++kq, blockIdx.x, gridDim.x)) {
       const Item it = decode_item(iv_next);
       const int L = L_next;
-      if (idx + static_cast<int>(gridDim.x) < n_items) {
-        iv_next = p.items[idx + gridDim.x];
+      if (cta_item(kq + 1, blockIdx.x, gridDim.x) < n_items) {
+        iv_next = p.items[cta_item(kq + 1, blockIdx.x, gridDim.x)];
         L_next = p.seq_info[iv_next.x & kSeqMask].z;
       }
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
@@ -469,11 +472,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     // The next item's descriptor and sequence are loaded one item ahead.
     int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
     int4 si_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
+         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
       const Item it = decode_item(iv_next);
       const int4 si = si_next;
-      const bool has_next = idx + static_cast<int>(gridDim.x) < n_items;
-      if (has_next) iv_next = p.items[idx + gridDim.x];
+      const int idx_next = cta_item(kq + 1, blockIdx.x, gridDim.x);
+      const bool has_next = idx_next < n_items;
+      if (has_next) iv_next = p.items[idx_next];
       const int q0 = si.x, ql = si.y, L = si.z;
       const int tok = it.qt * T + t_local;
       const bool valid = (t_local < T) && (tok < ql);
@@ -672,11 +677,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     bool ok = true;
     int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
     int4 si_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
+         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
       const Item it = decode_item(iv_next);
       const int4 si = si_next;
-      const bool has_next = idx + static_cast<int>(gridDim.x) < n_items;
-      if (has_next) iv_next = p.items[idx + gridDim.x];
+      const int idx_next = cta_item(kq + 1, blockIdx.x, gridDim.x);
+      const bool has_next = idx_next < n_items;
+      if (has_next) iv_next = p.items[idx_next];
       const int q0 = si.x, ql = si.y, L = si.z;
       const int tok = it.qt * T + t_local;
       const bool valid = (t_local < T) && (tok < ql);

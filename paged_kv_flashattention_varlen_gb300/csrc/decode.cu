@@ -313,7 +313,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     bool ok = true;
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
+         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
       const int4 iv = p.items[idx];
       const int b = iv.x & kSeqMask, hk = iv.y >> 16;
       const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
@@ -418,7 +419,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         umma_commit(bar(kDPVDone0 + (m & 1u)));
         return true;
       };
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++itl) {
+      for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
+         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
         const int4 iv = p.items[idx];
         const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
         if (!(ok = wait_one(bar(kDQFull), itl & 1u, ctl))) break;
@@ -453,7 +455,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     // ------------------------------------------------------------ ring forwarder / V tail fix
     uint32_t n = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok; idx = cta_item(++kq, blockIdx.x, gridDim.x)) {
       const int4 iv = p.items[idx];
       const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
       const int L = p.seq_info[iv.x & kSeqMask].z;
@@ -484,7 +486,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     // warps' path.
     uint32_t nsp = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok; idx = cta_item(++kq, blockIdx.x, gridDim.x)) {
       const int4 iv = p.items[idx];
       if (iv.w < 0) continue;
       if (!(ok = wait_warp(bar(kDMerge0), nsp & 1u, ctl))) break;
@@ -519,7 +521,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     x.merge_flag = reinterpret_cast<volatile int*>(misc + 32);
     uint32_t n = 0, itl = 0, nsp = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok; idx = cta_item(++kq, blockIdx.x, gridDim.x)) {
       const int4 iv = p.items[idx];
       const int4 si = p.seq_info[iv.x & kSeqMask];
       const int rows = si.y * G;

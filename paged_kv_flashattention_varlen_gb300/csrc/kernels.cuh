@@ -103,6 +103,13 @@ struct AttnParams {
 
 
 // Launchers (defined in the .cu files; return the launch error).
+// The k-th work item of CTA c out of P. The item lists are sorted longest first
+// and the rounds alternate direction (c, 2P-1-c, 2P+c, 4P-1-c, ...), so that
+// each CTA's share of the sorted costs comes out about even. Increasing in k.
+__device__ __forceinline__ int cta_item(int k, int c, int P) {
+  return (k & 1) ? (k + 1) * P - 1 - c : k * P + c;
+}
+
 // Kernel launch; with `dependent` the grid may begin (up to its grid_dep_wait)
 // while the previous grid in the stream finishes.
 template <typename... KArgs, typename... Args>
