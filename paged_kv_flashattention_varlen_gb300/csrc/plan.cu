@@ -182,10 +182,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     }
     __syncthreads();
   }
-  atomicAdd(&s_tiles, my_tiles * static_cast<unsigned long long>(p.n_heads_kv));
+  // total work: a warp sum, then one shared-memory atomic per warp that has any
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) my_tiles += __shfl_xor_sync(0xffffffffu, my_tiles, o);
+  if (lane == 0 && my_tiles != 0)
+    atomicAdd(&s_tiles, my_tiles * static_cast<unsigned long long>(p.n_heads_kv));
 
   // ---- pass 1b: every live block-table entry must name a pool page (a warp per
-  // sequence, four independent loads per lane in flight)
+  // sequence, eight independent loads per lane in flight)
   if (p.block_table) {
     for (int b = warp; b < B; b += kPlanThreads / 32) {
       const int4 sq = seq_at(b);
@@ -193,15 +197,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       const int np = cdiv(sq.z, kPage);
       const int32_t* row = p.block_table + static_cast<size_t>(b) * p.bt_stride;
       bool bad = false;
-      for (int s0 = 0; s0 < np; s0 += 128) {
-        int pg[4];
+      for (int s0 = 0; s0 < np; s0 += 256) {
+        int pg[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const int s = s0 + u * 32 + lane;
           pg[u] = s < np ? row[s] : 0;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) bad |= pg[u] < 0 || pg[u] >= p.num_pages;
+        for (int u = 0; u < 8; ++u) bad |= pg[u] < 0 || pg[u] >= p.num_pages;
       }
       if (__any_sync(0xffffffffu, bad) && lane == 0) {
         ws.seq_info[b].y = -1;
