@@ -1,0 +1,121 @@
+"""Pins for the quantised-QK oracle (CPU only): the e4m3 format from its
+definition, the scale rule, the block layout of the K codes, the smoothing
+invariance, and the dequantised attention against the C oracle where the
+quantisation is exact."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from oracle import quant
+
+
+def e4m3_from_definition(code: int) -> float:
+    """Value of an e4m3 byte: sign, 4 exponent bits (bias 7), 3 mantissa bits;
+    exponent 0 is subnormal; 0x7F / 0xFF are NaN."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def test_e4m3_values_match_the_format_definition():
+    codes = np.arange(256, dtype=np.uint8)
+    got = quant.e4m3_values(codes)
+    for c in range(256):
+        want = e4m3_from_definition(c)
+        if math.isnan(want):
+            assert math.isnan(got[c])
+        else:
+            assert got[c] == want, c
+
+
+@pytest.mark.parametrize("x,code", [
+    (0.0, 0x00), (1.0, 0x38), (-1.0, 0xB8), (448.0, 0x7E), (1000.0, 0x7E), (-1000.0, 0xFE),
+    (2.0 ** -9, 0x01),                      # smallest subnormal
+    (1.0625, 0x38), (1.1875, 0x3A),          # ties go to the even mantissa
+    (1.0625 + 1e-6, 0x39), (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02),
+])
+def test_e4m3_rounding(x, code):
+    assert int(quant.e4m3_codes(np.array([x], dtype=np.float32))[0]) == code
+
+
+def test_codes_are_nearest_and_saturated():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(4096) * 100).astype(np.float32)
+    c = quant.e4m3_codes(x)
+    v = quant.e4m3_values(c)
+    grid = np.array(sorted({e4m3_from_definition(k) for k in range(256) if not math.isnan(e4m3_from_definition(k))}))
+    clipped = np.clip(x.astype(np.float64), -448, 448)
+    nearest = grid[np.abs(grid[None, :] - clipped[:, None]).argmin(axis=1)]
+    assert np.all(np.abs(v - clipped) <= np.abs(nearest - clipped) + 0.0)
+
+
+def test_row_scale_maps_amax_to_448_and_zero_rows_to_zero():
+    q = np.zeros((3, 2, 128), dtype=np.float32)
+    q[0, 0, 5] = -3.25
+    q[0, 0, 7] = 1.0
+    q[1, 1] = np.linspace(-2, 7, 128, dtype=np.float32)
+    codes, s = quant.quantize_q(q)
+    assert s[0, 0] == np.float32(3.25) / np.float32(448)
+    assert quant.e4m3_values(codes[0, 0, 5:6])[0] == -448.0
+    assert s[2, 0] == 1.0 and not codes[2].any()
+    assert quant.e4m3_values(codes[1, 1]).max() == 448.0
+
+
+def test_k_blocks_of_64_keys_and_zero_tail():
+    rng = np.random.default_rng(5)
+    k = rng.standard_normal((100, 2, 128)).astype(np.float32)
+    m = quant.k_mean(k)
+    assert m.dtype == np.float32
+    assert np.allclose(m, k.astype(np.float64).mean(axis=0), atol=1e-7)
+    codes, scales = quant.quantize_k(k, m)
+    assert codes.shape == (128, 2, 128) and scales.shape == (2, 2)
+    assert not codes[100:].any()
+    x = k - m[None]
+    assert scales[1, 0] == np.float32(np.abs(x[64:100, 0]).max()) / np.float32(448)
+
+
+def test_exact_quantisation_reproduces_the_plain_attention():
+    # values on the e4m3 grid with a power-of-two row maximum of 448 * 2^-6, and
+    # K in +- pairs per channel (zero mean): the codes are exact, so the
+    # dequantised attention must equal the float64 C oracle on the same inputs
+    rng = np.random.default_rng(7)
+    grid = np.array([0.0, 0.25, 0.5, 1.0, 1.5, 2.0, 3.0, 448.0])
+    T, Hq, Hkv, D, L = 4, 4, 2, 128, 64
+    q = rng.choice(grid, size=(T, Hq, D)) * rng.choice([-1, 1], size=(T, Hq, D))
+    q[..., 0] = 448.0
+    half = rng.choice(grid[:-1], size=(L // 2, Hkv, D)) * rng.choice([-1, 1], size=(L // 2, Hkv, D))
+    k = np.concatenate([half, -half], axis=0)
+    k[0, :, 1] = 448.0
+    k[L // 2, :, 1] = -448.0
+    scale_pow = 2.0 ** -6
+    q *= scale_pow
+    k *= scale_pow
+    wl = workloads.make_paged("exactq", 3, [T], [L], Hq, Hkv, D, causal=True, extra_pages=1)
+    wl.q.copy_(torch.from_numpy(q).to(torch.bfloat16))
+    page = int(wl.block_table[0, 0])
+    wl.kv_pool[page, 0, :L].copy_(torch.from_numpy(k).to(torch.bfloat16))
+    qz = quant.quantize_workload(wl)
+    assert np.array_equal(quant.e4m3_values(qz["q_codes"]) * qz["q_scale"][:, :, None], q)
+    assert np.array_equal(qz["k_mean"][0], np.zeros((Hkv, D), np.float32))
+    got = quant.attention_dequantized(wl, qz=qz)
+    ref, _ = oracle.forward_workload(wl)
+    assert np.abs(got - ref).max() < 1e-12
+
+
+def test_smoothing_keeps_channel_offsets_out_of_the_error():
+    # K with a large per-channel offset: with the mean removed the quantised
+    # attention stays close to the exact one
+    wl = workloads.make_contiguous("smooth", 9, [40], [300], 8, 2, 128, causal=False, k_offset_std=4.0)
+    ref, _ = oracle.forward_workload(wl)
+    got = quant.attention_dequantized(wl)
+    err = np.abs(got - ref)
+    assert err.max() < 0.1 and err.mean() < 0.01, (err.max(), err.mean())
