@@ -120,6 +120,54 @@ pattn_status pattn_forward_append(void *out, const void *q, const void *k_new, c
                                   int n_heads_kv, int head_dim, int page_size, int num_pages,
                                   float scale, int causal, pattn_stream_t stream);
 
+/*
+ * pattn_forward_fp8qk -- the quantised-QK variant: SageAttention2's preparation
+ * phases as on the GB10 "sage2" benchmark page (K-mean smoothing, Q and K
+ * quantisation; phases k_mean_and_smoothing_preparation, q_int8_quantization,
+ * k_int8_subtract_mean_quantization), with e4m3 codes instead of int8 (on this
+ * part the e4m3 tensor rate is twice the bf16 one and the int8 rate is far
+ * below it), then attention with S = Q K^T from e4m3 codes and O = P V in bf16.
+ * Same arguments and output as pattn_forward; head_dim 128 only.
+ *
+ *   K is smoothed per (sequence, KV head, channel) by its mean over the
+ *   sequence's keys (the softmax cancels the shift); each 64-key block of a
+ *   sequence and KV head gets one scale, each query row (token, head) one:
+ *   scale = amax / 448, code = e4m3 round-to-nearest-even of x / scale,
+ *   saturated. The result is attention over the dequantised Q and K.
+ *   Units of at most 16 packed query rows (decode) take the bf16 decode kernel.
+ *   Needs pattn_workspace_size_fp8qk bytes of workspace.
+ */
+pattn_status pattn_forward_fp8qk(void *out, const void *q, const void *kv_pool,
+                                 const int32_t *block_table, const int32_t *seq_lens,
+                                 const int32_t *cu_q, int num_seqs, int total_q, int max_q,
+                                 int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
+                                 int page_size, int num_pages, float scale, int causal,
+                                 pattn_stream_t stream);
+
+/*
+ * pattn_quantize_qk -- only the codes and scales of pattn_forward_fp8qk, into
+ * caller-owned device buffers (nb = 2 * ceil(max_kv / 128)):
+ *
+ *   q8       e4m3 bytes [total_q][n_heads_q][128], 16-byte aligned
+ *   q_scale  fp32 [total_q][n_heads_q]
+ *   k8       e4m3 bytes [num_seqs * nb][64][n_heads_kv][128], 16-byte aligned:
+ *            64-key block j of sequence b is block b * nb + j; key rows past
+ *            L_b in its last block are zero; later blocks are not written
+ *   k_scale  fp32 [num_seqs * nb][n_heads_kv] (written for the same blocks)
+ *
+ * Other arguments as for pattn_forward. Rejected sequences (device error word)
+ * are not written.
+ */
+pattn_status pattn_quantize_qk(void *q8, float *q_scale, void *k8, float *k_scale, const void *q,
+                               const void *kv_pool, const int32_t *block_table,
+                               const int32_t *seq_lens, const int32_t *cu_q, int num_seqs,
+                               int total_q, int max_q, int max_kv, int n_heads_q, int n_heads_kv,
+                               int head_dim, int page_size, int num_pages, pattn_stream_t stream);
+
+/* Workspace bytes pattn_forward_fp8qk needs for these bounds (0 if unsupported). */
+size_t pattn_workspace_size_fp8qk(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
+                                  int n_heads_kv, int head_dim, int page_size);
+
 /* Bytes of the fixed device scratch behind pattn_forward_noalloc. */
 #define PATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -116,53 +116,58 @@ def quantize_workload(wl):
                 k_scale=kss)
 
 
-def dequantized_workload(wl, qz=None):
-    """Dequantised Q (float64 [T, Hq, D]) and, per sequence, dequantised smoothed
-    K (float64 [L, Hkv, D]): code * scale, exact in float64."""
-    qz = qz or quantize_workload(wl)
-    q_deq = e4m3_values(qz["q_codes"]) * qz["q_scale"].astype(np.float64)[:, :, None]
-    k_rows = []
-    for b in range(wl.num_seqs):
-        L = int(wl.seq_lens[b])
-        kd = e4m3_values(qz["k_codes"][b]) * np.repeat(qz["k_scale"][b].astype(np.float64), 64, axis=0)[:, :, None]
-        k_rows.append(kd[:L])
-    return q_deq, k_rows
-
-
 def attention_dequantized(wl, rows=None, qz=None):
     """float64 attention of the quantised-QK method: softmax(scale * q^ . k^) v
     with q^, k^ the dequantised (smoothed) Q and K and v the bf16 V, per query
-    token (all, or the global token indices in ``rows``). Returns [n, Hq, D]."""
-    q_deq, k_rows = dequantized_workload(wl, qz)
-    G = wl.n_heads_q // wl.n_heads_kv
+    token (all, or the global token indices in ``rows``). Returns [n, Hq, D].
+
+    Q rows are quantised independently, so only the requested ones are; K is
+    quantised (and dequantised head by head) for the sequences those rows
+    belong to. ``qz`` (from :func:`quantize_workload`) may be given instead.
+    """
     cu = wl.cu_q.numpy().astype(np.int64)
     sl = wl.seq_lens.numpy().astype(np.int64)
     starts = np.concatenate([[0], np.cumsum(sl)])
+    toks = np.arange(int(cu[-1])) if rows is None else np.asarray(list(rows), dtype=np.int64)
+    G = wl.n_heads_q // wl.n_heads_kv
+    if qz is None:
+        qc, qs = quantize_q(_bf16_to_f32(wl.q[torch_index(toks)]))
+    else:
+        qc, qs = qz["q_codes"][toks], qz["q_scale"][toks]
+    q_deq = e4m3_values(qc) * qs.astype(np.float64)[:, :, None]
+    seq_of = np.searchsorted(cu, toks, side="right") - 1
     pool = wl.kv_pool.detach().cpu()
-    toks = range(int(cu[-1])) if rows is None else rows
     out = np.zeros((len(toks), wl.n_heads_q, wl.head_dim), dtype=np.float64)
-    seq_of = np.searchsorted(cu, np.asarray(list(toks), dtype=np.int64), side="right") - 1
-    cache_v = {}
-    for n, (t, b) in enumerate(zip(toks, seq_of)):
+    for b in np.unique(seq_of):
+        b = int(b)
         L = int(sl[b])
         ql = int(cu[b + 1] - cu[b])
-        pos = L - ql + (t - int(cu[b]))
-        if b not in cache_v:
-            if wl.block_table is None:
-                v = pool[1, starts[b]:starts[b] + L].double().numpy()
-            else:
-                j = np.arange(L)
-                pages = wl.block_table[b].numpy()[j // wl.page_size]
-                v = pool[pages, 1, j % wl.page_size].double().numpy()
-            cache_v[b] = v
-        v = cache_v[b]
-        k = k_rows[b]
-        nk = min(L, pos + 1) if wl.causal else L
-        if nk <= 0:
-            continue
-        for h in range(wl.n_heads_q):
-            hk = h // G
-            s = (k[:nk, hk] @ q_deq[t, h]) * wl.scale
-            w = np.exp(s - s.max())
-            out[n, h] = (w @ v[:nk, hk]) / w.sum()
+        if qz is None:
+            k32 = logical_k(wl.kv_pool, wl.block_table, wl.seq_lens, b, wl.page_size, int(starts[b]))
+            kc, ks = quantize_k(k32, k_mean(k32))
+        else:
+            kc, ks = qz["k_codes"][b], qz["k_scale"][b]
+        if wl.block_table is None:
+            v = pool[1, starts[b]:starts[b] + L]
+        else:
+            j = np.arange(L)
+            v = pool[wl.block_table[b].numpy()[j // wl.page_size], 1, j % wl.page_size]
+        mine = np.nonzero(seq_of == b)[0]
+        for hk in range(wl.n_heads_kv):
+            k = e4m3_values(kc[:L, hk]) * np.repeat(ks[:, hk].astype(np.float64), 64)[:L, None]
+            vh = v[:, hk].double().numpy()
+            for n in mine:
+                pos = L - ql + (int(toks[n]) - int(cu[b]))
+                nk = min(L, pos + 1) if wl.causal else L
+                if nk <= 0:
+                    continue
+                for h in range(hk * G, (hk + 1) * G):
+                    s = (k[:nk] @ q_deq[n, h]) * wl.scale
+                    w = np.exp(s - s.max())
+                    out[n, h] = (w @ vh[:nk]) / w.sum()
     return out
+
+
+def torch_index(idx):
+    import torch
+    return torch.as_tensor(np.asarray(idx, dtype=np.int64))

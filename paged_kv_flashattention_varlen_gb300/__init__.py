@@ -14,7 +14,8 @@ from typing import Optional, Tuple
 
 from . import _lib
 
-__all__ = ["PattnError", "forward", "forward_append", "forward_noalloc", "forward_host", "workspace_size",
+__all__ = ["PattnError", "forward", "forward_append", "forward_fp8qk", "quantize_qk", "forward_noalloc",
+           "forward_host", "workspace_size",
            "set_workspace", "device_status", "status_string", "profile_enable", "profile_read",
            "profile_read_kernels", "STATUS", "library_path"]
 
@@ -125,6 +126,59 @@ def forward_append(out, q, k_new, v_new, kv_pool, block_table, seq_lens, cu_q, *
     if check:
         _check(rc, "pattn_forward_append")
     return rc
+
+
+def _check_device_args(out, q, kv_pool, block_table, seq_lens, cu_q):
+    import torch
+    for name, t, dt in (("out", out, torch.bfloat16), ("q", q, torch.bfloat16),
+                        ("kv_pool", kv_pool, torch.bfloat16), ("seq_lens", seq_lens, torch.int32),
+                        ("cu_q", cu_q, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name}: expected a contiguous CUDA {dt} tensor")
+    if block_table is not None and (block_table.dtype != torch.int32 or not block_table.is_cuda
+                                    or not block_table.is_contiguous()):
+        raise TypeError("block_table: expected a contiguous CUDA int32 tensor or None")
+
+
+def forward_fp8qk(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,
+                  n_heads_kv: int, scale: float, causal: bool, num_pages: Optional[int] = None,
+                  stream=None, check: bool = True) -> int:
+    """Quantised-QK attention (``pattn_forward_fp8qk``): K smoothed by its mean,
+    Q and K as e4m3 codes with row / 64-key block scales, PV in bf16. head_dim 128.
+    Arguments as for :func:`forward`."""
+    _check_device_args(out, q, kv_pool, block_table, seq_lens, cu_q)
+    total_q, hq, d, page, pages = _shape_args(q, kv_pool, block_table, n_heads_kv, num_pages)
+    rc = _lib.load().pattn_forward_fp8qk(
+        _ptr(out), _ptr(q), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens), _ptr(cu_q),
+        int(seq_lens.numel()), total_q, int(max_q), int(max_kv), hq, int(n_heads_kv), d, page,
+        pages, float(scale), int(bool(causal)), _stream_handle(stream))
+    if check:
+        _check(rc, "pattn_forward_fp8qk")
+    return rc
+
+
+def quantize_qk(q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,
+                n_heads_kv: int, num_pages: Optional[int] = None, stream=None):
+    """The e4m3 codes and scales of :func:`forward_fp8qk` (``pattn_quantize_qk``).
+
+    Returns ``(q8 uint8 [T, Hq, D], q_scale f32 [T, Hq], k8 uint8 [B * nb, 64, Hkv, D],
+    k_scale f32 [B * nb, Hkv])`` with ``nb = 2 * ceil(max_kv / 128)``; block j of
+    sequence b is ``b * nb + j``."""
+    import torch
+    total_q, hq, d, page, pages = _shape_args(q, kv_pool, block_table, n_heads_kv, num_pages)
+    B = int(seq_lens.numel())
+    nb = 2 * max(1, -(-int(max_kv) // 128))
+    dev = q.device
+    q8 = torch.zeros((total_q, hq, d), dtype=torch.uint8, device=dev)
+    qs = torch.zeros((total_q, hq), dtype=torch.float32, device=dev)
+    k8 = torch.zeros((B * nb, 64, int(n_heads_kv), d), dtype=torch.uint8, device=dev)
+    ks = torch.zeros((B * nb, int(n_heads_kv)), dtype=torch.float32, device=dev)
+    rc = _lib.load().pattn_quantize_qk(
+        _ptr(q8), _ptr(qs), _ptr(k8), _ptr(ks), _ptr(q), _ptr(kv_pool), _ptr(block_table),
+        _ptr(seq_lens), _ptr(cu_q), B, total_q, int(max_q), int(max_kv), hq, int(n_heads_kv), d, page,
+        pages, _stream_handle(stream))
+    _check(rc, "pattn_quantize_qk")
+    return q8, qs, k8, ks
 
 
 def forward_noalloc(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,

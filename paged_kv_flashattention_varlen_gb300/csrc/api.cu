@@ -194,14 +194,55 @@ pattn_status ensure_workspace(DeviceState& st, size_t need) {
 }
 
 pattn_status encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-                    const cuuint64_t* strides, const cuuint32_t* box) {
+                    const cuuint64_t* strides, const cuuint32_t* box,
+                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+  CUresult r = g_encode(m, dtype, static_cast<cuuint32_t>(rank),
                         const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PATTN_OK : PATTN_ERR_CUDA;
 }
+
+// Workspace regions of the quantised-QK variant, after the regular ones (see
+// QuantParams for the layouts). nb_max is even, so that both key halves of a
+// 128-key tile have a block.
+struct Fp8Layout {
+  size_t k_sum, q8, q_scale, k8, k_scale, total;
+  int nb_max;
+};
+Fp8Layout fp8_layout(size_t base, int num_seqs, int total_q, int max_kv, int hq, int hkv, int d) {
+  Fp8Layout f{};
+  f.nb_max = 2 * std::max(1, cdiv(max_kv, 2 * kPage));
+  const size_t B = static_cast<size_t>(num_seqs), nb = static_cast<size_t>(f.nb_max);
+  size_t off = align_up(base, 256);
+  f.k_sum = off;
+  off += B * hkv * d * sizeof(double);
+  f.q8 = off = align_up(off, 256);
+  off += static_cast<size_t>(total_q) * hq * d;
+  f.q_scale = off = align_up(off, 256);
+  off += static_cast<size_t>(total_q) * hq * sizeof(float);
+  f.k8 = off = align_up(off, 256);
+  off += B * nb * kPage * hkv * d;
+  f.k_scale = off = align_up(off, 256);
+  off += B * nb * hkv * sizeof(float);
+  f.total = align_up(off, 256);
+  return f;
+}
+
+// What one call computes: attention (bf16 Q/K), attention with e4m3 Q/K codes,
+// or only the e4m3 codes of Q and K.
+enum class Mode { kBf16, kFp8, kQuantOnly };
+
+// Device buffers of the e4m3 codes (workspace regions or caller buffers).
+struct QuantBufs {
+  uint8_t* q8 = nullptr;
+  float* q_scale = nullptr;
+  uint8_t* k8 = nullptr;
+  float* k_scale = nullptr;
+  double* k_sum = nullptr;
+  int nb_max = 0;
+};
 
 ProfileRec take_events(DeviceState& st) {
   ProfileRec r{};
@@ -221,7 +262,8 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
                         const int32_t* cu_q, int num_seqs, int total_q, int max_q, int max_kv,
                         int hq, int hkv, int d, int num_pages, float scale, int causal,
                         cudaStream_t stream, const Shape& sh, const void* k_new = nullptr,
-                        const void* v_new = nullptr) {
+                        const void* v_new = nullptr, Mode mode = Mode::kBf16,
+                        const QuantBufs* qb = nullptr) {
   pattn_status s = PATTN_OK;
 
   Workspace ws{};
@@ -341,7 +383,13 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   // sets itself up while its predecessor finishes and waits for it on the device.
   // Profiling events between the launches turn that overlap off.
   const bool dep = !prof;
-  cudaError_t e = launch_plan(pp, stream);
+  cudaError_t e = cudaSuccess;
+  if (mode != Mode::kBf16) {
+    // the key sums of the quantisation start from zero
+    e = cudaMemsetAsync(qb->k_sum, 0, static_cast<size_t>(num_seqs) * hkv * d * sizeof(double), stream);
+    if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  }
+  e = launch_plan(pp, stream);
   if (e != cudaSuccess) return PATTN_ERR_CUDA;
   if (prof) cudaEventRecord(rec.ev[1], stream);
   if (k_new) {
@@ -363,14 +411,70 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     e = launch_kv_write(wp, st.sms, stream);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
+  if (mode != Mode::kBf16) {
+    // e4m3 codes and scales of Q and of the smoothed K (dependent launches)
+    QuantParams qp{};
+    qp.q = static_cast<const __nv_bfloat16*>(q);
+    qp.kv_pool = static_cast<const __nv_bfloat16*>(kv);
+    qp.block_table = bt;
+    qp.seq_info = ws.seq_info;
+    qp.q8 = qb->q8;
+    qp.q_scale = qb->q_scale;
+    qp.k8 = qb->k8;
+    qp.k_scale = qb->k_scale;
+    qp.k_sum = qb->k_sum;
+    qp.num_seqs = num_seqs;
+    qp.total_q = total_q;
+    qp.n_heads_q = hq;
+    qp.n_heads_kv = hkv;
+    qp.head_dim = d;
+    qp.bt_stride = pp.bt_stride;
+    qp.num_pages = num_pages;
+    qp.nb_max = qb->nb_max;
+    e = launch_quant_qk(qp, st.sms, stream);
+    if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  }
   if (prof) cudaEventRecord(rec.ev[2], stream);
+  if (mode == Mode::kQuantOnly) {
+    if (prof) {
+      for (int k = 3; k < 6; ++k) cudaEventRecord(rec.ev[k], stream);
+      st.prof.push_back(rec);
+    }
+    return PATTN_OK;
+  }
   if (dec_enabled) {
     e = launch_decode(dp, tq_dec, tkv, d, st.sms, stream, dep);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (prof) cudaEventRecord(rec.ev[3], stream);
   if (run_prefill) {
-    e = launch_attention(ap, tq, tkv, d, st.sms, stream, dep);
+    if (mode == Mode::kFp8) {
+      // e4m3 Q [total_q][hq][d] and K blocks [B * nb_max][64][hkv][d], one byte each
+      CUtensorMap tq8, tk8;
+      const cuuint64_t qdims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
+                                   static_cast<cuuint64_t>(hkv),
+                                   static_cast<cuuint64_t>(std::max(total_q, 1))};
+      const cuuint64_t qstr[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g) * d,
+                                  static_cast<cuuint64_t>(hq) * d};
+      const cuuint32_t qbox[4] = {128, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(T)};
+      if ((s = encode(&tq8, qb->q8, 4, qdims, qstr, qbox, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != PATTN_OK)
+        return s;
+      const cuuint64_t kdims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kPage),
+                                   static_cast<cuuint64_t>(hkv),
+                                   static_cast<cuuint64_t>(num_seqs) * qb->nb_max};
+      const cuuint64_t kstr[3] = {static_cast<cuuint64_t>(hkv) * d, static_cast<cuuint64_t>(d),
+                                  static_cast<cuuint64_t>(kPage) * hkv * d};
+      const cuuint32_t kbox[4] = {128, static_cast<cuuint32_t>(kPage), 1, 1};
+      if ((s = encode(&tk8, qb->k8, 4, kdims, kstr, kbox, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != PATTN_OK)
+        return s;
+      AttnParams fp = ap;
+      fp.q_scale = qb->q_scale;
+      fp.k_scale = qb->k_scale;
+      fp.nb_max = qb->nb_max;
+      e = launch_attention_fp8(fp, tq8, tk8, tkv, st.sms, stream, dep);
+    } else {
+      e = launch_attention(ap, tq, tkv, d, st.sms, stream, dep);
+    }
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (prof) cudaEventRecord(rec.ev[4], stream);
@@ -392,17 +496,27 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
                             int total_q, int max_q, int max_kv, int hq, int hkv, int d, int page,
                             int num_pages, float scale, int causal, cudaStream_t stream,
                             const Shape& sh, const void* k_new = nullptr,
-                            const void* v_new = nullptr) {
+                            const void* v_new = nullptr, Mode mode = Mode::kBf16) {
   (void)page;
   DeviceState* stp = nullptr;
   pattn_status s = device_state(&stp);
   if (s != PATTN_OK) return s;
   DeviceState& st = *stp;
   const WsLayout L = ws_layout(num_seqs, total_q, max_q, hq, hkv, d);
-  if ((s = ensure_workspace(st, L.total)) != PATTN_OK) return s;
-  return launch_all(st, static_cast<uint8_t*>(st.ws), L, out, q, kv, bt, seq_lens, cu_q, num_seqs,
-                    total_q, max_q, max_kv, hq, hkv, d, num_pages, scale, causal, stream, sh, k_new,
-                    v_new);
+  const Fp8Layout F = fp8_layout(L.total, num_seqs, total_q, max_kv, hq, hkv, d);
+  if ((s = ensure_workspace(st, mode == Mode::kBf16 ? L.total : F.total)) != PATTN_OK) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(st.ws);
+  QuantBufs qb;
+  if (mode != Mode::kBf16) {
+    qb.q8 = wsb + F.q8;
+    qb.q_scale = reinterpret_cast<float*>(wsb + F.q_scale);
+    qb.k8 = wsb + F.k8;
+    qb.k_scale = reinterpret_cast<float*>(wsb + F.k_scale);
+    qb.k_sum = reinterpret_cast<double*>(wsb + F.k_sum);
+    qb.nb_max = F.nb_max;
+  }
+  return launch_all(st, wsb, L, out, q, kv, bt, seq_lens, cu_q, num_seqs, total_q, max_q, max_kv, hq,
+                    hkv, d, num_pages, scale, causal, stream, sh, k_new, v_new, mode, &qb);
 }
 
 // ---------------------------------------------------------------------------
@@ -469,6 +583,74 @@ pattn_status pattn_forward_append(void* out, const void* q, const void* k_new, c
   return forward_locked(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
                         max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, scale,
                         causal, reinterpret_cast<cudaStream_t>(stream), sh, k_new, v_new);
+}
+
+pattn_status pattn_forward_fp8qk(void* out, const void* q, const void* kv_pool,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 const int32_t* cu_q, int num_seqs, int total_q, int max_q, int max_kv,
+                                 int n_heads_q, int n_heads_kv, int head_dim, int page_size,
+                                 int num_pages, float scale, int causal, pattn_stream_t stream) {
+  Shape sh{};
+  pattn_status s = check_args(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                              max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size,
+                              num_pages, scale, causal, &sh);
+  if (s != PATTN_OK) return s;
+  if (head_dim != 128) return PATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_seqs) * n_heads_kv > 0x7fffffffLL) return PATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return forward_locked(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
+                        max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, scale,
+                        causal, reinterpret_cast<cudaStream_t>(stream), sh, nullptr, nullptr,
+                        Mode::kFp8);
+}
+
+pattn_status pattn_quantize_qk(void* q8, float* q_scale, void* k8, float* k_scale, const void* q,
+                               const void* kv_pool, const int32_t* block_table,
+                               const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
+                               int total_q, int max_q, int max_kv, int n_heads_q, int n_heads_kv,
+                               int head_dim, int page_size, int num_pages, pattn_stream_t stream) {
+  Shape sh{};
+  // the attention's argument rules (a dummy output pointer; scale and causal unused)
+  pattn_status s = check_args(q, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
+                              max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, 1.0f, 0,
+                              &sh);
+  if (s != PATTN_OK) return s;
+  if (!q8 || !q_scale || !k8 || !k_scale || !aligned(q8, 16) || !aligned(k8, 16) ||
+      !aligned(q_scale, 4) || !aligned(k_scale, 4))
+    return PATTN_ERR_INVALID_ARG;
+  if (head_dim != 128) return PATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* stp = nullptr;
+  if ((s = device_state(&stp)) != PATTN_OK) return s;
+  DeviceState& st = *stp;
+  const WsLayout L = ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim);
+  const Fp8Layout F = fp8_layout(L.total, num_seqs, total_q, max_kv, n_heads_q, n_heads_kv, head_dim);
+  const size_t need = align_up(F.k_sum + static_cast<size_t>(num_seqs) * n_heads_kv * head_dim * 8, 256);
+  if ((s = ensure_workspace(st, need)) != PATTN_OK) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(st.ws);
+  QuantBufs qb;
+  qb.q8 = static_cast<uint8_t*>(q8);
+  qb.q_scale = q_scale;
+  qb.k8 = static_cast<uint8_t*>(k8);
+  qb.k_scale = k_scale;
+  qb.k_sum = reinterpret_cast<double*>(wsb + F.k_sum);
+  qb.nb_max = F.nb_max;
+  return launch_all(st, wsb, L, nullptr, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                    max_q, max_kv, n_heads_q, n_heads_kv, head_dim, num_pages, 1.0f, 0,
+                    reinterpret_cast<cudaStream_t>(stream), sh, nullptr, nullptr, Mode::kQuantOnly,
+                    &qb);
+}
+
+size_t pattn_workspace_size_fp8qk(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
+                                  int n_heads_kv, int head_dim, int page_size) {
+  (void)page_size;
+  if (num_seqs < 0 || total_q < 0 || max_q < 0 || max_kv < 0 || n_heads_q <= 0 || n_heads_kv <= 0 ||
+      n_heads_q % n_heads_kv != 0 || n_heads_q / n_heads_kv > kBM || head_dim != 128)
+    return 0;
+  const WsLayout L = ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim);
+  return fp8_layout(L.total, num_seqs, total_q, max_kv, n_heads_q, n_heads_kv, head_dim).total;
 }
 
 pattn_status pattn_forward_noalloc(void* out, const void* q, const void* kv_pool,

@@ -50,10 +50,17 @@
 namespace pattn {
 namespace {
 
-template <int D, int BN>
+template <int D, int BN, bool kF8 = false>
 struct Cfg {
-  static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kKVStage = BN * D * 2;
+  // kF8: Q and K as e4m3 codes (one byte), S = Q K^T with kind::f8f6f4 MMAs; V
+  // stays bf16.
+  static constexpr int kQKElem = kF8 ? 1 : 2;          // bytes per Q / K element
+  static constexpr int kQBytes = kBM * D * kQKElem;
+  static constexpr int kKStage = BN * D * kQKElem;
+  static constexpr int kVStage = BN * D * 2;
+  static constexpr int kQKBlocks = D * kQKElem / 128;  // 128-byte swizzle columns of a Q / K row
+  static constexpr int kQKBlockElems = 128 / kQKElem;
+  static constexpr int kQKSteps = D * kQKElem / 32;    // MMAs of one QK (32 bytes of K each)
   static constexpr bool kSplitO = D == 128;          // one O per softmax warpgroup
   static constexpr bool kAliasP = D == 128;          // P over its S buffer
   static constexpr int kSBufs = 2;
@@ -65,8 +72,8 @@ struct Cfg {
   // shared memory
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBufs * kQBytes;
-  static constexpr int kOffV = kOffK + kKStages * kKVStage;
-  static constexpr int kOffX = kOffV + kVStages * kKVStage;  // row sum / max / l exchange
+  static constexpr int kOffV = kOffK + kKStages * kKStage;
+  static constexpr int kOffX = kOffV + kVStages * kVStage;  // row sum / max / l exchange
   static constexpr int kXBytes = (2 * 2 + 2 * 2 + 2) * kBM * 4;
   static constexpr int kOffBar = kOffX + kXBytes;
   static constexpr int kBarBytes = 512;
@@ -84,7 +91,7 @@ struct Cfg {
     return kAliasP ? kColS + b * BN + (kk / (BN / 32)) * (BN / 2) + (kk % (BN / 32)) * 8
                    : kColP + b * kPCols + kk * 8;
   }
-  static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns per row
+  static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns of a V row
   static constexpr int kPagesPerTile = BN / kPage;
   static_assert(kColS + kSBufs * BN + (kAliasP ? 0 : kPBufs * kPCols) <= kTmemCols, "TMEM budget");
   static_assert(kSBufs <= 3 && kPBufs <= 3 && kPVBars <= 3 && kQBufs <= 2, "barrier slots");
@@ -168,11 +175,11 @@ __device__ __forceinline__ float max_row(const uint32_t (&sr)[KH / 32][32], int 
                fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
 }
 
-template <int D, int BN>
+template <int D, int BN, bool kF8>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
-            const AttnParams p) {
-  using C = Cfg<D, BN>;
+            const __grid_constant__ CUtensorMap tmap_k8, const AttnParams p) {
+  using C = Cfg<D, BN, kF8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -218,6 +225,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     mbar_init_fence();
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_kv);
+    if constexpr (kF8) tma_prefetch_desc(&tmap_k8);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -257,10 +265,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         const uint32_t qb = itl % C::kQBufs, qu = itl / C::kQBufs;
         ok = wait_one(bar(kQEmpty0 + qb), (qu & 1u) ^ 1u, ctl);
         if (ok) {
-          mbar_arrive_expect_tx(bar(kQFull0 + qb), static_cast<uint32_t>(C::kDBlocks * 128 * G * T));
-          for (int c = 0; c < C::kDBlocks; ++c)
-            tma_load_4d(sQ + qb * C::kQBytes + c * (kBM * 128), &tmap_q, bar(kQFull0 + qb), c * 64, 0,
-                        it.hk, q0 + it.qt * T, pol_q);
+          mbar_arrive_expect_tx(bar(kQFull0 + qb), static_cast<uint32_t>(C::kQKBlocks * 128 * G * T));
+          for (int c = 0; c < C::kQKBlocks; ++c)
+            tma_load_4d(sQ + qb * C::kQBytes + c * (kBM * 128), &tmap_q, bar(kQFull0 + qb),
+                        c * C::kQKBlockElems, 0, it.hk, q0 + it.qt * T, pol_q);
         }
       }
       ok = __shfl_sync(fullmask, ok, 0);
@@ -302,11 +310,18 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
               ok = wait_one(pv_bar(n - stages), pv_par(n - stages), ctl);
             }
             if (ok) {
-              mbar_arrive_expect_tx(bar(full + st), static_cast<uint32_t>(nload * C::kDBlocks * kPage * 128));
-              const uint32_t dst0 = (kind ? sV : sK) + st * C::kKVStage;
+              const int blocks = (kF8 && kind == 0) ? C::kQKBlocks : C::kDBlocks;
+              mbar_arrive_expect_tx(bar(full + st), static_cast<uint32_t>(nload * blocks * kPage * 128));
+              const uint32_t dst0 = kind ? sV + st * C::kVStage : sK + st * C::kKStage;
 #pragma unroll
               for (int j = 0; j < C::kPagesPerTile; ++j) {
                 if (a[j] < 0) continue;
+                if (kF8 && kind == 0) {
+                  // e4m3 K: 64-key block (tile * pages per tile + j) of the sequence
+                  const int kblk = it.b * p.nb_max + (it.kt0 + t0 + i) * C::kPagesPerTile + j;
+                  tma_load_4d(dst0 + j * (kPage * 128), &tmap_k8, bar(full + st), 0, 0, it.hk, kblk, pol_kv);
+                  continue;
+                }
                 for (int c = 0; c < C::kDBlocks; ++c) {
                   const uint32_t dst = dst0 + c * (BN * 128) + j * (kPage * 128);
                   if (p.paged)
@@ -344,7 +359,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     // the two streams touch disjoint TMEM (S / P, O) and feed the tensor pipe
     // independently, so that neither one's waits leave the pipe idle.
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, BN, false, false);
+      constexpr uint32_t idesc_qk = kF8 ? idesc_e4m3_f32(kBM, BN) : idesc_bf16_f32(kBM, BN, false, false);
       // operand descriptors built once; each MMA adds a compile-time offset
       const SmemDesc dq = sw128_desc_split(sQ, 16, 1024);
       const SmemDesc dk = sw128_desc_split(sK, 16, 1024);
@@ -369,12 +384,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           const uint32_t free_par = ((n / C::kSBufs) & 1u) ^ 1u;
           if (!(ok = wait_two(bar(kKFull0 + ks), (n / C::kKStages) & 1u, free_bar, free_par, ctl))) break;
           tc_fence_after();
-          const uint32_t k_lo = desc_lo_at(dk, ks * C::kKVStage);
+          const uint32_t k_lo = desc_lo_at(dk, ks * C::kKStage);
+          // 32 bytes of K per MMA: 16 bf16 or 32 e4m3 elements
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < C::kQKSteps; ++kk) {
             const uint32_t b_lo = k_lo + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
             const uint32_t a_lo = q_lo + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
-            umma_f16_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
+            if constexpr (kF8)
+              umma_f8_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
+            else
+              umma_f16_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
           }
           umma_commit(bar(kKEmpty0 + ks));
           umma_commit(bar(kSFull0 + s));
@@ -409,7 +428,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         if (!(ok = wait_warp(bar(kVFull0 + s), (n / C::kVStages) & 1u, ctl))) break;
         const int live = L - kt * BN;
         if (live < BN) {
-          uint8_t* v0 = smem + C::kOffV + s * C::kKVStage;
+          uint8_t* v0 = smem + C::kOffV + s * C::kVStage;
           const int dead = BN - live;
           const int chunks = dead * 8;  // 16-byte chunks per block
           for (int c = 0; c < C::kDBlocks; ++c) {
@@ -425,7 +444,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           if (ok) {
             tc_fence_after();
             const bool first = kt == it.kt0;
-            const uint32_t v_lo = desc_lo_at(dv, s * C::kKVStage);
+            const uint32_t v_lo = desc_lo_at(dv, s * C::kVStage);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
               const uint32_t b_lo = v_lo + ((kk * (16 * 128)) >> 4);
@@ -485,6 +504,14 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       int lim = 0;  // keys [0, lim) visible to this row
       if (valid) lim = p.causal ? min(L, L - ql + tok + 1) : L;
       const bool warp_live = __any_sync(0xffffffffu, valid) != 0;
+      // e4m3 scores: c times the row's Q scale times the K block's scale; the
+      // block of this warpgroup's keys of tile kt is kt * (BN / 64) + h
+      float cq = c, ksc_next = 1.f;
+      if constexpr (kF8) {
+        if (valid) cq = c * p.q_scale[static_cast<size_t>(q0 + tok) * p.n_heads_q + it.hk * G + g];
+        ksc_next = p.k_scale[(static_cast<size_t>(it.b) * p.nb_max + it.kt0 * C::kPagesPerTile + h) *
+                                 p.n_heads_kv + it.hk];
+      }
       float m_used = -INFINITY, l = 0.f;
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
         const uint32_t sb = n % C::kSBufs, su = n / C::kSBufs;
@@ -507,6 +534,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           if (lane == 0) mbar_arrive(bar(kSFree0 + sb));
         }
         if (kt + 1 == it.kt1 && has_next) si_next = p.seq_info[iv_next.x & kSeqMask];
+        float ct = c;
+        if constexpr (kF8) {
+          ct = cq * ksc_next;
+          if (kt + 1 < it.kt1)
+            ksc_next = p.k_scale[(static_cast<size_t>(it.b) * p.nb_max + (kt + 1) * C::kPagesPerTile + h) *
+                                     p.n_heads_kv + it.hk];
+        }
 
         const int key0 = kt * BN + h * KH;
         const bool full_tile = key0 + KH <= lim;
@@ -522,8 +556,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           float lt = 0.f;
           bool exact = first || m_used == -INFINITY;
           if (!exact) {
-            lt = full_tile ? exp_row<KH, false>(sr, c, m_used, KH, pk)
-                           : exp_row<KH, true>(sr, c, m_used, nv, pk);
+            lt = full_tile ? exp_row<KH, false>(sr, ct, m_used, KH, pk)
+                           : exp_row<KH, true>(sr, ct, m_used, nv, pk);
             exact = !(lt <= kSumLimit);  // also true for inf / NaN
           }
           if (__any_sync(0xffffffffu, exact)) {
@@ -544,7 +578,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             }
             const float mx = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
                                    fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
-            const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * c;
+            const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * ct;
             const float m_new = fmaxf(m_used, mx_s);
             if (first) {
               m_used = m_new;
@@ -574,8 +608,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
               }
             }
             const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-            lt = full_tile ? exp_row<KH, false>(sr, c, m_ref, KH, pk)
-                           : exp_row<KH, true>(sr, c, m_ref, nv, pk);
+            lt = full_tile ? exp_row<KH, false>(sr, ct, m_ref, KH, pk)
+                           : exp_row<KH, true>(sr, ct, m_ref, nv, pk);
           }
           l += lt;
         }
@@ -860,21 +894,30 @@ size_t attention_smem_bytes(int head_dim) {
 }
 
 cudaError_t attention_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<128, 128>,
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<128, 128, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<128, 128>::kSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_kernel<256, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_kernel<128, 128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128, 128, true>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_kernel<256, 64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Cfg<256, 64>::kSmem);
 }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                              int head_dim, int grid, cudaStream_t s, bool dependent) {
   if (head_dim == 128)
-    return launch_kernel(attn_kernel<128, 128>, grid, kAttnThreads, Cfg<128, 128>::kSmem, s,
-                         dependent, tq, tkv, p);
-  return launch_kernel(attn_kernel<256, 64>, grid, kAttnThreads, Cfg<256, 64>::kSmem, s, dependent,
-                       tq, tkv, p);
+    return launch_kernel(attn_kernel<128, 128, false>, grid, kAttnThreads, Cfg<128, 128>::kSmem, s,
+                         dependent, tq, tkv, tkv, p);
+  return launch_kernel(attn_kernel<256, 64, false>, grid, kAttnThreads, Cfg<256, 64>::kSmem, s,
+                       dependent, tq, tkv, tkv, p);
+}
+
+cudaError_t launch_attention_fp8(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
+                                 const CUtensorMap& tkv, int grid, cudaStream_t s, bool dependent) {
+  return launch_kernel(attn_kernel<128, 128, true>, grid, kAttnThreads, Cfg<128, 128, true>::kSmem, s,
+                       dependent, tq8, tkv, tk8, p);
 }
 
 }  // namespace pattn

@@ -83,6 +83,25 @@ struct KvWriteParams {
   int row_elems;                // n_heads_kv * head_dim
 };
 
+// Preparation of the quantised-QK variant (quant.cu). Layouts:
+//   q8 [total_q][n_heads_q][head_dim] e4m3, q_scale [total_q][n_heads_q] fp32;
+//   k8 [num_seqs * nb_max][64][n_heads_kv][head_dim] e4m3 (sequence b's 64-key
+//   block j is block b * nb_max + j), k_scale [num_seqs * nb_max][n_heads_kv];
+//   k_sum [num_seqs][n_heads_kv][head_dim] float64, zeroed before the call.
+struct QuantParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* kv_pool;
+  const int32_t* block_table;
+  const int4* seq_info;
+  uint8_t* q8;
+  float* q_scale;
+  uint8_t* k8;
+  float* k_scale;
+  double* k_sum;
+  int num_seqs, total_q, n_heads_q, n_heads_kv, head_dim, bt_stride, num_pages;
+  int nb_max;  // 64-key blocks per sequence in k8: ceil(max_kv / 64)
+};
+
 struct AttnParams {
   const int4* items;
   const int* hdr;
@@ -99,6 +118,11 @@ struct AttnParams {
   int paged;
   const int4* seq_plan;  // z = splits, w = first split unit of the sequence
   int* unit_cnt;         // finished splits per split unit
+  // quantised-QK variant: e4m3 scales of Q rows [total_q][n_heads_q] and of K
+  // blocks [num_seqs * nb_max][n_heads_kv] (see QuantParams)
+  const float* q_scale;
+  const float* k_scale;
+  int nb_max;
 };
 
 
@@ -130,8 +154,13 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_kv_write(const KvWriteParams& p, int sms, cudaStream_t s);
+cudaError_t launch_quant_qk(const QuantParams& p, int sms, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                              int head_dim, int grid, cudaStream_t s, bool dependent);
+// Quantised-QK prefill (head_dim 128): tq8 over the e4m3 Q codes, tk8 over the
+// e4m3 K blocks, tkv over the bf16 cache (V).
+cudaError_t launch_attention_fp8(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
+                                 const CUtensorMap& tkv, int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                           int head_dim, int grid, cudaStream_t s, bool dependent);

@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       for (int qt = 0; qt < nqt && qtile_kv_tiles(p, sq.y, sq.z, qt) == 0; ++qt)
         z1 = q0 + min(sq.y, (qt + 1) * p.tokens_per_tile);
     }
-    if (z1 > q0) {
+    if (z1 > q0 && p.out) {  // (no output when only the quantised Q/K are wanted)
       const size_t row = static_cast<size_t>(p.n_heads_q) * p.head_dim;
       uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(q0) * row);
       const size_t n16 = static_cast<size_t>(z1 - q0) * row / 8;

@@ -257,6 +257,21 @@ __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint32_t a_lo, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], kind::f8f6f4: 8-bit A and B (K = 32 per MMA),
+// descriptors as 32-bit words.
+__device__ __forceinline__ void umma_f8_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                           uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem] with B's descriptor as 32-bit words.
 __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                             uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
@@ -277,6 +292,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((static_cast<uint32_t>(N) >> 3) << 17) |
          ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4: f32 accumulator, e4m3 A and B (format
+// 0 in bits 7-9 and 10-12), both K-major; N and M fields as above.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | ((static_cast<uint32_t>(N) >> 3) << 17) | ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
 // 32 lanes x 32 bit, 32 consecutive columns: thread i of the warp gets lane

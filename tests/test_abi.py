@@ -22,7 +22,7 @@ def lib():
 def header_functions():
     text = open(os.path.join(ROOT, "include", "pattn.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pattn_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(pattn_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():

@@ -1,0 +1,103 @@
+"""GPU parity of the quantised-QK variant (pattn_quantize_qk, pattn_forward_fp8qk)
+against the oracle in oracle/quant.py: the e4m3 codes and scales bit for bit,
+the attention over the dequantised Q and K within the parity bar."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from helpers import MAX_ABS, MEAN_ABS, sample_rows, to_device
+from oracle import quant
+
+pytestmark = pytest.mark.gpu
+
+
+def _cases():
+    return {
+        "paged_causal": workloads.named(3, scale_down=16),                        # 4 x 512, G 4
+        "contig_noncausal_offset": workloads.named(4, scale_down=32),             # K channel offsets
+        "paged_varlen": workloads.make_paged("varlen8", 61, [17, 200, 64, 1], [300, 200, 1000, 129],
+                                             16, 4, 128, causal=True, extra_pages=5),
+    }
+
+
+@pytest.mark.parametrize("name", ["paged_causal", "contig_noncausal_offset", "paged_varlen"])
+def test_codes_and_scales_bitwise(name):
+    import paged_kv_flashattention_varlen_gb300 as pk
+    wl = _cases()[name]
+    d = to_device(wl)
+    q8, qs, k8, ks = pk.quantize_qk(d["q"], d["kv"], d["bt"], d["sl"], d["cu"], max_q=wl.max_q,
+                                     max_kv=wl.max_kv, n_heads_kv=wl.n_heads_kv, num_pages=wl.num_pages)
+    torch.cuda.synchronize()
+    assert pk.device_status() == 0
+    ref = quant.quantize_workload(wl)
+    assert np.array_equal(q8.cpu().numpy(), ref["q_codes"])
+    assert np.array_equal(qs.cpu().numpy().view(np.uint32), ref["q_scale"].view(np.uint32))
+    nb = k8.shape[0] // wl.num_seqs
+    k8c, ksc = k8.cpu().numpy(), ks.cpu().numpy()
+    for b in range(wl.num_seqs):
+        kc, kss = ref["k_codes"][b], ref["k_scale"][b]
+        nblk = kss.shape[0]
+        got = k8c[b * nb:b * nb + nblk].reshape(nblk * 64, wl.n_heads_kv, wl.head_dim)
+        assert np.array_equal(got, kc), f"sequence {b}: K codes"
+        assert np.array_equal(ksc[b * nb:b * nb + nblk].view(np.uint32), kss.view(np.uint32)), f"seq {b}"
+
+
+@pytest.mark.parametrize("name", ["paged_causal", "contig_noncausal_offset", "paged_varlen"])
+def test_attention_over_dequantised_qk(name):
+    import paged_kv_flashattention_varlen_gb300 as pk
+    wl = _cases()[name]
+    d = to_device(wl)
+    out = torch.full_like(d["q"], float("nan"))
+    pk.forward_fp8qk(out, d["q"], d["kv"], d["bt"], d["sl"], d["cu"], max_q=wl.max_q, max_kv=wl.max_kv,
+                     n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal, num_pages=wl.num_pages)
+    torch.cuda.synchronize()
+    assert pk.device_status() == 0
+    rows = sample_rows(wl, per_seq=8)
+    ref = quant.attention_dequantized(wl, rows=rows)
+    got = out[torch.as_tensor(rows, device=out.device)].float().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
+
+
+def test_full_size_noncausal_sampled_rows():
+    """The 37,810-token non-causal shape (one sequence, 56 heads) on sampled rows."""
+    import paged_kv_flashattention_varlen_gb300 as pk
+    wl = workloads.named(4)
+    d = to_device(wl)
+    out = torch.full_like(d["q"], float("nan"))
+    pk.forward_fp8qk(out, d["q"], d["kv"], d["bt"], d["sl"], d["cu"], max_q=wl.max_q, max_kv=wl.max_kv,
+                     n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal, num_pages=wl.num_pages)
+    torch.cuda.synchronize()
+    assert pk.device_status() == 0
+    rows = [0, 1, 127, 128, 18905, 37808, 37809]
+    ref = quant.attention_dequantized(wl, rows=rows)
+    got = out[torch.as_tensor(rows, device=out.device)].float().cpu().numpy()
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, (err.max(), err.mean())
+
+
+def test_decode_units_take_the_bf16_decode_kernel():
+    import paged_kv_flashattention_varlen_gb300 as pk
+    wl = workloads.named(2, scale_down=8)
+    d = to_device(wl)
+    a = torch.full_like(d["q"], float("nan"))
+    b = torch.full_like(d["q"], float("nan"))
+    kw = dict(max_q=wl.max_q, max_kv=wl.max_kv, n_heads_kv=wl.n_heads_kv, scale=wl.scale,
+              causal=wl.causal, num_pages=wl.num_pages)
+    pk.forward_fp8qk(a, d["q"], d["kv"], d["bt"], d["sl"], d["cu"], **kw)
+    pk.forward(b, d["q"], d["kv"], d["bt"], d["sl"], d["cu"], **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_unsupported_head_dim():
+    import paged_kv_flashattention_varlen_gb300 as pk
+    wl = workloads.named(1)  # head_dim 256
+    d = to_device(wl)
+    out = torch.empty_like(d["q"])
+    rc = pk.forward_fp8qk(out, d["q"], d["kv"], d["bt"], d["sl"], d["cu"], max_q=wl.max_q,
+                          max_kv=wl.max_kv, n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
+                          num_pages=wl.num_pages, check=False)
+    assert rc == 2
