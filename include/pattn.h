@@ -130,12 +130,15 @@ pattn_status pattn_forward_append(void *out, const void *q, const void *k_new, c
  * Same arguments and output as pattn_forward; head_dim 128 only.
  *
  *   K is smoothed per (sequence, KV head, channel) by its mean over the
- *   sequence's keys (the softmax cancels the shift); each 64-key block of a
+ *   sequence's keys (the softmax cancels the shift), summed exactly in fixed
+ *   point: each key clamped to +-1024 and rounded to a multiple of 2^-32, then
+ *   sum * 2^-32 / L in float64, rounded to fp32; each 64-key block of a
  *   sequence and KV head gets one scale, each query row (token, head) one:
  *   scale = amax / 448, code = e4m3 round-to-nearest-even of x / scale,
  *   saturated. The result is attention over the dequantised Q and K.
  *   Units of at most 16 packed query rows (decode) take the bf16 decode kernel.
- *   Needs pattn_workspace_size_fp8qk bytes of workspace.
+ *   Needs pattn_workspace_size_fp8qk bytes of workspace. PATTN_ERR_UNSUPPORTED
+ *   for head_dim != 128 or max_kv > 2^20.
  */
 pattn_status pattn_forward_fp8qk(void *out, const void *q, const void *kv_pool,
                                  const int32_t *block_table, const int32_t *seq_lens,

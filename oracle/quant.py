@@ -14,11 +14,20 @@ Readings (the page names the phases and gives the scheduler's block sizes
   64-key K block; for a paged cache that is one page.
 * Q codes: one scale per query row (token, head), finer than the 32-row warp
   block, so that no block crosses a sequence boundary.
-* scale = amax / 448 in fp32 (448 = largest e4m3 value; amax = 0 gives scale 1
-  and all-zero codes); code = e4m3 round-to-nearest-even of (x / scale)
-  computed in fp32 and saturated to +-448.
-* the mean is the exact sum of the bf16 keys (exact in float64) divided by L in
-  float64, then rounded to fp32; x = key - mean in fp32.
+* scale = amax / 448 in fp32 (448 = largest e4m3 value); code = e4m3
+  round-to-nearest-even of x * inv, the product rounded to fp32, with
+  inv = 448 / amax in fp32 (capped at the largest finite fp32), saturated to
+  +-448. amax = 0 gives scale 1 and all-zero codes. amax is taken as C's fmaxf
+  does, ignoring NaN. The page fixes no precision for the division by the
+  scale; one reciprocal per block and a multiply per element is the plain
+  reading of "divide by the scale" on a GPU, and the dequantised value
+  code * scale differs from x by the e4m3 rounding plus a few fp32 ulps.
+* the mean is summed exactly in fixed point: each bf16 key value is clamped to
+  +-1024 and rounded (to nearest even) to a multiple of 2^-32, the integer
+  counts are added exactly, and mean = count * 2^-32 / L in float64, rounded
+  to fp32; x = key - mean in fp32. This is the plain mean of K for keys of
+  magnitude 2^-25 ... 1024 (every bf16 value there lies on the 2^-32 grid);
+  any per-channel offset is a valid smoothing, since the softmax cancels it.
 
 Both sides take every rounding decision in the same precision, so the codes
 and scales are reproducible bit for bit.
@@ -44,10 +53,33 @@ def e4m3_values(codes: np.ndarray) -> np.ndarray:
     return t.to(torch.float64).numpy()
 
 
+FLT_MAX = np.float32(np.finfo(np.float32).max)
+
+
+def _amax(x32: np.ndarray, axis) -> np.ndarray:
+    """max |x| over ``axis``, NaN ignored (0 for an all-NaN or all-zero block)."""
+    return np.fmax.reduce(np.abs(np.asarray(x32, dtype=np.float32)), axis=axis, initial=np.float32(0))
+
+
 def _scale(amax32: np.ndarray) -> np.ndarray:
+    """Dequantisation scale amax / 448 in fp32 (1 where amax = 0)."""
     a = np.asarray(amax32, dtype=np.float32)
-    s = (a / np.float32(E4M3_MAX)).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        s = (a / np.float32(E4M3_MAX)).astype(np.float32)
     return np.where(a > 0, s, np.float32(1.0)).astype(np.float32)
+
+
+def _inv_scale(amax32: np.ndarray) -> np.ndarray:
+    """Quantisation multiplier 448 / amax in fp32, capped at the largest finite fp32 (1 where amax = 0)."""
+    a = np.asarray(amax32, dtype=np.float32)
+    with np.errstate(divide="ignore", over="ignore"):
+        inv = np.minimum((np.float32(E4M3_MAX) / np.where(a > 0, a, np.float32(1))).astype(np.float32), FLT_MAX)
+    return np.where(a > 0, inv, np.float32(1.0)).astype(np.float32)
+
+
+def _codes(x32: np.ndarray, inv32: np.ndarray) -> np.ndarray:
+    with np.errstate(invalid="ignore", over="ignore"):
+        return e4m3_codes((np.asarray(x32, dtype=np.float32) * inv32).astype(np.float32))
 
 
 def _bf16_to_f32(t) -> np.ndarray:
@@ -66,12 +98,26 @@ def logical_k(kv_pool, block_table, seq_lens, b: int, page_size: int = 64, start
     return pool[pages, 0, j % page_size].float().numpy().astype(np.float32)
 
 
+SUM_CLAMP = 1024.0
+SUM_UNIT = 2.0 ** 32
+
+
+def k_sum_units(k32: np.ndarray) -> np.ndarray:
+    """Per (KV head, channel) exact sum of the keys in units of 2^-32 (int64):
+    each value clamped to +-1024 (NaN to the lower bound, as C's fmaxf does)
+    and rounded to the nearest multiple of 2^-32, ties to even."""
+    x = np.fmin(np.fmax(np.asarray(k32, dtype=np.float32), np.float32(-SUM_CLAMP)), np.float32(SUM_CLAMP))
+    units = np.rint(x * np.float32(SUM_UNIT)).astype(np.int64)
+    return units.sum(axis=0, dtype=np.int64)
+
+
 def k_mean(k32: np.ndarray) -> np.ndarray:
-    """Per (KV head, channel) mean over the keys: exact float64 sum / L, rounded to fp32."""
+    """Per (KV head, channel) smoothing offset: the fixed-point sum * 2^-32 / L in
+    float64, rounded to fp32 (the mean of K for keys within the grid's range)."""
     L = k32.shape[0]
     if L == 0:
         return np.zeros(k32.shape[1:], dtype=np.float32)
-    return (k32.astype(np.float64).sum(axis=0) / L).astype(np.float32)
+    return (k_sum_units(k32).astype(np.float64) * (1.0 / SUM_UNIT) / L).astype(np.float32)
 
 
 def quantize_k(k32: np.ndarray, mean32: np.ndarray, block: int = 64):
@@ -84,17 +130,16 @@ def quantize_k(k32: np.ndarray, mean32: np.ndarray, block: int = 64):
     scales = np.zeros((nblk, H), dtype=np.float32)
     for i in range(nblk):
         xb = x[i * block:(i + 1) * block]
-        s = _scale(np.abs(xb).max(axis=(0, 2)))
-        scales[i] = s
-        codes[i * block:i * block + xb.shape[0]] = e4m3_codes((xb / s[None, :, None]).astype(np.float32))
+        amax = _amax(xb, axis=(0, 2))
+        scales[i] = _scale(amax)
+        codes[i * block:i * block + xb.shape[0]] = _codes(xb, _inv_scale(amax)[None, :, None])
     return codes, scales
 
 
 def quantize_q(q32: np.ndarray):
     """Q fp32 [T, Hq, D] -> (codes uint8 [T, Hq, D], scales fp32 [T, Hq]), one scale per row."""
-    s = _scale(np.abs(q32).max(axis=2))
-    codes = e4m3_codes((q32 / s[:, :, None]).astype(np.float32))
-    return codes, s
+    amax = _amax(q32, axis=2)
+    return _codes(q32, _inv_scale(amax)[:, :, None]), _scale(amax)
 
 
 def quantize_workload(wl):

@@ -204,11 +204,15 @@ pattn_status encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t
   return r == CUDA_SUCCESS ? PATTN_OK : PATTN_ERR_CUDA;
 }
 
+// Longest sequence of the quantised-QK path: the fixed-point key sums (units of
+// 2^-32, values clamped to +-1024) stay below 2^62 in magnitude.
+constexpr int kFp8MaxKv = 1 << 20;
+
 // Workspace regions of the quantised-QK variant, after the regular ones (see
 // QuantParams for the layouts). nb_max is even, so that both key halves of a
 // 128-key tile have a block.
 struct Fp8Layout {
-  size_t k_sum, q8, q_scale, k8, k_scale, total;
+  size_t k_sum, q8, q_scale, k8, k_scale, total;  // k_sum: the quant_scratch_bytes region
   int nb_max;
 };
 Fp8Layout fp8_layout(size_t base, int num_seqs, int total_q, int max_kv, int hq, int hkv, int d) {
@@ -217,7 +221,7 @@ Fp8Layout fp8_layout(size_t base, int num_seqs, int total_q, int max_kv, int hq,
   const size_t B = static_cast<size_t>(num_seqs), nb = static_cast<size_t>(f.nb_max);
   size_t off = align_up(base, 256);
   f.k_sum = off;
-  off += B * hkv * d * sizeof(double);
+  off += quant_scratch_bytes(num_seqs, hkv, d);
   f.q8 = off = align_up(off, 256);
   off += static_cast<size_t>(total_q) * hq * d;
   f.q_scale = off = align_up(off, 256);
@@ -240,7 +244,7 @@ struct QuantBufs {
   float* q_scale = nullptr;
   uint8_t* k8 = nullptr;
   float* k_scale = nullptr;
-  double* k_sum = nullptr;
+  void* scratch = nullptr;  // quant_scratch_bytes
   int nb_max = 0;
 };
 
@@ -386,7 +390,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   cudaError_t e = cudaSuccess;
   if (mode != Mode::kBf16) {
     // the key sums of the quantisation start from zero
-    e = cudaMemsetAsync(qb->k_sum, 0, static_cast<size_t>(num_seqs) * hkv * d * sizeof(double), stream);
+    e = cudaMemsetAsync(qb->scratch, 0, quant_zero_bytes(num_seqs, hkv, d), stream);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   e = launch_plan(pp, stream);
@@ -422,7 +426,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     qp.q_scale = qb->q_scale;
     qp.k8 = qb->k8;
     qp.k_scale = qb->k_scale;
-    qp.k_sum = qb->k_sum;
+    quant_scratch_split(qb->scratch, num_seqs, hkv, d, &qp.k_sum, &qp.k_cnt, &qp.k_mean);
     qp.num_seqs = num_seqs;
     qp.total_q = total_q;
     qp.n_heads_q = hq;
@@ -512,7 +516,7 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
     qb.q_scale = reinterpret_cast<float*>(wsb + F.q_scale);
     qb.k8 = wsb + F.k8;
     qb.k_scale = reinterpret_cast<float*>(wsb + F.k_scale);
-    qb.k_sum = reinterpret_cast<double*>(wsb + F.k_sum);
+    qb.scratch = wsb + F.k_sum;
     qb.nb_max = F.nb_max;
   }
   return launch_all(st, wsb, L, out, q, kv, bt, seq_lens, cu_q, num_seqs, total_q, max_q, max_kv, hq,
@@ -595,7 +599,7 @@ pattn_status pattn_forward_fp8qk(void* out, const void* q, const void* kv_pool,
                               max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size,
                               num_pages, scale, causal, &sh);
   if (s != PATTN_OK) return s;
-  if (head_dim != 128) return PATTN_ERR_UNSUPPORTED;
+  if (head_dim != 128 || max_kv > kFp8MaxKv) return PATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_seqs) * n_heads_kv > 0x7fffffffLL) return PATTN_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0) return PATTN_OK;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -619,7 +623,7 @@ pattn_status pattn_quantize_qk(void* q8, float* q_scale, void* k8, float* k_scal
   if (!q8 || !q_scale || !k8 || !k_scale || !aligned(q8, 16) || !aligned(k8, 16) ||
       !aligned(q_scale, 4) || !aligned(k_scale, 4))
     return PATTN_ERR_INVALID_ARG;
-  if (head_dim != 128) return PATTN_ERR_UNSUPPORTED;
+  if (head_dim != 128 || max_kv > kFp8MaxKv) return PATTN_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q == 0) return PATTN_OK;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* stp = nullptr;
@@ -627,7 +631,7 @@ pattn_status pattn_quantize_qk(void* q8, float* q_scale, void* k8, float* k_scal
   DeviceState& st = *stp;
   const WsLayout L = ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim);
   const Fp8Layout F = fp8_layout(L.total, num_seqs, total_q, max_kv, n_heads_q, n_heads_kv, head_dim);
-  const size_t need = align_up(F.k_sum + static_cast<size_t>(num_seqs) * n_heads_kv * head_dim * 8, 256);
+  const size_t need = align_up(F.k_sum + quant_scratch_bytes(num_seqs, n_heads_kv, head_dim), 256);
   if ((s = ensure_workspace(st, need)) != PATTN_OK) return s;
   uint8_t* wsb = static_cast<uint8_t*>(st.ws);
   QuantBufs qb;
@@ -635,7 +639,7 @@ pattn_status pattn_quantize_qk(void* q8, float* q_scale, void* k8, float* k_scal
   qb.q_scale = q_scale;
   qb.k8 = static_cast<uint8_t*>(k8);
   qb.k_scale = k_scale;
-  qb.k_sum = reinterpret_cast<double*>(wsb + F.k_sum);
+  qb.scratch = wsb + F.k_sum;
   qb.nb_max = F.nb_max;
   return launch_all(st, wsb, L, nullptr, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
                     max_q, max_kv, n_heads_q, n_heads_kv, head_dim, num_pages, 1.0f, 0,
@@ -647,7 +651,8 @@ size_t pattn_workspace_size_fp8qk(int num_seqs, int total_q, int max_q, int max_
                                   int n_heads_kv, int head_dim, int page_size) {
   (void)page_size;
   if (num_seqs < 0 || total_q < 0 || max_q < 0 || max_kv < 0 || n_heads_q <= 0 || n_heads_kv <= 0 ||
-      n_heads_q % n_heads_kv != 0 || n_heads_q / n_heads_kv > kBM || head_dim != 128)
+      n_heads_q % n_heads_kv != 0 || n_heads_q / n_heads_kv > kBM || head_dim != 128 ||
+      max_kv > kFp8MaxKv)
     return 0;
   const WsLayout L = ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim);
   return fp8_layout(L.total, num_seqs, total_q, max_kv, n_heads_q, n_heads_kv, head_dim).total;

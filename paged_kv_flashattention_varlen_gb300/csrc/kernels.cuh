@@ -87,7 +87,28 @@ struct KvWriteParams {
 //   q8 [total_q][n_heads_q][head_dim] e4m3, q_scale [total_q][n_heads_q] fp32;
 //   k8 [num_seqs * nb_max][64][n_heads_kv][head_dim] e4m3 (sequence b's 64-key
 //   block j is block b * nb_max + j), k_scale [num_seqs * nb_max][n_heads_kv];
-//   k_sum [num_seqs][n_heads_kv][head_dim] float64, zeroed before the call.
+//   scratch (quant_scratch_bytes): k_sum [num_seqs][n_heads_kv][head_dim] int64
+//   (units of 2^-32) and k_cnt [num_seqs][n_heads_kv] uint32, both zeroed
+//   before the call (the first quant_zero_bytes), then k_mean
+//   [num_seqs][n_heads_kv][head_dim] fp32.
+inline size_t quant_zero_bytes(int num_seqs, int n_heads_kv, int head_dim) {
+  const size_t n = static_cast<size_t>(num_seqs) * n_heads_kv;
+  return n * head_dim * sizeof(long long) + n * sizeof(unsigned int);
+}
+inline size_t quant_scratch_bytes(int num_seqs, int n_heads_kv, int head_dim) {
+  const size_t n = static_cast<size_t>(num_seqs) * n_heads_kv;
+  return (quant_zero_bytes(num_seqs, n_heads_kv, head_dim) + 15) / 16 * 16 + n * head_dim * sizeof(float);
+}
+// The three scratch arrays inside a quant_scratch_bytes region.
+inline void quant_scratch_split(void* base, int num_seqs, int n_heads_kv, int head_dim, long long** k_sum,
+                                unsigned int** k_cnt, float** k_mean) {
+  const size_t n = static_cast<size_t>(num_seqs) * n_heads_kv;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  *k_sum = reinterpret_cast<long long*>(b);
+  *k_cnt = reinterpret_cast<unsigned int*>(b + n * head_dim * sizeof(long long));
+  *k_mean = reinterpret_cast<float*>(b + (quant_zero_bytes(num_seqs, n_heads_kv, head_dim) + 15) / 16 * 16);
+}
+
 struct QuantParams {
   const __nv_bfloat16* q;
   const __nv_bfloat16* kv_pool;
@@ -97,7 +118,9 @@ struct QuantParams {
   float* q_scale;
   uint8_t* k8;
   float* k_scale;
-  double* k_sum;
+  long long* k_sum;
+  unsigned int* k_cnt;
+  float* k_mean;
   int num_seqs, total_q, n_heads_q, n_heads_kv, head_dim, bt_stride, num_pages;
   int nb_max;  // 64-key blocks per sequence in k8: ceil(max_kv / 64)
 };

@@ -5,15 +5,18 @@
 // and the int8 rate is far below it.
 //
 //   * k_sum_kernel: per (sequence, KV head, channel), the sum of the sequence's
-//     keys in float64. Each CTA adds up 1024 keys and adds its partial sums
-//     into the total with float64 atomics. Sums of bf16 values are exact in
-//     float64 at these lengths, so the order does not matter.
-//   * k_quant_kernel: per (sequence, 64-key block, KV head): the mean (sum / L
-//     in float64, rounded to fp32), x = k - mean in fp32, scale = amax / 448
-//     (IEEE division; 1 when amax = 0), code = e4m3 round-to-nearest-even of
-//     x / scale (IEEE division), saturated. Rows past L are zero codes.
-//   * q_quant_kernel: per query row (token, head): scale = amax / 448 and codes
-//     as above.
+//     keys in fixed point: each key value clamped to +-1024 and rounded to the
+//     2^-32 grid (exact for |x| >= 2^-25), as an int64 count. Each CTA adds up
+//     256 keys in int32 lanes and adds its partial sums with 64-bit integer
+//     atomics; the sums are exact, so the order does not matter. The CTA that
+//     finishes last for its (sequence, KV head) turns the sums into the fp32
+//     smoothing offsets (sum * 2^-32 / L in float64, rounded to fp32).
+//   * k_quant_kernel: per (sequence, 64-key block, KV head): x = k - offset in
+//     fp32, amax = max |x|, scale = amax / 448, inv = 448 / amax (IEEE
+//     divisions, once per block; inv capped at the largest finite fp32; 1 and 1
+//     when amax = 0), code = e4m3 round-to-nearest-even of x * inv, saturated.
+//     Rows past L are zero codes.
+//   * q_quant_kernel: per query row (token, head): scale and codes as above.
 //
 // Every rounding decision is taken in the precision the oracle uses, so codes
 // and scales agree with it bit for bit. The kernels run after the plan (they
@@ -27,11 +30,44 @@
 namespace pattn {
 namespace {
 
-constexpr int kSumKeys = 1024;  // keys per k_sum CTA
+constexpr int kSumKeys = 256;  // keys per k_sum CTA
 constexpr float kE4m3Max = 448.0f;
+constexpr float kSumClamp = 1024.0f;            // key values are clamped to +-1024 for the sum
+constexpr float kSumUnit = 4294967296.0f;       // 2^32: the sum counts units of 2^-32
+constexpr float kSplitBias = 26388279066624.0f; // 1.5 * 2^44: x + it rounds x to a multiple of 2^21
+constexpr float kIntBias = 12582912.0f;         // 1.5 * 2^23: x + it rounds x to an integer
+constexpr int kIntBiasBits = 0x4B400000;        // the fp32 bits of 1.5 * 2^23
+constexpr float kHiStep = 4.76837158203125e-07f;  // 2^-21
+
+// Adds two key values (a bf16 pair) to per-channel int32 counters, exactly.
+// With u = clamp(v, +-1024) * 2^32 (exact, |u| <= 2^42): u_hi = u rounded to a
+// multiple of 2^21 and u_lo = u - u_hi (exact, |u_lo| <= 2^20), so that
+// round(u) = u_hi + round(u_lo), ties to even (u_hi is even). u_hi / 2^21 and
+// round(u_lo) are read off the bits of t + 1.5 * 2^23, whose fp32 grid there
+// is the integers; the bias is taken off in the same integer add.
+__device__ __forceinline__ void add_units(uint32_t pair, int& hi0, int& lo0, int& hi1, int& lo1) {
+  __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pair);
+  v = __hmin2(__hmax2(v, __float2bfloat162_rn(-kSumClamp)), __float2bfloat162_rn(kSumClamp));
+  const float2 f = __bfloat1622float2(v);
+  const float2 unit = make_float2(kSumUnit, kSumUnit);
+  const float2 t = __ffma2_rn(f, unit, make_float2(kSplitBias, kSplitBias));
+  const float2 uh = __fadd2_rn(t, make_float2(-kSplitBias, -kSplitBias));
+  const float2 ul = __ffma2_rn(f, unit, make_float2(-uh.x, -uh.y));
+  const float2 a = __fadd2_rn(ul, make_float2(kIntBias, kIntBias));
+  const float2 h = __ffma2_rn(uh, make_float2(kHiStep, kHiStep), make_float2(kIntBias, kIntBias));
+  lo0 += __float_as_int(a.x) - kIntBiasBits;
+  lo1 += __float_as_int(a.y) - kIntBiasBits;
+  hi0 += __float_as_int(h.x) - kIntBiasBits;
+  hi1 += __float_as_int(h.y) - kIntBiasBits;
+}
 
 __device__ __forceinline__ float e4m3_scale(float amax) {
   return amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
+}
+
+// The quantisation multiplier 448 / amax (capped at the largest finite fp32; 1 for amax = 0).
+__device__ __forceinline__ float e4m3_inv_scale(float amax) {
+  return amax > 0.f ? fminf(__fdiv_rn(kE4m3Max, amax), 3.402823466e38f) : 1.0f;
 }
 
 // Two fp32 values -> two e4m3 bytes (first value in the low byte).
@@ -51,66 +87,102 @@ __device__ __forceinline__ const __nv_bfloat16* key_row(const QuantParams& p, in
   return p.kv_pool + (static_cast<size_t>(si.w) + j) * row + static_cast<size_t>(hk) * p.head_dim;
 }
 
-// grid (num_seqs * n_heads_kv, key chunks), block head_dim threads: thread d
-// sums channel d of kSumKeys keys.
-__global__ void __launch_bounds__(128) k_sum_kernel(const QuantParams p) {
+// grid (num_seqs * n_heads_kv, key chunks of kSumKeys), 256 threads: thread t
+// adds channels 8 (t % 16) ... + 7 of keys j0 + t / 16, + 16, ... (16-byte
+// loads, four keys of a lane in flight); the 16 key lanes are then summed in
+// shared memory and the CTA adds its 128 partial sums with int64 atomics. The
+// last CTA of a (sequence, KV head) writes the 128 offsets.
+__global__ void __launch_bounds__(256) k_sum_kernel(const QuantParams p) {
   grid_dep_launch();
   grid_dep_wait();  // the plan is complete
+  __shared__ long long s_part[16][128];
+  __shared__ int s_last;
   const int b = blockIdx.x / p.n_heads_kv, hk = blockIdx.x % p.n_heads_kv;
   const int4 si = p.seq_info[b];
   if (si.y < 0) return;
   const int L = si.z;
   const int j0 = blockIdx.y * kSumKeys, j1 = min(L, j0 + kSumKeys);
   if (j0 >= j1) return;
-  const int d = threadIdx.x;
-  double acc[4] = {0.0, 0.0, 0.0, 0.0};
-  int j = j0;
-  for (; j + 4 <= j1; j += 4) {
-    float v[4];
+  const int cg = threadIdx.x & 15, kl = threadIdx.x >> 4;
+  int hi[8], lo[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) hi[e] = lo[e] = 0;
+  for (int jb = j0; jb < j1; jb += 64) {
+    uint4 raw[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const __nv_bfloat16* r = key_row(p, b, si, j + u, hk);
-      v[u] = r ? __bfloat162float(r[d]) : 0.f;
+      const int j = jb + u * 16 + kl;
+      const __nv_bfloat16* r = j < j1 ? key_row(p, b, si, j, hk) : nullptr;
+      raw[u] = r ? *reinterpret_cast<const uint4*>(r + cg * 8) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[u] += static_cast<double>(v[u]);
+    for (int u = 0; u < 4; ++u) {
+      add_units(raw[u].x, hi[0], lo[0], hi[1], lo[1]);
+      add_units(raw[u].y, hi[2], lo[2], hi[3], lo[3]);
+      add_units(raw[u].z, hi[4], lo[4], hi[5], lo[5]);
+      add_units(raw[u].w, hi[6], lo[6], hi[7], lo[7]);
+    }
   }
-  for (; j < j1; ++j) {
-    const __nv_bfloat16* r = key_row(p, b, si, j, hk);
-    acc[0] += r ? static_cast<double>(__bfloat162float(r[d])) : 0.0;
+  // |hi| <= 16 * 2^21 and |lo| <= 16 * 2^20 per lane: no int32 overflow
+#pragma unroll
+  for (int e = 0; e < 8; ++e) s_part[kl][cg * 8 + e] = static_cast<long long>(hi[e]) * (1ll << 21) + lo[e];
+  __syncthreads();
+  const size_t base = (static_cast<size_t>(b) * p.n_heads_kv + hk) * p.head_dim;
+  if (threadIdx.x < 128) {
+    long long t = 0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) t += s_part[k][threadIdx.x];
+    atomicAdd(reinterpret_cast<unsigned long long*>(p.k_sum + base + threadIdx.x),
+              static_cast<unsigned long long>(t));
+    __threadfence();
   }
-  atomicAdd(p.k_sum + (static_cast<size_t>(b) * p.n_heads_kv + hk) * p.head_dim + d,
-            (acc[0] + acc[1]) + (acc[2] + acc[3]));
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned chunks = static_cast<unsigned>((L + kSumKeys - 1) / kSumKeys);
+    s_last = atomicAdd(p.k_cnt + static_cast<size_t>(b) * p.n_heads_kv + hk, 1u) == chunks - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x < 128) {
+    const long long sum = __ldcg(p.k_sum + base + threadIdx.x);
+    p.k_mean[base + threadIdx.x] =
+        __double2float_rn(static_cast<double>(sum) * (1.0 / 4294967296.0) / static_cast<double>(L));
+  }
 }
 
 // grid (num_seqs * n_heads_kv, blocks per sequence), 256 threads: thread t
 // quantises row t / 4 of the 64-key block, channels (t % 4) * 32 ... + 31.
 __global__ void __launch_bounds__(256) k_quant_kernel(const QuantParams p) {
   grid_dep_launch();
-  grid_dep_wait();  // the key sums are complete
+  grid_dep_wait();  // the offsets are complete
   __shared__ float s_amax[8];
+  __shared__ float s_mean[128];
   const int b = blockIdx.x / p.n_heads_kv, hk = blockIdx.x % p.n_heads_kv;
   const int blk = blockIdx.y;
   const int4 si = p.seq_info[b];
   if (si.y < 0) return;
   const int L = si.z;
   if (blk * kPage >= L) return;
+  if (threadIdx.x < 128)
+    s_mean[threadIdx.x] = p.k_mean[(static_cast<size_t>(b) * p.n_heads_kv + hk) * p.head_dim + threadIdx.x];
   const int r = threadIdx.x >> 2, c0 = (threadIdx.x & 3) * 32;
   const int j = blk * kPage + r;
-  const double* sum = p.k_sum + (static_cast<size_t>(b) * p.n_heads_kv + hk) * p.head_dim + c0;
+  const __nv_bfloat16* kr = j < L ? key_row(p, b, si, j, hk) : nullptr;
+  uint4 raw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    raw[i] = kr ? *reinterpret_cast<const uint4*>(kr + c0 + i * 8) : make_uint4(0, 0, 0, 0);
+  __syncthreads();
   float x[32];
   float amax = 0.f;
-  const __nv_bfloat16* kr = j < L ? key_row(p, b, si, j, hk) : nullptr;
 #pragma unroll
-  for (int i = 0; i < 32; i += 8) {
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (kr) raw = *reinterpret_cast<const uint4*>(kr + c0 + i);
-    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&raw);
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&raw[i]);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float mean = __double2float_rn(sum[i + e] / static_cast<double>(L));
-      x[i + e] = kr ? __fsub_rn(__bfloat162float(h[e]), mean) : 0.f;
-      amax = fmaxf(amax, fabsf(x[i + e]));
+      x[i * 8 + e] = kr ? __fsub_rn(__bfloat162float(h[e]), s_mean[c0 + i * 8 + e]) : 0.f;
+      amax = fmaxf(amax, fabsf(x[i * 8 + e]));
     }
   }
 #pragma unroll
@@ -120,65 +192,83 @@ __global__ void __launch_bounds__(256) k_quant_kernel(const QuantParams p) {
   amax = s_amax[0];
 #pragma unroll
   for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_amax[w]);
-  const float scale = e4m3_scale(amax);
+  const float inv = e4m3_inv_scale(amax);
   const size_t gblk = static_cast<size_t>(b) * p.nb_max + blk;
   uint32_t w[8];
 #pragma unroll
   for (int i = 0; i < 32; i += 4) {
-    const uint32_t lo = e4m3x2(__fdiv_rn(x[i], scale), __fdiv_rn(x[i + 1], scale));
-    const uint32_t hi = e4m3x2(__fdiv_rn(x[i + 2], scale), __fdiv_rn(x[i + 3], scale));
+    const uint32_t lo = e4m3x2(__fmul_rn(x[i], inv), __fmul_rn(x[i + 1], inv));
+    const uint32_t hi = e4m3x2(__fmul_rn(x[i + 2], inv), __fmul_rn(x[i + 3], inv));
     w[i / 4] = kr ? (lo | (hi << 16)) : 0u;
   }
   uint4* dst = reinterpret_cast<uint4*>(
       p.k8 + ((gblk * kPage + r) * p.n_heads_kv + hk) * p.head_dim + c0);
   dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
   dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  if (threadIdx.x == 0) p.k_scale[gblk * p.n_heads_kv + hk] = scale;
+  if (threadIdx.x == 0) p.k_scale[gblk * p.n_heads_kv + hk] = e4m3_scale(amax);
 }
 
-// One warp per query row (token, head), lane l holding channels 4l ... 4l + 3.
-// It needs nothing of the plan, but its completion is what the attention kernel
-// waits for, so it waits for the K quantisation before it exits.
+// Query rows (token, head): eight lanes per row (lane holds 16 channels, two
+// 16-byte loads), four rows per warp pass and two passes in flight. It needs
+// nothing of the plan, but its completion is what the attention kernel waits
+// for, so it waits for the K quantisation before it exits.
 __global__ void __launch_bounds__(256) q_quant_kernel(const QuantParams p) {
   grid_dep_launch();
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, g = lane >> 3, sub = lane & 7;
   const size_t rows = static_cast<size_t>(p.total_q) * p.n_heads_q;
   const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x >> 5);
-  for (size_t row = static_cast<size_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
-       row += warps) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(p.q + row * p.head_dim + lane * 4);
-    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&raw);
-    float x[4];
-    float amax = 0.f;
+  for (size_t r0 = (static_cast<size_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 8; r0 < rows;
+       r0 += warps * 8) {
+    uint4 raw[2][2];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[e] = __bfloat162float(h[e]);
-      amax = fmaxf(amax, fabsf(x[e]));
+    for (int u = 0; u < 2; ++u) {
+      const size_t row = r0 + u * 4 + g;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + row * 128 + sub * 16);
+      raw[u][0] = row < rows ? src[0] : make_uint4(0, 0, 0, 0);
+      raw[u][1] = row < rows ? src[1] : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float scale = e4m3_scale(amax);
-    const uint32_t lo = e4m3x2(__fdiv_rn(x[0], scale), __fdiv_rn(x[1], scale));
-    const uint32_t hi = e4m3x2(__fdiv_rn(x[2], scale), __fdiv_rn(x[3], scale));
-    reinterpret_cast<uint32_t*>(p.q8 + row * p.head_dim)[lane] = lo | (hi << 16);
-    if (lane == 0) p.q_scale[row] = scale;
+    for (int u = 0; u < 2; ++u) {
+      const size_t row = r0 + u * 4 + g;
+      const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&raw[u][0]);
+      float x[16];
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        x[e] = __bfloat162float(h[e]);
+        amax = fmaxf(amax, fabsf(x[e]));
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      if (row >= rows) continue;
+      const float inv = e4m3_inv_scale(amax);
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) {
+        const uint32_t lo = e4m3x2(__fmul_rn(x[i], inv), __fmul_rn(x[i + 1], inv));
+        const uint32_t hi = e4m3x2(__fmul_rn(x[i + 2], inv), __fmul_rn(x[i + 3], inv));
+        w[i / 4] = lo | (hi << 16);
+      }
+      reinterpret_cast<uint4*>(p.q8 + row * 128)[sub] = make_uint4(w[0], w[1], w[2], w[3]);
+      if (sub == 0) p.q_scale[row] = e4m3_scale(amax);
+    }
   }
   grid_dep_wait();  // the K codes are complete before this grid is
 }
 
 }  // namespace
 
-// After the plan (k_sum zeroed before it, in stream order): key sums, K codes,
-// Q codes, each a dependent launch.
+// After the plan (key sums and counters zeroed before it, in stream order): key
+// sums and offsets, K codes, Q codes, each a dependent launch.
 cudaError_t launch_quant_qk(const QuantParams& p, int sms, cudaStream_t s) {
   cudaError_t e = launch_kernel(k_sum_kernel, dim3(p.num_seqs * p.n_heads_kv,
                                                    (p.nb_max * kPage + kSumKeys - 1) / kSumKeys),
-                                128, 0, s, true, p);
+                                256, 0, s, true, p);
   if (e != cudaSuccess) return e;
   e = launch_kernel(k_quant_kernel, dim3(p.num_seqs * p.n_heads_kv, p.nb_max), 256, 0, s, true, p);
   if (e != cudaSuccess) return e;
   const size_t rows = static_cast<size_t>(p.total_q) * p.n_heads_q;
-  const int blocks = static_cast<int>(std::min<size_t>((rows + 7) / 8, static_cast<size_t>(sms) * 16));
+  const int blocks = static_cast<int>(std::min<size_t>((rows + 63) / 64, static_cast<size_t>(sms) * 8));
   return launch_kernel(q_quant_kernel, std::max(blocks, 1), 256, 0, s, true, p);
 }
 

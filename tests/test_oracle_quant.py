@@ -70,6 +70,32 @@ def test_row_scale_maps_amax_to_448_and_zero_rows_to_zero():
     assert quant.e4m3_values(codes[1, 1]).max() == 448.0
 
 
+def test_codes_dequantise_within_half_an_e4m3_step():
+    # code * scale is x up to the e4m3 rounding (relative 2^-4 for normal codes,
+    # absolute 2^-10 * scale for subnormal ones) plus fp32 slack from the
+    # multiplier, and the row maximum maps to +-448
+    rng = np.random.default_rng(8)
+    q = (rng.standard_normal((64, 4, 128)) * rng.uniform(0.01, 50, (64, 4, 1))).astype(np.float32)
+    codes, s = quant.quantize_q(q)
+    deq = quant.e4m3_values(codes) * s[:, :, None].astype(np.float64)
+    bound = np.maximum(np.abs(q) * 2.0 ** -4, 2.0 ** -10 * s[:, :, None]) * (1 + 1e-5)
+    assert np.all(np.abs(deq - q) <= bound)
+    vmax = np.abs(quant.e4m3_values(codes)).max(axis=2)
+    assert np.all(vmax == 448.0)
+
+
+def test_tiny_and_nan_rows_give_finite_codes():
+    q = np.zeros((3, 1, 128), dtype=np.float32)
+    q[0, 0, :4] = [1e-39, -5e-40, 0.0, 2e-45]   # 448 / amax overflows fp32: capped
+    q[1, 0, :3] = [np.nan, 2.0, -1.0]           # NaN ignored by amax
+    codes, s = quant.quantize_q(q)
+    vals = quant.e4m3_values(codes)
+    assert np.isfinite(vals[0]).all() and s[0, 0] == np.float32(1e-39) / np.float32(448)
+    assert s[1, 0] == np.float32(2.0) / np.float32(448) and vals[1, 0, 1] == 448.0
+    assert np.isnan(vals[1, 0, 0])               # the NaN element itself stays NaN
+    assert not codes[2].any() and s[2, 0] == 1.0
+
+
 def test_k_blocks_of_64_keys_and_zero_tail():
     rng = np.random.default_rng(5)
     k = rng.standard_normal((100, 2, 128)).astype(np.float32)
@@ -81,6 +107,34 @@ def test_k_blocks_of_64_keys_and_zero_tail():
     assert not codes[100:].any()
     x = k - m[None]
     assert scales[1, 0] == np.float32(np.abs(x[64:100, 0]).max()) / np.float32(448)
+
+
+def test_k_mean_is_the_plain_mean_for_keys_on_the_grid():
+    # bf16 keys of magnitude 2^-25 ... 1024 lie on the 2^-32 grid, so the
+    # fixed-point sum is the exact sum and the offset is the fp32-rounded mean
+    rng = np.random.default_rng(11)
+    k = torch.from_numpy(rng.standard_normal((333, 3, 128)) * 50).to(torch.bfloat16).float().numpy()
+    k = np.where(np.abs(k) < 2.0 ** -25, 0.0, k).astype(np.float32)
+    k[0, 0, 0] = 1024.0
+    k[1, 0, 0] = -1024.0
+    exact = np.array([[sum(float(v) for v in k[:, h, c]) for c in range(128)] for h in range(3)])
+    assert np.array_equal(quant.k_sum_units(k), (exact * 2.0 ** 32).astype(np.int64))
+    assert np.array_equal(quant.k_mean(k), (exact / 333).astype(np.float32))
+
+
+def test_k_sum_clamps_and_rounds_to_the_grid():
+    k = np.zeros((6, 1, 128), dtype=np.float32)
+    k[0, 0, 0] = 4096.0                 # clamped to 1024
+    k[1, 0, 0] = -3.0e38                # clamped to -1024
+    k[2, 0, 1] = 2.0 ** -33             # half a unit: ties to even -> 0
+    k[3, 0, 1] = 3 * 2.0 ** -33         # one and a half units -> 2
+    k[4, 0, 2] = 2.0 ** -30             # 4 units, exact
+    k[5, 0, 2] = -(2.0 ** -34)          # a quarter unit -> 0
+    k[0, 0, 3] = np.nan                 # NaN counts as the lower bound
+    units = quant.k_sum_units(k)[0]
+    assert units[0] == 0 and units[1] == 2 and units[2] == 4
+    assert units[3] == -1024 * 2 ** 32
+    assert quant.k_mean(k)[0, 2] == np.float32(4 * 2.0 ** -32 / 6)
 
 
 def test_exact_quantisation_reproduces_the_plain_attention():
