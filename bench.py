@@ -53,6 +53,8 @@ def parse():
                     help="profiling runs: time one workload only")
     ap.add_argument("--workload", default=None,
                     help="time named workload(s) 1-5 (comma list or 'all'): one JSON line each")
+    ap.add_argument("--fp8qk", action="store_true",
+                    help="with --workload: the quantised-QK variant (pattn_forward_fp8qk)")
     ap.add_argument("--append", action="store_true",
                     help="with --workload: each step first writes the query tokens' K/V rows into "
                          "their cache slots (pattn_forward_append)")
@@ -441,7 +443,11 @@ def run_workloads(args):
             k_new, v_new = (t.to(dev) for t in workloads.new_kv_rows(wl, 900 + i))
 
         def step():
-            if args.append:
+            if args.fp8qk:
+                pk.forward_fp8qk(out, q, kv, bt, sl, cu, max_q=wl.max_q, max_kv=wl.max_kv,
+                                 n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
+                                 num_pages=wl.num_pages, check=False)
+            elif args.append:
                 pk.forward_append(out, q, k_new, v_new, kv, bt, sl, cu, max_q=wl.max_q,
                                   max_kv=wl.max_kv, n_heads_kv=wl.n_heads_kv, scale=wl.scale,
                                   causal=wl.causal, num_pages=wl.num_pages, check=False)
@@ -480,6 +486,14 @@ def run_workloads(args):
             "bytes": nbytes, "flops": flops, "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 {tc} TFLOP/s",
             "device_status": pk.device_status(),
         }
+        if args.fp8qk:
+            # QK on e4m3 tensor cores (twice the bf16 rate), PV in bf16: the tensor
+            # roofline time is 0.75 of the bf16 one; the quantisation passes are
+            # the "cache write" slot of the per-kernel record
+            line["workload"] += "+fp8qk"
+            line["quant_ms"] = round(t_write / max(calls, 1), 5)
+            line["tensor_frac_attention_fp8qk_roofline"] = round(
+                flops / (attn_ms * 1e-3) / 1e12 / (tc / 0.75), 4)
         if args.append:
             # K and V rows of every query token read once and written once
             wbytes = 4 * int(wl.q.shape[0]) * wl.n_heads_kv * wl.head_dim * 2
