@@ -31,6 +31,8 @@ Readings (the page names the phases and gives the scheduler's block sizes
 
 Both sides take every rounding decision in the same precision, so the codes
 and scales are reproducible bit for bit.
+
+Test infrastructure only: the product path never imports this module.
 """
 from __future__ import annotations
 
@@ -216,3 +218,98 @@ def attention_dequantized(wl, rows=None, qz=None):
 def torch_index(idx):
     import torch
     return torch.as_tensor(np.asarray(idx, dtype=np.int64))
+
+
+# ---------------------------------------------------------------------------
+# fp8 P.V: the V phases of the same page (``v_fp8_transpose_scale_quantization``
+# with its transpose/pad/permute and scale/fp8 parts, ``v_scale_fp8_quantization``)
+# and the attention with e4m3 P and V.
+#
+# Readings: one V scale per (sequence, KV head, channel) over the sequence's keys
+# (a per-channel scale is constant along the keys, so it factors out of P.V and
+# is applied to O); the codes are stored transposed, keys innermost, in tiles of
+# 128 keys padded with zero codes: [tile][KV head][channel][128 keys].
+
+V_TILE = 128
+P_SCALE_LOG2 = 5       # P is coded as e4m3 of p * 2^5
+P_SLACK_LOG2 = 3       # the running max may trail the tile max by up to 2^3
+
+
+def logical_v(kv_pool, block_table, seq_lens, b: int, page_size: int = 64, start: int = 0):
+    """V of sequence b as fp32 [L, Hkv, D] (exact bf16 values)."""
+    L = int(seq_lens[b])
+    if block_table is None:
+        return _bf16_to_f32(kv_pool[1, start:start + L])
+    j = np.arange(L)
+    bt = np.asarray(block_table[b].cpu().numpy() if hasattr(block_table, "cpu") else block_table[b])
+    pool = kv_pool.detach().cpu()
+    return pool[bt[j // page_size], 1, j % page_size].float().numpy().astype(np.float32)
+
+
+def quantize_v(v32: np.ndarray):
+    """V fp32 [L, Hkv, D] -> (codes uint8 [ntiles, Hkv, D, 128], scales fp32 [Hkv, D]):
+    per channel scale = amax / 448, code = e4m3(v * (448 / amax)), keys innermost,
+    zero codes past L."""
+    L, H, D = v32.shape
+    amax = _amax(v32, axis=0)
+    nt = (L + V_TILE - 1) // V_TILE
+    c = np.zeros((nt * V_TILE, H, D), dtype=np.uint8)
+    c[:L] = _codes(v32, _inv_scale(amax)[None])
+    return np.ascontiguousarray(c.reshape(nt, V_TILE, H, D).transpose(0, 2, 3, 1)), _scale(amax)
+
+
+def dequantize_v(codes: np.ndarray, scale: np.ndarray, L: int) -> np.ndarray:
+    """Inverse layout of :func:`quantize_v`: float64 [L, Hkv, D]."""
+    nt, H, D, _ = codes.shape
+    vals = e4m3_values(codes.transpose(0, 3, 1, 2).reshape(nt * V_TILE, H, D))[:L]
+    return vals * scale.astype(np.float64)[None]
+
+
+def attention_fp8(wl, rows=None):
+    """The fp8 P.V method against the float64 attention over the dequantised
+    Q, K and V: returns (out, bound), both [n, Hq, D].
+
+    ``out`` is softmax(scale * q^ . k^) v^ with the exact softmax. The method
+    also rounds each probability to e4m3: with p relative to the row max,
+    the coded value p * 2^(5 + d), 0 <= d <= 3 (the trailing running max), is
+    within 2^-4 of it relatively or 2^-10 absolutely, so the output moves by at
+    most (2^-4 sum p |v^| + 2^-15 sum |v^|) / sum p; ``bound`` is that plus
+    the bf16 rounding of the output (2^-8 |out|) and 1e-4 for fp32 sums and
+    exp2 approximations.
+    """
+    cu = wl.cu_q.numpy().astype(np.int64)
+    sl = wl.seq_lens.numpy().astype(np.int64)
+    starts = np.concatenate([[0], np.cumsum(sl)])
+    toks = np.arange(int(cu[-1])) if rows is None else np.asarray(list(rows), dtype=np.int64)
+    G = wl.n_heads_q // wl.n_heads_kv
+    qc, qs = quantize_q(_bf16_to_f32(wl.q[torch_index(toks)]))
+    q_deq = e4m3_values(qc) * qs.astype(np.float64)[:, :, None]
+    seq_of = np.searchsorted(cu, toks, side="right") - 1
+    out = np.zeros((len(toks), wl.n_heads_q, wl.head_dim), dtype=np.float64)
+    bound = np.zeros_like(out)
+    for b in np.unique(seq_of):
+        b = int(b)
+        L = int(sl[b])
+        ql = int(cu[b + 1] - cu[b])
+        k32 = logical_k(wl.kv_pool, wl.block_table, wl.seq_lens, b, wl.page_size, int(starts[b]))
+        kc, ks = quantize_k(k32, k_mean(k32))
+        vc, vs = quantize_v(logical_v(wl.kv_pool, wl.block_table, wl.seq_lens, b, wl.page_size,
+                                      int(starts[b])))
+        v_deq = dequantize_v(vc, vs, L)
+        mine = np.nonzero(seq_of == b)[0]
+        for hk in range(wl.n_heads_kv):
+            k = e4m3_values(kc[:L, hk]) * np.repeat(ks[:, hk].astype(np.float64), 64)[:L, None]
+            vh = v_deq[:, hk]
+            for n in mine:
+                pos = L - ql + (int(toks[n]) - int(cu[b]))
+                nk = min(L, pos + 1) if wl.causal else L
+                if nk <= 0:
+                    continue
+                for h in range(hk * G, (hk + 1) * G):
+                    s = (k[:nk] @ q_deq[n, h]) * wl.scale
+                    w = np.exp(s - s.max())
+                    o = (w @ vh[:nk]) / w.sum()
+                    out[n, h] = o
+                    bound[n, h] = ((2.0 ** -4) * (w @ np.abs(vh[:nk])) + (2.0 ** -15) * np.abs(vh[:nk]).sum(0)) \
+                        / w.sum() + (2.0 ** -8) * np.abs(o) + 1e-4
+    return out, bound

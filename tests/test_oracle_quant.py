@@ -173,3 +173,82 @@ def test_smoothing_keeps_channel_offsets_out_of_the_error():
     got = quant.attention_dequantized(wl)
     err = np.abs(got - ref)
     assert err.max() < 0.1 and err.mean() < 0.01, (err.max(), err.mean())
+
+
+# ---------------------------------------------------------------------------
+# fp8 P.V: V codes and the error bound of the e4m3 probabilities
+
+
+def test_v_codes_layout_scale_and_padding():
+    rng = np.random.default_rng(21)
+    L, H, D = 130, 2, 128
+    v = torch.from_numpy(rng.standard_normal((L, H, D)) * 3).to(torch.bfloat16).float().numpy()
+    v[:, 1, 7] = 0.0                                   # an all-zero channel
+    codes, scale = quant.quantize_v(v)
+    assert codes.shape == (2, H, D, 128) and scale.shape == (H, D)
+    assert scale[1, 7] == 1.0 and not codes[:, 1, 7].any()
+    amax = np.abs(v[:, 0, 3]).max()
+    assert scale[0, 3] == np.float32(amax) / np.float32(448)
+    # key j of tile t sits at codes[t, hk, d, j]; rows past L are zero codes
+    for (j, hk, d) in [(0, 0, 0), (129, 1, 127), (64, 0, 5), (127, 1, 64)]:
+        inv = np.float32(448) / np.float32(np.abs(v[:, hk, d]).max())
+        want = quant.e4m3_codes(np.array([np.float32(v[j, hk, d]) * inv], dtype=np.float32))[0]
+        assert codes[j // 128, hk, d, j % 128] == want
+    assert not codes[1, :, :, 2:].any()
+    # the channel maximum maps to +-448
+    assert np.all(np.abs(quant.e4m3_values(codes)).max(axis=(0, 3))[0] == 448.0)
+
+
+def test_v_on_the_e4m3_grid_dequantises_exactly():
+    rng = np.random.default_rng(22)
+    grid = np.array([0.0, 0.5, 1.0, 1.75, 3.0, 6.5, 448.0])
+    v = rng.choice(grid, size=(70, 1, 128)) * rng.choice([-1, 1], size=(70, 1, 128))
+    v[3, 0, :] = 448.0
+    v *= 2.0 ** -5
+    codes, scale = quant.quantize_v(v.astype(np.float32))
+    assert np.array_equal(quant.dequantize_v(codes, scale, 70), v)
+
+
+def test_exactly_coded_inputs_give_the_plain_attention():
+    # Q, K and V on the e4m3 grid with power-of-two block maxima and zero-mean K:
+    # every code is exact, so the oracle's fp8 output is the float64 C oracle's
+    rng = np.random.default_rng(23)
+    grid = np.array([0.0, 0.25, 0.5, 1.0, 1.5, 2.0, 3.0, 448.0])
+    T, Hq, Hkv, D, L = 4, 4, 2, 128, 64
+    q = rng.choice(grid, size=(T, Hq, D)) * rng.choice([-1, 1], size=(T, Hq, D))
+    q[..., 0] = 448.0
+    half = rng.choice(grid[:-1], size=(L // 2, Hkv, D)) * rng.choice([-1, 1], size=(L // 2, Hkv, D))
+    k = np.concatenate([half, -half], axis=0)
+    k[0, :, 1] = 448.0
+    k[L // 2, :, 1] = -448.0
+    v = rng.choice(grid[:-1], size=(L, Hkv, D)) * rng.choice([-1, 1], size=(L, Hkv, D))
+    v[5] = 448.0
+    q, k, v = q * 2.0 ** -6, k * 2.0 ** -6, v * 2.0 ** -7
+    wl = workloads.make_paged("exactv", 3, [T], [L], Hq, Hkv, D, causal=True, extra_pages=1)
+    wl.q.copy_(torch.from_numpy(q).to(torch.bfloat16))
+    page = int(wl.block_table[0, 0])
+    wl.kv_pool[page, 0, :L].copy_(torch.from_numpy(k).to(torch.bfloat16))
+    wl.kv_pool[page, 1, :L].copy_(torch.from_numpy(v).to(torch.bfloat16))
+    got, bound = quant.attention_fp8(wl)
+    ref, _ = oracle.forward_workload(wl)
+    assert np.abs(got - ref).max() < 1e-12
+    assert np.all(bound > 0)
+
+
+def test_bound_covers_simulated_probability_rounding():
+    # round every p * 2^(5 + d) to e4m3 for a trailing max d in [0, 3] (fp32
+    # row sum of the unrounded p): the output error stays within the bound
+    rng = np.random.default_rng(24)
+    for n in [1, 2, 3, 7, 64, 300, 5000]:
+        for trial in range(20):
+            s = rng.standard_normal(n) * rng.uniform(0.5, 6)
+            v = rng.standard_normal((n, 16)) * rng.uniform(0.1, 4)
+            w = np.exp(s - s.max())
+            d = rng.uniform(0, 3)
+            scaled = w * 2.0 ** (P := quant.P_SCALE_LOG2) * 2.0 ** d
+            ph = quant.e4m3_values(quant.e4m3_codes(scaled.astype(np.float32)))
+            o_hat = (ph @ v) / scaled.sum()
+            o = (w @ v) / w.sum()
+            bnd = ((2.0 ** -4) * (w @ np.abs(v)) + (2.0 ** -15) * np.abs(v).sum(0)) / w.sum()
+            assert np.all(np.abs(o_hat - o) <= bnd * (1 + 1e-6) + 1e-12), (n, trial)
+    assert P == 5 and quant.P_SLACK_LOG2 + quant.P_SCALE_LOG2 <= 8   # p * 2^5 <= 2^8 < 448
