@@ -55,6 +55,8 @@ def parse():
                     help="time named workload(s) 1-5 (comma list or 'all'): one JSON line each")
     ap.add_argument("--fp8qk", action="store_true",
                     help="with --workload: the quantised-QK variant (pattn_forward_fp8qk)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="with --workload: the fp8 Q/K/P/V variant (pattn_forward_fp8)")
     ap.add_argument("--append", action="store_true",
                     help="with --workload: each step first writes the query tokens' K/V rows into "
                          "their cache slots (pattn_forward_append)")
@@ -443,7 +445,11 @@ def run_workloads(args):
             k_new, v_new = (t.to(dev) for t in workloads.new_kv_rows(wl, 900 + i))
 
         def step():
-            if args.fp8qk:
+            if args.fp8:
+                pk.forward_fp8(out, q, kv, bt, sl, cu, max_q=wl.max_q, max_kv=wl.max_kv,
+                               n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
+                               num_pages=wl.num_pages, check=False)
+            elif args.fp8qk:
                 pk.forward_fp8qk(out, q, kv, bt, sl, cu, max_q=wl.max_q, max_kv=wl.max_kv,
                                  n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
                                  num_pages=wl.num_pages, check=False)
@@ -494,6 +500,12 @@ def run_workloads(args):
             line["quant_ms"] = round(t_write / max(calls, 1), 5)
             line["tensor_frac_attention_fp8qk_roofline"] = round(
                 flops / (attn_ms * 1e-3) / 1e12 / (tc / 0.75), 4)
+        if args.fp8:
+            # QK and PV on e4m3 tensor cores: half the bf16 roofline time
+            line["workload"] += "+fp8"
+            line["quant_ms"] = round(t_write / max(calls, 1), 5)
+            line["tensor_frac_attention_fp8_roofline"] = round(
+                flops / (attn_ms * 1e-3) / 1e12 / (2 * tc), 4)
         if args.append:
             # K and V rows of every query token read once and written once
             wbytes = 4 * int(wl.q.shape[0]) * wl.n_heads_kv * wl.head_dim * 2

@@ -171,6 +171,55 @@ pattn_status pattn_quantize_qk(void *q8, float *q_scale, void *k8, float *k_scal
 size_t pattn_workspace_size_fp8qk(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
                                   int n_heads_kv, int head_dim, int page_size);
 
+/*
+ * pattn_forward_fp8 -- pattn_forward_fp8qk with P and V in e4m3 as well: the V
+ * phases of the same GB10 "sage2" page (v_fp8_transpose_scale_quantization:
+ * transpose/pad/permute and scale/fp8; v_scale_fp8_quantization), then
+ * O = P V as e4m3 MMAs with fp32 accumulation. Same arguments and output as
+ * pattn_forward; head_dim 128 and max_kv <= 2^20 only (else
+ * PATTN_ERR_UNSUPPORTED). Needs pattn_workspace_size_fp8 bytes of workspace.
+ *
+ *   V: one scale per (sequence, KV head, channel), scale = amax / 448 over the
+ *   sequence's keys, code = e4m3 of v * (448 / amax) as for Q and K, stored
+ *   transposed (keys innermost) in zero-padded 128-key tiles. P: e4m3 of
+ *   p * 2^5 with p taken against a running row max that trails the true one
+ *   by at most 2^3, so no code saturates; the row sum is the fp32 sum of the
+ *   unrounded p. The output is the attention over the dequantised Q, K and V
+ *   up to the rounding of P: per element at most
+ *   (2^-4 sum_j p_j |v_j| + 2^-15 sum_j |v_j|) / sum_j p_j
+ *   (p relative to the row max, v the dequantised V) plus the bf16 rounding of
+ *   the output. Units of at most 16 packed query rows take the bf16 decode kernel.
+ */
+pattn_status pattn_forward_fp8(void *out, const void *q, const void *kv_pool,
+                               const int32_t *block_table, const int32_t *seq_lens,
+                               const int32_t *cu_q, int num_seqs, int total_q, int max_q,
+                               int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
+                               int page_size, int num_pages, float scale, int causal,
+                               pattn_stream_t stream);
+
+/*
+ * pattn_quantize_v -- only the V codes and scales of pattn_forward_fp8, into
+ * caller-owned device buffers (nb = 2 * ceil(max_kv / 128)):
+ *
+ *   v8       e4m3 bytes [num_seqs * nb / 2][n_heads_kv][128 channels][128 keys],
+ *            16-byte aligned: 128-key tile t of sequence b is tile b * nb / 2 + t;
+ *            keys past L_b in its last tile are zero codes; later tiles are
+ *            not written
+ *   v_scale  fp32 [num_seqs][n_heads_kv][128], 16-byte aligned
+ *
+ * Other arguments as for pattn_forward (no queries are read). Rejected
+ * sequences (device error word) are not written.
+ */
+pattn_status pattn_quantize_v(void *v8, float *v_scale, const void *kv_pool,
+                              const int32_t *block_table, const int32_t *seq_lens,
+                              const int32_t *cu_q, int num_seqs, int total_q, int max_q, int max_kv,
+                              int n_heads_q, int n_heads_kv, int head_dim, int page_size,
+                              int num_pages, pattn_stream_t stream);
+
+/* Workspace bytes pattn_forward_fp8 needs for these bounds (0 if unsupported). */
+size_t pattn_workspace_size_fp8(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
+                                int n_heads_kv, int head_dim, int page_size);
+
 /* Bytes of the fixed device scratch behind pattn_forward_noalloc. */
 #define PATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 

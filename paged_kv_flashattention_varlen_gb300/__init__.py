@@ -14,7 +14,8 @@ from typing import Optional, Tuple
 
 from . import _lib
 
-__all__ = ["PattnError", "forward", "forward_append", "forward_fp8qk", "quantize_qk", "forward_noalloc",
+__all__ = ["PattnError", "forward", "forward_append", "forward_fp8qk", "quantize_qk", "forward_fp8",
+           "quantize_v", "forward_noalloc",
            "forward_host", "workspace_size",
            "set_workspace", "device_status", "status_string", "profile_enable", "profile_read",
            "profile_read_kernels", "STATUS", "library_path"]
@@ -179,6 +180,45 @@ def quantize_qk(q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: 
         pages, _stream_handle(stream))
     _check(rc, "pattn_quantize_qk")
     return q8, qs, k8, ks
+
+
+def forward_fp8(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,
+                n_heads_kv: int, scale: float, causal: bool, num_pages: Optional[int] = None,
+                stream=None, check: bool = True) -> int:
+    """fp8 attention (``pattn_forward_fp8``): Q, K (mean-smoothed), P and V as
+    e4m3 codes, S and P.V on e4m3 tensor cores. head_dim 128. Arguments as for
+    :func:`forward`."""
+    _check_device_args(out, q, kv_pool, block_table, seq_lens, cu_q)
+    total_q, hq, d, page, pages = _shape_args(q, kv_pool, block_table, n_heads_kv, num_pages)
+    rc = _lib.load().pattn_forward_fp8(
+        _ptr(out), _ptr(q), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens), _ptr(cu_q),
+        int(seq_lens.numel()), total_q, int(max_q), int(max_kv), hq, int(n_heads_kv), d, page,
+        pages, float(scale), int(bool(causal)), _stream_handle(stream))
+    if check:
+        _check(rc, "pattn_forward_fp8")
+    return rc
+
+
+def quantize_v(q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,
+               n_heads_kv: int, num_pages: Optional[int] = None, stream=None):
+    """The e4m3 V codes and per-channel scales of :func:`forward_fp8`
+    (``pattn_quantize_v``; ``q`` gives the shapes only).
+
+    Returns ``(v8 uint8 [B * nt, Hkv, D, 128], v_scale f32 [B, Hkv, D])`` with
+    ``nt = ceil(max_kv / 128)``; 128-key tile t of sequence b is ``b * nt + t``,
+    keys innermost."""
+    import torch
+    total_q, hq, d, page, pages = _shape_args(q, kv_pool, block_table, n_heads_kv, num_pages)
+    B = int(seq_lens.numel())
+    nt = max(1, -(-int(max_kv) // 128))
+    dev = q.device
+    v8 = torch.zeros((B * nt, int(n_heads_kv), d, 128), dtype=torch.uint8, device=dev)
+    vs = torch.zeros((B, int(n_heads_kv), d), dtype=torch.float32, device=dev)
+    rc = _lib.load().pattn_quantize_v(
+        _ptr(v8), _ptr(vs), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens), _ptr(cu_q), B, total_q,
+        int(max_q), int(max_kv), hq, int(n_heads_kv), d, page, pages, _stream_handle(stream))
+    _check(rc, "pattn_quantize_v")
+    return v8, vs
 
 
 def forward_noalloc(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,

@@ -24,6 +24,9 @@ SIGNATURES = {
     "pattn_quantize_qk": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
                                _i, _vp]),
     "pattn_workspace_size_fp8qk": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "pattn_forward_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "pattn_quantize_v": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
+    "pattn_workspace_size_fp8": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "pattn_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
                                    _vp]),
     "pattn_forward_host": (_i, [_vp, _vp, _vp, _sz, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,

@@ -208,14 +208,15 @@ pattn_status encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t
 // 2^-32, values clamped to +-1024) stay below 2^62 in magnitude.
 constexpr int kFp8MaxKv = 1 << 20;
 
-// Workspace regions of the quantised-QK variant, after the regular ones (see
-// QuantParams for the layouts). nb_max is even, so that both key halves of a
-// 128-key tile have a block.
+// Workspace regions of the quantised variants, after the regular ones (see
+// QuantParams for the layouts; the V regions only with_v). nb_max is even, so
+// that both key halves of a 128-key tile have a block.
 struct Fp8Layout {
-  size_t k_sum, q8, q_scale, k8, k_scale, total;  // k_sum: the quant_scratch_bytes region
+  size_t k_sum, q8, q_scale, k8, k_scale, v8, v_scale, total;  // k_sum: the quant_scratch_bytes region
   int nb_max;
 };
-Fp8Layout fp8_layout(size_t base, int num_seqs, int total_q, int max_kv, int hq, int hkv, int d) {
+Fp8Layout fp8_layout(size_t base, int num_seqs, int total_q, int max_kv, int hq, int hkv, int d,
+                     bool with_v = false) {
   Fp8Layout f{};
   f.nb_max = 2 * std::max(1, cdiv(max_kv, 2 * kPage));
   const size_t B = static_cast<size_t>(num_seqs), nb = static_cast<size_t>(f.nb_max);
@@ -230,13 +231,19 @@ Fp8Layout fp8_layout(size_t base, int num_seqs, int total_q, int max_kv, int hq,
   off += B * nb * kPage * hkv * d;
   f.k_scale = off = align_up(off, 256);
   off += B * nb * hkv * sizeof(float);
+  if (with_v) {
+    f.v8 = off = align_up(off, 256);
+    off += B * (nb / 2) * hkv * d * 128;
+    f.v_scale = off = align_up(off, 256);
+    off += B * hkv * d * sizeof(float);
+  }
   f.total = align_up(off, 256);
   return f;
 }
 
-// What one call computes: attention (bf16 Q/K), attention with e4m3 Q/K codes,
-// or only the e4m3 codes of Q and K.
-enum class Mode { kBf16, kFp8, kQuantOnly };
+// What one call computes: attention (bf16), attention with e4m3 Q/K codes,
+// attention with e4m3 Q/K/P/V codes, or only codes (those QuantBufs names).
+enum class Mode { kBf16, kFp8, kFp8Pv, kQuantOnly };
 
 // Device buffers of the e4m3 codes (workspace regions or caller buffers).
 struct QuantBufs {
@@ -244,6 +251,8 @@ struct QuantBufs {
   float* q_scale = nullptr;
   uint8_t* k8 = nullptr;
   float* k_scale = nullptr;
+  uint8_t* v8 = nullptr;
+  float* v_scale = nullptr;
   void* scratch = nullptr;  // quant_scratch_bytes
   int nb_max = 0;
 };
@@ -416,7 +425,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (mode != Mode::kBf16) {
-    // e4m3 codes and scales of Q and of the smoothed K (dependent launches)
+    // e4m3 codes and scales of Q, of the smoothed K and of V (dependent launches)
     QuantParams qp{};
     qp.q = static_cast<const __nv_bfloat16*>(q);
     qp.kv_pool = static_cast<const __nv_bfloat16*>(kv);
@@ -426,7 +435,9 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     qp.q_scale = qb->q_scale;
     qp.k8 = qb->k8;
     qp.k_scale = qb->k_scale;
-    quant_scratch_split(qb->scratch, num_seqs, hkv, d, &qp.k_sum, &qp.k_cnt, &qp.k_mean);
+    qp.v8 = qb->v8;
+    qp.v_scale = qb->v_scale;
+    qp.sc = quant_scratch_split(qb->scratch, num_seqs, hkv, d);
     qp.num_seqs = num_seqs;
     qp.total_q = total_q;
     qp.n_heads_q = hq;
@@ -435,7 +446,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     qp.bt_stride = pp.bt_stride;
     qp.num_pages = num_pages;
     qp.nb_max = qb->nb_max;
-    e = launch_quant_qk(qp, st.sms, stream);
+    e = launch_quant(qp, st.sms, stream);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (prof) cudaEventRecord(rec.ev[2], stream);
@@ -452,7 +463,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   }
   if (prof) cudaEventRecord(rec.ev[3], stream);
   if (run_prefill) {
-    if (mode == Mode::kFp8) {
+    if (mode == Mode::kFp8 || mode == Mode::kFp8Pv) {
       // e4m3 Q [total_q][hq][d] and K blocks [B * nb_max][64][hkv][d], one byte each
       CUtensorMap tq8, tk8;
       const cuuint64_t qdims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
@@ -475,7 +486,21 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
       fp.q_scale = qb->q_scale;
       fp.k_scale = qb->k_scale;
       fp.nb_max = qb->nb_max;
-      e = launch_attention_fp8(fp, tq8, tk8, tkv, st.sms, stream, dep);
+      if (mode == Mode::kFp8Pv) {
+        // transposed e4m3 V tiles [B * nb_max / 2][hkv][d][128 keys]
+        CUtensorMap tv8;
+        const cuuint64_t vdims[4] = {128, static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                                     static_cast<cuuint64_t>(num_seqs) * (qb->nb_max / 2)};
+        const cuuint64_t vstr[3] = {128, static_cast<cuuint64_t>(d) * 128,
+                                    static_cast<cuuint64_t>(hkv) * d * 128};
+        const cuuint32_t vbox[4] = {128, static_cast<cuuint32_t>(d), 1, 1};
+        if ((s = encode(&tv8, qb->v8, 4, vdims, vstr, vbox, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != PATTN_OK)
+          return s;
+        fp.v_scale = qb->v_scale;
+        e = launch_attention_fp8pv(fp, tq8, tk8, tv8, st.sms, stream, dep);
+      } else {
+        e = launch_attention_fp8(fp, tq8, tk8, tkv, st.sms, stream, dep);
+      }
     } else {
       e = launch_attention(ap, tq, tkv, d, st.sms, stream, dep);
     }
@@ -507,7 +532,7 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
   if (s != PATTN_OK) return s;
   DeviceState& st = *stp;
   const WsLayout L = ws_layout(num_seqs, total_q, max_q, hq, hkv, d);
-  const Fp8Layout F = fp8_layout(L.total, num_seqs, total_q, max_kv, hq, hkv, d);
+  const Fp8Layout F = fp8_layout(L.total, num_seqs, total_q, max_kv, hq, hkv, d, mode == Mode::kFp8Pv);
   if ((s = ensure_workspace(st, mode == Mode::kBf16 ? L.total : F.total)) != PATTN_OK) return s;
   uint8_t* wsb = static_cast<uint8_t*>(st.ws);
   QuantBufs qb;
@@ -518,6 +543,10 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
     qb.k_scale = reinterpret_cast<float*>(wsb + F.k_scale);
     qb.scratch = wsb + F.k_sum;
     qb.nb_max = F.nb_max;
+    if (mode == Mode::kFp8Pv) {
+      qb.v8 = wsb + F.v8;
+      qb.v_scale = reinterpret_cast<float*>(wsb + F.v_scale);
+    }
   }
   return launch_all(st, wsb, L, out, q, kv, bt, seq_lens, cu_q, num_seqs, total_q, max_q, max_kv, hq,
                     hkv, d, num_pages, scale, causal, stream, sh, k_new, v_new, mode, &qb);
@@ -609,6 +638,25 @@ pattn_status pattn_forward_fp8qk(void* out, const void* q, const void* kv_pool,
                         Mode::kFp8);
 }
 
+pattn_status pattn_forward_fp8(void* out, const void* q, const void* kv_pool, const int32_t* block_table,
+                               const int32_t* seq_lens, const int32_t* cu_q, int num_seqs, int total_q,
+                               int max_q, int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
+                               int page_size, int num_pages, float scale, int causal, pattn_stream_t stream) {
+  Shape sh{};
+  pattn_status s = check_args(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                              max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size,
+                              num_pages, scale, causal, &sh);
+  if (s != PATTN_OK) return s;
+  if (head_dim != 128 || max_kv > kFp8MaxKv) return PATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_seqs) * n_heads_kv > 0x7fffffffLL) return PATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return forward_locked(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
+                        max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, scale,
+                        causal, reinterpret_cast<cudaStream_t>(stream), sh, nullptr, nullptr,
+                        Mode::kFp8Pv);
+}
+
 pattn_status pattn_quantize_qk(void* q8, float* q_scale, void* k8, float* k_scale, const void* q,
                                const void* kv_pool, const int32_t* block_table,
                                const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
@@ -645,6 +693,49 @@ pattn_status pattn_quantize_qk(void* q8, float* q_scale, void* k8, float* k_scal
                     max_q, max_kv, n_heads_q, n_heads_kv, head_dim, num_pages, 1.0f, 0,
                     reinterpret_cast<cudaStream_t>(stream), sh, nullptr, nullptr, Mode::kQuantOnly,
                     &qb);
+}
+
+pattn_status pattn_quantize_v(void* v8, float* v_scale, const void* kv_pool, const int32_t* block_table,
+                              const int32_t* seq_lens, const int32_t* cu_q, int num_seqs, int total_q,
+                              int max_q, int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
+                              int page_size, int num_pages, pattn_stream_t stream) {
+  Shape sh{};
+  // the attention's argument rules (dummy output and query pointers: neither is read)
+  pattn_status s = check_args(kv_pool, kv_pool, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                              max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, 1.0f,
+                              0, &sh);
+  if (s != PATTN_OK) return s;
+  if (!v8 || !v_scale || !aligned(v8, 16) || !aligned(v_scale, 16)) return PATTN_ERR_INVALID_ARG;
+  if (head_dim != 128 || max_kv > kFp8MaxKv) return PATTN_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* stp = nullptr;
+  if ((s = device_state(&stp)) != PATTN_OK) return s;
+  DeviceState& st = *stp;
+  const WsLayout L = ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim);
+  const Fp8Layout F = fp8_layout(L.total, num_seqs, total_q, max_kv, n_heads_q, n_heads_kv, head_dim);
+  const size_t need = align_up(F.k_sum + quant_scratch_bytes(num_seqs, n_heads_kv, head_dim), 256);
+  if ((s = ensure_workspace(st, need)) != PATTN_OK) return s;
+  uint8_t* wsb = static_cast<uint8_t*>(st.ws);
+  QuantBufs qb;
+  qb.v8 = static_cast<uint8_t*>(v8);
+  qb.v_scale = v_scale;
+  qb.scratch = wsb + F.k_sum;
+  qb.nb_max = F.nb_max;
+  return launch_all(st, wsb, L, nullptr, kv_pool, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                    max_q, max_kv, n_heads_q, n_heads_kv, head_dim, num_pages, 1.0f, 0,
+                    reinterpret_cast<cudaStream_t>(stream), sh, nullptr, nullptr, Mode::kQuantOnly, &qb);
+}
+
+size_t pattn_workspace_size_fp8(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
+                                int n_heads_kv, int head_dim, int page_size) {
+  (void)page_size;
+  if (num_seqs < 0 || total_q < 0 || max_q < 0 || max_kv < 0 || n_heads_q <= 0 || n_heads_kv <= 0 ||
+      n_heads_q % n_heads_kv != 0 || n_heads_q / n_heads_kv > kBM || head_dim != 128 ||
+      max_kv > kFp8MaxKv)
+    return 0;
+  const WsLayout L = ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim);
+  return fp8_layout(L.total, num_seqs, total_q, max_kv, n_heads_q, n_heads_kv, head_dim, true).total;
 }
 
 size_t pattn_workspace_size_fp8qk(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,

@@ -41,28 +41,41 @@
 // each warp has just read, so that QK of tile n waits only for the PV of tile
 // n - 2. D = 256: O | S0 | S1 | P0 | P1.
 //
+// Quantised instances (head_dim 128): kF8 takes e4m3 Q and K codes for S (four
+// kind::f8f6f4 MMAs of K = 32) and scales each warpgroup's scores by the Q row
+// and K block scales. kF8V also codes P and V: the softmax computes the tile
+// max every tile (the running max may trail it by at most 2^3), writes e4m3 of
+// p * 2^5 (at most 2^8, inside the e4m3 range) into a shared-memory P buffer in
+// the 128-byte-swizzled K-major layout, and O += P V runs as kind::f8f6f4 MMAs
+// with both operands in shared memory (V as transposed e4m3 tiles); the
+// per-channel V scale is applied in the epilogue.
+//
 // At the end of an item the softmax warps divide by l and store bf16 rows, or
 // (split items) write the normalised partial O and (m, l); merge_kernel then
 // merges each split unit.
+#include <cuda_fp8.h>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 
 namespace pattn {
 namespace {
 
-template <int D, int BN, bool kF8 = false>
+template <int D, int BN, bool kF8 = false, bool kF8V = false>
 struct Cfg {
   // kF8: Q and K as e4m3 codes (one byte), S = Q K^T with kind::f8f6f4 MMAs; V
-  // stays bf16.
+  // stays bf16 unless kF8V (P and V e4m3, P in shared memory).
+  static_assert(!kF8V || (kF8 && D == 128 && BN == 128), "fp8 P.V: head_dim 128, 128-key tiles");
   static constexpr int kQKElem = kF8 ? 1 : 2;          // bytes per Q / K element
   static constexpr int kQBytes = kBM * D * kQKElem;
   static constexpr int kKStage = BN * D * kQKElem;
-  static constexpr int kVStage = BN * D * 2;
+  static constexpr int kVStage = BN * D * (kF8V ? 1 : 2);
+  static constexpr int kPSmem = kF8V ? kBM * BN : 0;   // one e4m3 P buffer in shared memory
   static constexpr int kQKBlocks = D * kQKElem / 128;  // 128-byte swizzle columns of a Q / K row
   static constexpr int kQKBlockElems = 128 / kQKElem;
   static constexpr int kQKSteps = D * kQKElem / 32;    // MMAs of one QK (32 bytes of K each)
   static constexpr bool kSplitO = D == 128;          // one O per softmax warpgroup
-  static constexpr bool kAliasP = D == 128;          // P over its S buffer
+  static constexpr bool kAliasP = D == 128 && !kF8V;  // P over its S buffer
   static constexpr int kSBufs = 2;
   static constexpr int kPBufs = kAliasP ? kSBufs : 2;
   static constexpr int kPVBars = kAliasP ? kSBufs : 2;  // pv_done barriers, by tile index
@@ -73,7 +86,8 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBufs * kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKStage;
-  static constexpr int kOffX = kOffV + kVStages * kVStage;  // row sum / max / l exchange
+  static constexpr int kOffP = kOffV + kVStages * kVStage;  // kF8V: P buffers
+  static constexpr int kOffX = kOffP + kPBufs * kPSmem;     // row sum / max / l exchange
   static constexpr int kXBytes = (2 * 2 + 2 * 2 + 2) * kBM * 4;
   static constexpr int kOffBar = kOffX + kXBytes;
   static constexpr int kBarBytes = 512;
@@ -93,7 +107,7 @@ struct Cfg {
   }
   static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns of a V row
   static constexpr int kPagesPerTile = BN / kPage;
-  static_assert(kColS + kSBufs * BN + (kAliasP ? 0 : kPBufs * kPCols) <= kTmemCols, "TMEM budget");
+  static_assert(kColS + kSBufs * BN + ((kAliasP || kF8V) ? 0 : kPBufs * kPCols) <= kTmemCols, "TMEM budget");
   static_assert(kSBufs <= 3 && kPBufs <= 3 && kPVBars <= 3 && kQBufs <= 2, "barrier slots");
   static_assert((kSplitO ? 2 * D : D) <= kColS, "O columns");
   static_assert(BN % kPage == 0 && BN % 32 == 0, "tile");
@@ -160,6 +174,45 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[KH / 32][32], floa
   return a.x + a.y;
 }
 
+// The same for the fp8 P.V instance: p_i = 2^(S_i c - m_ref) with m_ref the
+// running max minus 5 (p scaled by 2^5), as e4m3 codes, four per word in key
+// order, returning the fp32 sum of the unrounded p_i.
+template <int KH, bool kMasked>
+__device__ __forceinline__ float exp_row_f8(const uint32_t (&sr)[KH / 32][32], float c, float m_ref,
+                                            int nv, uint32_t (&pk)[KH / 4]) {
+  const float2 c2 = make_float2(c, c);
+  const float2 nm2 = make_float2(-m_ref, -m_ref);
+  float2 acc[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) acc[u] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < KH / 32; ++j) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        const int k = i + 2 * hv;
+        const float2 x =
+            __ffma2_rn(make_float2(__uint_as_float(sr[j][k]), __uint_as_float(sr[j][k + 1])), c2, nm2);
+        float p0 = ex2(x.x);
+        float p1 = ex2(x.y);
+        if constexpr (kMasked) {
+          p0 = j * 32 + k < nv ? p0 : 0.f;
+          p1 = j * 32 + k + 1 < nv ? p1 : 0.f;
+        }
+        acc[(k >> 1) & 3] = __fadd2_rn(acc[(k >> 1) & 3], make_float2(p0, p1));
+        const uint32_t pair = static_cast<uint32_t>(
+            __nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3));
+        w |= pair << (16 * hv);
+      }
+      pk[(j * 32 + i) >> 2] = w;
+    }
+  }
+  const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+  return a.x + a.y;
+}
+
 // Max of the first nv of a row's KH scores (all of them when !kMasked).
 template <int KH, bool kMasked>
 __device__ __forceinline__ float max_row(const uint32_t (&sr)[KH / 32][32], int nv) {
@@ -175,11 +228,12 @@ __device__ __forceinline__ float max_row(const uint32_t (&sr)[KH / 32][32], int 
                fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
 }
 
-template <int D, int BN, bool kF8>
+template <int D, int BN, bool kF8, bool kF8V>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
-            const __grid_constant__ CUtensorMap tmap_k8, const AttnParams p) {
-  using C = Cfg<D, BN, kF8>;
+            const __grid_constant__ CUtensorMap tmap_k8, const __grid_constant__ CUtensorMap tmap_v8,
+            const AttnParams p) {
+  using C = Cfg<D, BN, kF8, kF8V>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -187,6 +241,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   const uint32_t sQ = s_base + C::kOffQ;
   const uint32_t sK = s_base + C::kOffK;
   const uint32_t sV = s_base + C::kOffV;
+  const uint32_t sP = s_base + C::kOffP;
   const uint32_t sBar = s_base + C::kOffBar;
   uint8_t* misc = smem + C::kOffMisc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
@@ -226,6 +281,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_kv);
     if constexpr (kF8) tma_prefetch_desc(&tmap_k8);
+    if constexpr (kF8V) tma_prefetch_desc(&tmap_v8);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -309,7 +365,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
               // a V stage is free once the PV of the tile it held is done
               ok = wait_one(pv_bar(n - stages), pv_par(n - stages), ctl);
             }
-            if (ok) {
+            if (ok && kF8V && kind == 1) {
+              // transposed e4m3 V: the whole 128-key tile of this head in one box
+              // (zero codes past the sequence end)
+              mbar_arrive_expect_tx(bar(full + st), static_cast<uint32_t>(C::kVStage));
+              tma_load_4d(sV + st * C::kVStage, &tmap_v8, bar(full + st), 0, 0, it.hk,
+                          it.b * (p.nb_max / 2) + it.kt0 + t0 + i, pol_kv);
+            } else if (ok) {
               const int blocks = (kF8 && kind == 0) ? C::kQKBlocks : C::kDBlocks;
               mbar_arrive_expect_tx(bar(full + st), static_cast<uint32_t>(nload * blocks * kPage * 128));
               const uint32_t dst0 = kind ? sV + st * C::kVStage : sK + st * C::kKStage;
@@ -409,8 +471,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     // ------------------------------------------------------------ V tail + PV MMA warp
     // Zeroes the V rows past the sequence end in a stage (whole 128-byte rows, so
     // the swizzle does not matter), then one thread issues O += P V for the tile.
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
-    const SmemDesc dv = sw128_desc_split(sV, BN * 128, 1024);
+    constexpr uint32_t idesc_pv = kF8V ? idesc_e4m3_f32(kBM, D) : idesc_bf16_f32(kBM, D, false, true);
+    // bf16 V: MN-major; e4m3 V: K-major transposed tiles, like the P buffers
+    const SmemDesc dv = kF8V ? sw128_desc_split(sV, 16, 1024) : sw128_desc_split(sV, BN * 128, 1024);
+    const SmemDesc dp = sw128_desc_split(sP, 16, 1024);
     const unsigned fullmask = 0xffffffffu;
     uint32_t n = 0;
     bool ok = true;
@@ -427,7 +491,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         const uint32_t s = n % C::kVStages;
         if (!(ok = wait_warp(bar(kVFull0 + s), (n / C::kVStages) & 1u, ctl))) break;
         const int live = L - kt * BN;
-        if (live < BN) {
+        if (!kF8V && live < BN) {
           uint8_t* v0 = smem + C::kOffV + s * C::kVStage;
           const int dead = BN - live;
           const int chunks = dead * 8;  // 16-byte chunks per block
@@ -445,8 +509,18 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             tc_fence_after();
             const bool first = kt == it.kt0;
             const uint32_t v_lo = desc_lo_at(dv, s * C::kVStage);
+            if constexpr (kF8V) {
+              // 32 keys (bytes) per MMA; key half hh into its own O
+              const uint32_t p_lo = desc_lo_at(dp, pb * C::kPSmem);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
+              for (int kk = 0; kk < BN / 32; ++kk) {
+                const int hh = kk / (BN / 64);
+                umma_f8_ss(tmem + C::kColO + hh * D, p_lo + ((kk * 32) >> 4), dp.hi, v_lo + ((kk * 32) >> 4),
+                           dv.hi, idesc_pv, (first && kk == hh * (BN / 64)) ? 0u : 1u);
+              }
+            }
+#pragma unroll
+            for (int kk = 0; kk < (kF8V ? 0 : BN / 16); ++kk) {
               const uint32_t b_lo = v_lo + ((kk * (16 * 128)) >> 4);
               const uint32_t a = tmem + C::p_col(static_cast<int>(pb), kk);
               if constexpr (C::kSplitO) {
@@ -546,6 +620,67 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         const bool full_tile = key0 + KH <= lim;
         const int nv = lim - key0;  // visible keys of this row in the chunk (any sign)
         uint32_t pk[KH / 2];
+        if constexpr (kF8V) {
+          // e4m3 P: the tile max first, every tile. The running max is kept
+          // while the tile max exceeds it by at most 3 (log2 units), so that
+          // every p * 2^5 stays at most 2^8; otherwise O is rescaled first.
+          uint32_t pk8[KH / 4];
+          if (warp_live) {
+            const float mx = full_tile ? max_row<KH, false>(sr, KH) : max_row<KH, true>(sr, nv);
+            const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * ct;
+            const float m_new = fmaxf(m_used, mx_s);
+            if (first) {
+              m_used = m_new;
+            } else {
+              const bool need = m_new > m_used + 3.0f;
+              if (__any_sync(0xffffffffu, need)) {
+                const uint32_t pm = n - 1;
+                if (!(ok = wait_warp(pv_bar(pm), pv_par(pm), ctl))) break;
+                tc_fence_after();
+                const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                if (need) {
+                  l *= alpha;
+                  m_used = m_new;
+                }
+#pragma unroll 1
+                for (int j = 0; j < D / 32; ++j) {
+                  uint32_t o[32];
+                  tmem_ld32(o_own + j * 32, o);
+                  tmem_wait_ld();
+                  reg_fence(o);
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                  tmem_st32(o_own + j * 32, o);
+                }
+                tmem_wait_st();
+              }
+            }
+            const float m_ref = ((m_used == -INFINITY) ? 0.f : m_used) - 5.0f;
+            l += full_tile ? exp_row_f8<KH, false>(sr, ct, m_ref, KH, pk8)
+                           : exp_row_f8<KH, true>(sr, ct, m_ref, nv, pk8);
+          }
+          // P buffer pb was last read by the PV of tile n - kPBufs
+          if (n >= static_cast<uint32_t>(C::kPBufs)) {
+            const uint32_t pm = n - C::kPBufs;
+            if (!(ok = wait_warp(pv_bar(pm), pv_par(pm), ctl))) break;
+          }
+          if (warp_live) {
+            // row r, keys [h KH, h KH + KH): 16-byte chunks 4h ... 4h + 3 of the
+            // 128-byte row, placed by the 128-byte swizzle (chunk ^ row % 8)
+            uint8_t* prow = smem + C::kOffP + pb * C::kPSmem + r * 128;
+#pragma unroll
+            for (int i = 0; i < KH / 16; ++i) {
+              const int chunk = (h * (KH / 16) + i) ^ (r & 7);
+              *reinterpret_cast<uint4*>(prow + chunk * 16) =
+                  make_uint4(pk8[4 * i], pk8[4 * i + 1], pk8[4 * i + 2], pk8[4 * i + 3]);
+            }
+            fence_proxy_async_smem();
+          }
+          tc_fence_before();  // an O rescale above precedes the next PV
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kPFull0 + pb));
+          continue;
+        }
         if (warp_live) {
           // Probabilities against the running max first. Their sum bounds every
           // one of them, so a sum of at most 2^8 shows that the tile max exceeds
@@ -660,6 +795,19 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           float v[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(o0[i]) * c0 + __uint_as_float(o1[i]) * c1;
+          if constexpr (kF8V) {
+            // per-channel V scale (P's 2^5 cancels against l)
+            const float4* vs = reinterpret_cast<const float4*>(
+                p.v_scale + (static_cast<size_t>(it.b) * p.n_heads_kv + it.hk) * D + col);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const float4 f = vs[q4];
+              v[q4 * 4] *= f.x;
+              v[q4 * 4 + 1] *= f.y;
+              v[q4 * 4 + 2] *= f.z;
+              v[q4 * 4 + 3] *= f.w;
+            }
+          }
           if (it.part < 0) {
             uint4* dst = reinterpret_cast<uint4*>(
                 p.out + (static_cast<size_t>(q0 + tok) * p.n_heads_q + hq) * D + col);
@@ -894,30 +1042,39 @@ size_t attention_smem_bytes(int head_dim) {
 }
 
 cudaError_t attention_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<128, 128, false>,
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<128, 128, false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<128, 128>::kSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_kernel<128, 128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_kernel<128, 128, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128, 128, true>::kSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_kernel<256, 64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_kernel<128, 128, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128, 128, true, true>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_kernel<256, 64, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Cfg<256, 64>::kSmem);
 }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                              int head_dim, int grid, cudaStream_t s, bool dependent) {
   if (head_dim == 128)
-    return launch_kernel(attn_kernel<128, 128, false>, grid, kAttnThreads, Cfg<128, 128>::kSmem, s,
-                         dependent, tq, tkv, tkv, p);
-  return launch_kernel(attn_kernel<256, 64, false>, grid, kAttnThreads, Cfg<256, 64>::kSmem, s,
-                       dependent, tq, tkv, tkv, p);
+    return launch_kernel(attn_kernel<128, 128, false, false>, grid, kAttnThreads, Cfg<128, 128>::kSmem, s,
+                         dependent, tq, tkv, tkv, tkv, p);
+  return launch_kernel(attn_kernel<256, 64, false, false>, grid, kAttnThreads, Cfg<256, 64>::kSmem, s,
+                       dependent, tq, tkv, tkv, tkv, p);
 }
 
 cudaError_t launch_attention_fp8(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
                                  const CUtensorMap& tkv, int grid, cudaStream_t s, bool dependent) {
-  return launch_kernel(attn_kernel<128, 128, true>, grid, kAttnThreads, Cfg<128, 128, true>::kSmem, s,
-                       dependent, tq8, tkv, tk8, p);
+  return launch_kernel(attn_kernel<128, 128, true, false>, grid, kAttnThreads, Cfg<128, 128, true>::kSmem,
+                       s, dependent, tq8, tkv, tk8, tkv, p);
+}
+
+cudaError_t launch_attention_fp8pv(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
+                                   const CUtensorMap& tv8, int grid, cudaStream_t s, bool dependent) {
+  return launch_kernel(attn_kernel<128, 128, true, true>, grid, kAttnThreads,
+                       Cfg<128, 128, true, true>::kSmem, s, dependent, tq8, tv8, tk8, tv8, p);
 }
 
 }  // namespace pattn

@@ -83,30 +83,42 @@ struct KvWriteParams {
   int row_elems;                // n_heads_kv * head_dim
 };
 
-// Preparation of the quantised-QK variant (quant.cu). Layouts:
+// Preparation of the quantised variants (quant.cu). Layouts:
 //   q8 [total_q][n_heads_q][head_dim] e4m3, q_scale [total_q][n_heads_q] fp32;
 //   k8 [num_seqs * nb_max][64][n_heads_kv][head_dim] e4m3 (sequence b's 64-key
 //   block j is block b * nb_max + j), k_scale [num_seqs * nb_max][n_heads_kv];
-//   scratch (quant_scratch_bytes): k_sum [num_seqs][n_heads_kv][head_dim] int64
-//   (units of 2^-32) and k_cnt [num_seqs][n_heads_kv] uint32, both zeroed
-//   before the call (the first quant_zero_bytes), then k_mean
-//   [num_seqs][n_heads_kv][head_dim] fp32.
+//   v8 [num_seqs * nb_max / 2][n_heads_kv][head_dim][128] e4m3: V transposed,
+//   keys innermost, 128-key tile t of sequence b at b * nb_max / 2 + t, zero
+//   codes past the sequence end; v_scale [num_seqs][n_heads_kv][head_dim] fp32.
+//   Scratch (quant_scratch_bytes), per (sequence, KV head): first, zeroed before
+//   the call (quant_zero_bytes), k_sum [..][head_dim] int64 (units of 2^-32),
+//   v_amax [..][head_dim] uint32 (fp32 bits of max |v|), k_cnt [..] uint32;
+//   then k_mean [..][head_dim] fp32 and v_inv [..][head_dim] fp32 (448 / amax).
+struct QuantScratch {
+  long long* k_sum;
+  unsigned int* v_amax;
+  unsigned int* k_cnt;
+  float* k_mean;
+  float* v_inv;
+};
 inline size_t quant_zero_bytes(int num_seqs, int n_heads_kv, int head_dim) {
   const size_t n = static_cast<size_t>(num_seqs) * n_heads_kv;
-  return n * head_dim * sizeof(long long) + n * sizeof(unsigned int);
+  return n * head_dim * (sizeof(long long) + sizeof(unsigned int)) + n * sizeof(unsigned int);
 }
 inline size_t quant_scratch_bytes(int num_seqs, int n_heads_kv, int head_dim) {
   const size_t n = static_cast<size_t>(num_seqs) * n_heads_kv;
-  return (quant_zero_bytes(num_seqs, n_heads_kv, head_dim) + 15) / 16 * 16 + n * head_dim * sizeof(float);
+  return (quant_zero_bytes(num_seqs, n_heads_kv, head_dim) + 15) / 16 * 16 + 2 * n * head_dim * sizeof(float);
 }
-// The three scratch arrays inside a quant_scratch_bytes region.
-inline void quant_scratch_split(void* base, int num_seqs, int n_heads_kv, int head_dim, long long** k_sum,
-                                unsigned int** k_cnt, float** k_mean) {
-  const size_t n = static_cast<size_t>(num_seqs) * n_heads_kv;
+inline QuantScratch quant_scratch_split(void* base, int num_seqs, int n_heads_kv, int head_dim) {
+  const size_t n = static_cast<size_t>(num_seqs) * n_heads_kv, nd = n * head_dim;
   uint8_t* b = static_cast<uint8_t*>(base);
-  *k_sum = reinterpret_cast<long long*>(b);
-  *k_cnt = reinterpret_cast<unsigned int*>(b + n * head_dim * sizeof(long long));
-  *k_mean = reinterpret_cast<float*>(b + (quant_zero_bytes(num_seqs, n_heads_kv, head_dim) + 15) / 16 * 16);
+  QuantScratch q;
+  q.k_sum = reinterpret_cast<long long*>(b);
+  q.v_amax = reinterpret_cast<unsigned int*>(b + nd * sizeof(long long));
+  q.k_cnt = q.v_amax + nd;
+  q.k_mean = reinterpret_cast<float*>(b + (quant_zero_bytes(num_seqs, n_heads_kv, head_dim) + 15) / 16 * 16);
+  q.v_inv = q.k_mean + nd;
+  return q;
 }
 
 struct QuantParams {
@@ -114,15 +126,15 @@ struct QuantParams {
   const __nv_bfloat16* kv_pool;
   const int32_t* block_table;
   const int4* seq_info;
-  uint8_t* q8;
+  uint8_t* q8;       // nullptr: no Q codes
   float* q_scale;
-  uint8_t* k8;
+  uint8_t* k8;       // nullptr: no K codes
   float* k_scale;
-  long long* k_sum;
-  unsigned int* k_cnt;
-  float* k_mean;
+  uint8_t* v8;       // nullptr: no V codes (nor V maxima)
+  float* v_scale;
+  QuantScratch sc;
   int num_seqs, total_q, n_heads_q, n_heads_kv, head_dim, bt_stride, num_pages;
-  int nb_max;  // 64-key blocks per sequence in k8: ceil(max_kv / 64)
+  int nb_max;  // 64-key blocks per sequence in k8 (even): 2 * ceil(max_kv / 128)
 };
 
 struct AttnParams {
@@ -146,6 +158,8 @@ struct AttnParams {
   const float* q_scale;
   const float* k_scale;
   int nb_max;
+  // fp8 P.V variant: per-channel V scales [num_seqs][n_heads_kv][head_dim]
+  const float* v_scale;
 };
 
 
@@ -177,13 +191,18 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_kv_write(const KvWriteParams& p, int sms, cudaStream_t s);
-cudaError_t launch_quant_qk(const QuantParams& p, int sms, cudaStream_t s);
+// Key sums and V maxima, then the K, V and Q codes that QuantParams asks for.
+cudaError_t launch_quant(const QuantParams& p, int sms, cudaStream_t s);
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                              int head_dim, int grid, cudaStream_t s, bool dependent);
 // Quantised-QK prefill (head_dim 128): tq8 over the e4m3 Q codes, tk8 over the
 // e4m3 K blocks, tkv over the bf16 cache (V).
 cudaError_t launch_attention_fp8(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
                                  const CUtensorMap& tkv, int grid, cudaStream_t s, bool dependent);
+// fp8 P.V prefill (head_dim 128): as above, with tv8 over the transposed e4m3
+// V tiles [tiles][n_heads_kv][128 channels][128 keys] in place of the bf16 V.
+cudaError_t launch_attention_fp8pv(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
+                                   const CUtensorMap& tv8, int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                           int head_dim, int grid, cudaStream_t s, bool dependent);

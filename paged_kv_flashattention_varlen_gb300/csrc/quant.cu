@@ -17,6 +17,11 @@
 //     when amax = 0), code = e4m3 round-to-nearest-even of x * inv, saturated.
 //     Rows past L are zero codes.
 //   * q_quant_kernel: per query row (token, head): scale and codes as above.
+//   * V (fp8 P.V variant): k_sum_kernel also takes max |v| per (sequence, KV
+//     head, channel), and its last CTA writes scale = amax / 448 and
+//     inv = 448 / amax; v_quant_kernel writes code = e4m3(v * inv) per 128-key
+//     tile and head, transposed through shared memory to [channel][key] (the
+//     K-major B operand of the P.V MMA), with zero codes past the sequence end.
 //
 // Every rounding decision is taken in the precision the oracle uses, so codes
 // and scales agree with it bit for bit. The kernels run after the plan (they
@@ -75,27 +80,38 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-// Pointer to key row j of sequence b, KV head hk (nullptr if its page is not
-// a pool page; the plan has then rejected the sequence already).
-__device__ __forceinline__ const __nv_bfloat16* key_row(const QuantParams& p, int b, int4 si, int j, int hk) {
+// Pointer to the K (plane 0) or V (plane 1) row j of sequence b, KV head hk
+// (nullptr if its page is not a pool page; the plan has then rejected the
+// sequence already). A contiguous cache holds num_pages rows per plane.
+__device__ __forceinline__ const __nv_bfloat16* kv_row(const QuantParams& p, int b, int4 si, int j, int hk,
+                                                       int plane) {
   const size_t row = static_cast<size_t>(p.n_heads_kv) * p.head_dim;
   if (p.block_table) {
     const int page = p.block_table[static_cast<size_t>(b) * p.bt_stride + j / kPage];
     if (page < 0 || page >= p.num_pages) return nullptr;
-    return p.kv_pool + (static_cast<size_t>(page) * 2 * kPage + (j % kPage)) * row + static_cast<size_t>(hk) * p.head_dim;
+    return p.kv_pool + ((static_cast<size_t>(page) * 2 + plane) * kPage + (j % kPage)) * row +
+           static_cast<size_t>(hk) * p.head_dim;
   }
-  return p.kv_pool + (static_cast<size_t>(si.w) + j) * row + static_cast<size_t>(hk) * p.head_dim;
+  return p.kv_pool + (static_cast<size_t>(plane) * p.num_pages + si.w + j) * row +
+         static_cast<size_t>(hk) * p.head_dim;
+}
+__device__ __forceinline__ const __nv_bfloat16* key_row(const QuantParams& p, int b, int4 si, int j, int hk) {
+  return kv_row(p, b, si, j, hk, 0);
 }
 
 // grid (num_seqs * n_heads_kv, key chunks of kSumKeys), 256 threads: thread t
 // adds channels 8 (t % 16) ... + 7 of keys j0 + t / 16, + 16, ... (16-byte
-// loads, four keys of a lane in flight); the 16 key lanes are then summed in
-// shared memory and the CTA adds its 128 partial sums with int64 atomics. The
-// last CTA of a (sequence, KV head) writes the 128 offsets.
+// loads, four keys of a lane in flight) and, when V codes are wanted, takes
+// the max |v| of the same rows; the 16 key lanes are then combined in shared
+// memory and the CTA adds its 128 partial sums with int64 atomics (and its
+// maxima with uint32 atomic max on the fp32 bits, which order like the values
+// for non-negative floats). The last CTA of a (sequence, KV head) writes the
+// 128 K offsets and V scales.
 __global__ void __launch_bounds__(256) k_sum_kernel(const QuantParams p) {
   grid_dep_launch();
   grid_dep_wait();  // the plan is complete
   __shared__ long long s_part[16][128];
+  __shared__ float s_vmax[16][128];
   __shared__ int s_last;
   const int b = blockIdx.x / p.n_heads_kv, hk = blockIdx.x % p.n_heads_kv;
   const int4 si = p.seq_info[b];
@@ -103,17 +119,26 @@ __global__ void __launch_bounds__(256) k_sum_kernel(const QuantParams p) {
   const int L = si.z;
   const int j0 = blockIdx.y * kSumKeys, j1 = min(L, j0 + kSumKeys);
   if (j0 >= j1) return;
+  const bool want_v = p.v8 != nullptr;
   const int cg = threadIdx.x & 15, kl = threadIdx.x >> 4;
   int hi[8], lo[8];
+  float vmax[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) hi[e] = lo[e] = 0;
+  for (int e = 0; e < 8; ++e) {
+    hi[e] = lo[e] = 0;
+    vmax[e] = 0.f;
+  }
   for (int jb = j0; jb < j1; jb += 64) {
-    uint4 raw[4];
+    uint4 raw[4], rv[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int j = jb + u * 16 + kl;
       const __nv_bfloat16* r = j < j1 ? key_row(p, b, si, j, hk) : nullptr;
       raw[u] = r ? *reinterpret_cast<const uint4*>(r + cg * 8) : make_uint4(0, 0, 0, 0);
+      if (want_v) {
+        const __nv_bfloat16* rv_ptr = j < j1 ? kv_row(p, b, si, j, hk, 1) : nullptr;
+        rv[u] = rv_ptr ? *reinterpret_cast<const uint4*>(rv_ptr + cg * 8) : make_uint4(0, 0, 0, 0);
+      }
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -121,33 +146,51 @@ __global__ void __launch_bounds__(256) k_sum_kernel(const QuantParams p) {
       add_units(raw[u].y, hi[2], lo[2], hi[3], lo[3]);
       add_units(raw[u].z, hi[4], lo[4], hi[5], lo[5]);
       add_units(raw[u].w, hi[6], lo[6], hi[7], lo[7]);
+      if (want_v) {
+        const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&rv[u]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vmax[e] = fmaxf(vmax[e], fabsf(__bfloat162float(h[e])));
+      }
     }
   }
   // |hi| <= 16 * 2^21 and |lo| <= 16 * 2^20 per lane: no int32 overflow
 #pragma unroll
-  for (int e = 0; e < 8; ++e) s_part[kl][cg * 8 + e] = static_cast<long long>(hi[e]) * (1ll << 21) + lo[e];
+  for (int e = 0; e < 8; ++e) {
+    s_part[kl][cg * 8 + e] = static_cast<long long>(hi[e]) * (1ll << 21) + lo[e];
+    s_vmax[kl][cg * 8 + e] = vmax[e];
+  }
   __syncthreads();
   const size_t base = (static_cast<size_t>(b) * p.n_heads_kv + hk) * p.head_dim;
   if (threadIdx.x < 128) {
     long long t = 0;
+    float vm = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) t += s_part[k][threadIdx.x];
-    atomicAdd(reinterpret_cast<unsigned long long*>(p.k_sum + base + threadIdx.x),
+    for (int k = 0; k < 16; ++k) {
+      t += s_part[k][threadIdx.x];
+      vm = fmaxf(vm, s_vmax[k][threadIdx.x]);
+    }
+    atomicAdd(reinterpret_cast<unsigned long long*>(p.sc.k_sum + base + threadIdx.x),
               static_cast<unsigned long long>(t));
+    if (want_v) atomicMax(p.sc.v_amax + base + threadIdx.x, __float_as_uint(vm));
     __threadfence();
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned chunks = static_cast<unsigned>((L + kSumKeys - 1) / kSumKeys);
-    s_last = atomicAdd(p.k_cnt + static_cast<size_t>(b) * p.n_heads_kv + hk, 1u) == chunks - 1;
+    s_last = atomicAdd(p.sc.k_cnt + static_cast<size_t>(b) * p.n_heads_kv + hk, 1u) == chunks - 1;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   if (threadIdx.x < 128) {
-    const long long sum = __ldcg(p.k_sum + base + threadIdx.x);
-    p.k_mean[base + threadIdx.x] =
+    const long long sum = __ldcg(p.sc.k_sum + base + threadIdx.x);
+    p.sc.k_mean[base + threadIdx.x] =
         __double2float_rn(static_cast<double>(sum) * (1.0 / 4294967296.0) / static_cast<double>(L));
+    if (want_v) {
+      const float amax = __uint_as_float(__ldcg(p.sc.v_amax + base + threadIdx.x));
+      p.v_scale[base + threadIdx.x] = e4m3_scale(amax);
+      p.sc.v_inv[base + threadIdx.x] = e4m3_inv_scale(amax);
+    }
   }
 }
 
@@ -165,7 +208,7 @@ __global__ void __launch_bounds__(256) k_quant_kernel(const QuantParams p) {
   const int L = si.z;
   if (blk * kPage >= L) return;
   if (threadIdx.x < 128)
-    s_mean[threadIdx.x] = p.k_mean[(static_cast<size_t>(b) * p.n_heads_kv + hk) * p.head_dim + threadIdx.x];
+    s_mean[threadIdx.x] = p.sc.k_mean[(static_cast<size_t>(b) * p.n_heads_kv + hk) * p.head_dim + threadIdx.x];
   const int r = threadIdx.x >> 2, c0 = (threadIdx.x & 3) * 32;
   const int j = blk * kPage + r;
   const __nv_bfloat16* kr = j < L ? key_row(p, b, si, j, hk) : nullptr;
@@ -206,6 +249,51 @@ __global__ void __launch_bounds__(256) k_quant_kernel(const QuantParams p) {
   dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
   dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   if (threadIdx.x == 0) p.k_scale[gblk * p.n_heads_kv + hk] = e4m3_scale(amax);
+}
+
+// grid (num_seqs * n_heads_kv, 128-key tiles per sequence), 256 threads:
+// thread t codes keys 8 (t % 16) ... + 7 of the tile at channels 8 (t / 16) ...
+// + 7, packs the eight codes of each channel into 8 bytes of the transposed
+// tile in shared memory ([channel][key]: 16 lanes fill one 128-byte channel
+// row), and the CTA then writes the 16 KB tile out with 16-byte stores.
+__global__ void __launch_bounds__(256) v_quant_kernel(const QuantParams p) {
+  grid_dep_launch();
+  grid_dep_wait();  // the V scales are complete
+  __shared__ __align__(16) uint8_t s_t[128 * 128];
+  const int b = blockIdx.x / p.n_heads_kv, hk = blockIdx.x % p.n_heads_kv;
+  const int tile = blockIdx.y;
+  const int4 si = p.seq_info[b];
+  if (si.y < 0) return;
+  const int L = si.z;
+  if (tile * 128 >= L) return;
+  const int kg = threadIdx.x & 15, cg = threadIdx.x >> 4;
+  const size_t base = (static_cast<size_t>(b) * p.n_heads_kv + hk) * p.head_dim + cg * 8;
+  const float4 i0 = *reinterpret_cast<const float4*>(p.sc.v_inv + base);
+  const float4 i1 = *reinterpret_cast<const float4*>(p.sc.v_inv + base + 4);
+  const float inv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+  uint4 raw[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int j = tile * 128 + kg * 8 + u;
+    const __nv_bfloat16* r = j < L ? kv_row(p, b, si, j, hk, 1) : nullptr;
+    raw[u] = r ? *reinterpret_cast<const uint4*>(r + cg * 8) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      x[u] = __fmul_rn(__bfloat162float(reinterpret_cast<const __nv_bfloat16*>(&raw[u])[e]), inv[e]);
+    const uint32_t w0 = e4m3x2(x[0], x[1]) | (e4m3x2(x[2], x[3]) << 16);
+    const uint32_t w1 = e4m3x2(x[4], x[5]) | (e4m3x2(x[6], x[7]) << 16);
+    *reinterpret_cast<uint2*>(s_t + (cg * 8 + e) * 128 + kg * 8) = make_uint2(w0, w1);
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(
+      p.v8 + ((static_cast<size_t>(b) * (p.nb_max / 2) + tile) * p.n_heads_kv + hk) * (128 * 128));
+  const uint4* src = reinterpret_cast<const uint4*>(s_t);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[threadIdx.x + i * 256] = src[threadIdx.x + i * 256];
 }
 
 // Query rows (token, head): eight lanes per row (lane holds 16 channels, two
@@ -258,15 +346,19 @@ __global__ void __launch_bounds__(256) q_quant_kernel(const QuantParams p) {
 
 }  // namespace
 
-// After the plan (key sums and counters zeroed before it, in stream order): key
-// sums and offsets, K codes, Q codes, each a dependent launch.
-cudaError_t launch_quant_qk(const QuantParams& p, int sms, cudaStream_t s) {
+// After the plan (the zeroed part of the scratch cleared before it, in stream
+// order): key sums, offsets and V scales, then K codes, V codes and Q codes as
+// requested, each a dependent launch. The Q pass, when present, is last: its
+// completion covers the others.
+cudaError_t launch_quant(const QuantParams& p, int sms, cudaStream_t s) {
   cudaError_t e = launch_kernel(k_sum_kernel, dim3(p.num_seqs * p.n_heads_kv,
                                                    (p.nb_max * kPage + kSumKeys - 1) / kSumKeys),
                                 256, 0, s, true, p);
-  if (e != cudaSuccess) return e;
-  e = launch_kernel(k_quant_kernel, dim3(p.num_seqs * p.n_heads_kv, p.nb_max), 256, 0, s, true, p);
-  if (e != cudaSuccess) return e;
+  if (e == cudaSuccess && p.k8)
+    e = launch_kernel(k_quant_kernel, dim3(p.num_seqs * p.n_heads_kv, p.nb_max), 256, 0, s, true, p);
+  if (e == cudaSuccess && p.v8)
+    e = launch_kernel(v_quant_kernel, dim3(p.num_seqs * p.n_heads_kv, p.nb_max / 2), 256, 0, s, true, p);
+  if (e != cudaSuccess || !p.q8) return e;
   const size_t rows = static_cast<size_t>(p.total_q) * p.n_heads_q;
   const int blocks = static_cast<int>(std::min<size_t>((rows + 63) / 64, static_cast<size_t>(sms) * 8));
   return launch_kernel(q_quant_kernel, std::max(blocks, 1), 256, 0, s, true, p);
