@@ -182,11 +182,11 @@ size_t pattn_workspace_size_fp8qk(int num_seqs, int total_q, int max_q, int max_
  *   V: one scale per (sequence, KV head, channel), scale = amax / 448 over the
  *   sequence's keys, code = e4m3 of v * (448 / amax) as for Q and K, stored
  *   transposed (keys innermost) in zero-padded 128-key tiles. P: e4m3 of
- *   p * 2^5 with p taken against a running row max that trails the true one
- *   by at most 2^3, so no code saturates; the row sum is the fp32 sum of the
+ *   p * 2^2 with p taken against a running row max that the tile's codes never
+ *   exceed 2^8 under, so no code saturates; the row sum is the fp32 sum of the
  *   unrounded p. The output is the attention over the dequantised Q, K and V
  *   up to the rounding of P: per element at most
- *   (2^-4 sum_j p_j |v_j| + 2^-15 sum_j |v_j|) / sum_j p_j
+ *   (2^-4 sum_j p_j |v_j| + 2^-12 sum_j |v_j|) / sum_j p_j
  *   (p relative to the row max, v the dequantised V) plus the bf16 rounding of
  *   the output. Units of at most 16 packed query rows take the bf16 decode kernel.
  */

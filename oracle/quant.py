@@ -231,8 +231,8 @@ def torch_index(idx):
 # 128 keys padded with zero codes: [tile][KV head][channel][128 keys].
 
 V_TILE = 128
-P_SCALE_LOG2 = 5       # P is coded as e4m3 of p * 2^5
-P_SLACK_LOG2 = 3       # the running max may trail the tile max by up to 2^3
+P_SCALE_LOG2 = 2       # P is coded as e4m3 of p * 2^2
+P_SLACK_LOG2 = 6       # codes stay at most 2^(2 + 6): the running max may trail by up to 2^6
 
 
 def logical_v(kv_pool, block_table, seq_lens, b: int, page_size: int = 64, start: int = 0):
@@ -271,9 +271,10 @@ def attention_fp8(wl, rows=None):
 
     ``out`` is softmax(scale * q^ . k^) v^ with the exact softmax. The method
     also rounds each probability to e4m3: with p relative to the row max,
-    the coded value p * 2^(5 + d), 0 <= d <= 3 (the trailing running max), is
-    within 2^-4 of it relatively or 2^-10 absolutely, so the output moves by at
-    most (2^-4 sum p |v^| + 2^-15 sum |v^|) / sum p; ``bound`` is that plus
+    the coded value p * 2^(2 + d), d >= 0 (a running max that trails the row
+    max; no code above 2^8, so none saturates), is within 2^-4 of it relatively
+    or 2^-10 absolutely, i.e. 2^-12 in units of p, so the output moves by at
+    most (2^-4 sum p |v^| + 2^-12 sum |v^|) / sum p; ``bound`` is that plus
     the bf16 rounding of the output (2^-8 |out|) and 1e-4 for fp32 sums and
     exp2 approximations.
     """
@@ -310,6 +311,7 @@ def attention_fp8(wl, rows=None):
                     w = np.exp(s - s.max())
                     o = (w @ vh[:nk]) / w.sum()
                     out[n, h] = o
-                    bound[n, h] = ((2.0 ** -4) * (w @ np.abs(vh[:nk])) + (2.0 ** -15) * np.abs(vh[:nk]).sum(0)) \
+                    bound[n, h] = ((2.0 ** -4) * (w @ np.abs(vh[:nk]))
+                                   + (2.0 ** -(10 + P_SCALE_LOG2)) * np.abs(vh[:nk]).sum(0)) \
                         / w.sum() + (2.0 ** -8) * np.abs(o) + 1e-4
     return out, bound

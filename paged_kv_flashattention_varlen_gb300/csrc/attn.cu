@@ -44,10 +44,10 @@
 // Quantised instances (head_dim 128): kF8 takes e4m3 Q and K codes for S (four
 // kind::f8f6f4 MMAs of K = 32) and scales each warpgroup's scores by the Q row
 // and K block scales. kF8V also codes P and V: the softmax computes the tile
-// max every tile (the running max may trail it by at most 2^3), writes e4m3 of
-// p * 2^5 (at most 2^8, inside the e4m3 range) into a shared-memory P buffer in
-// the 128-byte-swizzled K-major layout, and O += P V runs as kind::f8f6f4 MMAs
-// with both operands in shared memory (V as transposed e4m3 tiles); the
+// max only when needed (as for bf16 P, with its own limits), writes e4m3 of
+// p * 2^2 (at most 2^8, inside the e4m3 range) into TMEM over the S columns it has just
+// read (four codes per column), and O += P V runs as kind::f8f6f4 MMAs with P
+// from TMEM and V from shared memory as transposed e4m3 tiles (K-major); the
 // per-channel V scale is applied in the epilogue.
 //
 // At the end of an item the softmax warps divide by l and store bf16 rows, or
@@ -70,24 +70,22 @@ struct Cfg {
   static constexpr int kQBytes = kBM * D * kQKElem;
   static constexpr int kKStage = BN * D * kQKElem;
   static constexpr int kVStage = BN * D * (kF8V ? 1 : 2);
-  static constexpr int kPSmem = kF8V ? kBM * BN : 0;   // one e4m3 P buffer in shared memory
   static constexpr int kQKBlocks = D * kQKElem / 128;  // 128-byte swizzle columns of a Q / K row
   static constexpr int kQKBlockElems = 128 / kQKElem;
   static constexpr int kQKSteps = D * kQKElem / 32;    // MMAs of one QK (32 bytes of K each)
   static constexpr bool kSplitO = D == 128;          // one O per softmax warpgroup
-  static constexpr bool kAliasP = D == 128 && !kF8V;  // P over its S buffer
+  static constexpr bool kAliasP = D == 128;          // P over its S buffer
   static constexpr int kSBufs = 2;
   static constexpr int kPBufs = kAliasP ? kSBufs : 2;
   static constexpr int kPVBars = kAliasP ? kSBufs : 2;  // pv_done barriers, by tile index
   static constexpr int kQBufs = D == 128 ? 2 : 1;    // D = 128: the next item's Q lands early
-  static constexpr int kKStages = 2;
-  static constexpr int kVStages = 2;
+  static constexpr int kKStages = kF8V ? 3 : 2;       // e4m3 tiles are half as large
+  static constexpr int kVStages = kF8V ? 3 : 2;
   // shared memory
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBufs * kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKStage;
-  static constexpr int kOffP = kOffV + kVStages * kVStage;  // kF8V: P buffers
-  static constexpr int kOffX = kOffP + kPBufs * kPSmem;     // row sum / max / l exchange
+  static constexpr int kOffX = kOffV + kVStages * kVStage;  // row sum / max / l exchange
   static constexpr int kXBytes = (2 * 2 + 2 * 2 + 2) * kBM * 4;
   static constexpr int kOffBar = kOffX + kXBytes;
   static constexpr int kBarBytes = 512;
@@ -101,14 +99,20 @@ struct Cfg {
   // TMEM column of P buffer b for keys [16 kk, 16 kk + 16): over its own S
   // buffer (each warpgroup's half at the start of the half it read), or in a P
   // buffer.
+  // kF8V: e4m3 P, keys [32 kk, 32 kk + 32) in 8 columns over S the same way.
   __device__ static constexpr int p_col(int b, int kk) {
-    return kAliasP ? kColS + b * BN + (kk / (BN / 32)) * (BN / 2) + (kk % (BN / 32)) * 8
-                   : kColP + b * kPCols + kk * 8;
+    return kF8V ? kColS + b * BN + (kk / (BN / 64)) * (BN / 2) + (kk % (BN / 64)) * 8
+           : kAliasP ? kColS + b * BN + (kk / (BN / 32)) * (BN / 2) + (kk % (BN / 32)) * 8
+                     : kColP + b * kPCols + kk * 8;
   }
   static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns of a V row
   static constexpr int kPagesPerTile = BN / kPage;
   static_assert(kColS + kSBufs * BN + ((kAliasP || kF8V) ? 0 : kPBufs * kPCols) <= kTmemCols, "TMEM budget");
   static_assert(kSBufs <= 3 && kPBufs <= 3 && kPVBars <= 3 && kQBufs <= 2, "barrier slots");
+  static_assert(kKStages <= 3 && kVStages <= 3, "ring barrier slots");
+  // bf16 V stages are released through the pv_done barrier of their tile, e4m3
+  // ones through their own empty barriers
+  static_assert(kF8V || kVStages <= kPVBars, "V stage release");
   static_assert((kSplitO ? 2 * D : D) <= kColS, "O columns");
   static_assert(BN % kPage == 0 && BN % 32 == 0, "tile");
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -116,8 +120,8 @@ struct Cfg {
 
 // mbarrier slots
 enum Bar {
-  kQFull0 = 0, kQFull1, kQEmpty0, kQEmpty1, kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1,
-  kSFull0, kSFull1, kSFull2, kSFree0, kSFree1, kSFree2, kPFull0, kPFull1, kPFull2, kPVDone0,
+  kQFull0 = 0, kQFull1, kQEmpty0, kQEmpty1, kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2,
+  kVFull0, kVFull1, kVFull2, kVEmpty0, kVEmpty1, kVEmpty2, kSFull0, kSFull1, kSFull2, kSFree0, kSFree1, kSFree2, kPFull0, kPFull1, kPFull2, kPVDone0,
   kPVDone1, kPVDone2, kDrain, kDrainPV, kPairA0, kPairA1, kPairA2, kPairA3, kPairB0, kPairB1,
   kPairB2, kPairB3, kXSum, kNumBars
 };
@@ -175,7 +179,7 @@ __device__ __forceinline__ float exp_row(const uint32_t (&sr)[KH / 32][32], floa
 }
 
 // The same for the fp8 P.V instance: p_i = 2^(S_i c - m_ref) with m_ref the
-// running max minus 5 (p scaled by 2^5), as e4m3 codes, four per word in key
+// running max minus 2 (p scaled by 2^2), as e4m3 codes, four per word in key
 // order, returning the fp32 sum of the unrounded p_i.
 template <int KH, bool kMasked>
 __device__ __forceinline__ float exp_row_f8(const uint32_t (&sr)[KH / 32][32], float c, float m_ref,
@@ -193,8 +197,8 @@ __device__ __forceinline__ float exp_row_f8(const uint32_t (&sr)[KH / 32][32], f
 #pragma unroll
       for (int hv = 0; hv < 2; ++hv) {
         const int k = i + 2 * hv;
-        const float2 x =
-            __ffma2_rn(make_float2(__uint_as_float(sr[j][k]), __uint_as_float(sr[j][k + 1])), c2, nm2);
+        const float s0 = __uint_as_float(sr[j][k]), s1 = __uint_as_float(sr[j][k + 1]);
+        const float2 x = __ffma2_rn(make_float2(s0, s1), c2, nm2);
         float p0 = ex2(x.x);
         float p1 = ex2(x.y);
         if constexpr (kMasked) {
@@ -241,7 +245,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   const uint32_t sQ = s_base + C::kOffQ;
   const uint32_t sK = s_base + C::kOffK;
   const uint32_t sV = s_base + C::kOffV;
-  const uint32_t sP = s_base + C::kOffP;
   const uint32_t sBar = s_base + C::kOffBar;
   uint8_t* misc = smem + C::kOffMisc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
@@ -260,11 +263,12 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kQFull0 + b), 1);
       mbar_init(bar(kQEmpty0 + b), 1);  // the item's last QK MMA releases the buffer
+    }
+    for (int b = 0; b < 3; ++b) {
       mbar_init(bar(kKFull0 + b), 1);
       mbar_init(bar(kKEmpty0 + b), 1);
       mbar_init(bar(kVFull0 + b), 1);
-    }
-    for (int b = 0; b < 3; ++b) {
+      mbar_init(bar(kVEmpty0 + b), 1);
       mbar_init(bar(kSFull0 + b), 1);
       mbar_init(bar(kSFree0 + b), kSoftmaxWarps);
       mbar_init(bar(kPFull0 + b), kSoftmaxWarps);  // both key halves of P written
@@ -361,6 +365,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             const uint32_t st = n % stages;
             if (kind == 0) {
               ok = wait_one(bar(kKEmpty0 + st), ((n / stages) & 1u) ^ 1u, ctl);
+            } else if (kF8V) {
+              ok = wait_one(bar(kVEmpty0 + st), ((n / stages) & 1u) ^ 1u, ctl);
             } else if (n >= stages) {
               // a V stage is free once the PV of the tile it held is done
               ok = wait_one(pv_bar(n - stages), pv_par(n - stages), ctl);
@@ -474,7 +480,6 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     constexpr uint32_t idesc_pv = kF8V ? idesc_e4m3_f32(kBM, D) : idesc_bf16_f32(kBM, D, false, true);
     // bf16 V: MN-major; e4m3 V: K-major transposed tiles, like the P buffers
     const SmemDesc dv = kF8V ? sw128_desc_split(sV, 16, 1024) : sw128_desc_split(sV, BN * 128, 1024);
-    const SmemDesc dp = sw128_desc_split(sP, 16, 1024);
     const unsigned fullmask = 0xffffffffu;
     uint32_t n = 0;
     bool ok = true;
@@ -511,13 +516,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
             const uint32_t v_lo = desc_lo_at(dv, s * C::kVStage);
             if constexpr (kF8V) {
               // 32 keys (bytes) per MMA; key half hh into its own O
-              const uint32_t p_lo = desc_lo_at(dp, pb * C::kPSmem);
 #pragma unroll
               for (int kk = 0; kk < BN / 32; ++kk) {
                 const int hh = kk / (BN / 64);
-                umma_f8_ss(tmem + C::kColO + hh * D, p_lo + ((kk * 32) >> 4), dp.hi, v_lo + ((kk * 32) >> 4),
-                           dv.hi, idesc_pv, (first && kk == hh * (BN / 64)) ? 0u : 1u);
+                umma_f8_ts(tmem + C::kColO + hh * D, tmem + C::p_col(static_cast<int>(pb), kk),
+                           v_lo + ((kk * 32) >> 4), dv.hi, idesc_pv, (first && kk == hh * (BN / 64)) ? 0u : 1u);
               }
+              umma_commit(bar(kVEmpty0 + s));
             }
 #pragma unroll
             for (int kk = 0; kk < (kF8V ? 0 : BN / 16); ++kk) {
@@ -621,62 +626,63 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         const int nv = lim - key0;  // visible keys of this row in the chunk (any sign)
         uint32_t pk[KH / 2];
         if constexpr (kF8V) {
-          // e4m3 P: the tile max first, every tile. The running max is kept
-          // while the tile max exceeds it by at most 3 (log2 units), so that
-          // every p * 2^5 stays at most 2^8; otherwise O is rescaled first.
+          // e4m3 of p * 2^2 against the running max first. A tile sum of at
+          // most 2^8 bounds every code by 2^8 (inside the e4m3 range): then the
+          // running max is kept. Otherwise (and on an item's first tile) the tile
+          // max decides: O is rescaled if the max grew by more than 6 (log2
+          // units), which again bounds every code by 2^(6 + 2), and P is recomputed.
           uint32_t pk8[KH / 4];
           if (warp_live) {
-            const float mx = full_tile ? max_row<KH, false>(sr, KH) : max_row<KH, true>(sr, nv);
-            const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * ct;
-            const float m_new = fmaxf(m_used, mx_s);
-            if (first) {
-              m_used = m_new;
-            } else {
-              const bool need = m_new > m_used + 3.0f;
-              if (__any_sync(0xffffffffu, need)) {
-                const uint32_t pm = n - 1;
-                if (!(ok = wait_warp(pv_bar(pm), pv_par(pm), ctl))) break;
-                tc_fence_after();
-                const float alpha = need ? ex2(m_used - m_new) : 1.0f;
-                if (need) {
-                  l *= alpha;
-                  m_used = m_new;
-                }
+            const float kSumLimit = 256.0f;
+            float lt = 0.f;
+            bool exact = first || m_used == -INFINITY;
+            if (!exact) {
+              lt = full_tile ? exp_row_f8<KH, false>(sr, ct, m_used - 2.0f, KH, pk8)
+                             : exp_row_f8<KH, true>(sr, ct, m_used - 2.0f, nv, pk8);
+              exact = !(lt <= kSumLimit);  // also true for inf / NaN
+            }
+            if (__any_sync(0xffffffffu, exact)) {
+              const float mx = full_tile ? max_row<KH, false>(sr, KH) : max_row<KH, true>(sr, nv);
+              const float mx_s = (mx == -INFINITY) ? -INFINITY : mx * ct;
+              const float m_new = fmaxf(m_used, mx_s);
+              if (first) {
+                m_used = m_new;
+              } else {
+                const bool need = m_new > m_used + 6.0f;
+                if (__any_sync(0xffffffffu, need)) {
+                  const uint32_t pm = n - 1;
+                  if (!(ok = wait_warp(pv_bar(pm), pv_par(pm), ctl))) break;
+                  tc_fence_after();
+                  const float alpha = need ? ex2(m_used - m_new) : 1.0f;
+                  if (need) {
+                    l *= alpha;
+                    m_used = m_new;
+                  }
 #pragma unroll 1
-                for (int j = 0; j < D / 32; ++j) {
-                  uint32_t o[32];
-                  tmem_ld32(o_own + j * 32, o);
-                  tmem_wait_ld();
-                  reg_fence(o);
+                  for (int j = 0; j < D / 32; ++j) {
+                    uint32_t o[32];
+                    tmem_ld32(o_own + j * 32, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
 #pragma unroll
-                  for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                  tmem_st32(o_own + j * 32, o);
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(o_own + j * 32, o);
+                  }
+                  tmem_wait_st();
                 }
-                tmem_wait_st();
               }
+              const float m_ref = ((m_used == -INFINITY) ? 0.f : m_used) - 2.0f;
+              lt = full_tile ? exp_row_f8<KH, false>(sr, ct, m_ref, KH, pk8)
+                             : exp_row_f8<KH, true>(sr, ct, m_ref, nv, pk8);
             }
-            const float m_ref = ((m_used == -INFINITY) ? 0.f : m_used) - 5.0f;
-            l += full_tile ? exp_row_f8<KH, false>(sr, ct, m_ref, KH, pk8)
-                           : exp_row_f8<KH, true>(sr, ct, m_ref, nv, pk8);
+            l += lt;
           }
-          // P buffer pb was last read by the PV of tile n - kPBufs
-          if (n >= static_cast<uint32_t>(C::kPBufs)) {
-            const uint32_t pm = n - C::kPBufs;
-            if (!(ok = wait_warp(pv_bar(pm), pv_par(pm), ctl))) break;
-          }
+          // P over the S columns this warp has just read (nothing to wait for)
           if (warp_live) {
-            // row r, keys [h KH, h KH + KH): 16-byte chunks 4h ... 4h + 3 of the
-            // 128-byte row, placed by the 128-byte swizzle (chunk ^ row % 8)
-            uint8_t* prow = smem + C::kOffP + pb * C::kPSmem + r * 128;
-#pragma unroll
-            for (int i = 0; i < KH / 16; ++i) {
-              const int chunk = (h * (KH / 16) + i) ^ (r & 7);
-              *reinterpret_cast<uint4*>(prow + chunk * 16) =
-                  make_uint4(pk8[4 * i], pk8[4 * i + 1], pk8[4 * i + 2], pk8[4 * i + 3]);
-            }
-            fence_proxy_async_smem();
+            tmem_st_cols<KH / 4>(tmem + lane_base + C::p_col(static_cast<int>(pb), h * (BN / 64)), pk8);
+            tmem_wait_st();
           }
-          tc_fence_before();  // an O rescale above precedes the next PV
+          tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kPFull0 + pb));
           continue;
@@ -796,7 +802,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(o0[i]) * c0 + __uint_as_float(o1[i]) * c1;
           if constexpr (kF8V) {
-            // per-channel V scale (P's 2^5 cancels against l)
+            // per-channel V scale (P's 2^2 cancels against l)
             const float4* vs = reinterpret_cast<const float4*>(
                 p.v_scale + (static_cast<size_t>(it.b) * p.n_heads_kv + it.hk) * D + col);
 #pragma unroll

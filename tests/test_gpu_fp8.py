@@ -75,7 +75,7 @@ def test_attention_within_the_probability_rounding_bound(name):
 
 def test_equal_keys_give_the_exact_mean_of_the_values():
     # every key of a head equal: smoothed K is zero, every score 0 and every
-    # p * 2^5 = 32 exact in e4m3, so the output is the mean of the dequantised V
+    # p * 2^2 = 4 exact in e4m3, so the output is the mean of the dequantised V
     # rows up to fp32 sums and the bf16 output
     wl = workloads.make_paged("eqk", 62, [40, 300, 7], [300, 700, 129], 16, 4, 128, causal=True,
                               extra_pages=3)
