@@ -36,7 +36,9 @@ PREFILL = 3
 NOMINAL_HBM_GBS = 7900.0
 NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["attn.cu", "decode.cu", "ptx.cuh", "kernels.cuh", "merge.cuh"]
+# the sources each profiled kernel is compiled from (its ncu summary names their hash)
+KERNEL_SOURCES = {"decode": ["decode.cu", "merge.cuh", "ptx.cuh", "kernels.cuh"],
+                  "prefill": ["attn.cu", "ptx.cuh", "kernels.cuh"]}
 
 
 def parse():
@@ -73,9 +75,9 @@ def peaks():
         return dict(FALLBACK), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kind: str) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "paged_kv_flashattention_varlen_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -91,7 +93,7 @@ def ncu_traffic(kind: str):
         return None
     src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     val = re.search(r"traffic_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
-    if not src or not val or src.group(1) != kernel_source_hash():
+    if not src or not val or src.group(1) != kernel_source_hash(kind):
         return None
     return float(val.group(1))
 
