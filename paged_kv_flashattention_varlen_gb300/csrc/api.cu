@@ -52,6 +52,7 @@ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 struct Shape {
   int group, tokens_per_tile, block_n;
+  bool pair;  // head_dim 256 prefill on CTA pairs (some sequence may have two q tiles)
 };
 
 pattn_status check_args(const void* out, const void* q, const void* kv, const int32_t* bt,
@@ -74,7 +75,8 @@ pattn_status check_args(const void* out, const void* q, const void* kv, const in
   if (g > kBM) return PATTN_ERR_UNSUPPORTED;
   sh->group = g;
   sh->tokens_per_tile = kBM / g;
-  sh->block_n = attention_block_n(d);
+  sh->pair = d == 256 && max_q > sh->tokens_per_tile;
+  sh->block_n = attention_block_n(d, sh->pair);
   // item encoding keeps q tiles and KV tiles in 16 bits
   if (cdiv(max_q, sh->tokens_per_tile) > 65535) return PATTN_ERR_UNSUPPORTED;
   if (cdiv(max_kv, sh->block_n) > 65535) return PATTN_ERR_UNSUPPORTED;
@@ -353,6 +355,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   pp.head_dim = d;
   pp.tokens_per_tile = T;
   pp.block_n = sh.block_n;
+  pp.pair = sh.pair ? 1 : 0;
   pp.bt_stride = std::max(1, cdiv(max_kv, kPage));
   pp.num_pages = num_pages;
   pp.causal = causal;
@@ -502,7 +505,8 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
         e = launch_attention_fp8(fp, tq8, tk8, tkv, st.sms, stream, dep);
       }
     } else {
-      e = launch_attention(ap, tq, tkv, d, st.sms, stream, dep);
+      e = sh.pair ? launch_attention_pair(ap, tq, tkv, st.sms, stream, dep)
+                  : launch_attention(ap, tq, tkv, d, st.sms, stream, dep);
     }
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }

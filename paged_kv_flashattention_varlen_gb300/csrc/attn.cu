@@ -61,20 +61,25 @@
 namespace pattn {
 namespace {
 
-template <int D, int BN, bool kF8 = false, bool kF8V = false>
+template <int D, int BN, bool kF8 = false, bool kF8V = false, bool kPair = false>
 struct Cfg {
   // kF8: Q and K as e4m3 codes (one byte), S = Q K^T with kind::f8f6f4 MMAs; V
-  // stays bf16 unless kF8V (P and V e4m3, P in shared memory).
+  // stays bf16 unless kF8V (P and V e4m3, P in TMEM).
+  // kPair: a CTA pair shares each tile's MMAs (cta_group::2): a CTA holds its
+  // own q tile, half of the K rows (one page) and half of the V columns.
   static_assert(!kF8V || (kF8 && D == 128 && BN == 128), "fp8 P.V: head_dim 128, 128-key tiles");
+  static_assert(!kPair || (D == 256 && BN == 128 && !kF8), "CTA pairs: head_dim 256, 128-key tiles, bf16");
   static constexpr int kQKElem = kF8 ? 1 : 2;          // bytes per Q / K element
   static constexpr int kQBytes = kBM * D * kQKElem;
-  static constexpr int kKStage = BN * D * kQKElem;
-  static constexpr int kVStage = BN * D * (kF8V ? 1 : 2);
+  static constexpr int kKRows = kPair ? BN / 2 : BN;   // K rows of a tile held by this CTA
+  static constexpr int kKStage = kKRows * D * kQKElem;
+  static constexpr int kVCols = kPair ? D / 2 : D;     // V columns of a tile held by this CTA
+  static constexpr int kVStage = BN * kVCols * (kF8V ? 1 : 2);
   static constexpr int kQKBlocks = D * kQKElem / 128;  // 128-byte swizzle columns of a Q / K row
   static constexpr int kQKBlockElems = 128 / kQKElem;
   static constexpr int kQKSteps = D * kQKElem / 32;    // MMAs of one QK (32 bytes of K each)
   static constexpr bool kSplitO = D == 128;          // one O per softmax warpgroup
-  static constexpr bool kAliasP = D == 128;          // P over its S buffer
+  static constexpr bool kAliasP = D == 128 || kPair;  // P over its S buffer
   static constexpr int kSBufs = 2;
   static constexpr int kPBufs = kAliasP ? kSBufs : 2;
   static constexpr int kPVBars = kAliasP ? kSBufs : 2;  // pv_done barriers, by tile index
@@ -105,7 +110,7 @@ struct Cfg {
            : kAliasP ? kColS + b * BN + (kk / (BN / 32)) * (BN / 2) + (kk % (BN / 32)) * 8
                      : kColP + b * kPCols + kk * 8;
   }
-  static constexpr int kDBlocks = D / 64;             // 128-byte swizzle columns of a V row
+  static constexpr int kDBlocks = kVCols / 64;        // 128-byte swizzle columns of this CTA's V rows
   static constexpr int kPagesPerTile = BN / kPage;
   static_assert(kColS + kSBufs * BN + ((kAliasP || kF8V) ? 0 : kPBufs * kPCols) <= kTmemCols, "TMEM budget");
   static_assert(kSBufs <= 3 && kPBufs <= 3 && kPVBars <= 3 && kQBufs <= 2, "barrier slots");
@@ -123,7 +128,9 @@ enum Bar {
   kQFull0 = 0, kQFull1, kQEmpty0, kQEmpty1, kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2,
   kVFull0, kVFull1, kVFull2, kVEmpty0, kVEmpty1, kVEmpty2, kSFull0, kSFull1, kSFull2, kSFree0, kSFree1, kSFree2, kPFull0, kPFull1, kPFull2, kPVDone0,
   kPVDone1, kPVDone2, kDrain, kDrainPV, kPairA0, kPairA1, kPairA2, kPairA3, kPairB0, kPairB1,
-  kPairB2, kPairB3, kXSum, kNumBars
+  kPairB2, kPairB3, kXSum,
+  // CTA pairs, in the rank-0 CTA: the peer's Q, K stage and V stage are ready
+  kPeerQ, kPeerK0, kPeerK1, kPeerK2, kPeerV0, kPeerV1, kPeerV2, kNumBars
 };
 static_assert(kNumBars * 8 <= 512, "mbarrier area");
 constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
@@ -232,12 +239,12 @@ __device__ __forceinline__ float max_row(const uint32_t (&sr)[KH / 32][32], int 
                fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
 }
 
-template <int D, int BN, bool kF8, bool kF8V>
+template <int D, int BN, bool kF8, bool kF8V, bool kPair>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
             const __grid_constant__ CUtensorMap tmap_k8, const __grid_constant__ CUtensorMap tmap_v8,
             const AttnParams p) {
-  using C = Cfg<D, BN, kF8, kF8V>;
+  using C = Cfg<D, BN, kF8, kF8V, kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -249,6 +256,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   uint8_t* misc = smem + C::kOffMisc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 16);
+  // CTA pairs: 16-byte source and destination of the peer's signalling copies
+  const uint32_t sig_src = smem_addr(misc + 32), sig_dst = smem_addr(misc + 48);
   auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
   // pv_done of tile m: barrier m % kPVBars, phase m / kPVBars
   auto pv_bar = [&](uint32_t m) { return bar(kPVDone0 + static_cast<int>(m % C::kPVBars)); };
@@ -257,6 +266,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtl ctl{abort_flag, p.err};
+  // CTA pairs walk the item list together (pair c = CTAs 2c, 2c + 1); the
+  // rank-0 CTA issues the MMAs of both
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
+  const int cid = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ncl = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -271,7 +285,11 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       mbar_init(bar(kVEmpty0 + b), 1);
       mbar_init(bar(kSFull0 + b), 1);
       mbar_init(bar(kSFree0 + b), kSoftmaxWarps);
-      mbar_init(bar(kPFull0 + b), kSoftmaxWarps);  // both key halves of P written
+      // both key halves of P written; in the rank-0 CTA of a pair also the
+      // PV thread's arrival that posts the peer's 16-byte signal
+      mbar_init(bar(kPFull0 + b), (kPair && rank == 0) ? kSoftmaxWarps + 1 : kSoftmaxWarps);
+      mbar_init(bar(kPeerK0 + b), 1);
+      mbar_init(bar(kPeerV0 + b), 1);
       mbar_init(bar(kPVDone0 + b), 1);             // also frees that tile's V stage
     }
     for (int b = 0; b < 4; ++b) {
@@ -281,6 +299,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kDrainPV), 1);
     mbar_init(bar(kXSum), kSoftmaxWarps);
+    mbar_init(bar(kPeerQ), 1);
     mbar_init_fence();
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_kv);
@@ -288,11 +307,17 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     if constexpr (kF8V) tma_prefetch_desc(&tmap_v8);
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   grid_dep_wait();    // the plan (and whatever ran before) is complete from here on
@@ -314,8 +339,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     uint32_t n = 0, itl = 0;
     bool ok = true;
     const uint64_t pol_q = l2_policy_evict_last();
-    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
-         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
+    for (int kq = 0, idx = cid; idx < n_items && ok;
+         idx = cta_item(++kq, cid, ncl), ++itl) {
       const Item it = decode_item(p.items[idx]);
       const int4 si = p.seq_info[it.b];
       const int q0 = si.x, L = si.z, kv0 = si.w;
@@ -328,7 +353,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           mbar_arrive_expect_tx(bar(kQFull0 + qb), static_cast<uint32_t>(C::kQKBlocks * 128 * G * T));
           for (int c = 0; c < C::kQKBlocks; ++c)
             tma_load_4d(sQ + qb * C::kQBytes + c * (kBM * 128), &tmap_q, bar(kQFull0 + qb),
-                        c * C::kQKBlockElems, 0, it.hk, q0 + it.qt * T, pol_q);
+                        c * C::kQKBlockElems, 0, it.hk, q0 + (it.qt + static_cast<int>(rank)) * T, pol_q);
         }
       }
       ok = __shfl_sync(fullmask, ok, 0);
@@ -371,7 +396,35 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
               // a V stage is free once the PV of the tile it held is done
               ok = wait_one(pv_bar(n - stages), pv_par(n - stages), ctl);
             }
-            if (ok && kF8V && kind == 1) {
+            if (ok && kPair && kind == 0) {
+              // this CTA's page of the tile: rank r holds keys [64 r, 64 r + 64)
+              const int pgk = rank ? a[C::kPagesPerTile - 1] : a[0];
+              mbar_arrive_expect_tx(bar(full + st), pgk >= 0 ? static_cast<uint32_t>((D / 64) * kPage * 128) : 0u);
+              if (pgk >= 0) {
+                for (int c = 0; c < D / 64; ++c) {
+                  const uint32_t dst = sK + st * C::kKStage + c * (kPage * 128);
+                  if (p.paged)
+                    tma_load_4d(dst, &tmap_kv, bar(full + st), c * 64, 0, it.hk, 2 * pgk, pol_kv);
+                  else
+                    tma_load_4d(dst, &tmap_kv, bar(full + st), c * 64, it.hk, pgk, 0, pol_kv);
+                }
+              }
+            } else if (ok && kPair) {
+              // this CTA's half of the V columns, both pages
+              mbar_arrive_expect_tx(bar(full + st), static_cast<uint32_t>(nload * C::kDBlocks * kPage * 128));
+#pragma unroll
+              for (int j = 0; j < C::kPagesPerTile; ++j) {
+                if (a[j] < 0) continue;
+                for (int c = 0; c < C::kDBlocks; ++c) {
+                  const int gc = static_cast<int>(rank) * C::kDBlocks + c;
+                  const uint32_t dst = sV + st * C::kVStage + c * (BN * 128) + j * (kPage * 128);
+                  if (p.paged)
+                    tma_load_4d(dst, &tmap_kv, bar(full + st), gc * 64, 0, it.hk, 2 * a[j] + 1, pol_kv);
+                  else
+                    tma_load_4d(dst, &tmap_kv, bar(full + st), gc * 64, it.hk, a[j], 1, pol_kv);
+                }
+              }
+            } else if (ok && kF8V && kind == 1) {
               // transposed e4m3 V: the whole 128-key tile of this head in one box
               // (zero codes past the sequence end)
               mbar_arrive_expect_tx(bar(full + st), static_cast<uint32_t>(C::kVStage));
@@ -426,21 +479,41 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     // S = Q K^T for every tile, issued by one thread. The PV MMAs come from warp 2:
     // the two streams touch disjoint TMEM (S / P, O) and feed the tensor pipe
     // independently, so that neither one's waits leave the pipe idle.
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = kF8 ? idesc_e4m3_f32(kBM, BN) : idesc_bf16_f32(kBM, BN, false, false);
+    if (kPair && rank != 0 && lane == 0) {
+      // the peer of a pair: forward "Q / K stage landed here" to the rank-0 CTA,
+      // whose thread issues the MMAs of both
+      uint32_t n = 0, itl = 0;
+      bool ok = true;
+      for (int kq = 0, idx = cid; idx < n_items && ok; idx = cta_item(++kq, cid, ncl), ++itl) {
+        const Item it = decode_item(p.items[idx]);
+        if (!(ok = wait_one(bar(kQFull0), itl & 1u, ctl))) break;
+        signal_remote_tx(sig_dst, sig_src, bar(kPeerQ), 0);
+        for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
+          const uint32_t ks = n % C::kKStages;
+          if (!(ok = wait_one(bar(kKFull0 + ks), (n / C::kKStages) & 1u, ctl))) break;
+          signal_remote_tx(sig_dst, sig_src, bar(kPeerK0 + static_cast<int>(ks)), 0);
+        }
+      }
+    } else if (lane == 0) {
+      constexpr uint32_t idesc_qk = kF8 ? idesc_e4m3_f32(kBM, BN)
+                                        : idesc_bf16_f32(kPair ? 2 * kBM : kBM, BN, false, false);
       // operand descriptors built once; each MMA adds a compile-time offset
       const SmemDesc dq = sw128_desc_split(sQ, 16, 1024);
       const SmemDesc dk = sw128_desc_split(sK, 16, 1024);
       uint32_t n = 0, itl = 0;
       bool ok = true;
-      int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
-      for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
-         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
+      int4 iv_next = cid < n_items ? p.items[cid] : make_int4(0, 0, 0, 0);
+      for (int kq = 0, idx = cid; idx < n_items && ok;
+         idx = cta_item(++kq, cid, ncl), ++itl) {
         const Item it = decode_item(iv_next);
-        if (cta_item(kq + 1, blockIdx.x, gridDim.x) < n_items)
-          iv_next = p.items[cta_item(kq + 1, blockIdx.x, gridDim.x)];
+        if (cta_item(kq + 1, cid, ncl) < n_items)
+          iv_next = p.items[cta_item(kq + 1, cid, ncl)];
         const uint32_t qb = itl % C::kQBufs, qu = itl / C::kQBufs;
         if (!(ok = wait_one(bar(kQFull0 + qb), qu & 1u, ctl))) break;
+        if (kPair) {
+          mbar_arrive_expect_tx(bar(kPeerQ), 16);  // the peer's Q signal
+          if (!(ok = wait_one_cl(bar(kPeerQ), itl & 1u, ctl))) break;
+        }
         tc_fence_after();
         const uint32_t q_lo = desc_lo_at(dq, qb * C::kQBytes);
         for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
@@ -451,25 +524,38 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           const uint32_t free_bar = C::kAliasP ? pv_bar(n) : bar(kSFree0 + static_cast<int>(s));
           const uint32_t free_par = ((n / C::kSBufs) & 1u) ^ 1u;
           if (!(ok = wait_two(bar(kKFull0 + ks), (n / C::kKStages) & 1u, free_bar, free_par, ctl))) break;
+          if (kPair) {
+            mbar_arrive_expect_tx(bar(kPeerK0 + static_cast<int>(ks)), 16);  // the peer's K signal
+            if (!(ok = wait_one_cl(bar(kPeerK0 + static_cast<int>(ks)), (n / C::kKStages) & 1u, ctl))) break;
+          }
           tc_fence_after();
           const uint32_t k_lo = desc_lo_at(dk, ks * C::kKStage);
           // 32 bytes of K per MMA: 16 bf16 or 32 e4m3 elements
 #pragma unroll
           for (int kk = 0; kk < C::kQKSteps; ++kk) {
-            const uint32_t b_lo = k_lo + (((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
+            const uint32_t b_lo = k_lo + (((kk >> 2) * (C::kKRows * 128) + (kk & 3) * 32) >> 4);
             const uint32_t a_lo = q_lo + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
             if constexpr (kF8)
               umma_f8_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
+            else if constexpr (kPair)
+              umma_f16_ss_pair(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
             else
               umma_f16_ss(tmem + C::kColS + s * BN, a_lo, dq.hi, b_lo, dk.hi, idesc_qk, kk > 0 ? 1u : 0u);
           }
-          umma_commit(bar(kKEmpty0 + ks));
-          umma_commit(bar(kSFull0 + s));
-          if (kt + 1 == it.kt1) umma_commit(bar(kQEmpty0 + qb));  // item's last QK
+          if constexpr (kPair) {
+            umma_commit_pair(bar(kKEmpty0 + ks));
+            umma_commit_pair(bar(kSFull0 + s));
+            if (kt + 1 == it.kt1) umma_commit_pair(bar(kQEmpty0 + qb));
+          } else {
+            umma_commit(bar(kKEmpty0 + ks));
+            umma_commit(bar(kSFull0 + s));
+            if (kt + 1 == it.kt1) umma_commit(bar(kQEmpty0 + qb));  // item's last QK
+          }
         }
       }
       // Drain: all UMMAs issued by this thread complete before TMEM is freed.
-      umma_commit(bar(kDrain));
+      if constexpr (kPair) umma_commit_pair(bar(kDrain));
+      else umma_commit(bar(kDrain));
       wait_one(bar(kDrain), 0, ctl);
     }
     __syncwarp();
@@ -477,19 +563,20 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     // ------------------------------------------------------------ V tail + PV MMA warp
     // Zeroes the V rows past the sequence end in a stage (whole 128-byte rows, so
     // the swizzle does not matter), then one thread issues O += P V for the tile.
-    constexpr uint32_t idesc_pv = kF8V ? idesc_e4m3_f32(kBM, D) : idesc_bf16_f32(kBM, D, false, true);
+    constexpr uint32_t idesc_pv =
+        kF8V ? idesc_e4m3_f32(kBM, D) : idesc_bf16_f32(kPair ? 2 * kBM : kBM, D, false, true);
     // bf16 V: MN-major; e4m3 V: K-major transposed tiles, like the P buffers
     const SmemDesc dv = kF8V ? sw128_desc_split(sV, 16, 1024) : sw128_desc_split(sV, BN * 128, 1024);
     const unsigned fullmask = 0xffffffffu;
     uint32_t n = 0;
     bool ok = true;
-    int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
-    int L_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask].z : 0;
-    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok; idx = cta_item(++kq, blockIdx.x, gridDim.x)) {
+    int4 iv_next = cid < n_items ? p.items[cid] : make_int4(0, 0, 0, 0);
+    int L_next = cid < n_items ? p.seq_info[iv_next.x & kSeqMask].z : 0;
+    for (int kq = 0, idx = cid; idx < n_items && ok; idx = cta_item(++kq, cid, ncl)) {
       const Item it = decode_item(iv_next);
       const int L = L_next;
-      if (cta_item(kq + 1, blockIdx.x, gridDim.x) < n_items) {
-        iv_next = p.items[cta_item(kq + 1, blockIdx.x, gridDim.x)];
+      if (cta_item(kq + 1, cid, ncl) < n_items) {
+        iv_next = p.items[cta_item(kq + 1, cid, ncl)];
         L_next = p.seq_info[iv_next.x & kSeqMask].z;
       }
       for (int kt = it.kt0; kt < it.kt1; ++kt, ++n) {
@@ -507,9 +594,33 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           fence_proxy_async_smem();
         }
         __syncwarp();
+        if (kPair && rank != 0) {
+          // the peer of a pair: its V half (tail zeroed), then its P, are ready for
+          // the rank-0 CTA's PV. One remote arrive per tile: its softmax warps
+          // arrive here, on their own CTA's barrier.
+          if (lane == 0) {
+            signal_remote_tx(sig_dst, sig_src, bar(kPeerV0 + static_cast<int>(s)), 0);
+            const uint32_t pb = n % C::kPBufs, pu = n / C::kPBufs;
+            ok = wait_one(bar(kPFull0 + pb), pu & 1u, ctl);
+            tc_fence_after();
+            tc_fence_before();
+            if (ok) signal_remote_tx(sig_dst, sig_src, bar(kPFull0 + pb), 0);
+          }
+          ok = __shfl_sync(fullmask, ok, 0);
+          if (!ok) break;
+          continue;
+        }
         if (lane == 0) {
           const uint32_t pb = n % C::kPBufs, pu = n / C::kPBufs;
-          ok = wait_one(bar(kPFull0 + pb), pu & 1u, ctl);
+          if (kPair) {
+            // the peer's V half, then both CTAs' P (its softmax warps arrive here)
+            mbar_arrive_expect_tx(bar(kPeerV0 + static_cast<int>(s)), 16);  // the peer's V signal
+            mbar_arrive_expect_tx(bar(kPFull0 + pb), 16);                    // the peer's P signal
+            ok = wait_one_cl(bar(kPeerV0 + static_cast<int>(s)), (n / C::kVStages) & 1u, ctl) &&
+                 wait_one_cl(bar(kPFull0 + pb), pu & 1u, ctl);
+          } else {
+            ok = wait_one(bar(kPFull0 + pb), pu & 1u, ctl);
+          }
           if (ok) {
             tc_fence_after();
             const bool first = kt == it.kt0;
@@ -533,19 +644,24 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
                 const int hh = kk / (BN / 32);
                 umma_f16_ts(tmem + C::kColO + hh * D, a, b_lo, dv.hi, idesc_pv,
                             (first && kk == hh * (BN / 32)) ? 0u : 1u);
+              } else if constexpr (kPair) {
+                umma_f16_ts_pair(tmem + C::kColO, a, b_lo, dv.hi, idesc_pv, (first && kk == 0) ? 0u : 1u);
               } else {
                 umma_f16_ts(tmem + C::kColO, a, b_lo, dv.hi, idesc_pv, (first && kk == 0) ? 0u : 1u);
               }
             }
-            umma_commit(pv_bar(n));  // PV of tile n done; its P and V stage are free
+            // PV of tile n done; its P and V stage are free (in both CTAs of a pair)
+            if constexpr (kPair) umma_commit_pair(pv_bar(n));
+            else umma_commit(pv_bar(n));
           }
         }
         ok = __shfl_sync(fullmask, ok, 0);
         if (!ok) break;
       }
     }
-    if (lane == 0) {
-      umma_commit(bar(kDrainPV));
+    if (lane == 0 && (!kPair || rank == 0)) {
+      if constexpr (kPair) umma_commit_pair(bar(kDrainPV));
+      else umma_commit(bar(kDrainPV));
       wait_one(bar(kDrainPV), 0, ctl);
     }
     __syncwarp();
@@ -568,13 +684,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     uint32_t n = 0, itl = 0;
     bool ok = true;
     // The next item's descriptor and sequence are loaded one item ahead.
-    int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
-    int4 si_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
-    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
-         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
+    int4 iv_next = cid < n_items ? p.items[cid] : make_int4(0, 0, 0, 0);
+    int4 si_next = cid < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
+    for (int kq = 0, idx = cid; idx < n_items && ok;
+         idx = cta_item(++kq, cid, ncl), ++itl) {
       const Item it = decode_item(iv_next);
       const int4 si = si_next;
-      const int idx_next = cta_item(kq + 1, blockIdx.x, gridDim.x);
+      const int idx_next = cta_item(kq + 1, cid, ncl);
       const bool has_next = idx_next < n_items;
       if (has_next) iv_next = p.items[idx_next];
       const int q0 = si.x, ql = si.y, L = si.z;
@@ -863,17 +979,17 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     uint32_t n = 0, itl = 0;
     uint32_t na = 0, nb = 0;  // row-sum / row-max exchanges of this warp pair
     bool ok = true;
-    int4 iv_next = blockIdx.x < n_items ? p.items[blockIdx.x] : make_int4(0, 0, 0, 0);
-    int4 si_next = blockIdx.x < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
-    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
-         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
+    int4 iv_next = cid < n_items ? p.items[cid] : make_int4(0, 0, 0, 0);
+    int4 si_next = cid < n_items ? p.seq_info[iv_next.x & kSeqMask] : make_int4(0, 0, 0, 0);
+    for (int kq = 0, idx = cid; idx < n_items && ok;
+         idx = cta_item(++kq, cid, ncl), ++itl) {
       const Item it = decode_item(iv_next);
       const int4 si = si_next;
-      const int idx_next = cta_item(kq + 1, blockIdx.x, gridDim.x);
+      const int idx_next = cta_item(kq + 1, cid, ncl);
       const bool has_next = idx_next < n_items;
       if (has_next) iv_next = p.items[idx_next];
       const int q0 = si.x, ql = si.y, L = si.z;
-      const int tok = it.qt * T + t_local;
+      const int tok = (it.qt + static_cast<int>(rank)) * T + t_local;  // a pair's peer: the next q tile
       const bool valid = (t_local < T) && (tok < ql);
       int lim = 0;  // keys [0, lim) visible to this row
       if (valid) lim = p.causal ? min(L, L - ql + tok + 1) : L;
@@ -978,7 +1094,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kPFull0 + pb));
+        if (lane == 0) mbar_arrive(bar(kPFull0 + pb));  // (a pair's peer forwards it from warp 2)
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -1034,13 +1150,18 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
+  // a pair leaves together: no cross-CTA arrive or MMA targets a CTA that has left
+  if constexpr (kPair) cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 }  // namespace
 
-int attention_block_n(int head_dim) { return head_dim == 128 ? 128 : 64; }
+int attention_block_n(int head_dim, bool pair) { return head_dim == 128 || pair ? 128 : 64; }
 
 size_t attention_smem_bytes(int head_dim) {
   return head_dim == 128 ? static_cast<size_t>(Cfg<128, 128>::kSmem)
@@ -1048,39 +1169,48 @@ size_t attention_smem_bytes(int head_dim) {
 }
 
 cudaError_t attention_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<128, 128, false, false>,
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<128, 128, false, false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg<128, 128>::kSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_kernel<128, 128, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_kernel<128, 128, true, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128, 128, true>::kSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_kernel<128, 128, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_kernel<128, 128, true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128, 128, true, true>::kSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_kernel<256, 64, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(attn_kernel<256, 128, false, false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<256, 128, false, false, true>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_kernel<256, 64, false, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Cfg<256, 64>::kSmem);
 }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                              int head_dim, int grid, cudaStream_t s, bool dependent) {
   if (head_dim == 128)
-    return launch_kernel(attn_kernel<128, 128, false, false>, grid, kAttnThreads, Cfg<128, 128>::kSmem, s,
+    return launch_kernel(attn_kernel<128, 128, false, false, false>, grid, kAttnThreads, Cfg<128, 128>::kSmem, s,
                          dependent, tq, tkv, tkv, tkv, p);
-  return launch_kernel(attn_kernel<256, 64, false, false>, grid, kAttnThreads, Cfg<256, 64>::kSmem, s,
+  return launch_kernel(attn_kernel<256, 64, false, false, false>, grid, kAttnThreads, Cfg<256, 64>::kSmem, s,
                        dependent, tq, tkv, tkv, tkv, p);
 }
 
 cudaError_t launch_attention_fp8(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
                                  const CUtensorMap& tkv, int grid, cudaStream_t s, bool dependent) {
-  return launch_kernel(attn_kernel<128, 128, true, false>, grid, kAttnThreads, Cfg<128, 128, true>::kSmem,
+  return launch_kernel(attn_kernel<128, 128, true, false, false>, grid, kAttnThreads, Cfg<128, 128, true>::kSmem,
                        s, dependent, tq8, tkv, tk8, tkv, p);
 }
 
 cudaError_t launch_attention_fp8pv(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
                                    const CUtensorMap& tv8, int grid, cudaStream_t s, bool dependent) {
-  return launch_kernel(attn_kernel<128, 128, true, true>, grid, kAttnThreads,
+  return launch_kernel(attn_kernel<128, 128, true, true, false>, grid, kAttnThreads,
                        Cfg<128, 128, true, true>::kSmem, s, dependent, tq8, tv8, tk8, tv8, p);
+}
+
+cudaError_t launch_attention_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
+                                  int grid, cudaStream_t s, bool dependent) {
+  return launch_kernel_pair(attn_kernel<256, 128, false, false, true>, grid & ~1, kAttnThreads,
+                            Cfg<256, 128, false, false, true>::kSmem, s, dependent, tq, tkv, tkv, tkv, p);
 }
 
 }  // namespace pattn

@@ -63,6 +63,7 @@ struct PlanParams {
   int n_heads_q, n_heads_kv, group, head_dim;
   int tokens_per_tile;  // T = kBM / group
   int block_n;          // keys per KV tile of the prefill kernel
+  int pair;             // prefill items of two q tiles (CTA-pair kernel)
   int dec_enabled;      // group <= kDecRows: units of <= kDecRows packed rows go to the decode kernel
   int bt_stride, num_pages;
   int causal;
@@ -189,6 +190,27 @@ inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The same for a kernel whose CTAs run as pairs (clusters of two).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel_pair(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                      cudaStream_t s, bool dependent, const Args&... args) {
+  cudaLaunchAttribute attr[2] = {};
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_kv_write(const KvWriteParams& p, int sms, cudaStream_t s);
 // Key sums and V maxima, then the K, V and Q codes that QuantParams asks for.
@@ -203,12 +225,17 @@ cudaError_t launch_attention_fp8(const AttnParams& p, const CUtensorMap& tq8, co
 // V tiles [tiles][n_heads_kv][128 channels][128 keys] in place of the bf16 V.
 cudaError_t launch_attention_fp8pv(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
                                    const CUtensorMap& tv8, int grid, cudaStream_t s, bool dependent);
+// head_dim 256 with CTA pairs (cta_group::2 MMAs, 128-key tiles): items of two
+// q tiles from a plan made with PlanParams::pair; grid even.
+cudaError_t launch_attention_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
+                                  int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                           int head_dim, int grid, cudaStream_t s, bool dependent);
 size_t decode_smem_bytes(int head_dim);
 cudaError_t decode_set_attributes();
-int attention_block_n(int head_dim);
+// Keys per KV tile of the prefill kernel (head_dim 256: 128 with CTA pairs, else 64).
+int attention_block_n(int head_dim, bool pair = false);
 size_t attention_smem_bytes(int head_dim);
 cudaError_t attention_set_attributes();
 

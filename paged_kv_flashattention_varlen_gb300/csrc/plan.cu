@@ -282,13 +282,24 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   };
   auto qtile_first = [&](int b) { return b < kSmemSeqs ? s_qt_prefix[b] : ws.seq_plan[b].x; };
 
+  // q tile qt of a sequence with ql queries makes an item unless it is the odd
+  // half of a CTA pair's two q tiles; the item's KV tiles are those of its last
+  // q tile (the later of a pair, which sees at least as many keys)
+  auto item_tiles = [&](int ql, int L, int qt) -> int {
+    if (p.pair && !is_decode(p, ql)) {
+      if (qt & 1) return 0;
+      return qtile_kv_tiles(p, ql, L, min(qt + 1, cdiv(ql, p.tokens_per_tile) - 1));
+    }
+    return qtile_kv_tiles(p, ql, L, qt);
+  };
+
   // ---- pass 3: histogram of item costs (KV tiles per item), one per kernel
   if (!overflow) {
     for (int gq = threadIdx.x; gq < total_qt; gq += kPlanThreads) {
       const int b = seq_of_qtile(gq);
       const int4 sq = seq_at(b);
       if (sq.y <= 0) continue;
-      const int tiles = qtile_kv_tiles(p, sq.y, sq.z, gq - qtile_first(b));
+      const int tiles = item_tiles(sq.y, sq.z, gq - qtile_first(b));
       if (tiles == 0) continue;
       const int list = is_decode(p, sq.y) ? 1 : 0;
       for (int s = 0; s < sq.w; ++s) {
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       const int4 sq = seq_at(b);
       if (sq.y <= 0) continue;
       const int qt = gq - qtile_first(b);
-      const int tiles = qtile_kv_tiles(p, sq.y, sq.z, qt);
+      const int tiles = item_tiles(sq.y, sq.z, qt);
       if (tiles == 0) continue;
       const int S = sq.w;
       const int rows = sq.y * G;

@@ -123,6 +123,27 @@ def test_long_decode_splits_and_short_sequences_mixed():
     assert_parity(run_gpu(wl2), wl2)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_head_dim_256_pairs_with_single_tile_and_split_units(causal):
+    # head_dim 256, G 8 (16 tokens per q tile): the CTA-pair kernel takes items
+    # of two q tiles; a 40-token sequence ends in a half pair, 3- and 2-token
+    # sequences (one q tile, long KV ranges) run as split items with the pair's
+    # second CTA holding no rows, and 1-token sequences go to the decode kernel
+    q_lens = [3, 40, 1, 17, 33, 2, 130]
+    kv_lens = [6000, 300, 5000, 17, 2000, 65, 8191]
+    wl = workloads.make_paged("pairs256", 21 + causal, q_lens, kv_lens, 16, 2, 256, 64,
+                              causal=causal, extra_pages=3)
+    assert_parity(run_gpu(wl), wl)
+    assert _status() == 0
+
+
+def test_head_dim_256_contiguous_pairs():
+    wl = workloads.make_contiguous("pairs256c", 23, [37, 200, 5], [37, 900, 5], 32, 4, 256,
+                                   causal=True)
+    assert_parity(run_gpu(wl), wl)
+    assert _status() == 0
+
+
 # --------------------------------------------------------------- degenerate inputs
 def test_empty_and_queries_before_the_first_key():
     # L = 0 (no key), ql = 0 (no query), and non-causal/causal ql > L rows
