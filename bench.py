@@ -38,7 +38,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # the sources each profiled kernel is compiled from (its ncu summary names their hash)
 KERNEL_SOURCES = {"decode": ["decode.cu", "merge.cuh", "ptx.cuh", "kernels.cuh"],
-                  "prefill": ["attn.cu", "ptx.cuh", "kernels.cuh"]}
+                  "prefill": ["attn.cu", "merge.cuh", "ptx.cuh", "kernels.cuh"]}
 
 
 def parse():

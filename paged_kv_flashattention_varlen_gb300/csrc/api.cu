@@ -511,12 +511,8 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   if (prof) cudaEventRecord(rec.ev[4], stream);
-  if (run_prefill) {
-    // split units of the prefill kernel (single-q-tile units of more than
-    // kDecRows rows) are merged by a separate pass; the decode kernel merges its own
-    e = launch_merge(ap, d, std::min(ws.max_items, 2 * st.sms), stream, dep);
-    if (e != cudaSuccess) return PATTN_ERR_CUDA;
-  }
+  // (split units are merged inside the attention kernels, by the CTA that
+  // finishes a unit's last split)
   if (prof) {
     cudaEventRecord(rec.ev[5], stream);
     st.prof.push_back(rec);

@@ -51,11 +51,12 @@
 // per-channel V scale is applied in the epilogue.
 //
 // At the end of an item the softmax warps divide by l and store bf16 rows, or
-// (split items) write the normalised partial O and (m, l); merge_kernel then
-// merges each split unit.
+// (split items) write the normalised partial O and (m, l), count the split in
+// its unit, and the CTA that finishes a unit's last split merges it.
 #include <cuda_fp8.h>
 
 #include "kernels.cuh"
+#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace pattn {
@@ -95,7 +96,7 @@ struct Cfg {
   static constexpr int kOffBar = kOffX + kXBytes;
   static constexpr int kBarBytes = 512;
   static constexpr int kOffMisc = kOffBar + kBarBytes;
-  static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
+  static constexpr int kSmem = kOffMisc + 128 + 1024;  // + alignment slack
   // tensor memory
   static constexpr int kColO = 0;
   static constexpr int kColS = kSplitO ? 2 * D : D;
@@ -130,15 +131,18 @@ enum Bar {
   kPVDone1, kPVDone2, kDrain, kDrainPV, kPairA0, kPairA1, kPairA2, kPairA3, kPairB0, kPairB1,
   kPairB2, kPairB3, kXSum,
   // CTA pairs, in the rank-0 CTA: the peer's Q, K stage and V stage are ready
-  kPeerQ, kPeerK0, kPeerK1, kPeerK2, kPeerV0, kPeerV1, kPeerV2, kNumBars
+  kPeerQ, kPeerK0, kPeerK1, kPeerK2, kPeerV0, kPeerV1, kPeerV2,
+  // split items: every softmax warp's partials written; the unit counter read
+  kMergeA, kMergeB, kNumBars
 };
 static_assert(kNumBars * 8 <= 512, "mbarrier area");
 constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
 constexpr int kSoftmaxWarps = 8;
 
-// part: first partial row of this split, -1 if the item is not split.
+// part: first partial row of this split, -1 if the item is not split; split:
+// the split's index in its unit.
 struct Item {
-  int b, hk, qt, kt0, kt1, part;
+  int b, hk, qt, kt0, kt1, part, split;
 };
 
 __device__ __forceinline__ Item decode_item(int4 v) {
@@ -149,7 +153,47 @@ __device__ __forceinline__ Item decode_item(int4 v) {
   it.kt0 = (v.z >> 16) & 0xFFFF;
   it.kt1 = v.z & 0xFFFF;
   it.part = v.w;
+  it.split = v.x >> kSeqBits;
   return it;
+}
+
+// After a split item's partials are written (softmax warps 4-11): count the
+// split in its unit's counter; the CTA that finishes the unit's last split
+// merges the unit's rows (the decode manifest's last-CTA reduction through its
+// counter scratch). Bounded waits only: warp 4 takes the count once all eight
+// warps have fenced their writes, then releases them with the result.
+template <int D>
+__device__ __forceinline__ bool split_done(const AttnParams& p, const Item& it, int4 si, uint32_t bar_a,
+                                           uint32_t bar_b, volatile int* flag, uint32_t& nsp, int warp,
+                                           const WaitCtl& ctl) {
+  const int lane = threadIdx.x & 31;
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_a);
+  bool ok = true;
+  if (warp == 4) {
+    if (lane == 0) {
+      ok = wait_one(bar_a, nsp & 1u, ctl);
+      int last = 0;
+      if (ok) {
+        const int4 sp = p.seq_plan[it.b];
+        last = atomicAdd(&p.unit_cnt[sp.w + it.hk], 1) == sp.z - 1;
+        if (last) __threadfence();
+      }
+      *flag = last;
+      mbar_arrive(bar_b);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+  }
+  if (!wait_warp(bar_b, nsp & 1u, ctl)) ok = false;
+  ++nsp;
+  if (!ok) return false;
+  if (*flag) {
+    const int4 sp = p.seq_plan[it.b];
+    const int rows = si.y * p.group;
+    merge_unit<D>(p, si.x, it.hk, sp.z, it.part - it.split * rows, rows, warp - 4, kSoftmaxWarps);
+  }
+  return true;
 }
 
 // One row's probabilities for KH keys: p_i = 2^(S_i c - m_ref) as bf16 pairs in
@@ -256,6 +300,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   uint8_t* misc = smem + C::kOffMisc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 16);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(misc + 64);  // this CTA merges the unit
   // CTA pairs: 16-byte source and destination of the peer's signalling copies
   const uint32_t sig_src = smem_addr(misc + 32), sig_dst = smem_addr(misc + 48);
   auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
@@ -300,6 +345,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     mbar_init(bar(kDrainPV), 1);
     mbar_init(bar(kXSum), kSoftmaxWarps);
     mbar_init(bar(kPeerQ), 1);
+    mbar_init(bar(kMergeA), kSoftmaxWarps);
+    mbar_init(bar(kMergeB), 1);
     mbar_init_fence();
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_kv);
@@ -682,6 +729,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     const int g = r - t_local * G;
     const float c = p.scale_log2;
     uint32_t n = 0, itl = 0;
+    uint32_t n_split = 0;  // split items finished (merge handshakes)
     bool ok = true;
     // The next item's descriptor and sequence are loaded one item ahead.
     int4 iv_next = cid < n_items ? p.items[cid] : make_int4(0, 0, 0, 0);
@@ -954,6 +1002,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           p.part_ml[it.part + r] = make_float2(den > 0.f ? M : -INFINITY, den);
       }
       tc_fence_before();
+      if (it.part >= 0 &&
+          !(ok = split_done<D>(p, it, si, bar(kMergeA), bar(kMergeB), merge_flag, n_split, warp, ctl)))
+        break;
     }
     } else {
     // ------------------------------------------------------------ softmax: two warpgroups
@@ -977,6 +1028,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     const float kSumLimit = 256.0f;  // 2^8: the running max is kept while every p <= 2^8
     const unsigned full = 0xffffffffu;
     uint32_t n = 0, itl = 0;
+    uint32_t n_split = 0;  // split items finished (merge handshakes)
     uint32_t na = 0, nb = 0;  // row-sum / row-max exchanges of this warp pair
     bool ok = true;
     int4 iv_next = cid < n_items ? p.items[cid] : make_int4(0, 0, 0, 0);
@@ -1144,6 +1196,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           p.part_ml[it.part + r] = make_float2(l_all > 0.f ? m_used : -INFINITY, l_all);
       }
       tc_fence_before();
+      // (a pair's peer holds no rows of a split item: single-q-tile units only)
+      if (it.part >= 0 && (!kPair || rank == 0) &&
+          !(ok = split_done<D>(p, it, si, bar(kMergeA), bar(kMergeB), merge_flag, n_split, warp, ctl)))
+        break;
     }
     }
   }

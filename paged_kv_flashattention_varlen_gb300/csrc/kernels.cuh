@@ -229,7 +229,6 @@ cudaError_t launch_attention_fp8pv(const AttnParams& p, const CUtensorMap& tq8, 
 // q tiles from a plan made with PlanParams::pair; grid even.
 cudaError_t launch_attention_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                                   int grid, cudaStream_t s, bool dependent);
-cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_decode(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                           int head_dim, int grid, cudaStream_t s, bool dependent);
 size_t decode_smem_bytes(int head_dim);

@@ -16,13 +16,9 @@
 //   4. orders the items longest first (counting sort on the number of KV
 //      tiles) so that round-robin assignment to persistent CTAs balances;
 //   5. zero-fills the output rows of q tiles that see no key at all, and
-//      zeroes the finished-split counter of every split unit (the decode
-//      kernel merges a unit's partials in the CTA that finishes it last).
-//
-// merge_kernel merges the split units of the prefill kernel's items (one per
-// unit, found at its split-0 item), after that kernel.
+//      zeroes the finished-split counter of every split unit (the attention
+//      kernels merge a unit's partials in the CTA that finishes it last).
 #include "kernels.cuh"
-#include "merge.cuh"
 #include "ptx.cuh"
 
 namespace pattn {
@@ -388,27 +384,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(256) merge_kernel(const AttnParams p) {
-  grid_dep_wait();  // every split of the prefill kernel is written
-  const int n_items = p.hdr[kHdrItems];
-  const int warp = threadIdx.x >> 5;
-  for (int idx = blockIdx.x; idx < n_items; idx += gridDim.x) {
-    const int4 iv = p.items[idx];
-    if (iv.w < 0 || (iv.x >> kSeqBits) != 0) continue;  // one CTA per unit: its split 0
-    const int b = iv.x & kSeqMask;
-    const int4 si = p.seq_info[b];
-    const int4 sp = p.seq_plan[b];
-    merge_unit<D>(p, si.x, iv.y >> 16, sp.z, iv.w, si.y * p.group, warp, 8);
-  }
-}
-
 }  // namespace
 
-cudaError_t launch_merge(const AttnParams& p, int head_dim, int grid, cudaStream_t s, bool dependent) {
-  if (head_dim == 128) return launch_kernel(merge_kernel<128>, grid, 256, 0, s, dependent, p);
-  return launch_kernel(merge_kernel<256>, grid, 256, 0, s, dependent, p);
-}
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
