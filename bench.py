@@ -59,6 +59,8 @@ def parse():
                     help="with --workload: the quantised-QK variant (pattn_forward_fp8qk)")
     ap.add_argument("--fp8", action="store_true",
                     help="with --workload: the fp8 Q/K/P/V variant (pattn_forward_fp8)")
+    ap.add_argument("--workload-steps", type=int, default=0,
+                    help="with --workload: time at most this many steps (profiling runs)")
     ap.add_argument("--append", action="store_true",
                     help="with --workload: each step first writes the query tokens' K/V rows into "
                          "their cache slots (pattn_forward_append)")
@@ -471,6 +473,8 @@ def run_workloads(args):
         torch.cuda.synchronize()
         est = 1e-3 * max(flops / 9e14, nbytes / 6e12, 2e-5) * 1e3
         steps = max(5, min(2000, int(1.0 / max(est, 1e-6))))
+        if args.workload_steps > 0:
+            steps = min(steps, args.workload_steps)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(steps):
