@@ -9,8 +9,10 @@
 //      per q tile, keeps only the KV tiles the causal mask leaves visible
 //      (tiles wholly above the diagonal are never scheduled, the "fully
 //      masked" status of the FlashAttention-4 kernel doc's mask_status);
-//   3. splits the KV range of single-q-tile units (decode) so that the whole
-//      job has about `target_items` items of at least `min_chunk` tiles (the
+//   3. splits the KV range of single-q-tile units (decode) so that each
+//      kernel's list (the decode kernel's, the prefill kernel's: they run one
+//      after the other) has about `target_items` items of at least `min_chunk`
+//      tiles of its own work (the
 //      decode manifest's "MultiCtasKv": several CTAs per sequence and KV
 //      head, with partial O and (max, sum) statistics in scratch);
 //   4. orders the items longest first (counting sort on the number of KV
@@ -114,8 +116,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   __shared__ int4 s_seq[kCacheSeqs];     // x = first token, y = query length (-1 rejected), z = L, w = splits
   __shared__ int s_part[kCacheSeqs];     // first partial row of the sequence's split units
   __shared__ int s_carry[4];
-  __shared__ unsigned long long s_tiles;
-  __shared__ int s_chunk;
+  __shared__ unsigned long long s_tiles[2];  // work of the prefill [0] and decode [1] kernels
+  __shared__ int s_chunk[2];
   __shared__ int s_list_items[2];
   const Workspace& ws = p.ws;
   const int B = p.num_seqs;
@@ -132,14 +134,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   // they read nothing of the plan before the plan grid has completed.
   grid_dep_launch();
   if (threadIdx.x == 0) {
-    s_tiles = 0ull;
+    s_tiles[0] = s_tiles[1] = 0ull;
     s_carry[0] = s_carry[1] = s_carry[2] = s_carry[3] = 0;
   }
   for (int i = threadIdx.x; i < 2 * kHistBuckets; i += kPlanThreads) (&hist[0][0])[i] = 0;
   __syncthreads();
 
   // ---- pass 1: lengths, KV prefix (contiguous cache), q tile prefix, total work
-  unsigned long long my_tiles = 0;
+  unsigned long long my_tiles[2] = {0ull, 0ull};
   for (int base = 0; base < B; base += kPlanThreads) {
     const int b = base + threadIdx.x;
     int q0 = 0, ql = 0, L = 0, nqt = 0;
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       if (!ok) atomicOr(ws.hdr + kHdrErr, kErrBadInput);
       if (ok) {
         nqt = cdiv(ql, p.tokens_per_tile);
-        my_tiles += seq_blocks(p, ql, L, nqt);
+        my_tiles[is_decode(p, ql) ? 1 : 0] += seq_blocks(p, ql, L, nqt);
       }
     }
     int kv_excl, qt_excl;
@@ -180,9 +182,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   }
   // total work: a warp sum, then one shared-memory atomic per warp that has any
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) my_tiles += __shfl_xor_sync(0xffffffffu, my_tiles, o);
-  if (lane == 0 && my_tiles != 0)
-    atomicAdd(&s_tiles, my_tiles * static_cast<unsigned long long>(p.n_heads_kv));
+  for (int k = 0; k < 2; ++k) {
+    for (int o = 16; o > 0; o >>= 1) my_tiles[k] += __shfl_xor_sync(0xffffffffu, my_tiles[k], o);
+    if (lane == 0 && my_tiles[k] != 0)
+      atomicAdd(&s_tiles[k], my_tiles[k] * static_cast<unsigned long long>(p.n_heads_kv));
+  }
 
   // ---- pass 1b: every live block-table entry must name a pool page (a warp per
   // sequence, eight independent loads per lane in flight)
@@ -213,14 +217,16 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   __syncthreads();
   const int total_qt = s_carry[1];
   if (threadIdx.x == 0) {
-    const unsigned long long t = s_tiles;
+    // the two kernels run one after the other, each over all SMs: each list's
+    // split size comes from its own work
     const unsigned long long want = static_cast<unsigned long long>(max(p.target_items, 1));
-    const int chunk = static_cast<int>((t + want - 1) / want);
-    s_chunk = max(chunk, max(p.min_chunk, 1));
+    for (int k = 0; k < 2; ++k) {
+      const int chunk = static_cast<int>((s_tiles[k] + want - 1) / want);
+      s_chunk[k] = max(chunk, max(p.min_chunk, 1));
+    }
     s_carry[2] = s_carry[3] = 0;
   }
   __syncthreads();
-  const int chunk = s_chunk;
 
   // ---- pass 2: splits of single-q-tile units, partial rows and unit slots
   for (int base = 0; base < B; base += kPlanThreads) {
@@ -230,8 +236,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       const int4 sq = seq_at(b);
       if (sq.y > 0 && cdiv(sq.y, p.tokens_per_tile) == 1) {
         const int tiles = qtile_kv_tiles(p, sq.y, sq.z, 0);
-        const int per_tile = is_decode(p, sq.y) ? kDecBlockN / kPage : p.block_n / kPage;
-        const int chunk_tiles = max(1, cdiv(chunk, per_tile));
+        const bool dec = is_decode(p, sq.y);
+        const int per_tile = dec ? kDecBlockN / kPage : p.block_n / kPage;
+        const int chunk_tiles = max(1, cdiv(s_chunk[dec ? 1 : 0], per_tile));
         if (tiles >= 2) S = min(min(cdiv(tiles, chunk_tiles), kMaxSplits), tiles);
         rows = sq.y * G;
       }
