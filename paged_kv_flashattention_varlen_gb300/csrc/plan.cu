@@ -248,10 +248,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     int part_excl, unit_excl;
     const int2 tot = block_exclusive_scan2(part_rows, units, &part_excl, &unit_excl, warp_sums);
     if (b < B) {
-      int4 sp = ws.seq_plan[b];
-      sp.z = S;
-      sp.w = s_carry[3] + unit_excl;
-      ws.seq_plan[b] = sp;
+      // (z, w) of the sequence's plan, stored without reading back its (x, y)
+      const int2 sp = make_int2(S, s_carry[3] + unit_excl);
+      *reinterpret_cast<int2*>(&ws.seq_plan[b].z) = sp;
       ws.seq_part[b] = s_carry[2] + part_excl;
       if (b < kCacheSeqs) {
         s_seq[b].w = S;
@@ -259,8 +258,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       }
       // the finished-split counters of the unit's KV heads start at zero (a plan
       // with more units than the workspace holds is rejected below)
-      if (S >= 2 && sp.w + p.n_heads_kv <= ws.max_units)
-        for (int hk = 0; hk < p.n_heads_kv; ++hk) ws.unit_cnt[sp.w + hk] = 0;
+      if (S >= 2 && sp.y + p.n_heads_kv <= ws.max_units)
+        for (int hk = 0; hk < p.n_heads_kv; ++hk) ws.unit_cnt[sp.y + hk] = 0;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -306,8 +305,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       if (tiles == 0) continue;
       const int list = is_decode(p, sq.y) ? 1 : 0;
       for (int s = 0; s < sq.w; ++s) {
-        const int k0 = static_cast<int>(static_cast<long long>(s) * tiles / sq.w);
-        const int k1 = static_cast<int>(static_cast<long long>(s + 1) * tiles / sq.w);
+        // (s <= 64 and tiles < 2^16: 32-bit products)
+        const int k0 = s * tiles / sq.w;
+        const int k1 = (s + 1) * tiles / sq.w;
         atomicAdd(&hist[list][min(k1 - k0, kHistBuckets - 1)], p.n_heads_kv);
       }
     }
@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       int4* dst = list ? ws.dec_items : ws.items;
       const int part0 = S >= 2 ? part_at(b) : 0;
       for (int s = 0; s < S; ++s) {
-        const int k0 = static_cast<int>(static_cast<long long>(s) * tiles / S);
-        const int k1 = static_cast<int>(static_cast<long long>(s + 1) * tiles / S);
+        const int k0 = s * tiles / S;
+        const int k1 = (s + 1) * tiles / S;
         const int pos = atomicAdd(&hist[list][min(k1 - k0, kHistBuckets - 1)], p.n_heads_kv);
         for (int hk = 0; hk < p.n_heads_kv; ++hk) {
           if (S >= 2)  // split s of the (b, hk) unit (q tile 0)
@@ -363,9 +363,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   // every sequence if the workspace could not hold the plan). Each thread takes
   // whole sequences; only degenerate inputs reach the stores.
   for (int b = threadIdx.x; b < B; b += kPlanThreads) {
-    const int q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
-    if (!(q0 >= 0 && q1 >= q0 && q1 <= p.total_q) || q1 == q0) continue;
+    // the query range of a live sequence from the cached plan; a rejected one's
+    // from cu_q (it may be out of range)
     const int4 sq = seq_at(b);
+    int q0 = sq.x, q1 = sq.x + sq.y;
+    if (sq.y < 0) {
+      q0 = p.cu_q[b];
+      q1 = p.cu_q[b + 1];
+    }
+    if (!(q0 >= 0 && q1 >= q0 && q1 <= p.total_q) || q1 == q0) continue;
     int z1 = q0;  // rows [q0, z1) get zeros
     if (sq.y < 0 || bad_plan) {
       z1 = q1;
