@@ -368,7 +368,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   grid_dep_wait();    // the plan (and whatever ran before) is complete from here on
-  grid_dep_launch();  // the merge pass may take SMs as this grid's CTAs leave
+  grid_dep_launch();  // a dependent launch after this grid may take SMs as its CTAs leave
 
   const int n_items = p.hdr[kHdrItems];
   const int G = p.group;
