@@ -220,6 +220,16 @@ pattn_status pattn_quantize_v(void *v8, float *v_scale, const void *kv_pool,
 size_t pattn_workspace_size_fp8(int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
                                 int n_heads_kv, int head_dim, int page_size);
 
+/*
+ * pattn_selftest_wait_timeout -- failure-detection self-test: launches one warp
+ * that waits, with the attention kernels' bounded-wait code, on an mbarrier
+ * phase that nothing completes. After the wait limit (2 s) it sets the timeout
+ * bit of the device error word and returns; nothing faults or hangs, and the
+ * context stays usable. The next pattn_get_device_status on the stream returns
+ * PATTN_ERR_DEVICE_TIMEOUT. Returns the launch status.
+ */
+pattn_status pattn_selftest_wait_timeout(pattn_stream_t stream);
+
 /* Bytes of the fixed device scratch behind pattn_forward_noalloc. */
 #define PATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -17,7 +17,8 @@ from . import _lib
 __all__ = ["PattnError", "forward", "forward_append", "forward_fp8qk", "quantize_qk", "forward_fp8",
            "quantize_v", "forward_noalloc",
            "forward_host", "workspace_size",
-           "set_workspace", "device_status", "status_string", "profile_enable", "profile_read",
+           "set_workspace", "device_status", "status_string", "selftest_wait_timeout", "profile_enable",
+           "profile_read",
            "profile_read_kernels", "STATUS", "library_path"]
 
 STATUS = {
@@ -279,6 +280,13 @@ def set_workspace(buf=None) -> None:
 def device_status(stream=None) -> int:
     """Synchronise, read and clear the device error word (0 = fine)."""
     return int(_lib.load().pattn_get_device_status(_stream_handle(stream)))
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Launch the failure-detection self-test (``pattn_selftest_wait_timeout``):
+    a bounded wait that runs out after its limit and sets the timeout bit that
+    :func:`device_status` then reports."""
+    _check(_lib.load().pattn_selftest_wait_timeout(_stream_handle(stream)), "pattn_selftest_wait_timeout")
 
 
 def profile_enable(on: bool = True) -> None:

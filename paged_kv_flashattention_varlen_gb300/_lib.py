@@ -34,6 +34,7 @@ SIGNATURES = {
     "pattn_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "pattn_set_workspace": (_i, [_vp, _sz]),
     "pattn_get_device_status": (_i, [_vp]),
+    "pattn_selftest_wait_timeout": (_i, [_vp]),
     "pattn_status_string": (ctypes.c_char_p, [_i]),
     "pattn_profile_enable": (_i, [_i]),
     "pattn_profile_read": (_i, [_dp, _dp, _dp, _ip]),

@@ -891,6 +891,16 @@ pattn_status pattn_get_device_status(pattn_stream_t stream) {
   return PATTN_OK;
 }
 
+pattn_status pattn_selftest_wait_timeout(pattn_stream_t stream) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* stp = nullptr;
+  pattn_status s = device_state(&stp);
+  if (s != PATTN_OK) return s;
+  if ((s = ensure_workspace(*stp, kHdrWords * sizeof(int))) != PATTN_OK) return s;
+  const cudaError_t e = launch_wait_selftest(static_cast<int*>(stp->ws), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PATTN_OK : PATTN_ERR_CUDA;
+}
+
 const char* pattn_status_string(pattn_status status) {
   switch (status) {
     case PATTN_OK: return "ok";

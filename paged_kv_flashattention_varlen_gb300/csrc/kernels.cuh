@@ -212,6 +212,9 @@ inline cudaError_t launch_kernel_pair(void (*kernel)(KArgs...), dim3 grid, dim3 
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
+// One warp waits on an mbarrier that nothing completes until the bounded wait
+// gives up and sets the timeout bit in *err (failure-detection self-test).
+cudaError_t launch_wait_selftest(int* err, cudaStream_t s);
 cudaError_t launch_kv_write(const KvWriteParams& p, int sms, cudaStream_t s);
 // Key sums and V maxima, then the K, V and Q codes that QuantParams asks for.
 cudaError_t launch_quant(const QuantParams& p, int sms, cudaStream_t s);

@@ -397,11 +397,33 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   }
 }
 
+// A bounded wait that nothing ends: one warp waits on a fresh mbarrier for a
+// phase no thread completes, with the attention kernels' own wait helper, so
+// that after its time limit it sets the abort flag and the timeout bit of the
+// device error word and returns (the self-test of failure detection).
+__global__ void __launch_bounds__(32) wait_selftest_kernel(int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_addr(&bar), 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  const WaitCtl ctl{&abort_flag, err};
+  wait_warp(smem_addr(&bar), 0, ctl);
+}
+
 }  // namespace
 
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int* err, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(err);
   return cudaGetLastError();
 }
 

@@ -248,3 +248,17 @@ def test_profile_counts_launches():
     pk.profile_enable(False)
     plan, attn, comb, calls = pk.profile_read()
     assert calls == 3 and attn > 0 and plan > 0
+
+
+# --------------------------------------------------------------- failure detection
+def test_bounded_wait_runs_out_into_an_error_status_and_the_context_survives():
+    # a wait on an mbarrier phase that nothing completes gives up after its
+    # limit, sets the timeout bit and returns: the host reads the status, and
+    # the next call on the same context runs normally
+    import paged_kv_flashattention_varlen_gb300 as pk
+    pk.selftest_wait_timeout()
+    assert pk.device_status() == 6  # PATTN_ERR_DEVICE_TIMEOUT
+    assert pk.device_status() == 0  # read and cleared
+    wl = workloads.named(2, scale_down=8)
+    assert_parity(run_gpu(wl), wl)
+    assert _status() == 0
