@@ -21,7 +21,7 @@ constexpr int kMaxDevices = 64;
 // batch 0.200 -> 0.185 ms against 4 items per SM of the whole job's work).
 constexpr int kTargetHalfItemsPerSm = 3;
 constexpr int kTargetItemsCap = 1024;  // bound used when sizing the workspace
-constexpr int kMinChunk = 8;           // 64-key blocks per split, at least
+constexpr int kMinChunk = 16;          // 64-key blocks per split, at least (split and merge cost more than short items save below this)
 constexpr int kProfileCap = 4096;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
