@@ -73,6 +73,18 @@ def test_attention_within_the_probability_rounding_bound(name):
     assert err.mean() <= 0.1 * bound.mean(), (err.mean(), bound.mean())
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_group_of_eight_ragged_lengths(causal):
+    # G 8 (16 tokens per q tile), lengths around the 64-key blocks and 128-key tiles
+    wl = workloads.make_paged("fp8g8", 63 + causal, [1, 65, 129, 200, 16], [1, 65, 1000, 200, 3000], 32, 4, 128,
+                              causal=causal, extra_pages=3)
+    out = _run(wl, to_device(wl))
+    rows = sample_rows(wl, per_seq=10)
+    ref, bound = quant.attention_fp8(wl, rows=rows)
+    got = out[torch.as_tensor(rows, device=out.device)].float().cpu().numpy()
+    _within_bound(got, ref, bound)
+
+
 def test_equal_keys_give_the_exact_mean_of_the_values():
     # every key of a head equal: smoothed K is zero, every score 0 and every
     # p * 2^2 = 4 exact in e4m3, so the output is the mean of the dequantised V

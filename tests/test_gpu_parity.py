@@ -137,6 +137,16 @@ def test_head_dim_256_pairs_with_single_tile_and_split_units(causal):
     assert _status() == 0
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 2)])
+def test_head_dim_256_pairs_group_sizes(hq, hkv):
+    # G 1 (128 tokens per q tile, pairs of 256 tokens) and G 16 (8 tokens per
+    # q tile): ragged lengths, a half pair at each sequence end
+    wl = workloads.make_paged("pairsg", 24 + hq, [300, 9, 130, 1], [300, 520, 4000, 77], hq, hkv, 256, 64,
+                              causal=True, extra_pages=2)
+    assert_parity(run_gpu(wl), wl)
+    assert _status() == 0
+
+
 def test_head_dim_256_contiguous_pairs():
     wl = workloads.make_contiguous("pairs256c", 23, [37, 200, 5], [37, 900, 5], 32, 4, 256,
                                    causal=True)
