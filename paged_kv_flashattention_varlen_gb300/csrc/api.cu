@@ -15,11 +15,12 @@ namespace pattn {
 namespace {
 
 constexpr int kMaxDevices = 64;
-// Split target: about 1.5 items per SM in each kernel's list (in halves). Fewer,
+// Split target: about 2 items per SM in each kernel's list (in halves). Fewer,
 // longer items cost less pipeline start-up; a unit is split only when it holds
-// more than about 2/3 of an SM's share of its kernel's work (measured: decode
-// batch 0.200 -> 0.185 ms against 4 items per SM of the whole job's work).
-constexpr int kTargetHalfItemsPerSm = 3;
+// more than about half an SM's share of its kernel's work (measured: decode
+// batch 0.200 -> 0.1855 ms against 4 items per SM of the whole job's work; its
+// units longer than ~7.7k keys still take the split-KV path).
+constexpr int kTargetHalfItemsPerSm = 4;
 constexpr int kTargetItemsCap = 1024;  // bound used when sizing the workspace
 constexpr int kMinChunk = 16;          // 64-key blocks per split, at least (split and merge cost more than short items save below this)
 constexpr int kProfileCap = 4096;
