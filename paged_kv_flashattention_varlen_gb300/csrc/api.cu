@@ -204,11 +204,12 @@ pattn_status ensure_workspace(DeviceState& st, size_t need) {
 
 pattn_status encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
                     const cuuint64_t* strides, const cuuint32_t* box,
-                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode(m, dtype, static_cast<cuuint32_t>(rank),
                         const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PATTN_OK : PATTN_ERR_CUDA;
 }
@@ -306,7 +307,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   const int g = sh.group, T = sh.tokens_per_tile;
   const bool dec_enabled = g <= kDecRows;
   const bool run_prefill = !dec_enabled || static_cast<long long>(max_q) * g > kDecRows;
-  CUtensorMap tq, tq_dec, tkv;
+  CUtensorMap tq, tq_dec, tkv, to;
   if (dec_enabled) {
     // decode items: the G heads of one KV head for kDecRows / G tokens
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
@@ -326,6 +327,15 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
                                static_cast<cuuint64_t>(hq) * d * 2};
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(T)};
     if ((s = encode(&tq, q, 4, dims, str, box)) != PATTN_OK) return s;
+    to = tq;
+    if (d == 128) {
+      // the output (q's shape): 32-channel slices of a q tile's rows, stored by
+      // the head_dim-128 prefill kernels
+      const cuuint32_t obox[4] = {32, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(T)};
+      if ((s = encode(&to, out, 4, dims, str, obox, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CU_TENSOR_MAP_SWIZZLE_64B)) != PATTN_OK)
+        return s;
+    }
   }
   if (bt) {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kPage),
@@ -507,13 +517,13 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
         if ((s = encode(&tv8, qb->v8, 4, vdims, vstr, vbox, CU_TENSOR_MAP_DATA_TYPE_UINT8)) != PATTN_OK)
           return s;
         fp.v_scale = qb->v_scale;
-        e = launch_attention_fp8pv(fp, tq8, tk8, tv8, st.sms, stream, dep);
+        e = launch_attention_fp8pv(fp, tq8, tk8, tv8, to, st.sms, stream, dep);
       } else {
-        e = launch_attention_fp8(fp, tq8, tk8, tkv, st.sms, stream, dep);
+        e = launch_attention_fp8(fp, tq8, tk8, tkv, to, st.sms, stream, dep);
       }
     } else {
       e = sh.pair ? launch_attention_pair(ap, tq, tkv, st.sms, stream, dep)
-                  : launch_attention(ap, tq, tkv, d, st.sms, stream, dep);
+                  : launch_attention(ap, tq, tkv, to, d, st.sms, stream, dep);
     }
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }

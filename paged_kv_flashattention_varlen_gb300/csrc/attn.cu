@@ -91,7 +91,11 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBufs * kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKStage;
-  static constexpr int kOffX = kOffV + kVStages * kVStage;  // row sum / max / l exchange
+  // D = 128: each warpgroup stages a 32-column slice of its bf16 output rows
+  // (64-byte rows, 64-byte swizzle) for the tensor store
+  static constexpr int kOStage = kSplitO ? 2 * kBM * 64 : 0;
+  static constexpr int kOffO = kOffV + kVStages * kVStage;
+  static constexpr int kOffX = kOffO + kOStage;  // row sum / max / l exchange
   static constexpr int kXBytes = (2 * 2 + 2 * 2 + 2) * kBM * 4;
   static constexpr int kOffBar = kOffX + kXBytes;
   static constexpr int kBarBytes = 512;
@@ -287,7 +291,7 @@ template <int D, int BN, bool kF8, bool kF8V, bool kPair>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_kv,
             const __grid_constant__ CUtensorMap tmap_k8, const __grid_constant__ CUtensorMap tmap_v8,
-            const AttnParams p) {
+            const __grid_constant__ CUtensorMap tmap_o, const AttnParams p) {
   using C = Cfg<D, BN, kF8, kF8V, kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -352,6 +356,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     tma_prefetch_desc(&tmap_kv);
     if constexpr (kF8) tma_prefetch_desc(&tmap_k8);
     if constexpr (kF8V) tma_prefetch_desc(&tmap_v8);
+    if constexpr (C::kSplitO) tma_prefetch_desc(&tmap_o);
   }
   if (warp == 1) {
     if constexpr (kPair) {
@@ -950,7 +955,67 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
         if (!(ok = wait_warp(pv_bar(pm), pv_par(pm), ctl))) break;
       }
       tc_fence_after();
-      if (warp_live) {
+      // An unsplit item whose q tile is full leaves through the tensor store:
+      // each warpgroup stages a 32-column slice of its 128 rows and one thread
+      // stores the box [32 channels, G heads, 1, T tokens] (whole 64-byte row
+      // pieces instead of 16 bytes per thread and row). The other items store
+      // row by row below.
+      const bool tma_out = it.part < 0 && (it.qt + 1) * T <= ql;
+      if (tma_out) {
+        const uint32_t stage = s_base + C::kOffO + static_cast<uint32_t>(h * (kBM * 64));
+        const uint32_t row_addr = stage + static_cast<uint32_t>(r * 64);
+        const uint32_t sx = static_cast<uint32_t>((r >> 1) & 3);  // 64-byte swizzle of this row
+        const bool issuer = sw == 0 && lane == 0;
+#pragma unroll 1
+        for (int pp = 0; pp < 2; ++pp) {
+          const int col = h * (D / 2) + pp * 32;
+          // the slice buffer is free once the previous store has read it
+          if (issuer) bulk_wait_read_all();
+          named_bar_sync(1 + h, 128);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int cc = col + hf * 16;
+            float4 vsc[4];
+            if constexpr (kF8V) {
+              // per-channel V scale (P's 2^2 cancels against l)
+              const float4* vs = reinterpret_cast<const float4*>(
+                  p.v_scale + (static_cast<size_t>(it.b) * p.n_heads_kv + it.hk) * D + cc);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) vsc[q4] = vs[q4];
+            }
+            uint32_t o0[16], o1[16];
+            tmem_ld16(tmem + lane_base + C::kColO + cc, o0);
+            tmem_ld16(tmem + lane_base + C::kColO + D + cc, o1);
+            tmem_wait_ld();
+            reg_fence(o0);
+            reg_fence(o1);
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float a = __uint_as_float(o0[2 * e]) * c0 + __uint_as_float(o1[2 * e]) * c1;
+              float b = __uint_as_float(o0[2 * e + 1]) * c0 + __uint_as_float(o1[2 * e + 1]) * c1;
+              if constexpr (kF8V) {
+                const float4 f = vsc[e >> 1];
+                a *= (e & 1) ? f.z : f.x;
+                b *= (e & 1) ? f.w : f.y;
+              }
+              __nv_bfloat162 hh = __floats2bfloat162_rn(a, b);
+              w[e] = *reinterpret_cast<uint32_t*>(&hh);
+            }
+            // 16-byte chunks 2 hf and 2 hf + 1 of the row, swizzled
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2)
+              st_shared_v4(row_addr + ((static_cast<uint32_t>(2 * hf + c2) ^ sx) << 4), w[4 * c2],
+                           w[4 * c2 + 1], w[4 * c2 + 2], w[4 * c2 + 3]);
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1 + h, 128);
+          if (issuer) {
+            tma_store_4d(&tmap_o, stage, col, 0, it.hk, q0 + it.qt * T);
+            bulk_commit_group();
+          }
+        }
+      } else if (warp_live) {
         const int hq = it.hk * G + g;
 #pragma unroll 1
         for (int j = 0; j < (D / 2) / 16; ++j) {
@@ -1006,6 +1071,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
           !(ok = split_done<D>(p, it, si, bar(kMergeA), bar(kMergeB), merge_flag, n_split, warp, ctl)))
         break;
     }
+    // the output stores of this warpgroup complete before the CTA exits
+    if (sw == 0 && lane == 0) bulk_wait_all();
     } else {
     // ------------------------------------------------------------ softmax: two warpgroups
     // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) takes keys [h*KH, h*KH + KH)
@@ -1243,30 +1310,32 @@ cudaError_t attention_set_attributes() {
 }
 
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
-                             int head_dim, int grid, cudaStream_t s, bool dependent) {
+                             const CUtensorMap& to, int head_dim, int grid, cudaStream_t s, bool dependent) {
   if (head_dim == 128)
     return launch_kernel(attn_kernel<128, 128, false, false, false>, grid, kAttnThreads, Cfg<128, 128>::kSmem, s,
-                         dependent, tq, tkv, tkv, tkv, p);
+                         dependent, tq, tkv, tkv, tkv, to, p);
   return launch_kernel(attn_kernel<256, 64, false, false, false>, grid, kAttnThreads, Cfg<256, 64>::kSmem, s,
-                       dependent, tq, tkv, tkv, tkv, p);
+                       dependent, tq, tkv, tkv, tkv, tq, p);
 }
 
 cudaError_t launch_attention_fp8(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
-                                 const CUtensorMap& tkv, int grid, cudaStream_t s, bool dependent) {
+                                 const CUtensorMap& tkv, const CUtensorMap& to, int grid, cudaStream_t s,
+                                 bool dependent) {
   return launch_kernel(attn_kernel<128, 128, true, false, false>, grid, kAttnThreads, Cfg<128, 128, true>::kSmem,
-                       s, dependent, tq8, tkv, tk8, tkv, p);
+                       s, dependent, tq8, tkv, tk8, tkv, to, p);
 }
 
 cudaError_t launch_attention_fp8pv(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
-                                   const CUtensorMap& tv8, int grid, cudaStream_t s, bool dependent) {
+                                   const CUtensorMap& tv8, const CUtensorMap& to, int grid, cudaStream_t s,
+                                   bool dependent) {
   return launch_kernel(attn_kernel<128, 128, true, true, false>, grid, kAttnThreads,
-                       Cfg<128, 128, true, true>::kSmem, s, dependent, tq8, tv8, tk8, tv8, p);
+                       Cfg<128, 128, true, true>::kSmem, s, dependent, tq8, tv8, tk8, tv8, to, p);
 }
 
 cudaError_t launch_attention_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
                                   int grid, cudaStream_t s, bool dependent) {
   return launch_kernel_pair(attn_kernel<256, 128, false, false, true>, grid & ~1, kAttnThreads,
-                            Cfg<256, 128, false, false, true>::kSmem, s, dependent, tq, tkv, tkv, tkv, p);
+                            Cfg<256, 128, false, false, true>::kSmem, s, dependent, tq, tkv, tkv, tkv, tq, p);
 }
 
 }  // namespace pattn

@@ -218,16 +218,21 @@ cudaError_t launch_wait_selftest(int* err, cudaStream_t s);
 cudaError_t launch_kv_write(const KvWriteParams& p, int sms, cudaStream_t s);
 // Key sums and V maxima, then the K, V and Q codes that QuantParams asks for.
 cudaError_t launch_quant(const QuantParams& p, int sms, cudaStream_t s);
+// head_dim 128: `to` is the output map (bf16 [total_q][n_heads_q][128] as
+// [128, G, n_heads_kv, total_q], box [32, G, 1, T], 64-byte swizzle), through
+// which the kernel stores full q tiles; unused at head_dim 256.
 cudaError_t launch_attention(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
-                             int head_dim, int grid, cudaStream_t s, bool dependent);
+                             const CUtensorMap& to, int head_dim, int grid, cudaStream_t s, bool dependent);
 // Quantised-QK prefill (head_dim 128): tq8 over the e4m3 Q codes, tk8 over the
 // e4m3 K blocks, tkv over the bf16 cache (V).
 cudaError_t launch_attention_fp8(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
-                                 const CUtensorMap& tkv, int grid, cudaStream_t s, bool dependent);
+                                 const CUtensorMap& tkv, const CUtensorMap& to, int grid, cudaStream_t s,
+                                 bool dependent);
 // fp8 P.V prefill (head_dim 128): as above, with tv8 over the transposed e4m3
 // V tiles [tiles][n_heads_kv][128 channels][128 keys] in place of the bf16 V.
 cudaError_t launch_attention_fp8pv(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
-                                   const CUtensorMap& tv8, int grid, cudaStream_t s, bool dependent);
+                                   const CUtensorMap& tv8, const CUtensorMap& to, int grid, cudaStream_t s,
+                                   bool dependent);
 // head_dim 256 with CTA pairs (cta_group::2 MMAs, 128-key tiles): items of two
 // q tiles from a plan made with PlanParams::pair; grid even.
 cudaError_t launch_attention_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
