@@ -111,6 +111,24 @@ def test_edge_lengths(d, hq, hkv, causal):
     assert _status() == 0
 
 
+@pytest.mark.parametrize("hq,hkv", [(6, 1), (7, 1), (16, 1), (32, 2)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_head_dim_128_group_sizes_full_and_partial_q_tiles(hq, hkv, causal):
+    # head_dim 128 prefill at G = 6, 7, 16, 32 (q tiles of 21, 18, 8 and 4
+    # tokens: 126, 126, 128 and 128 rows). Full q tiles of unsplit items leave
+    # through the tensor store of [32, G, 1, T] boxes; the last, partial q tile
+    # of each sequence and the split single-q-tile units store row by row.
+    g = hq // hkv
+    t = 128 // g
+    q_lens = [3 * t, 3 * t + 1, t - 1, 200, 1, 2 * t]
+    kv_lens = [3 * t, 700, 9000, 1300, 64, 4 * t + 5]
+    wl = workloads.make_paged("groups128", 610 + hq + int(causal), q_lens, kv_lens, hq, hkv, 128, 64,
+                              causal=causal, extra_pages=2)
+    out = run_gpu(wl)
+    assert_parity(out, wl)
+    assert _status() == 0
+
+
 def test_long_decode_splits_and_short_sequences_mixed():
     rng = np.random.default_rng(7)
     kv = [1, 2, 64, 65, 129, 4000, 20000, 300, 8191, 8192, 8193]
