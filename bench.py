@@ -161,6 +161,25 @@ def profiled_pass(pk, step, steps):
     return pk.profile_read()
 
 
+def step_stats(step, steps):
+    """Distribution of single-step device times (ms): a separate pass with a CUDA
+    event pair around every step on the launching stream."""
+    import numpy as np
+    import torch
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    t = np.array([a.elapsed_time(b) for a, b in ev])
+    q = np.percentile(t, [50, 90, 95, 99])
+    return {"count": int(steps), "mean": round(float(t.mean()), 5), "p50": round(float(q[0]), 5),
+            "p90": round(float(q[1]), 5), "p95": round(float(q[2]), 5), "p99": round(float(q[3]), 5),
+            "min": round(float(t.min()), 5), "max": round(float(t.max()), 5)}
+
+
 def profiled_kernels(pk, step, steps):
     """As :func:`profiled_pass`, split by kernel: ((plan, cache write, decode,
     prefill, after) ms summed over the calls, calls)."""
@@ -231,6 +250,7 @@ def run_ours(args):
     ms = e0.elapsed_time(e1)
     ms_max = pdist.max_over_ranks(ms, dev if world > 1 else None)
     t_plan, t_attn, t_comb, calls = profiled_pass(pk, step, min(args.steps, 500))
+    stats = step_stats(step, min(args.steps, 500))
     status = pk.device_status()
     step_bytes = wl.kv_bytes() + wl.qo_bytes()
     ms_step = ms_max / args.steps
@@ -268,7 +288,8 @@ def run_ours(args):
                    "causal": wl.causal, "kv_bytes_per_step": wl.kv_bytes(),
                    "l2": "inputs larger than L2 (KV pool %.2f GB > 129 MB)" % (wl.kv_pool.numel() * 2 / 1e9),
                    "parallelism": f"weak x{world}: one batch per GPU, no collective"},
-        "roofline": roofline, "e2e": e2e, "gpu_launches": int(2 * args.steps), "clocks": clocks,
+        "roofline": roofline, "step_ms_stats": stats, "e2e": e2e, "gpu_launches": int(2 * args.steps),
+        "clocks": clocks,
         "device_status": status, "prefill": prefill,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -347,6 +368,7 @@ def run_prefill(args, pk, workloads, dev, world, pk_peaks, peak_kind):
     torch.cuda.synchronize()
     ms = pdist.max_over_ranks(e0.elapsed_time(e1), dev if world > 1 else None)
     t_plan, t_attn, t_comb, calls = profiled_pass(pk, step, args.prefill_steps)
+    stats = step_stats(step, args.prefill_steps)
     flops = 4.0 * wl.head_dim * wl.n_heads_q * wl.visible_pairs()
     attn_ms = t_attn / max(calls, 1)
     achieved = flops / (attn_ms * 1e-3) / 1e12
@@ -361,7 +383,7 @@ def run_prefill(args, pk, workloads, dev, world, pk_peaks, peak_kind):
                      "traffic": ncu_traffic("prefill"), "peak_source": f"{peak_kind} bf16_tflops (burst)",
                      "nominal_frac": round(achieved / NOMINAL_BF16_TFLOPS, 4),
                      "kernel": "attn_kernel<128,128>", "kernel_ms": round(attn_ms, 4)},
-        "gpu_launches": int(3 * args.prefill_steps),
+        "step_ms_stats": stats, "gpu_launches": int(3 * args.prefill_steps),
     }
 
 
