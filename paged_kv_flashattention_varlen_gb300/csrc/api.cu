@@ -278,8 +278,9 @@ ProfileRec take_events(DeviceState& st) {
   return r;
 }
 
-// Encodes the tensor maps and launches plan -> decode -> prefill -> combine with
-// the workspace at `wsb` (laid out as L). Caller holds g_mu.
+// Encodes the tensor maps and launches plan -> [cache write] -> [quantisation]
+// -> decode -> prefill with the workspace at `wsb` (laid out as L); the
+// attention kernels merge their own KV splits. Caller holds g_mu.
 pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* out, const void* q,
                         const void* kv, const int32_t* bt, const int32_t* seq_lens,
                         const int32_t* cu_q, int num_seqs, int total_q, int max_q, int max_kv,
