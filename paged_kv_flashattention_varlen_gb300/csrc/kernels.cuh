@@ -1,6 +1,5 @@
-// kernels.cuh -- parameters shared by the host side and the device kernels
-// (plan, cache write, quantisation, decode and prefill attention) of the
-// paged-KV varlen attention library.
+// kernels.cuh -- parameters shared by the host planner and the three device
+// kernels (plan, attention, combine) of the paged-KV varlen attention library.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
