@@ -230,6 +230,34 @@ size_t pattn_workspace_size_fp8(int num_seqs, int total_q, int max_q, int max_kv
  */
 pattn_status pattn_selftest_wait_timeout(pattn_stream_t stream);
 
+/*
+ * The tile plan of a batch, for inspection (tests): runs only the device-side
+ * planner that pattn_forward launches first (step "plan / tile scheduler" of
+ * the method: varlen q tiles of T = 128 / G tokens with GQA packing, causal
+ * tile skipping as the FlashAttention-4 kernel doc's mask_status describes,
+ * KV splits of single-q-tile units as the decode manifest's MultiCtasKv),
+ * then copies its two work lists to host memory and synchronises `stream`.
+ *
+ * Arguments as pattn_forward (no Q, cache or output pointers; scale is not
+ * needed). prefill_items / decode_items: host int32 [capacity][4] each,
+ * written with the first min(count, capacity) items of the head_dim-specific
+ * prefill kernel's list and of the swap-AB decode kernel's list, in list
+ * order (longest first). counts: host int32[4] = {prefill items, decode items,
+ * split units, partial rows}.
+ *
+ * Item record {x, y, z, w}: x = sequence | split << 24; y = kv_head << 16 |
+ * q tile (the first q tile of a CTA pair's two at head_dim 256); z = first KV
+ * tile << 16 | end KV tile (tiles of 128 keys, or 64 for the one-CTA
+ * head_dim-256 prefill kernel); w = first partial row of a split item, -1
+ * otherwise. Returns PATTN_ERR_NO_MEMORY if the plan did not fit the
+ * workspace; errors as pattn_forward otherwise.
+ */
+pattn_status pattn_plan_items(const int32_t *block_table, const int32_t *seq_lens, const int32_t *cu_q,
+                              int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
+                              int n_heads_kv, int head_dim, int page_size, int num_pages, int causal,
+                              int32_t *prefill_items, int32_t *decode_items, int capacity,
+                              int32_t *counts, pattn_stream_t stream);
+
 /* Bytes of the fixed device scratch behind pattn_forward_noalloc. */
 #define PATTN_NOALLOC_SCRATCH_BYTES (16u << 20)
 

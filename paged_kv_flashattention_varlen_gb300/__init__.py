@@ -17,7 +17,8 @@ from . import _lib
 __all__ = ["PattnError", "forward", "forward_append", "forward_fp8qk", "quantize_qk", "forward_fp8",
            "quantize_v", "forward_noalloc",
            "forward_host", "workspace_size",
-           "set_workspace", "device_status", "status_string", "selftest_wait_timeout", "profile_enable",
+           "set_workspace", "device_status", "status_string", "selftest_wait_timeout", "plan_items",
+           "profile_enable",
            "profile_read",
            "profile_read_kernels", "STATUS", "library_path"]
 
@@ -287,6 +288,30 @@ def selftest_wait_timeout(stream=None) -> None:
     a bounded wait that runs out after its limit and sets the timeout bit that
     :func:`device_status` then reports."""
     _check(_lib.load().pattn_selftest_wait_timeout(_stream_handle(stream)), "pattn_selftest_wait_timeout")
+
+
+def plan_items(block_table, seq_lens, cu_q, *, total_q: int, max_q: int, max_kv: int, n_heads_q: int,
+               n_heads_kv: int, head_dim: int, causal: bool, num_pages: int, capacity: int = 1 << 16,
+               stream=None):
+    """The tile plan of a batch (``pattn_plan_items``): runs only the device-side
+    planner and returns (prefill items, decode items, counts) as numpy int32
+    arrays, items [n, 4] = (sequence | split << 24, kv_head << 16 | q tile,
+    first KV tile << 16 | end KV tile, first partial row or -1) in list order,
+    counts = (prefill items, decode items, split units, partial rows)."""
+    import numpy as np
+    import torch
+    for name, t in (("seq_lens", seq_lens), ("cu_q", cu_q)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name}: expected a contiguous CUDA int32 tensor")
+    pre = np.zeros((capacity, 4), dtype=np.int32)
+    dec = np.zeros((capacity, 4), dtype=np.int32)
+    counts = np.zeros(4, dtype=np.int32)
+    rc = _lib.load().pattn_plan_items(
+        _ptr(block_table), _ptr(seq_lens), _ptr(cu_q), int(seq_lens.numel()), int(total_q), int(max_q),
+        int(max_kv), int(n_heads_q), int(n_heads_kv), int(head_dim), 64, int(num_pages), int(bool(causal)),
+        pre.ctypes.data, dec.ctypes.data, int(capacity), counts.ctypes.data, _stream_handle(stream))
+    _check(rc, "pattn_plan_items")
+    return pre[:min(int(counts[0]), capacity)], dec[:min(int(counts[1]), capacity)], counts
 
 
 def profile_enable(on: bool = True) -> None:

@@ -62,12 +62,12 @@ struct Shape {
   bool pair;  // head_dim 256 prefill on CTA pairs (some sequence may have two q tiles)
 };
 
-pattn_status check_args(const void* out, const void* q, const void* kv, const int32_t* bt,
-                        const int32_t* seq_lens, const int32_t* cu_q, int num_seqs, int total_q,
-                        int max_q, int max_kv, int hq, int hkv, int d, int page, int num_pages,
-                        float scale, int causal, Shape* sh) {
-  if (!out || !q || !kv || !seq_lens || !cu_q) return PATTN_ERR_INVALID_ARG;
-  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(kv, 16)) return PATTN_ERR_INVALID_ARG;
+// The batch description and head configuration (everything but the Q, K/V and
+// output pointers); fills the tiling of the batch.
+pattn_status check_shape(const int32_t* bt, const int32_t* seq_lens, const int32_t* cu_q, int num_seqs,
+                         int total_q, int max_q, int max_kv, int hq, int hkv, int d, int page,
+                         int num_pages, float scale, int causal, Shape* sh) {
+  if (!seq_lens || !cu_q) return PATTN_ERR_INVALID_ARG;
   if (!aligned(seq_lens, 4) || !aligned(cu_q, 4) || (bt && !aligned(bt, 4)))
     return PATTN_ERR_INVALID_ARG;
   if (num_seqs < 0 || total_q < 0 || max_q < 0 || max_kv < 0) return PATTN_ERR_INVALID_ARG;
@@ -91,6 +91,16 @@ pattn_status check_args(const void* out, const void* q, const void* kv, const in
   if (num_seqs > kSeqMask) return PATTN_ERR_UNSUPPORTED;  // item encoding: 24-bit sequence index
   if (static_cast<long long>(total_q) * hq * d > (1LL << 40)) return PATTN_ERR_UNSUPPORTED;
   return PATTN_OK;
+}
+
+pattn_status check_args(const void* out, const void* q, const void* kv, const int32_t* bt,
+                        const int32_t* seq_lens, const int32_t* cu_q, int num_seqs, int total_q,
+                        int max_q, int max_kv, int hq, int hkv, int d, int page, int num_pages,
+                        float scale, int causal, Shape* sh) {
+  if (!out || !q || !kv) return PATTN_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(kv, 16)) return PATTN_ERR_INVALID_ARG;
+  return check_shape(bt, seq_lens, cu_q, num_seqs, total_q, max_q, max_kv, hq, hkv, d, page, num_pages,
+                     scale, causal, sh);
 }
 
 struct WsLayout {
@@ -253,7 +263,7 @@ Fp8Layout fp8_layout(size_t base, int num_seqs, int total_q, int max_kv, int hq,
 
 // What one call computes: attention (bf16), attention with e4m3 Q/K codes,
 // attention with e4m3 Q/K/P/V codes, or only codes (those QuantBufs names).
-enum class Mode { kBf16, kFp8, kFp8Pv, kQuantOnly };
+enum class Mode { kBf16, kFp8, kFp8Pv, kQuantOnly, kPlanOnly };
 
 // Device buffers of the e4m3 codes (workspace regions or caller buffers).
 struct QuantBufs {
@@ -308,8 +318,8 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   const int g = sh.group, T = sh.tokens_per_tile;
   const bool dec_enabled = g <= kDecRows;
   const bool run_prefill = !dec_enabled || static_cast<long long>(max_q) * g > kDecRows;
-  CUtensorMap tq, tq_dec, tkv, to;
-  if (dec_enabled) {
+  CUtensorMap tq{}, tq_dec{}, tkv{}, to{};
+  if (mode != Mode::kPlanOnly && dec_enabled) {
     // decode items: the G heads of one KV head for kDecRows / G tokens
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
                                 static_cast<cuuint64_t>(hkv),
@@ -320,41 +330,43 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
                                static_cast<cuuint32_t>(kDecRows / g)};
     if ((s = encode(&tq_dec, q, 4, dims, str, box)) != PATTN_OK) return s;
   }
-  {
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
-                                static_cast<cuuint64_t>(hkv),
-                                static_cast<cuuint64_t>(std::max(total_q, 1))};
-    const cuuint64_t str[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(g) * d * 2,
-                               static_cast<cuuint64_t>(hq) * d * 2};
-    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(T)};
-    if ((s = encode(&tq, q, 4, dims, str, box)) != PATTN_OK) return s;
-    to = tq;
-    if (d == 128) {
-      // the output (q's shape): 32-channel slices of a q tile's rows, stored by
-      // the head_dim-128 prefill kernels
-      const cuuint32_t obox[4] = {32, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(T)};
-      if ((s = encode(&to, out, 4, dims, str, obox, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      CU_TENSOR_MAP_SWIZZLE_64B)) != PATTN_OK)
-        return s;
+  if (mode != Mode::kPlanOnly) {
+    {
+      const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(g),
+                                  static_cast<cuuint64_t>(hkv),
+                                  static_cast<cuuint64_t>(std::max(total_q, 1))};
+      const cuuint64_t str[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(g) * d * 2,
+                                 static_cast<cuuint64_t>(hq) * d * 2};
+      const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(T)};
+      if ((s = encode(&tq, q, 4, dims, str, box)) != PATTN_OK) return s;
+      to = tq;
+      if (d == 128) {
+        // the output (q's shape): 32-channel slices of a q tile's rows, stored by
+        // the head_dim-128 prefill kernels
+        const cuuint32_t obox[4] = {32, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(T)};
+        if ((s = encode(&to, out, 4, dims, str, obox, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        CU_TENSOR_MAP_SWIZZLE_64B)) != PATTN_OK)
+          return s;
+      }
     }
-  }
-  if (bt) {
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kPage),
-                                static_cast<cuuint64_t>(hkv),
-                                static_cast<cuuint64_t>(num_pages) * 2};
-    const cuuint64_t str[3] = {static_cast<cuuint64_t>(hkv) * d * 2,
-                               static_cast<cuuint64_t>(d) * 2,
-                               static_cast<cuuint64_t>(kPage) * hkv * d * 2};
-    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kPage), 1, 1};
-    if ((s = encode(&tkv, kv, 4, dims, str, box)) != PATTN_OK) return s;
-  } else {
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
-                                static_cast<cuuint64_t>(num_pages), 2};
-    const cuuint64_t str[3] = {static_cast<cuuint64_t>(d) * 2,
-                               static_cast<cuuint64_t>(hkv) * d * 2,
-                               static_cast<cuuint64_t>(num_pages) * hkv * d * 2};
-    const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kPage), 1};
-    if ((s = encode(&tkv, kv, 4, dims, str, box)) != PATTN_OK) return s;
+    if (bt) {
+      const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(kPage),
+                                  static_cast<cuuint64_t>(hkv),
+                                  static_cast<cuuint64_t>(num_pages) * 2};
+      const cuuint64_t str[3] = {static_cast<cuuint64_t>(hkv) * d * 2,
+                                 static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(kPage) * hkv * d * 2};
+      const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kPage), 1, 1};
+      if ((s = encode(&tkv, kv, 4, dims, str, box)) != PATTN_OK) return s;
+    } else {
+      const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                                  static_cast<cuuint64_t>(num_pages), 2};
+      const cuuint64_t str[3] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(hkv) * d * 2,
+                                 static_cast<cuuint64_t>(num_pages) * hkv * d * 2};
+      const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kPage), 1};
+      if ((s = encode(&tkv, kv, 4, dims, str, box)) != PATTN_OK) return s;
+    }
   }
 
   PlanParams pp{};
@@ -406,7 +418,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   dp.items = ws.dec_items;
   dp.tokens_per_tile = dec_enabled ? kDecRows / g : 0;
 
-  const bool prof = g_profile && st.prof.size() < static_cast<size_t>(kProfileCap);
+  const bool prof = g_profile && mode != Mode::kPlanOnly && st.prof.size() < static_cast<size_t>(kProfileCap);
   ProfileRec rec{};
   if (prof) {
     rec = take_events(st);
@@ -418,13 +430,14 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   // Profiling events between the launches turn that overlap off.
   const bool dep = !prof;
   cudaError_t e = cudaSuccess;
-  if (mode != Mode::kBf16) {
+  if (mode != Mode::kBf16 && mode != Mode::kPlanOnly) {
     // the key sums of the quantisation start from zero
     e = cudaMemsetAsync(qb->scratch, 0, quant_zero_bytes(num_seqs, hkv, d), stream);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
   e = launch_plan(pp, stream);
   if (e != cudaSuccess) return PATTN_ERR_CUDA;
+  if (mode == Mode::kPlanOnly) return PATTN_OK;
   if (prof) cudaEventRecord(rec.ev[1], stream);
   if (k_new) {
     // the new tokens' K and V rows into their cache slots, before any attention
@@ -551,10 +564,11 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
   DeviceState& st = *stp;
   const WsLayout L = ws_layout(num_seqs, total_q, max_q, hq, hkv, d);
   const Fp8Layout F = fp8_layout(L.total, num_seqs, total_q, max_kv, hq, hkv, d, mode == Mode::kFp8Pv);
-  if ((s = ensure_workspace(st, mode == Mode::kBf16 ? L.total : F.total)) != PATTN_OK) return s;
+  const bool quant = mode != Mode::kBf16 && mode != Mode::kPlanOnly;
+  if ((s = ensure_workspace(st, quant ? F.total : L.total)) != PATTN_OK) return s;
   uint8_t* wsb = static_cast<uint8_t*>(st.ws);
   QuantBufs qb;
-  if (mode != Mode::kBf16) {
+  if (quant) {
     qb.q8 = wsb + F.q8;
     qb.q_scale = reinterpret_cast<float*>(wsb + F.q_scale);
     qb.k8 = wsb + F.k8;
@@ -911,6 +925,47 @@ pattn_status pattn_selftest_wait_timeout(pattn_stream_t stream) {
   if ((s = ensure_workspace(*stp, kHdrWords * sizeof(int))) != PATTN_OK) return s;
   const cudaError_t e = launch_wait_selftest(static_cast<int*>(stp->ws), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PATTN_OK : PATTN_ERR_CUDA;
+}
+
+pattn_status pattn_plan_items(const int32_t* block_table, const int32_t* seq_lens, const int32_t* cu_q,
+                              int num_seqs, int total_q, int max_q, int max_kv, int n_heads_q,
+                              int n_heads_kv, int head_dim, int page_size, int num_pages, int causal,
+                              int32_t* prefill_items, int32_t* decode_items, int capacity, int32_t* counts,
+                              pattn_stream_t stream) {
+  Shape sh{};
+  pattn_status s = check_shape(block_table, seq_lens, cu_q, num_seqs, total_q, max_q, max_kv, n_heads_q,
+                               n_heads_kv, head_dim, page_size, num_pages, 1.0f, causal, &sh);
+  if (s != PATTN_OK) return s;
+  if (!counts || capacity < 0 || (capacity > 0 && (!prefill_items || !decode_items))) return PATTN_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i) counts[i] = 0;
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if ((s = forward_locked(nullptr, nullptr, nullptr, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
+                          max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, 1.0f, causal, cs, sh,
+                          nullptr, nullptr, Mode::kPlanOnly)) != PATTN_OK)
+    return s;
+  DeviceState* stp = nullptr;
+  if ((s = device_state(&stp)) != PATTN_OK) return s;
+  const WsLayout L = ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim);
+  const uint8_t* wsb = static_cast<const uint8_t*>(stp->ws);
+  int hdr[kHdrWords];
+  if (cudaMemcpyAsync(hdr, wsb + L.hdr, sizeof(hdr), cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+      cudaStreamSynchronize(cs) != cudaSuccess)
+    return PATTN_ERR_CUDA;
+  counts[0] = hdr[kHdrItems];
+  counts[1] = hdr[kHdrDecItems];
+  counts[2] = hdr[kHdrUnits];
+  counts[3] = hdr[kHdrPartRows];
+  const size_t n0 = static_cast<size_t>(std::min(std::max(hdr[kHdrItems], 0), capacity));
+  const size_t n1 = static_cast<size_t>(std::min(std::max(hdr[kHdrDecItems], 0), capacity));
+  if ((n0 && cudaMemcpyAsync(prefill_items, wsb + L.items, n0 * sizeof(int4), cudaMemcpyDeviceToHost, cs) !=
+                 cudaSuccess) ||
+      (n1 && cudaMemcpyAsync(decode_items, wsb + L.dec_items, n1 * sizeof(int4), cudaMemcpyDeviceToHost, cs) !=
+                 cudaSuccess) ||
+      cudaStreamSynchronize(cs) != cudaSuccess)
+    return PATTN_ERR_CUDA;
+  return hdr[kHdrOverflow] ? PATTN_ERR_NO_MEMORY : PATTN_OK;
 }
 
 const char* pattn_status_string(pattn_status status) {

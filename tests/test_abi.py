@@ -108,3 +108,30 @@ def test_status_strings(lib):
     for code in range(7):
         assert lib.pattn_status_string(code)
     assert b"unknown" in lib.pattn_status_string(99)
+
+
+def test_plan_items_host_validation(lib):
+    INVALID, UNSUP = 1, 2
+    counts = (ctypes.c_int32 * 4)()
+    buf = (ctypes.c_int32 * 16)()
+
+    def plan(**kw):
+        a = dict(bt=ALIGNED, sl=ALIGNED, cu=ALIGNED, B=2, tq=16, mq=8, mkv=650, hq=24, hkv=4, d=256, P=64,
+                 pages=22, causal=1, pre=ctypes.addressof(buf), dec=ctypes.addressof(buf), cap=4,
+                 counts=ctypes.addressof(counts))
+        a.update(kw)
+        return lib.pattn_plan_items(a["bt"], a["sl"], a["cu"], a["B"], a["tq"], a["mq"], a["mkv"], a["hq"],
+                                    a["hkv"], a["d"], a["P"], a["pages"], a["causal"], a["pre"], a["dec"],
+                                    a["cap"], a["counts"], None)
+
+    assert plan(sl=None) == INVALID
+    assert plan(cu=ALIGNED + 2) == INVALID
+    assert plan(hq=25) == INVALID
+    assert plan(d=64) == UNSUP
+    assert plan(P=32) == UNSUP
+    assert plan(counts=None) == INVALID
+    assert plan(cap=-1) == INVALID
+    assert plan(pre=None) == INVALID
+    # an empty batch needs no device: zero counts
+    counts[0] = 7
+    assert plan(B=0, tq=0) == 0 and list(counts) == [0, 0, 0, 0]
