@@ -50,9 +50,11 @@
 // from TMEM and V from shared memory as transposed e4m3 tiles (K-major); the
 // per-channel V scale is applied in the epilogue.
 //
-// At the end of an item the softmax warps divide by l and store bf16 rows, or
-// (split items) write the normalised partial O and (m, l), count the split in
-// its unit, and the CTA that finishes a unit's last split merges it.
+// At the end of an item the softmax warps divide by l and store bf16 rows (at
+// head_dim 128, a full q tile of an unsplit item as 32-column slices staged in
+// shared memory and written by a tensor store), or (split items) write the
+// normalised partial O and (m, l), count the split in its unit, and the CTA
+// that finishes a unit's last split merges it.
 #include <cuda_fp8.h>
 
 #include "kernels.cuh"

@@ -1,5 +1,6 @@
-// kernels.cuh -- parameters shared by the host planner and the three device
-// kernels (plan, attention, combine) of the paged-KV varlen attention library.
+// kernels.cuh -- parameters shared by the host side and the device kernels
+// (plan, cache write, quantisation, decode and prefill attention) of the
+// paged-KV varlen attention library.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -11,7 +12,7 @@ namespace pattn {
 
 constexpr int kBM = 128;            // packed query rows per tile (tokens x GQA group)
 constexpr int kPage = 64;           // page size handled by the gather (rows per TMA box)
-constexpr int kThreads = 256;       // 8 warps: load, MMA, V tail fix, idle, 4 x softmax
+constexpr int kThreads = 256;       // decode kernel: load, MMA, V tail fix, split merge, 4 x softmax
 constexpr int kTmemCols = 512;
 constexpr int kHistBuckets = 1024;  // cost buckets of the longest-first order, per item list
 constexpr int kDecRows = 16;        // packed query rows a swap-AB decode item holds
