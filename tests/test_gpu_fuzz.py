@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads
-from helpers import assert_parity, run_gpu
+from helpers import assert_parity, run_gpu, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -63,3 +63,33 @@ def test_random_shapes(seed):
     assert_parity(out, wl)
     import paged_kv_flashattention_varlen_gb300 as pk
     assert pk.device_status() == 0
+
+
+def _same_bits(a, b):
+    return torch.equal(a.cpu().view(torch.int16), b.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("seed", list(range(16)))
+def test_random_shapes_append(seed):
+    """The cache write of the new tokens then attention (pattn_forward_append) on
+    the same random shapes: the pool bit for bit against the oracle's write, the
+    output over every row against the oracle."""
+    import oracle
+    import paged_kv_flashattention_varlen_gb300 as pk
+    d, hq, hkv, causal, paged, q_lens, kv_lens = _case(9000 + seed)
+    if paged:
+        wl = workloads.make_paged("fuzz_app", 9200 + seed, q_lens, kv_lens, hq, hkv, d, 64, causal=causal,
+                                  extra_pages=3)
+    else:
+        wl = workloads.make_contiguous("fuzz_app", 9200 + seed, q_lens, kv_lens, hq, hkv, d, causal=causal)
+    k, v = workloads.new_kv_rows(wl, 9400 + seed)
+    ref_wl = oracle.append_workload(wl, k, v)
+    dev = to_device(wl)
+    out = torch.full_like(dev["q"], float("nan"))
+    pk.forward_append(out, dev["q"], k.to(dev["q"].device), v.to(dev["q"].device), dev["kv"], dev["bt"],
+                      dev["sl"], dev["cu"], max_q=wl.max_q, max_kv=wl.max_kv, n_heads_kv=wl.n_heads_kv,
+                      scale=wl.scale, causal=wl.causal, num_pages=wl.num_pages)
+    torch.cuda.synchronize()
+    assert pk.device_status() == 0
+    assert _same_bits(dev["kv"], ref_wl.kv_pool), "cache after the write differs from the oracle's"
+    assert_parity(out, ref_wl)
