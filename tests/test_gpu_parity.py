@@ -290,3 +290,22 @@ def test_bounded_wait_runs_out_into_an_error_status_and_the_context_survives():
     wl = workloads.named(2, scale_down=8)
     assert_parity(run_gpu(wl), wl)
     assert _status() == 0
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_head_shards_through_the_library_reassemble_the_output(world):
+    # head (tensor) sharding as one process per GPU would run it, one shard
+    # after the other on this GPU: each shard's KV heads and query heads through
+    # the C ABI, the blocks concatenated along the heads against the oracle
+    import paged_kv_flashattention_varlen_gb300 as pk
+    from paged_kv_flashattention_varlen_gb300 import dist as pdist
+    wl = workloads.make_paged("heads_gpu", 18, [1, 40, 300, 2], [700, 200, 900, 5000], 32, 8, 128, 64,
+                              causal=True, extra_pages=2)
+    blocks = []
+    for r in range(world):
+        q_r, kv_r, hq_r, hkv_r = pdist.shard_heads(wl.q, wl.kv_pool, wl.n_heads_q, wl.n_heads_kv, world, r)
+        part = workloads.Workload(**{**wl.__dict__, "q": q_r, "kv_pool": kv_r, "n_heads_q": hq_r,
+                                     "n_heads_kv": hkv_r})
+        blocks.append(run_gpu(part))
+        assert _status() == 0
+    assert_parity(torch.cat(blocks, dim=1), wl)
