@@ -74,6 +74,19 @@ def test_noncausal_contiguous_full_size_sampled():
     assert _status() == 0
 
 
+@pytest.mark.parametrize("n", [37760, 37761])
+def test_noncausal_tail_lengths_sampled(n):
+    # the video-DiT page's tail study: the 37,810-token shape cut to a multiple
+    # of the 128-row tile (37,760 = 295 x 128) and one past it, same recipe as
+    # the named workload (56 heads MHA, contiguous cache, K channel offsets)
+    wl = workloads.make_contiguous("tail", workloads.seed_for(4) + n, [n], [n], 56, 56, 128,
+                                   scale=1.0 / np.sqrt(128), causal=False, k_offset_std=0.5)
+    out = run_gpu(wl)
+    rows = sorted({0, 1, 127, 128, n // 2, n - 129, n - 128, n - 2, n - 1})
+    assert_parity(out, wl, rows=rows)
+    assert _status() == 0
+
+
 def test_mixed_batch_small_full():
     wl = workloads.named(5, scale_down=8)
     out = run_gpu(wl)
