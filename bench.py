@@ -32,6 +32,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DECODE = 2   # workload numbers of workloads.named
+# the headline metric, the same string on both arms (ours and the oracle's)
+HEADLINE_METRIC = "decode KV GB/s (live K/V bytes once per KV head + Q + O, per second)"
 PREFILL = 3
 NOMINAL_HBM_GBS = 7900.0
 NOMINAL_BF16_TFLOPS = 2250.0
@@ -194,6 +196,16 @@ def profiled_kernels(pk, step, steps):
     return pk.profile_read_kernels()
 
 
+def headline_config(workloads, wl, world: int) -> dict:
+    """The headline workload's description, the same on both arms."""
+    return {"workload": workloads.NAMES[DECODE - 1], "batch": wl.num_seqs, "q_per_seq": 1,
+            "kv_len": "uniform [1024, 8192], seeded", "n_heads_q": wl.n_heads_q,
+            "n_heads_kv": wl.n_heads_kv, "head_dim": wl.head_dim, "page_size": wl.page_size,
+            "causal": wl.causal, "kv_bytes_per_step": wl.kv_bytes(),
+            "l2": "inputs larger than L2 (KV pool %.2f GB > 129 MB)" % (wl.kv_pool.numel() * 2 / 1e9),
+            "parallelism": f"weak x{world}: one batch per GPU, no collective"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -278,16 +290,11 @@ def run_ours(args):
                                                               pk_peaks, peak_kind)
 
     line = {
-        "metric": "decode KV GB/s (live K/V bytes once per KV head + Q + O, per second)",
+        "metric": HEADLINE_METRIC,
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workloads.NAMES[DECODE - 1], "batch": wl.num_seqs, "q_per_seq": 1,
-                   "kv_len": "uniform [1024, 8192], seeded", "n_heads_q": wl.n_heads_q,
-                   "n_heads_kv": wl.n_heads_kv, "head_dim": wl.head_dim, "page_size": wl.page_size,
-                   "causal": wl.causal, "kv_bytes_per_step": wl.kv_bytes(),
-                   "l2": "inputs larger than L2 (KV pool %.2f GB > 129 MB)" % (wl.kv_pool.numel() * 2 / 1e9),
-                   "parallelism": f"weak x{world}: one batch per GPU, no collective"},
+        "config": headline_config(workloads, wl, world),
         "roofline": roofline, "step_ms_stats": stats, "e2e": e2e, "gpu_launches": int(2 * args.steps),
         "clocks": clocks,
         "device_status": status, "prefill": prefill,
@@ -431,14 +438,12 @@ def run_reference(args):
     el = time.perf_counter() - t0
     value = bytes_per_pass * steps / el / 1e9
     line = {
-        "impl": "reference", "metric": "decode KV GB/s (live K/V bytes once per KV head + Q + O, per second)",
+        "impl": "reference", "metric": HEADLINE_METRIC,
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": max(args.warmup, 0), "ms_per_step": round(el * 1e3 / steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": workloads.NAMES[DECODE - 1], "batch": wl.num_seqs,
-                   "n_heads_q": wl.n_heads_q, "n_heads_kv": wl.n_heads_kv, "head_dim": wl.head_dim,
-                   "page_size": wl.page_size},
+        "config": headline_config(workloads, wl, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n_threads, "kind": "oracle",
                          "sample": f"{steps} full pass(es) of the decode batch"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
