@@ -1,7 +1,7 @@
 """GPU parity on seeded random shapes: batch sizes, query and KV lengths, head
 groups, head dims, causal or not, paged or contiguous, each case compared with
 the float64 oracle over every output row. The shapes mix decode units (at most
-64 packed query rows), prefill units, split units and partial q tiles in one
+16 packed query rows, on the swap-AB kernel), prefill units, split units and partial q tiles in one
 call, so that both attention kernels, the planner's split rule and the two
 output paths of the prefill kernel meet in the same launch."""
 import numpy as np
