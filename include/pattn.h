@@ -273,18 +273,28 @@ pattn_status pattn_plan_items(const int32_t *block_table, const int32_t *seq_len
  * Same arguments, layouts and results as pattn_forward. Instead of the
  * library workspace it uses one fixed device array of
  * PATTN_NOALLOC_SCRATCH_BYTES, compiled into the library: every GPU that
- * loads the library holds it until the process exits. Batches whose
- * workspace (pattn_workspace_size) exceeds it are rejected with
- * PATTN_ERR_NO_MEMORY before anything is launched. Nothing here calls
+ * loads the library holds it until the process exits. Nothing here calls
  * cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Acceptance: the work list and split-KV scratch a batch can need are bounded
+ * from num_seqs, total_q, max_q, max_kv, the heads and the device's SM count
+ * (at most 64 splits per (sequence, KV head) unit, and at most ceil(max_kv /
+ * 64); per kernel list at most the planner's item target plus its units).
+ * A batch whose bound exceeds the array is rejected with PATTN_ERR_NO_MEMORY
+ * before anything is launched. The bound never exceeds pattn_workspace_size
+ * for the same arguments, so every batch whose pattn_workspace_size fits is
+ * accepted; some larger ones (short max_kv) are accepted too. For example,
+ * 64 sequences x 32/8 heads, head_dim 128, one query each and up to 8k keys
+ * fit.
  *
  * The first call on a device sets the scratch up (looks up its device
  * address and clears its header, a synchronous step), so make that first call
  * before any stream capture. All calls share the one array and it keeps the
  * previous call's contents: calls that overlap on the GPU (other streams,
  * other host threads) race on it and must be serialised by the caller.
- * Device-side data errors are recorded in the scratch's own error word, which
- * pattn_get_device_status does not read; rejected rows are still zero-filled.
+ * Device-side data errors (a rejected page or length, a wait that ran out)
+ * set the scratch's own error word; pattn_get_device_status reads and clears
+ * it together with the workspace's. Rejected rows are zero-filled.
  */
 pattn_status pattn_forward_noalloc(void *out, const void *q, const void *kv_pool,
                                    const int32_t *block_table, const int32_t *seq_lens,
@@ -325,9 +335,11 @@ size_t pattn_workspace_size(int num_seqs, int total_q, int max_q, int max_kv, in
 pattn_status pattn_set_workspace(void *ptr, size_t bytes);
 
 /*
- * Synchronises `stream`, reads and clears the device error word of the
- * current device. Returns PATTN_OK, PATTN_ERR_DEVICE_BAD_INPUT or
- * PATTN_ERR_DEVICE_TIMEOUT (timeout wins if both are set).
+ * Synchronises `stream`, reads and clears the device error words of the
+ * current device (the workspace's, and that of the fixed scratch behind
+ * pattn_forward_noalloc once it is set up). Allocates nothing. Returns
+ * PATTN_OK, PATTN_ERR_DEVICE_BAD_INPUT or PATTN_ERR_DEVICE_TIMEOUT (timeout
+ * wins if both are set).
  */
 pattn_status pattn_get_device_status(pattn_stream_t stream);
 

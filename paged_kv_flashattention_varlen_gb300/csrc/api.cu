@@ -21,7 +21,9 @@ constexpr int kMaxDevices = 64;
 // batch 0.200 -> 0.1855 ms against 4 items per SM of the whole job's work; its
 // units longer than ~7.7k keys still take the split-KV path).
 constexpr int kTargetHalfItemsPerSm = 4;
-constexpr int kTargetItemsCap = 1024;  // bound used when sizing the workspace
+// Most items per kernel list the split heuristic may aim at (the workspace
+// bound below assumes it when the device is not known).
+constexpr int kTargetItemsCap = 512;
 constexpr int kMinChunk = 16;          // 64-key blocks per split, at least (split and merge cost more than short items save below this)
 constexpr int kProfileCap = 4096;
 
@@ -108,10 +110,16 @@ struct WsLayout {
   int max_items, max_units, max_part_rows;
 };
 
-// Workspace layout for these bounds. With max_kv >= 0 the split bound also
-// uses the planner's per-unit limit (at most min(kMaxSplits, ceil(max_kv/64))
-// splits per unit) and `target` the planner's own item target; without it,
-// the bound assumes kTargetItemsCap items and no length limit.
+// Items per list the planner aims at on a device with `sms` SMs.
+inline int plan_target(int sms) { return std::min(kTargetHalfItemsPerSm * sms / 2, kTargetItemsCap); }
+
+// Workspace layout for these bounds. `target` is the planner's item target per
+// list (kTargetItemsCap when the device is not known). The planner sizes the
+// splits of each of its two lists (decode kernel, prefill kernel) from that
+// list's own work, so each list holds at most target + its units splits:
+// 2 * target + units in all. With max_kv >= 0 the split bound also uses the
+// planner's per-unit limit (at most min(kMaxSplits, ceil(max_kv/64)) splits
+// per unit).
 WsLayout ws_layout(int num_seqs, int total_q, int max_q, int hq, int hkv, int d, int max_kv = -1,
                    int target = kTargetItemsCap) {
   WsLayout w{};
@@ -119,9 +127,10 @@ WsLayout ws_layout(int num_seqs, int total_q, int max_q, int hq, int hkv, int d,
   const int T = kBM / g;
   const long long units = static_cast<long long>(num_seqs) * hkv;
   const long long qtiles = cdiv(total_q, T) + static_cast<long long>(num_seqs);
+  // per list: one item per (q tile, KV head), a split unit's S splits in place of its one
   const long long items = static_cast<long long>(hkv) * qtiles + target + units + 64;
   const long long rows_cap = std::min<long long>(kBM, static_cast<long long>(max_q) * g);
-  long long splits = target + units;
+  long long splits = 2LL * target + units;
   if (max_kv >= 0) {
     const long long per_unit = std::min<long long>(kMaxSplits, std::max(1, cdiv(max_kv, kPage)));
     splits = std::min(splits, units * per_unit);
@@ -390,7 +399,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   pp.num_pages = num_pages;
   pp.causal = causal;
   pp.dec_enabled = dec_enabled ? 1 : 0;
-  pp.target_items = std::min(kTargetHalfItemsPerSm * st.sms / 2, kTargetItemsCap);
+  pp.target_items = plan_target(st.sms);
   pp.min_chunk = kMinChunk;
 
   AttnParams ap{};
@@ -796,9 +805,8 @@ pattn_status pattn_forward_noalloc(void* out, const void* q, const void* kv_pool
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* stp = nullptr;
   if ((s = device_state(&stp)) != PATTN_OK) return s;
-  const int target = std::min(kTargetHalfItemsPerSm * stp->sms / 2, kTargetItemsCap);
-  const WsLayout L =
-      ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim, max_kv, target);
+  const WsLayout L = ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim, max_kv,
+                              plan_target(stp->sms));
   if (L.total > static_cast<size_t>(PATTN_NOALLOC_SCRATCH_BYTES)) return PATTN_ERR_NO_MEMORY;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PATTN_ERR_CUDA;
@@ -907,11 +915,19 @@ pattn_status pattn_get_device_status(pattn_stream_t stream) {
   if (s != PATTN_OK) return s;
   cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st_) != cudaSuccess) return PATTN_ERR_CUDA;
-  if (!stp->ws) return PATTN_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PATTN_ERR_CUDA;
+  // the error words of the library (or caller) workspace and of the fixed
+  // scratch behind pattn_forward_noalloc, each read and cleared (no allocation)
+  void* words[2] = {stp->ws, g_noalloc_ptr[dev]};
   int err = 0;
-  if (cudaMemcpy(&err, stp->ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return PATTN_ERR_CUDA;
-  if (cudaMemset(stp->ws, 0, sizeof(int)) != cudaSuccess) return PATTN_ERR_CUDA;
+  for (void* w : words) {
+    if (!w) continue;
+    int e = 0;
+    if (cudaMemcpy(&e, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PATTN_ERR_CUDA;
+    if (e && cudaMemset(w, 0, sizeof(int)) != cudaSuccess) return PATTN_ERR_CUDA;
+    err |= e;
+  }
   if (err & kErrTimeout) return PATTN_ERR_DEVICE_TIMEOUT;
   if (err & kErrBadInput) return PATTN_ERR_DEVICE_BAD_INPUT;
   return PATTN_OK;
