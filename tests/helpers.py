@@ -47,24 +47,36 @@ def assert_parity(gpu_out, wl, rows=None, n_threads=0):
     return mx, mean
 
 
-def sample_rows(wl, per_seq=6, tile=None, seed=0):
+def sample_rows(wl, per_seq=6, tile=None, seed=0, every_boundary=False, min_rows=0):
     """Query tokens the oracle computes one by one: the first and last rows of
-    every sequence, rows at q-tile boundaries (tile-1, tile, tile+1) and a few
-    seeded random rows."""
+    every sequence, rows at q-tile boundaries (tile-1, tile, tile+1) and seeded
+    random rows.
+
+    With ``every_boundary`` every q-tile boundary of every sequence is taken
+    (so every q tile, and with all heads every work item, has checked rows);
+    otherwise three boundaries per sequence. Random rows (at least ``per_seq``
+    per sequence) are added until there are ``min_rows`` rows in all."""
     rng = np.random.default_rng(seed)
     cu = wl.cu_q.numpy().astype(np.int64)
     G = wl.n_heads_q // wl.n_heads_kv
     T = tile or max(1, 128 // G)
     rows = set()
+    live = []
     for b in range(wl.num_seqs):
         a, e = int(cu[b]), int(cu[b + 1])
         if e == a:
             continue
+        live.append((a, e))
         rows.update({a, e - 1})
-        for k in (1, (e - a) // (2 * T), (e - a) // T - 1):
+        ks = range(1, (e - a + T - 1) // T) if every_boundary else (1, (e - a) // (2 * T), (e - a) // T - 1)
+        for k in ks:
             for off in (-1, 0, 1):
                 t = a + k * T + off
                 if a <= t < e:
                     rows.add(t)
         rows.update(int(x) for x in rng.integers(a, e, size=min(per_seq, e - a)))
+    total = sum(e - a for a, e in live)
+    while live and len(rows) < min(min_rows, total):
+        a, e = live[int(rng.integers(0, len(live)))]
+        rows.add(int(rng.integers(a, e)))
     return sorted(rows)

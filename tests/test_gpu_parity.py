@@ -2,9 +2,12 @@
 
 Small cases are compared element by element over every output; the five named
 workloads at full size are compared over every decode row and over sampled
-prefill rows (first/last rows of each sequence, q-tile boundaries, seeded
-random rows), which the oracle computes one by one. Bar: max |err| <= 2e-2 and
-mean |err| <= 2e-3 on the bf16 outputs.
+prefill rows, which the oracle computes one by one: the first and last rows of
+each sequence, the rows on both sides of every q-tile boundary (so that every
+q tile, and with all heads every work item of the persistent schedule, has
+checked rows) and seeded random rows, at least 1024 query rows x all heads per
+prefill workload. Bar: max |err| <= 2e-2 and mean |err| <= 2e-3 on the bf16
+outputs.
 """
 import numpy as np
 import pytest
@@ -53,10 +56,14 @@ def test_causal_prefill_small_full():
     assert_parity(out, wl)
 
 
-def test_causal_prefill_full_size_sampled():
+def test_causal_prefill_full_size_every_tile_boundary_over_3000_rows():
+    # 4 x 8192 tokens in q tiles of 32 tokens (G 4): rows q0-1, q0, q0+1 at each
+    # of the 255 boundaries per sequence, first/last and random rows
     wl = workloads.named(3)
     out = run_gpu(wl)
-    assert_parity(out, wl, rows=sample_rows(wl, per_seq=8))
+    rows = sample_rows(wl, per_seq=8, every_boundary=True, min_rows=1024)
+    assert len(rows) >= 3000
+    assert_parity(out, wl, rows=rows)
     assert _status() == 0
 
 
@@ -66,23 +73,28 @@ def test_noncausal_contiguous_small_full():
     assert_parity(out, wl)
 
 
-def test_noncausal_contiguous_full_size_sampled():
+def test_noncausal_contiguous_full_size_every_tile_boundary_1024_rows():
+    # 37,810 tokens in q tiles of 128 (G 1): rows q0-1, q0, q0+1 at each of the
+    # 295 boundaries, first/last rows, random rows up to 1024 rows x 56 heads
     wl = workloads.named(4)
     out = run_gpu(wl)
-    rows = sample_rows(wl, per_seq=4)
+    rows = sample_rows(wl, per_seq=4, every_boundary=True, min_rows=1024)
+    assert len(rows) >= 1024
     assert_parity(out, wl, rows=rows)
     assert _status() == 0
 
 
 @pytest.mark.parametrize("n", [37760, 37761])
-def test_noncausal_tail_lengths_sampled(n):
+def test_noncausal_tail_lengths_every_tile_boundary(n):
     # the video-DiT page's tail study: the 37,810-token shape cut to a multiple
     # of the 128-row tile (37,760 = 295 x 128) and one past it, same recipe as
-    # the named workload (56 heads MHA, contiguous cache, K channel offsets)
+    # the named workload (56 heads MHA, contiguous cache, K channel offsets);
+    # rows on both sides of every q-tile boundary and the last tile's rows
     wl = workloads.make_contiguous("tail", workloads.seed_for(4) + n, [n], [n], 56, 56, 128,
                                    scale=1.0 / np.sqrt(128), causal=False, k_offset_std=0.5)
     out = run_gpu(wl)
-    rows = sorted({0, 1, 127, 128, n // 2, n - 129, n - 128, n - 2, n - 1})
+    rows = sorted(set(sample_rows(wl, per_seq=4, every_boundary=True)) | {n - 129, n - 128, n - 2, n - 1})
+    assert len(rows) >= 3 * (n // 128)
     assert_parity(out, wl, rows=rows)
     assert _status() == 0
 
@@ -93,12 +105,16 @@ def test_mixed_batch_small_full():
     assert_parity(out, wl)
 
 
-def test_mixed_batch_full_size():
+def test_mixed_batch_full_size_every_decode_row_and_chunk_tile_boundary():
+    # all 96 decode rows; the four 2048-token chunks in q tiles of 16 tokens
+    # (G 8; pairs of q tiles on the CTA-pair kernel): rows on both sides of
+    # every boundary, first/last and random rows, over 1500 chunk rows
     wl = workloads.named(5)
     out = run_gpu(wl)
     decode_rows = list(range(96))
     assert_parity(out, wl, rows=decode_rows)
-    chunk_rows = [r for r in sample_rows(wl, per_seq=6) if r >= 96]
+    chunk_rows = [r for r in sample_rows(wl, per_seq=6, every_boundary=True, min_rows=1024) if r >= 96]
+    assert len(chunk_rows) >= 1500
     assert_parity(out, wl, rows=chunk_rows)
     assert _status() == 0
 
