@@ -107,8 +107,10 @@ pattn_status pattn_forward(void *out, const void *q, const void *kv_pool,
  *                 V planes). Nothing else in the pool is written.
  *   other arguments as for pattn_forward; seq_lens count the new tokens.
  *
- * The attention then reads the updated cache. Tokens at positions < 0 (more
- * queries than keys) are not written. Sequences rejected on the device
+ * The write runs in the plan kernel's grid (CTAs beyond the planning one, a
+ * warp per new token) while the plan is made, so it costs no launch of its
+ * own; the attention kernels then read the updated cache. Tokens at positions
+ * < 0 (more queries than keys) are not written. Sequences rejected on the device
  * (PATTN_ERR_DEVICE_BAD_INPUT) are neither written nor attended (rows zero).
  * k_new and v_new are caller-owned device buffers, 16-byte aligned; they must
  * not overlap kv_pool.
@@ -360,10 +362,12 @@ pattn_status pattn_profile_read(double *ms_plan, double *ms_attention, double *m
                                 int *calls);
 
 /*
- * The same record split by kernel: ms[0] plan, ms[1] cache write
- * (pattn_forward_append), ms[2] decode kernel, ms[3] prefill kernel, ms[4] time
- * after the attention kernels (the prefill split merge). ms holds 5 doubles.
- * Clears the record like pattn_profile_read.
+ * The same record split by kernel: ms[0] plan (with the cache write of
+ * pattn_forward_append, which runs in the plan's grid), ms[1] quantisation
+ * passes (pattn_forward_fp8qk, pattn_forward_fp8), ms[2] decode kernel, ms[3]
+ * prefill kernel, ms[4] time after the attention kernels (nothing runs there:
+ * both merge their own splits). ms holds 5 doubles. Clears the record like
+ * pattn_profile_read.
  */
 pattn_status pattn_profile_read_kernels(double *ms, int *calls);
 

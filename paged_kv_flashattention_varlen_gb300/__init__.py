@@ -319,7 +319,7 @@ def profile_enable(on: bool = True) -> None:
 
 
 def profile_read_kernels() -> Tuple[Tuple[float, float, float, float, float], int]:
-    """((ms plan, ms cache write, ms decode kernel, ms prefill kernel, ms after), calls)."""
+    """((ms plan with the cache write, ms quantisation, ms decode kernel, ms prefill kernel, ms after), calls)."""
     ms = (ctypes.c_double * 5)()
     n = ctypes.c_int()
     _check(_lib.load().pattn_profile_read_kernels(ms, ctypes.byref(n)), "pattn_profile_read_kernels")

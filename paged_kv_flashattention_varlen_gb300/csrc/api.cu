@@ -1,7 +1,7 @@
 // api.cu -- host side of libpattn: argument validation, per-device workspace,
-// TMA tensor-map encoding and the launch sequence plan -> (cache write,
-// quantisation) -> decode -> prefill (both attention kernels merge their own
-// split-KV partials).
+// TMA tensor-map encoding and the launch sequence plan (whose grid also writes
+// the new tokens' K/V rows for pattn_forward_append) -> (quantisation) ->
+// decode -> prefill (both attention kernels merge their own split-KV partials).
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -26,6 +26,7 @@ constexpr int kTargetHalfItemsPerSm = 4;
 constexpr int kTargetItemsCap = 512;
 constexpr int kMinChunk = 16;          // 64-key blocks per split, at least (split and merge cost more than short items save below this)
 constexpr int kProfileCap = 4096;
+constexpr int kPlanWarps = 32;         // warps of a plan-grid CTA (one new token each when writing)
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -297,9 +298,9 @@ ProfileRec take_events(DeviceState& st) {
   return r;
 }
 
-// Encodes the tensor maps and launches plan -> [cache write] -> [quantisation]
-// -> decode -> prefill with the workspace at `wsb` (laid out as L); the
-// attention kernels merge their own KV splits. Caller holds g_mu.
+// Encodes the tensor maps and launches plan (+ cache write in the same grid) ->
+// [quantisation] -> decode -> prefill with the workspace at `wsb` (laid out as
+// L); the attention kernels merge their own KV splits. Caller holds g_mu.
 pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* out, const void* q,
                         const void* kv, const int32_t* bt, const int32_t* seq_lens,
                         const int32_t* cu_q, int num_seqs, int total_q, int max_q, int max_kv,
@@ -401,6 +402,15 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   pp.dec_enabled = dec_enabled ? 1 : 0;
   pp.target_items = plan_target(st.sms);
   pp.min_chunk = kMinChunk;
+  if (k_new && mode != Mode::kPlanOnly) {
+    // the new tokens' K and V rows go into their cache slots from the plan
+    // grid's extra CTAs (a warp per token, at most two CTAs per SM), before any
+    // attention kernel reads the cache: those wait for the whole plan grid
+    pp.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    pp.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    pp.kv_pool = static_cast<__nv_bfloat16*>(const_cast<void*>(kv));
+    pp.write_ctas = std::min(cdiv(total_q, kPlanWarps), 2 * st.sms);
+  }
 
   AttnParams ap{};
   ap.items = ws.items;
@@ -448,25 +458,6 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   if (e != cudaSuccess) return PATTN_ERR_CUDA;
   if (mode == Mode::kPlanOnly) return PATTN_OK;
   if (prof) cudaEventRecord(rec.ev[1], stream);
-  if (k_new) {
-    // the new tokens' K and V rows into their cache slots, before any attention
-    // kernel reads the cache (which waits for this grid on the device)
-    KvWriteParams wp{};
-    wp.k_new = static_cast<const __nv_bfloat16*>(k_new);
-    wp.v_new = static_cast<const __nv_bfloat16*>(v_new);
-    wp.kv_pool = static_cast<__nv_bfloat16*>(const_cast<void*>(kv));
-    wp.block_table = bt;
-    wp.cu_q = cu_q;
-    wp.seq_info = ws.seq_info;
-    wp.err = ws.hdr + kHdrErr;
-    wp.num_seqs = num_seqs;
-    wp.total_q = total_q;
-    wp.bt_stride = pp.bt_stride;
-    wp.num_pages = num_pages;
-    wp.row_elems = hkv * d;
-    e = launch_kv_write(wp, st.sms, stream);
-    if (e != cudaSuccess) return PATTN_ERR_CUDA;
-  }
   if (mode != Mode::kBf16) {
     // e4m3 codes and scales of Q, of the smoothed K and of V (dependent launches)
     QuantParams qp{};

@@ -70,19 +70,13 @@ struct PlanParams {
   int causal;
   int target_items;     // items the split heuristic aims at (a multiple of the SM count)
   int min_chunk;        // fewest KV tiles per split
-};
-
-// Cache write of the new tokens' K and V rows (kvwrite.cu).
-struct KvWriteParams {
-  const __nv_bfloat16* k_new;   // [total_q][n_heads_kv][head_dim]
-  const __nv_bfloat16* v_new;   // [total_q][n_heads_kv][head_dim]
-  __nv_bfloat16* kv_pool;       // the cache (paged or contiguous layout)
-  const int32_t* block_table;   // nullptr: contiguous cache
-  const int32_t* cu_q;
-  const int4* seq_info;         // from the plan: (first token, ql or -1, L, first contiguous row)
-  int* err;
-  int num_seqs, total_q, bt_stride, num_pages;
-  int row_elems;                // n_heads_kv * head_dim
+  // cache write of the new tokens (pattn_forward_append): CTAs 1..write_ctas of
+  // the plan grid copy k_new / v_new [total_q][n_heads_kv][head_dim] into the
+  // pool while CTA 0 plans; write_ctas = 0 and null pointers otherwise
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* kv_pool;
+  int write_ctas;
 };
 
 // Preparation of the quantised variants (quant.cu). Layouts:
@@ -212,11 +206,11 @@ inline cudaError_t launch_kernel_pair(void (*kernel)(KArgs...), dim3 grid, dim3 
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// The plan grid: CTA 0 plans, CTAs 1..p.write_ctas write the new tokens' K/V rows.
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 // One warp waits on an mbarrier that nothing completes until the bounded wait
 // gives up and sets the timeout bit in *err (failure-detection self-test).
 cudaError_t launch_wait_selftest(int* err, cudaStream_t s);
-cudaError_t launch_kv_write(const KvWriteParams& p, int sms, cudaStream_t s);
 // Key sums and V maxima, then the K, V and Q codes that QuantParams asks for.
 cudaError_t launch_quant(const QuantParams& p, int sms, cudaStream_t s);
 // head_dim 128: `to` is the output map (bf16 [total_q][n_heads_q][128] as

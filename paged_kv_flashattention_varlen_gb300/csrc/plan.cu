@@ -20,6 +20,13 @@
 //   5. zero-fills the output rows of q tiles that see no key at all, and
 //      zeroes the finished-split counter of every split unit (the attention
 //      kernels merge a unit's partials in the CTA that finishes it last).
+//
+// With new tokens to cache (pattn_forward_append), the grid has more CTAs:
+// while CTA 0 plans, the others write the new tokens' K and V rows into their
+// cache slots, the `reshape_and_cache_flash` (kv_write) node that comes right
+// before `attend` in the GB10 model graph. The attention kernels wait for the
+// whole plan grid, so they read the updated cache, and no launch of its own
+// is spent on the write.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -106,6 +113,119 @@ __device__ __forceinline__ unsigned long long seq_blocks(const PlanParams& p, in
   return static_cast<unsigned long long>(keys / kPage + static_cast<long long>(nqt) * (bn / kPage) / 2 + 1);
 }
 
+// ---- cache write of the new tokens ----------------------------------------
+// Token i of sequence b (i < ql_b) is cache position L_b - ql_b + i, the same
+// bottom-right alignment the attention uses: slot pos / 64 of the block table
+// and row pos % 64 of that page, or row pos of the sequence in a contiguous
+// cache. A sequence the planner rejects is not written, so each writing warp
+// applies the planner's acceptance rules to the sequences of its tokens
+// itself (it cannot wait for CTA 0): query range inside [0, total_q] with
+// ql <= max_q, 0 <= L <= max_kv, and every live block-table entry inside the
+// pool (paged) or the sequence's rows inside the K/V planes (contiguous).
+struct SeqCheck {
+  int q0, q1, L;
+  long long row0;  // first row of the sequence in a contiguous cache
+  bool ok;
+};
+
+// One warp, same result in every lane.
+__device__ SeqCheck warp_check_seq(const PlanParams& p, int b) {
+  const unsigned full = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  SeqCheck c;
+  c.q0 = p.cu_q[b];
+  c.q1 = p.cu_q[b + 1];
+  c.L = p.seq_lens[b];
+  c.row0 = 0;
+  c.ok = c.q0 >= 0 && c.q1 >= c.q0 && c.q1 <= p.total_q && c.q1 - c.q0 <= p.max_q && c.L >= 0 &&
+         c.L <= p.max_kv;
+  if (!c.ok) return c;
+  if (p.block_table) {
+    const int np = cdiv(c.L, kPage);
+    const int32_t* row = p.block_table + static_cast<size_t>(b) * p.bt_stride;
+    bool bad = false;
+    for (int s = lane; s < np; s += 32) {
+      const int pg = row[s];
+      bad |= pg < 0 || pg >= p.num_pages;
+    }
+    c.ok = !__any_sync(full, bad);
+  } else {
+    // rows of the sequences before b (negative lengths count as zero, as in the plan)
+    long long sum = 0;
+    for (int i = lane; i < b; i += 32) sum += max(p.seq_lens[i], 0);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(full, sum, o);
+    c.row0 = sum;
+    c.ok = sum + c.L <= static_cast<long long>(p.num_pages);
+  }
+  return c;
+}
+
+// CTAs 1.. of the plan grid: one warp per run of consecutive tokens; each
+// token's K row and V row ([Hkv][D] each, contiguous) are copied with 16-byte
+// streaming loads, all loads of a chunk issued before its stores.
+__device__ void write_new_rows(const PlanParams& p) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (static_cast<int>(gridDim.x) - 1) * (kPlanThreads / 32);
+  const int w = (static_cast<int>(blockIdx.x) - 1) * (kPlanThreads / 32) + (threadIdx.x >> 5);
+  const int per = cdiv(p.total_q, warps);
+  const int t0 = w * per, t1 = min(p.total_q, t0 + per);
+  if (t0 >= t1) return;
+  // sequence of token t0: the last b with cu_q[b] <= t0 (each sequence found is
+  // checked below, so an out-of-order cu_q writes nothing)
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cu_q[mid] <= t0) lo = mid; else hi = mid - 1;
+  }
+  int b = lo, checked = -1;
+  SeqCheck c{};
+  const int row_elems = p.n_heads_kv * p.head_dim;
+  const int n16 = row_elems / 8;  // 16-byte chunks of one token's K (or V) row
+  for (int t = t0; t < t1; ++t) {
+    while (b + 1 < p.num_seqs && p.cu_q[b + 1] <= t) ++b;
+    if (b != checked) {
+      c = warp_check_seq(p, b);
+      checked = b;
+    }
+    if (!c.ok || t < c.q0 || t >= c.q1) continue;
+    const int pos = c.L - (c.q1 - c.q0) + (t - c.q0);
+    if (pos < 0) continue;  // more queries than keys: no slot for this token
+    size_t krow, vrow;      // element offsets of the destination rows
+    if (p.block_table) {
+      const int page = p.block_table[static_cast<size_t>(b) * p.bt_stride + pos / kPage];
+      krow = (static_cast<size_t>(page) * 2 * kPage + (pos % kPage)) * row_elems;
+      vrow = krow + static_cast<size_t>(kPage) * row_elems;
+    } else {
+      krow = static_cast<size_t>(c.row0 + pos) * row_elems;
+      vrow = krow + static_cast<size_t>(p.num_pages) * row_elems;
+    }
+    const uint4* ks = reinterpret_cast<const uint4*>(p.k_new + static_cast<size_t>(t) * row_elems);
+    const uint4* vs = reinterpret_cast<const uint4*>(p.v_new + static_cast<size_t>(t) * row_elems);
+    uint4* kd = reinterpret_cast<uint4*>(p.kv_pool + krow);
+    uint4* vd = reinterpret_cast<uint4*>(p.kv_pool + vrow);
+    for (int j0 = 0; j0 < n16; j0 += 4 * 32) {
+      uint4 kv[4], vv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * 32 + lane;
+        if (j < n16) {
+          kv[u] = __ldcs(ks + j);
+          vv[u] = __ldcs(vs + j);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * 32 + lane;
+        if (j < n16) {
+          kd[j] = kv[u];
+          vd[j] = vv[u];
+        }
+      }
+    }
+  }
+}
+
 constexpr int kSmemSeqs = 4096;   // sequences whose q-tile prefix is kept in shared memory
 constexpr int kCacheSeqs = 1024;  // sequences whose plan is kept in shared memory
 
@@ -131,8 +251,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   auto part_at = [&](int b) -> int { return b < kCacheSeqs ? s_part[b] : ws.seq_part[b]; };
 
   // The attention kernels launched after this one may set themselves up now;
-  // they read nothing of the plan before the plan grid has completed.
+  // they read nothing of the plan (nor the cache) before the plan grid has completed.
   grid_dep_launch();
+  if (blockIdx.x > 0) {
+    write_new_rows(p);
+    return;
+  }
   if (threadIdx.x == 0) {
     s_tiles[0] = s_tiles[1] = 0ull;
     s_carry[0] = s_carry[1] = s_carry[2] = s_carry[3] = 0;
@@ -418,7 +542,7 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(int* err) {
 
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  plan_kernel<<<1 + p.write_ctas, kPlanThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
