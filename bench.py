@@ -1,14 +1,26 @@
 #!/usr/bin/env python3
 """Benchmark of paged-KV varlen attention on GB300: one JSON line on stdout.
 
-A step is one pattn_forward call over one batch: the device plan, the fused
-attention kernel (page gather, QK^T, mask, online softmax, PV, epilogue) and
-the split-KV combine. The headline workload is the pure decode batch (64
-sequences x 1 query token, KV lengths uniform in [1024, 8192], 32 query / 8
-KV heads, head dim 128, pages of 64 shuffled over the pool); its metric is
-KV GB/s (live K and V rows once per KV head, plus Q and O). The causal
-prefill batch (4 x 8192 tokens, same heads) is reported alongside as
-attention TFLOP/s. Inputs are seeded synthetic data (numpy PCG64, bf16).
+A step is one pattn_forward call over one batch: the device plan and the
+attention kernels (page gather, QK^T, mask, online softmax, PV, epilogue, and
+the in-kernel merge of split-KV partials). Inputs are seeded synthetic data
+(numpy PCG64, bf16), resident in HBM before any timed region.
+
+Headline: the pure decode batch (64 sequences x 1 query token, KV lengths
+uniform in [1024, 8192], 32 query / 8 KV heads, head dim 128, pages of 64
+shuffled over the pool), metric KV GB/s (live K and V rows once per KV head,
+plus Q and O). `value` and `ms_per_step` time exactly `--steps` steps between
+one CUDA event pair.
+
+Every named workload (the tiny paged decode, the decode batch, the causal
+4 x 8192 prefill, the non-causal 37,810-token batch and the mixed batch) then
+gets one interleaved timing pass (`measure`) under its own clock record: plain
+steps (each in its own event pair, for the step-time distribution) alternate
+with steps that carry the library's per-launch events, so the attention-kernel
+times and the step times of an entry come from the same pass and clocks. The
+line's `roofline` is the decode kernel's, from that pass on the headline batch;
+`workloads` holds all five entries, each with its roofline (HBM, tensor, or
+both for the mixed batch) and the float64 oracle's time on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -49,7 +61,12 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--prefill-steps", type=int, default=30)
+    ap.add_argument("--prefill-steps", type=int, default=0,
+                    help="cap on the steps of each named workload's interleaved pass (0: by --workload-seconds)")
+    ap.add_argument("--workload-seconds", type=float, default=1.0,
+                    help="seconds of the interleaved timing pass of each named workload")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="headline only: skip the other named workloads")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -149,51 +166,151 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------- our arm
-def profiled_pass(pk, step, steps):
-    """Per-kernel device times: a second pass with the library's launch events on
-    (the events add a little time per call, so the headline pass runs without)."""
+def _events(n):
     import torch
-    torch.cuda.synchronize()
-    pk.profile_read()
-    pk.profile_enable(True)
-    for _ in range(steps):
-        step()
-    torch.cuda.synchronize()
-    pk.profile_enable(False)
-    return pk.profile_read()
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
 
 
-def step_stats(step, steps):
-    """Distribution of single-step device times (ms): a separate pass with a CUDA
-    event pair around every step on the launching stream."""
+def _stats(t):
     import numpy as np
-    import torch
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, b in ev:
-        a.record()
-        step()
-        b.record()
-    torch.cuda.synchronize()
-    t = np.array([a.elapsed_time(b) for a, b in ev])
+    t = np.asarray(t, dtype=np.float64)
     q = np.percentile(t, [50, 90, 95, 99])
-    return {"count": int(steps), "mean": round(float(t.mean()), 5), "p50": round(float(q[0]), 5),
+    return {"count": int(t.size), "mean": round(float(t.mean()), 5), "p50": round(float(q[0]), 5),
             "p90": round(float(q[1]), 5), "p95": round(float(q[2]), 5), "p99": round(float(q[3]), 5),
             "min": round(float(t.min()), 5), "max": round(float(t.max()), 5)}
 
 
-def profiled_kernels(pk, step, steps):
-    """As :func:`profiled_pass`, split by kernel: ((plan, cache write, decode,
-    prefill, after) ms summed over the calls, calls)."""
+def measure(pk, step, seconds, device_index, flush=None, max_steps=0):
+    """One interleaved timing pass of a workload, under one clock record.
+
+    Blocks of plain steps and blocks of profiled steps alternate (the library's
+    per-launch CUDA events on in the latter; those events turn the dependent-
+    launch overlap off, so they are kept out of the plain steps). Every step
+    has its own CUDA event pair on the launching stream; `flush` (a write of
+    twice the L2 size) runs before each step, outside the pair. Returns the
+    plain steps' time distribution, the profiled steps' mean and the per-kernel
+    device times of the profiled steps, all from the same pass, so that each
+    kernel time is part of a step timed under the same clocks."""
     import torch
-    torch.cuda.synchronize()
-    pk.profile_read()
-    pk.profile_enable(True)
-    for _ in range(steps):
+    for _ in range(3):
+        if flush:
+            flush()
         step()
     torch.cuda.synchronize()
-    pk.profile_enable(False)
-    return pk.profile_read_kernels()
+    (a, b), = _events(1)
+    if flush:
+        flush()
+    a.record()
+    step()
+    b.record()
+    torch.cuda.synchronize()
+    est_ms = max(a.elapsed_time(b), 1e-3)
+    total = max(4, int(seconds * 1e3 / est_ms))
+    if max_steps > 0:
+        total = max(2, min(total, max_steps))
+    total = min(total, 8000)  # the library keeps at most 4096 profiled calls
+    half = max(1, min(500, int(50.0 / est_ms), total // 2))
+    blocks = max(1, total // (2 * half))
+    pk.profile_read()
+    sampler = ClockSampler(device_index)
+    time.sleep(0.25)
+    plain, prof = [], []
+    for _ in range(blocks):
+        for profiled in (False, True):
+            evs = _events(half)
+            pk.profile_enable(profiled)
+            for x, y in evs:
+                if flush:
+                    flush()
+                x.record()
+                step()
+                y.record()
+            pk.profile_enable(False)
+            torch.cuda.synchronize()
+            (prof if profiled else plain).extend(x.elapsed_time(y) for x, y in evs)
+    clocks = sampler.stop()
+    kt, calls = pk.profile_read_kernels()
+    n = max(calls, 1)
+    kernel_ms = {"plan": kt[0] / n, "cache_write_or_quant": kt[1] / n, "decode": kt[2] / n,
+                 "prefill": kt[3] / n, "after": kt[4] / n}
+    return {"plain": plain, "profiled_ms_per_step": sum(prof) / max(len(prof), 1),
+            "kernel_ms": kernel_ms, "calls": calls, "clocks": clocks}
+
+
+def launches_per_step(wl) -> int:
+    """Kernels pattn_forward launches for this batch: the plan, the decode kernel
+    when the GQA group fits its 16 rows, the prefill kernel when some unit may
+    hold more than 16 packed rows."""
+    g = wl.n_heads_q // wl.n_heads_kv
+    dec = g <= 16
+    pre = (not dec) or wl.max_q * g > 16
+    return 1 + int(dec) + int(pre)
+
+
+KERNEL_NAMES = {1: "attn_kernel<256,64> (head_dim 256, one CTA; the decode kernel launches empty)",
+                2: "decode_kernel<128> (swap-AB)",
+                3: "attn_kernel<128,128>",
+                4: "attn_kernel<128,128>",
+                5: "decode_kernel<256> then attn_kernel<256,128,pair> (cta_group::2)"}
+L2_NOTES = {1: "cold L2: a %d MB buffer written before every step, outside its events",
+            2: "inputs larger than L2 (KV pool %.2f GB > 129 MB)",
+            3: "inputs larger than L2 (KV pool %.2f GB > 129 MB)",
+            4: "inputs larger than L2 (K/V planes %.2f GB > 129 MB)",
+            5: "inputs larger than L2 (KV pool %.2f GB > 129 MB)"}
+L2_FLUSH_BYTES = 2 * 129 * 1000 * 1000
+
+
+def workload_entry(idx, wl, meas, pk_peaks, peak_kind):
+    """Step time, attention-kernel time and the roofline of SURVEY-style
+    accounting for one named workload: HBM for the decode batches, tensor for
+    the prefill batches, max(bytes / BW, FLOPs / peak) for the mixed batch."""
+    flops = 4.0 * wl.head_dim * wl.n_heads_q * wl.visible_pairs()
+    nbytes = wl.kv_bytes() + wl.qo_bytes()
+    km = meas["kernel_ms"]
+    t_attn = km["decode"] + km["prefill"]
+    hbm = float(pk_peaks["hbm_gbs"])
+    tc = float(pk_peaks["bf16_tflops"])
+    tcs = float(pk_peaks.get("bf16_tflops_sustained", tc))
+    st = _stats(meas["plain"])
+    if idx in (1, 2):
+        ach = nbytes / (t_attn * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                "nominal_frac": round(ach / NOMINAL_HBM_GBS, 4),
+                "algorithmic_bytes_per_launch": nbytes}
+    elif idx in (3, 4):
+        ach = flops / (t_attn * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": tcs, "unit": "TFLOP/s",
+                "frac": round(ach / tcs, 4),
+                "peak_source": f"{peak_kind} bf16_tflops_sustained (the kernel loops for seconds)",
+                "frac_of_burst_peak": round(ach / tc, 4), "burst_peak": tc,
+                "nominal_frac": round(ach / NOMINAL_BF16_TFLOPS, 4), "algorithmic_flops_per_launch": flops}
+    else:
+        t_bw = nbytes / (hbm * 1e9) * 1e3
+        t_tc = flops / (tcs * 1e12) * 1e3
+        roof = {"bound": "hbm+tensor", "frac": round(max(t_bw, t_tc) / t_attn, 4),
+                "hbm_component": {"achieved": round(nbytes / (t_attn * 1e-3) / 1e9, 1), "peak": hbm,
+                                  "unit": "GB/s", "frac": round(t_bw / t_attn, 4), "roofline_ms": round(t_bw, 5)},
+                "tensor_component": {"achieved": round(flops / (t_attn * 1e-3) / 1e12, 1), "peak": tcs,
+                                     "unit": "TFLOP/s", "frac": round(t_tc / t_attn, 4),
+                                     "roofline_ms": round(t_tc, 5)},
+                "frac_of_burst_tensor_peak": round(max(t_bw, flops / (tc * 1e12) * 1e3) / t_attn, 4),
+                "peak_source": f"{peak_kind} hbm_gbs and bf16_tflops_sustained",
+                "algorithmic_bytes_per_launch": nbytes, "algorithmic_flops_per_launch": flops}
+    roof.update({"kernel": KERNEL_NAMES[idx], "kernel_ms": round(t_attn, 5),
+                 "decode_kernel_ms": round(km["decode"], 5), "prefill_kernel_ms": round(km["prefill"], 5),
+                 "plan_ms": round(km["plan"], 5), "profiled_ms_per_step": round(meas["profiled_ms_per_step"], 5),
+                 "source": "kernel_ms, profiled_ms_per_step and ms_per_step come from one interleaved pass "
+                           "(alternating plain and profiled blocks under one clock record)"})
+    if idx == 1:
+        l2 = L2_NOTES[1] % (L2_FLUSH_BYTES // 1000000)
+    else:
+        l2 = L2_NOTES[idx] % (wl.kv_pool.numel() * 2 / 1e9)
+    return {"workload": wl.name, "ms_per_step": st["mean"], "step_ms_stats": st,
+            "kv_gbs_step": round(nbytes / (st["mean"] * 1e-3) / 1e9, 1),
+            "tflops_step": round(flops / (st["mean"] * 1e-3) / 1e12, 1),
+            "roofline": roof, "clocks": meas["clocks"], "l2": l2,
+            "gpu_launches_per_step": launches_per_step(wl)}
 
 
 def headline_config(workloads, wl, world: int) -> dict:
@@ -204,6 +321,41 @@ def headline_config(workloads, wl, world: int) -> dict:
             "causal": wl.causal, "kv_bytes_per_step": wl.kv_bytes(),
             "l2": "inputs larger than L2 (KV pool %.2f GB > 129 MB)" % (wl.kv_pool.numel() * 2 / 1e9),
             "parallelism": f"weak x{world}: one batch per GPU, no collective"}
+
+
+def _device_inputs(wl, dev):
+    bt = None if wl.block_table is None else wl.block_table.to(dev)
+    return wl.q.to(dev), wl.kv_pool.to(dev), bt, wl.seq_lens.to(dev), wl.cu_q.to(dev)
+
+
+def _forward_step(pk, wl, q, kv, bt, sl, cu, out):
+    def step():
+        pk.forward(out, q, kv, bt, sl, cu, max_q=wl.max_q, max_kv=wl.max_kv,
+                   n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
+                   num_pages=wl.num_pages, check=False)
+    return step
+
+
+def run_named(pk, workloads, idx, dev, local, seconds, max_steps, pk_peaks, peak_kind, oracle_s):
+    """Measure one named workload (and time the oracle on it when oracle_s > 0)."""
+    import torch
+    wl = workloads.named(idx)
+    q, kv, bt, sl, cu = _device_inputs(wl, dev)
+    out = torch.empty_like(q)
+    flush = None
+    if idx == 1:
+        buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        flush = lambda: buf.fill_(1)  # noqa: E731
+    meas = measure(pk, _forward_step(pk, wl, q, kv, bt, sl, cu, out), seconds, local, flush, max_steps)
+    entry = workload_entry(idx, wl, meas, pk_peaks, peak_kind)
+    entry["device_status"] = pk.device_status()
+    if idx in (2, 3):
+        entry["roofline"]["traffic"] = ncu_traffic("decode" if idx == 2 else "prefill")
+    del q, kv, bt, sl, cu, out
+    torch.cuda.empty_cache()
+    if oracle_s > 0:
+        entry["oracle"] = oracle_time(idx, wl, entry["ms_per_step"])
+    return entry
 
 
 def run_ours(args):
@@ -226,22 +378,17 @@ def run_ours(args):
     pk._lib.load()
     pk_peaks, peak_kind = peaks()
     if args.only == "prefill":
-        res = run_prefill(args, pk, workloads, dev, world, pk_peaks, peak_kind)
+        res = run_named(pk, workloads, PREFILL, dev, local, args.workload_seconds, args.prefill_steps,
+                        pk_peaks, peak_kind, 0)
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
 
-    # ---- decode batch (headline)
+    # ---- decode batch (headline): exactly `steps` steps between one event pair
     wl = workloads.named(DECODE) if rank == 0 else _reseeded(workloads, DECODE, rank)
-    q, kv = wl.q.to(dev), wl.kv_pool.to(dev)
-    bt, sl, cu = wl.block_table.to(dev), wl.seq_lens.to(dev), wl.cu_q.to(dev)
+    q, kv, bt, sl, cu = _device_inputs(wl, dev)
     out = torch.empty_like(q)
-
-    def step():
-        pk.forward(out, q, kv, bt, sl, cu, max_q=wl.max_q, max_kv=wl.max_kv,
-                   n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
-                   num_pages=wl.num_pages, check=False)
-
+    step = _forward_step(pk, wl, q, kv, bt, sl, cu, out)
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -261,33 +408,24 @@ def run_ours(args):
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1)
     ms_max = pdist.max_over_ranks(ms, dev if world > 1 else None)
-    t_plan, t_attn, t_comb, calls = profiled_pass(pk, step, min(args.steps, 500))
-    stats = step_stats(step, min(args.steps, 500))
     status = pk.device_status()
     step_bytes = wl.kv_bytes() + wl.qo_bytes()
     ms_step = ms_max / args.steps
     value = world * step_bytes * args.steps / (ms_max * 1e-3) / 1e9
-    attn_ms = t_attn / max(calls, 1)
-    achieved = step_bytes / (attn_ms * 1e-3) / 1e9
-    hbm = float(pk_peaks["hbm_gbs"])
-    traffic = ncu_traffic("decode")
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": traffic,
-                "peak_source": f"{peak_kind} hbm_gbs", "nominal_frac": round(achieved / NOMINAL_HBM_GBS, 4),
-                "kernel": "decode_kernel<128> (swap-AB)", "kernel_ms": round(attn_ms, 5),
-                "share": {"plan": round(t_plan / max(t_plan + t_attn + t_comb, 1e-9), 4),
-                          "attention": round(t_attn / max(t_plan + t_attn + t_comb, 1e-9), 4),
-                          "combine": round(t_comb / max(t_plan + t_attn + t_comb, 1e-9), 4)},
-                "algorithmic_bytes_per_launch": step_bytes}
+
+    # ---- the decode kernel's roofline: an interleaved pass of the same batch
+    meas = measure(pk, step, args.workload_seconds, local)
+    head_entry = workload_entry(DECODE, wl, meas, pk_peaks, peak_kind)
+    roofline = dict(head_entry["roofline"])
+    roofline.update({"traffic": ncu_traffic("decode"), "pass_ms_per_step": head_entry["ms_per_step"],
+                     "pass_clocks": meas["clocks"], "pass_steps": len(meas["plain"]) + meas["calls"]})
 
     # ---- end to end through the host-buffer entry point (pinned memory)
     e2e = None
     if args.e2e_steps > 0:
         e2e = run_e2e(args, pk, wl, dev, world, step_bytes)
-
-    # ---- causal prefill (secondary)
-    prefill = None if args.only == "decode" else run_prefill(args, pk, workloads, dev, world,
-                                                              pk_peaks, peak_kind)
+    del q, kv, bt, sl, cu, out
+    torch.cuda.empty_cache()
 
     line = {
         "metric": HEADLINE_METRIC,
@@ -295,12 +433,26 @@ def run_ours(args):
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": headline_config(workloads, wl, world),
-        "roofline": roofline, "step_ms_stats": stats, "e2e": e2e, "gpu_launches": int(2 * args.steps),
-        "clocks": clocks,
-        "device_status": status, "prefill": prefill,
+        "roofline": roofline, "step_ms_stats": head_entry["step_ms_stats"], "e2e": e2e,
+        "gpu_launches": int(launches_per_step(wl) * args.steps),
+        "clocks": clocks, "device_status": status,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        head_entry["oracle"] = {"ms_per_step": round(line["cpu_baseline"]["ms_per_pass"], 3),
+                                "kind": "oracle, full passes", "cores": line["cpu_baseline"]["cores"],
+                                "gpu_speedup": round(line["cpu_baseline"]["ms_per_pass"] / head_entry["ms_per_step"], 1)}
+    del wl
+
+    # ---- the other named workloads (one GPU run only): same interleaved pass each
+    if world == 1 and not args.no_workloads and args.only is None:
+        entries = {}
+        for idx in (1, 3, 4, 5):
+            e = run_named(pk, workloads, idx, dev, local, args.workload_seconds, args.prefill_steps,
+                          pk_peaks, peak_kind, 0 if args.no_cpu_baseline else 1)
+            entries[workloads.NAMES[idx - 1]] = e
+        entries[workloads.NAMES[DECODE - 1]] = head_entry
+        line["workloads"] = {workloads.NAMES[i - 1]: entries[workloads.NAMES[i - 1]] for i in (1, 2, 3, 4, 5)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -337,7 +489,6 @@ def run_e2e(args, pk, wl, dev, world, step_bytes):
     return e2e
 
 
-
 def _reseeded(workloads, index, rank):
     import numpy as np
     # same shape, other values: another rank's batch
@@ -348,50 +499,6 @@ def _reseeded(workloads, index, rank):
                                 lens.tolist(), base.n_heads_q, base.n_heads_kv, base.head_dim,
                                 base.page_size, scale=base.scale, causal=base.causal,
                                 extra_pages=base.num_pages - int(np.sum(-(-lens // 64))))
-
-
-def run_prefill(args, pk, workloads, dev, world, pk_peaks, peak_kind):
-    import torch
-    from paged_kv_flashattention_varlen_gb300 import dist as pdist
-    wl = workloads.named(PREFILL)
-    q, kv = wl.q.to(dev), wl.kv_pool.to(dev)
-    bt, sl, cu = wl.block_table.to(dev), wl.seq_lens.to(dev), wl.cu_q.to(dev)
-    out = torch.empty_like(q)
-
-    def step():
-        pk.forward(out, q, kv, bt, sl, cu, max_q=wl.max_q, max_kv=wl.max_kv,
-                   n_heads_kv=wl.n_heads_kv, scale=wl.scale, causal=wl.causal,
-                   num_pages=wl.num_pages, check=False)
-
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    pdist.barrier(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.prefill_steps):
-        step()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = pdist.max_over_ranks(e0.elapsed_time(e1), dev if world > 1 else None)
-    t_plan, t_attn, t_comb, calls = profiled_pass(pk, step, args.prefill_steps)
-    stats = step_stats(step, args.prefill_steps)
-    flops = 4.0 * wl.head_dim * wl.n_heads_q * wl.visible_pairs()
-    attn_ms = t_attn / max(calls, 1)
-    achieved = flops / (attn_ms * 1e-3) / 1e12
-    peak = float(pk_peaks["bf16_tflops"])
-    return {
-        "workload": workloads.NAMES[PREFILL - 1], "metric": "causal prefill attention TFLOP/s",
-        "value": round(world * flops * args.prefill_steps / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-        "steps": args.prefill_steps, "ms_per_step": round(ms / args.prefill_steps, 4),
-        "flops_per_step": flops,
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": ncu_traffic("prefill"), "peak_source": f"{peak_kind} bf16_tflops (burst)",
-                     "nominal_frac": round(achieved / NOMINAL_BF16_TFLOPS, 4),
-                     "kernel": "attn_kernel<128,128>", "kernel_ms": round(attn_ms, 4)},
-        "step_ms_stats": stats, "gpu_launches": int(3 * args.prefill_steps),
-    }
 
 
 # --------------------------------------------------------------------- oracle (CPU)
@@ -412,7 +519,52 @@ def cpu_baseline(wl, seconds: float):
     return {"value": round(bytes_per_pass * reps / el / 1e9, 4), "unit": "GB/s", "cores": n_threads,
             "kind": "oracle",
             "sample": f"{reps} full pass(es) of the 64-sequence decode batch in {el:.1f} s "
-                      f"(float64 C, {n_threads} threads)"}
+                      f"(float64 C, {n_threads} threads)",
+            "ms_per_pass": el * 1e3 / reps}
+
+
+def _strided(first, end, n):
+    """n rows spread evenly over [first, end): the oracle's cost per row grows
+    along a causal sequence, so an even spread keeps the mean unbiased."""
+    import numpy as np
+    stride = max(1, (end - first) // max(n, 1))
+    return list(range(first + stride // 2, end, stride))
+
+
+def oracle_time(idx, wl, gpu_ms):
+    """The float64 oracle as it stands on the host cores, on one named workload:
+    whole passes of the tiny decode; the mixed batch's decode rows in full with
+    its chunk rows sampled; 1024 (causal prefill) or 128 (non-causal) evenly
+    spread query rows x all heads of the prefill batches. Sampled parts are
+    extrapolated linearly per row (output rows are independent)."""
+    import oracle
+    n_threads = oracle.threads()
+    total = wl.total_q
+
+    def timed(rows):
+        t0 = time.perf_counter()
+        oracle.forward_workload(wl, rows=rows, n_threads=n_threads)
+        return time.perf_counter() - t0
+
+    if idx == 1:
+        el = min(timed(None) for _ in range(5))
+        ms, kind = el * 1e3, "full pass (best of 5)"
+    elif idx == 5:
+        qls = wl.q_lens()
+        n_dec = int((qls == 1).sum())
+        t_dec = timed(list(range(n_dec)))
+        rows = _strided(n_dec, total, 512)
+        t_chunk = timed(rows) * (total - n_dec) / len(rows)
+        ms = (t_dec + t_chunk) * 1e3
+        kind = (f"decode rows in full ({t_dec * 1e3:.1f} ms); chunk rows extrapolated from {len(rows)} "
+                f"of {total - n_dec} evenly spread rows ({t_chunk * 1e3:.1f} ms)")
+    else:
+        n = 1024 if idx == 3 else 128
+        rows = _strided(0, total, n)
+        ms = timed(rows) * total / len(rows) * 1e3
+        kind = f"extrapolated from {len(rows)} of {total} evenly spread query rows x all heads"
+    return {"ms_per_step": round(ms, 3), "kind": kind, "cores": n_threads,
+            "gpu_speedup": round(ms / gpu_ms, 1)}
 
 
 def run_reference(args):
@@ -495,58 +647,47 @@ def run_workloads(args):
 
         flops = 4.0 * wl.head_dim * wl.n_heads_q * wl.visible_pairs()
         nbytes = wl.kv_bytes() + wl.qo_bytes()
-        for _ in range(3):
-            step()
-        torch.cuda.synchronize()
-        est = 1e-3 * max(flops / 9e14, nbytes / 6e12, 2e-5) * 1e3
-        steps = max(5, min(2000, int(1.0 / max(est, 1e-6))))
-        if args.workload_steps > 0:
-            steps = min(steps, args.workload_steps)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(steps):
-            step()
-        e1.record()
-        torch.cuda.synchronize()
-        kt, calls = profiled_kernels(pk, step, min(steps, 500))
-        t_plan, t_write, t_attn, t_comb = kt[0], kt[1], kt[2] + kt[3], kt[4]
-        ms = e0.elapsed_time(e1) / steps
-        attn_ms = t_attn / max(calls, 1)
+        meas = measure(pk, step, args.workload_seconds, 0, None, args.workload_steps)
+        km = meas["kernel_ms"]
+        t_write = km["cache_write_or_quant"]
+        attn_ms = km["decode"] + km["prefill"]
+        st = _stats(meas["plain"])
+        ms = st["mean"]
         line = {
-            "workload": workloads.NAMES[i - 1], "steps": steps, "ms_per_step": round(ms, 5),
+            "workload": workloads.NAMES[i - 1], "steps": st["count"], "ms_per_step": round(ms, 5),
             "kv_gbs_step": round(nbytes / (ms * 1e-3) / 1e9, 1),
             "tflops_step": round(flops / (ms * 1e-3) / 1e12, 1),
             "attention_kernels_ms": round(attn_ms, 5),
             "hbm_frac_attention": round(nbytes / (attn_ms * 1e-3) / 1e9 / hbm, 4),
             "tensor_frac_attention": round(flops / (attn_ms * 1e-3) / 1e12 / tc, 4),
-            "plan_ms": round(t_plan / max(calls, 1), 5), "combine_ms": round(t_comb / max(calls, 1), 5),
-            "decode_kernel_ms": round(kt[2] / max(calls, 1), 5),
-            "prefill_kernel_ms": round(kt[3] / max(calls, 1), 5),
+            "plan_ms": round(km["plan"], 5), "combine_ms": round(km["after"], 5),
+            "decode_kernel_ms": round(km["decode"], 5),
+            "prefill_kernel_ms": round(km["prefill"], 5),
+            "profiled_ms_per_step": round(meas["profiled_ms_per_step"], 5),
             "bytes": nbytes, "flops": flops, "peaks": f"{peak_kind}: hbm {hbm} GB/s, bf16 {tc} TFLOP/s",
-            "device_status": pk.device_status(),
+            "clocks": meas["clocks"], "device_status": pk.device_status(),
         }
         if args.fp8qk:
             # QK on e4m3 tensor cores (twice the bf16 rate), PV in bf16: the tensor
             # roofline time is 0.75 of the bf16 one; the quantisation passes are
-            # the "cache write" slot of the per-kernel record
+            # the quantisation slot of the per-kernel record
             line["workload"] += "+fp8qk"
-            line["quant_ms"] = round(t_write / max(calls, 1), 5)
+            line["quant_ms"] = round(t_write, 5)
             line["tensor_frac_attention_fp8qk_roofline"] = round(
                 flops / (attn_ms * 1e-3) / 1e12 / (tc / 0.75), 4)
         if args.fp8:
             # QK and PV on e4m3 tensor cores: half the bf16 roofline time
             line["workload"] += "+fp8"
-            line["quant_ms"] = round(t_write / max(calls, 1), 5)
+            line["quant_ms"] = round(t_write, 5)
             line["tensor_frac_attention_fp8_roofline"] = round(
                 flops / (attn_ms * 1e-3) / 1e12 / (2 * tc), 4)
         if args.append:
-            # K and V rows of every query token read once and written once
+            # K and V rows of every query token read once and written once, by the
+            # plan grid's extra CTAs while the plan is made (inside plan_ms)
             wbytes = 4 * int(wl.q.shape[0]) * wl.n_heads_kv * wl.head_dim * 2
-            write_ms = t_write / max(calls, 1)
             line["workload"] += "+kv_write"
-            line["kv_write_ms"] = round(write_ms, 5)
             line["kv_write_bytes"] = wbytes
-            line["kv_write_hbm_frac"] = round(wbytes / (write_ms * 1e-3) / 1e9 / hbm, 4)
+            line["kv_write"] = "in the plan grid (plan_ms includes it); no launch of its own"
         print(json.dumps(line), flush=True)
         del q, kv, bt, sl, cu, out
         torch.cuda.empty_cache()
