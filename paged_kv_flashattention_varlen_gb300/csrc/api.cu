@@ -395,6 +395,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   pp.head_dim = d;
   pp.tokens_per_tile = T;
   pp.block_n = sh.block_n;
+  pp.block_n_shift = sh.block_n == 128 ? 7 : 6;
   pp.pair = sh.pair ? 1 : 0;
   pp.bt_stride = std::max(1, cdiv(max_kv, kPage));
   pp.num_pages = num_pages;
@@ -443,10 +444,11 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     rec = take_events(st);
     cudaEventRecord(rec.ev[0], stream);
   }
-  // The plan is launched in stream order (it rewrites the workspace that the
-  // previous call's kernels read); each later kernel is a dependent launch that
-  // sets itself up while its predecessor finishes and waits for it on the device.
-  // Profiling events between the launches turn that overlap off.
+  // Every kernel is a dependent launch: it may become resident while its
+  // predecessor in the stream finishes, and waits for it on the device before
+  // reading anything (the plan rewrites the workspace that the previous call's
+  // kernels read, so it too waits for the whole previous grid). Profiling
+  // events between the launches turn that overlap off.
   const bool dep = !prof;
   cudaError_t e = cudaSuccess;
   if (mode != Mode::kBf16 && mode != Mode::kPlanOnly) {
@@ -454,7 +456,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
     e = cudaMemsetAsync(qb->scratch, 0, quant_zero_bytes(num_seqs, hkv, d), stream);
     if (e != cudaSuccess) return PATTN_ERR_CUDA;
   }
-  e = launch_plan(pp, stream);
+  e = launch_plan(pp, stream, dep);
   if (e != cudaSuccess) return PATTN_ERR_CUDA;
   if (mode == Mode::kPlanOnly) return PATTN_OK;
   if (prof) cudaEventRecord(rec.ev[1], stream);

@@ -17,6 +17,9 @@ constexpr int kTmemCols = 512;
 constexpr int kHistBuckets = 1024;  // cost buckets of the longest-first order, per item list
 constexpr int kDecRows = 16;        // packed query rows a swap-AB decode item holds
 constexpr int kDecBlockN = 128;     // keys per KV tile of the decode kernel
+constexpr int kDecBlockNShift = 7;
+constexpr int kPageShift = 6;
+static_assert(kDecBlockN == 1 << kDecBlockNShift && kPage == 1 << kPageShift, "tile shifts");
 constexpr int kMaxSplits = 64;
 
 // Bits of the device error word.
@@ -64,6 +67,7 @@ struct PlanParams {
   int n_heads_q, n_heads_kv, group, head_dim;
   int tokens_per_tile;  // T = kBM / group
   int block_n;          // keys per KV tile of the prefill kernel
+  int block_n_shift;    // log2(block_n)
   int pair;             // prefill items of two q tiles (CTA-pair kernel)
   int dec_enabled;      // group <= kDecRows: units of <= kDecRows packed rows go to the decode kernel
   int bt_stride, num_pages;
@@ -207,7 +211,9 @@ inline cudaError_t launch_kernel_pair(void (*kernel)(KArgs...), dim3 grid, dim3 
 }
 
 // The plan grid: CTA 0 plans, CTAs 1..p.write_ctas write the new tokens' K/V rows.
-cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
+// With `dependent` it may become resident while the previous grid in the stream
+// runs (it waits for that grid on the device before reading anything).
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s, bool dependent);
 // One warp waits on an mbarrier that nothing completes until the bounded wait
 // gives up and sets the timeout bit in *err (failure-detection self-test).
 cudaError_t launch_wait_selftest(int* err, cudaStream_t s);

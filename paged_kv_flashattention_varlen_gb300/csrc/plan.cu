@@ -42,6 +42,12 @@ __device__ __forceinline__ bool is_decode(const PlanParams& p, int ql) {
   return p.dec_enabled && ql >= 1 && ql * p.group <= kDecRows;
 }
 
+// log2 of the keys per KV tile of the kernel a unit of ql queries goes to (the
+// tile sizes are powers of two, so tile counts are shifts, not divisions).
+__device__ __forceinline__ int tile_shift(const PlanParams& p, int ql) {
+  return is_decode(p, ql) ? kDecBlockNShift : p.block_n_shift;
+}
+
 // Visible KV tiles of q tile qt: keys [0, kv_hi), kv_hi the largest limit of its rows.
 __device__ __forceinline__ int qtile_kv_tiles(const PlanParams& p, int ql, int L, int qt) {
   int hi = L;
@@ -49,14 +55,26 @@ __device__ __forceinline__ int qtile_kv_tiles(const PlanParams& p, int ql, int L
     const int last_tok = min(ql, (qt + 1) * p.tokens_per_tile);
     hi = min(L, L - ql + last_tok);
   }
-  const int bn = is_decode(p, ql) ? kDecBlockN : p.block_n;
-  return hi > 0 ? cdiv(hi, bn) : 0;
+  const int sh = tile_shift(p, ql);
+  return hi > 0 ? (hi + (1 << sh) - 1) >> sh : 0;
 }
 
 // Work of a q tile in 64-key blocks (comparable across the two kernels' tile sizes).
 __device__ __forceinline__ int qtile_blocks(const PlanParams& p, int ql, int L, int qt) {
-  const int bn = is_decode(p, ql) ? kDecBlockN : p.block_n;
-  return qtile_kv_tiles(p, ql, L, qt) * (bn / kPage);
+  return qtile_kv_tiles(p, ql, L, qt) << (tile_shift(p, ql) - kPageShift);
+}
+
+// Warp sum of a 64-bit count: two single-instruction 32-bit reductions when
+// every lane's value fits 32 bits (the usual case), else a shuffle tree.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+  const unsigned full = 0xffffffffu;
+  if (!__any_sync(full, (v >> 32) != 0ull)) {
+    const unsigned hi = __reduce_add_sync(full, static_cast<unsigned>(v >> 8));
+    const unsigned lo = __reduce_add_sync(full, static_cast<unsigned>(v & 255ull));
+    return (static_cast<unsigned long long>(hi) << 8) + lo;
+  }
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(full, v, o);
+  return v;
 }
 
 // Block-wide exclusive scan of two ints per thread; returns both block totals.
@@ -104,13 +122,14 @@ __device__ __forceinline__ unsigned long long seq_blocks(const PlanParams& p, in
     for (int qt = 0; qt < nqt; ++qt) t += static_cast<unsigned long long>(qtile_blocks(p, ql, L, qt));
     return t;
   }
-  const int bn = is_decode(p, ql) ? kDecBlockN : p.block_n;
-  if (!p.causal) return static_cast<unsigned long long>(nqt) * cdiv(L, bn) * (bn / kPage);
+  const int sh = tile_shift(p, ql);
+  if (!p.causal)
+    return static_cast<unsigned long long>(nqt) * (((L + (1 << sh) - 1) >> sh) << (sh - kPageShift));
   // keys [0, L - ql + (qt + 1) T) for qt < nqt - 1, keys [0, L) for the last q tile
   const long long T = p.tokens_per_tile;
   const long long n1 = nqt - 1;
   const long long keys = max(n1 * (static_cast<long long>(L) - ql) + T * n1 * (n1 + 1) / 2 + L, 0ll);
-  return static_cast<unsigned long long>(keys / kPage + static_cast<long long>(nqt) * (bn / kPage) / 2 + 1);
+  return static_cast<unsigned long long>((keys >> kPageShift) + (static_cast<long long>(nqt) << (sh - kPageShift)) / 2 + 1);
 }
 
 // ---- cache write of the new tokens ----------------------------------------
@@ -239,6 +258,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   __shared__ unsigned long long s_tiles[2];  // work of the prefill [0] and decode [1] kernels
   __shared__ int s_chunk[2];
   __shared__ int s_list_items[2];
+  __shared__ int s_need_zero;     // some sequence is rejected or has q tiles that see no key
   const Workspace& ws = p.ws;
   const int B = p.num_seqs;
   const int G = p.group;
@@ -253,6 +273,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   // The attention kernels launched after this one may set themselves up now;
   // they read nothing of the plan (nor the cache) before the plan grid has completed.
   grid_dep_launch();
+  // This grid is itself a dependent launch: it may have become resident while
+  // the kernel before it (the previous call's attention, or any other) still
+  // ran, and it reads and writes nothing before that grid has completed.
+  grid_dep_wait();
   if (blockIdx.x > 0) {
     write_new_rows(p);
     return;
@@ -260,6 +284,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   if (threadIdx.x == 0) {
     s_tiles[0] = s_tiles[1] = 0ull;
     s_carry[0] = s_carry[1] = s_carry[2] = s_carry[3] = 0;
+    s_need_zero = 0;
   }
   for (int i = threadIdx.x; i < 2 * kHistBuckets; i += kPlanThreads) (&hist[0][0])[i] = 0;
   __syncthreads();
@@ -277,9 +302,17 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       ql = q1 - q0;
       ok = q0 >= 0 && q1 >= q0 && q1 <= p.total_q && ql <= p.max_q && L >= 0 && L <= p.max_kv;
       if (!ok) atomicOr(ws.hdr + kHdrErr, kErrBadInput);
+      // rows to zero: a rejected sequence's, or a first q tile that sees no key
+      if (!ok || (ql > 0 && (L == 0 || (p.causal && L - ql + min(ql, p.tokens_per_tile) <= 0))))
+        s_need_zero = 1;
       if (ok) {
         nqt = cdiv(ql, p.tokens_per_tile);
-        my_tiles[is_decode(p, ql) ? 1 : 0] += seq_blocks(p, ql, L, nqt);
+        // (both slots updated with a select: a run-time index would put the
+        // array in local memory)
+        const unsigned long long w = seq_blocks(p, ql, L, nqt);
+        const bool dec = is_decode(p, ql);
+        my_tiles[0] += dec ? 0ull : w;
+        my_tiles[1] += dec ? w : 0ull;
       }
     }
     int kv_excl, qt_excl;
@@ -290,6 +323,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
           static_cast<long long>(s_carry[0]) + kv_excl + L > static_cast<long long>(p.num_pages)) {
         ok = false;
         atomicOr(ws.hdr + kHdrErr, kErrBadInput);
+        s_need_zero = 1;
       }
       const int4 si = make_int4(q0, ok ? ql : -1, L, s_carry[0] + kv_excl);
       ws.seq_info[b] = si;
@@ -307,7 +341,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   // total work: a warp sum, then one shared-memory atomic per warp that has any
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
-    for (int o = 16; o > 0; o >>= 1) my_tiles[k] += __shfl_xor_sync(0xffffffffu, my_tiles[k], o);
+    my_tiles[k] = warp_sum_u64(my_tiles[k]);
     if (lane == 0 && my_tiles[k] != 0)
       atomicAdd(&s_tiles[k], my_tiles[k] * static_cast<unsigned long long>(p.n_heads_kv));
   }
@@ -335,6 +369,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
         ws.seq_info[b].y = -1;
         if (b < kCacheSeqs) s_seq[b].y = -1;
         atomicOr(ws.hdr + kHdrErr, kErrBadInput);
+        s_need_zero = 1;
       }
     }
   }
@@ -358,11 +393,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     int S = 1, rows = 0;
     if (b < B) {
       const int4 sq = seq_at(b);
-      if (sq.y > 0 && cdiv(sq.y, p.tokens_per_tile) == 1) {
+      if (sq.y > 0 && sq.y <= p.tokens_per_tile) {  // one q tile
         const int tiles = qtile_kv_tiles(p, sq.y, sq.z, 0);
         const bool dec = is_decode(p, sq.y);
-        const int per_tile = dec ? kDecBlockN / kPage : p.block_n / kPage;
-        const int chunk_tiles = max(1, cdiv(s_chunk[dec ? 1 : 0], per_tile));
+        const int per_tile_shift = (dec ? kDecBlockNShift : p.block_n_shift) - kPageShift;
+        const int chunk_tiles = max(1, (s_chunk[dec ? 1 : 0] + (1 << per_tile_shift) - 1) >> per_tile_shift);
         if (tiles >= 2) S = min(min(cdiv(tiles, chunk_tiles), kMaxSplits), tiles);
         rows = sq.y * G;
       }
@@ -485,8 +520,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
 
   // ---- zero fill: rejected sequences and q tiles that see no key (all rows of
   // every sequence if the workspace could not hold the plan). Each thread takes
-  // whole sequences; only degenerate inputs reach the stores.
-  for (int b = threadIdx.x; b < B; b += kPlanThreads) {
+  // whole sequences; only degenerate inputs reach the stores, and the walk is
+  // skipped when pass 1 saw none.
+  for (int b = threadIdx.x; (s_need_zero || bad_plan) && b < B; b += kPlanThreads) {
     // the query range of a live sequence from the cached plan; a rejected one's
     // from cu_q (it may be out of range)
     const int4 sq = seq_at(b);
@@ -541,9 +577,8 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(int* err) {
 }  // namespace
 
 
-cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  plan_kernel<<<1 + p.write_ctas, kPlanThreads, 0, s>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s, bool dependent) {
+  return launch_kernel(plan_kernel, dim3(1 + p.write_ctas), dim3(kPlanThreads), 0, s, dependent, p);
 }
 
 cudaError_t launch_wait_selftest(int* err, cudaStream_t s) {
