@@ -233,6 +233,30 @@ size_t pattn_workspace_size_fp8(int num_seqs, int total_q, int max_q, int max_kv
 pattn_status pattn_selftest_wait_timeout(pattn_stream_t stream);
 
 /*
+ * pattn_selftest_attention_timeout -- failure-detection self-test of the
+ * attention kernels' own abort path. Runs pattn_forward on the given batch
+ * (same arguments and rules) with one change: in each attention kernel the
+ * batch launches that has work (the swap-AB decode kernel, the one-CTA
+ * prefill kernel), the first CTA's MMA-issuing thread first waits for a
+ * barrier phase that nothing completes before that thread's own drain. After
+ * the wait limit (about 2 s) the wait gives up: it sets the timeout bit of the
+ * device error word and the CTA's abort flag; every role of the CTA then
+ * leaves its loop, waits (bounded) for the copies and MMAs it has in flight,
+ * frees its tensor memory and exits. Nothing faults or hangs, and the context
+ * stays usable: the next pattn_get_device_status returns
+ * PATTN_ERR_DEVICE_TIMEOUT and later calls run normally. The output rows of
+ * the first CTA's items are unspecified. Batches that take the CTA-pair
+ * prefill kernel (head_dim 256 with two q tiles per sequence) return
+ * PATTN_ERR_UNSUPPORTED. Returns the launch status.
+ */
+pattn_status pattn_selftest_attention_timeout(void *out, const void *q, const void *kv_pool,
+                                              const int32_t *block_table, const int32_t *seq_lens,
+                                              const int32_t *cu_q, int num_seqs, int total_q, int max_q,
+                                              int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
+                                              int page_size, int num_pages, float scale, int causal,
+                                              pattn_stream_t stream);
+
+/*
  * The tile plan of a batch, for inspection (tests): runs only the device-side
  * planner that pattn_forward launches first (step "plan / tile scheduler" of
  * the method: varlen q tiles of T = 128 / G tokens with GQA packing, causal

@@ -17,7 +17,8 @@ from . import _lib
 __all__ = ["PattnError", "forward", "forward_append", "forward_fp8qk", "quantize_qk", "forward_fp8",
            "quantize_v", "forward_noalloc",
            "forward_host", "workspace_size",
-           "set_workspace", "device_status", "status_string", "selftest_wait_timeout", "plan_items",
+           "set_workspace", "device_status", "status_string", "selftest_wait_timeout",
+           "selftest_attention_timeout", "plan_items",
            "profile_enable",
            "profile_read",
            "profile_read_kernels", "STATUS", "library_path"]
@@ -288,6 +289,27 @@ def selftest_wait_timeout(stream=None) -> None:
     a bounded wait that runs out after its limit and sets the timeout bit that
     :func:`device_status` then reports."""
     _check(_lib.load().pattn_selftest_wait_timeout(_stream_handle(stream)), "pattn_selftest_wait_timeout")
+
+
+def selftest_attention_timeout(out, q, kv_pool, block_table, seq_lens, cu_q, *, max_q: int, max_kv: int,
+                               n_heads_kv: int, scale: float, causal: bool,
+                               num_pages: Optional[int] = None, stream=None) -> None:
+    """Launch the attention kernels' failure-detection self-test
+    (``pattn_selftest_attention_timeout``): :func:`forward` on this batch with
+    the first CTA's MMA-issuing thread made to wait on a phase that nothing
+    completes, so that its bounded wait runs out and the CTA takes its
+    abort-and-drain path; :func:`device_status` then reports the timeout."""
+    import torch
+    for name, t, dt in (("out", out, torch.bfloat16), ("q", q, torch.bfloat16),
+                        ("kv_pool", kv_pool, torch.bfloat16), ("seq_lens", seq_lens, torch.int32),
+                        ("cu_q", cu_q, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name}: expected a contiguous CUDA {dt} tensor")
+    total_q, hq, d, page, pages = _shape_args(q, kv_pool, block_table, n_heads_kv, num_pages)
+    _check(_lib.load().pattn_selftest_attention_timeout(
+        _ptr(out), _ptr(q), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens), _ptr(cu_q),
+        int(seq_lens.numel()), total_q, int(max_q), int(max_kv), hq, int(n_heads_kv), d, page,
+        pages, float(scale), int(bool(causal)), _stream_handle(stream)), "pattn_selftest_attention_timeout")
 
 
 def plan_items(block_table, seq_lens, cu_q, *, total_q: int, max_q: int, max_kv: int, n_heads_q: int,

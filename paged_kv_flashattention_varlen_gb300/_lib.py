@@ -35,6 +35,8 @@ SIGNATURES = {
     "pattn_set_workspace": (_i, [_vp, _sz]),
     "pattn_get_device_status": (_i, [_vp]),
     "pattn_selftest_wait_timeout": (_i, [_vp]),
+    "pattn_selftest_attention_timeout": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                              _f, _i, _vp]),
     "pattn_plan_items": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp]),
     "pattn_status_string": (ctypes.c_char_p, [_i]),
     "pattn_profile_enable": (_i, [_i]),

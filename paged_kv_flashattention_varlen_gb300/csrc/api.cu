@@ -307,7 +307,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
                         int hq, int hkv, int d, int num_pages, float scale, int causal,
                         cudaStream_t stream, const Shape& sh, const void* k_new = nullptr,
                         const void* v_new = nullptr, Mode mode = Mode::kBf16,
-                        const QuantBufs* qb = nullptr) {
+                        const QuantBufs* qb = nullptr, bool selftest_abort = false) {
   pattn_status s = PATTN_OK;
 
   Workspace ws{};
@@ -433,6 +433,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   ap.scale_log2 = scale * 1.4426950408889634f;
   ap.causal = causal;
   ap.paged = bt ? 1 : 0;
+  ap.selftest_abort = selftest_abort ? 1 : 0;
 
   AttnParams dp = ap;
   dp.items = ws.dec_items;
@@ -558,7 +559,8 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
                             int total_q, int max_q, int max_kv, int hq, int hkv, int d, int page,
                             int num_pages, float scale, int causal, cudaStream_t stream,
                             const Shape& sh, const void* k_new = nullptr,
-                            const void* v_new = nullptr, Mode mode = Mode::kBf16) {
+                            const void* v_new = nullptr, Mode mode = Mode::kBf16,
+                            bool selftest_abort = false) {
   (void)page;
   DeviceState* stp = nullptr;
   pattn_status s = device_state(&stp);
@@ -583,7 +585,7 @@ pattn_status forward_locked(void* out, const void* q, const void* kv, const int3
     }
   }
   return launch_all(st, wsb, L, out, q, kv, bt, seq_lens, cu_q, num_seqs, total_q, max_q, max_kv, hq,
-                    hkv, d, num_pages, scale, causal, stream, sh, k_new, v_new, mode, &qb);
+                    hkv, d, num_pages, scale, causal, stream, sh, k_new, v_new, mode, &qb, selftest_abort);
 }
 
 // ---------------------------------------------------------------------------
@@ -934,6 +936,26 @@ pattn_status pattn_selftest_wait_timeout(pattn_stream_t stream) {
   if ((s = ensure_workspace(*stp, kHdrWords * sizeof(int))) != PATTN_OK) return s;
   const cudaError_t e = launch_wait_selftest(static_cast<int*>(stp->ws), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PATTN_OK : PATTN_ERR_CUDA;
+}
+
+pattn_status pattn_selftest_attention_timeout(void* out, const void* q, const void* kv_pool,
+                                              const int32_t* block_table, const int32_t* seq_lens,
+                                              const int32_t* cu_q, int num_seqs, int total_q, int max_q,
+                                              int max_kv, int n_heads_q, int n_heads_kv, int head_dim,
+                                              int page_size, int num_pages, float scale, int causal,
+                                              pattn_stream_t stream) {
+  Shape sh{};
+  pattn_status s = check_args(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q,
+                              max_q, max_kv, n_heads_q, n_heads_kv, head_dim, page_size,
+                              num_pages, scale, causal, &sh);
+  if (s != PATTN_OK) return s;
+  if (sh.pair) return PATTN_ERR_UNSUPPORTED;  // the CTA-pair kernel has no self-test wait
+  if (num_seqs == 0 || total_q == 0) return PATTN_OK;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return forward_locked(out, q, kv_pool, block_table, seq_lens, cu_q, num_seqs, total_q, max_q,
+                        max_kv, n_heads_q, n_heads_kv, head_dim, page_size, num_pages, scale,
+                        causal, reinterpret_cast<cudaStream_t>(stream), sh, nullptr, nullptr,
+                        Mode::kBf16, true);
 }
 
 pattn_status pattn_plan_items(const int32_t* block_table, const int32_t* seq_lens, const int32_t* cu_q,

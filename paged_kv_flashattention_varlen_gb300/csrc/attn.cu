@@ -306,6 +306,9 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   uint8_t* misc = smem + C::kOffMisc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 16);
+  // drains wait on their own control word, which nothing sets: after an abort
+  // they still wait (bounded) for every copy and MMA in flight to complete
+  volatile int* never_abort = reinterpret_cast<volatile int*>(misc + 20);
   volatile int* merge_flag = reinterpret_cast<volatile int*>(misc + 64);  // this CTA merges the unit
   // CTA pairs: 16-byte source and destination of the peer's signalling copies
   const uint32_t sig_src = smem_addr(misc + 32), sig_dst = smem_addr(misc + 48);
@@ -317,6 +320,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtl ctl{abort_flag, p.err};
+  const WaitCtl drain_ctl{never_abort, p.err};
   // CTA pairs walk the item list together (pair c = CTAs 2c, 2c + 1); the
   // rank-0 CTA issues the MMAs of both
   const uint32_t rank = kPair ? cluster_rank() : 0u;
@@ -325,6 +329,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    *never_abort = 0;
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kQFull0 + b), 1);
       mbar_init(bar(kQEmpty0 + b), 1);  // the item's last QK MMA releases the buffer
@@ -517,13 +522,13 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       for (uint32_t st = 0; st < stages; ++st) {
         if (n <= st) continue;
         const uint32_t last = ((n - 1 - st) / stages) * stages + st;  // last fill on stage st
-        wait_one(bar(full + st), (last / stages) & 1u, WaitCtl{abort_flag, p.err});
+        wait_one(bar(full + st), (last / stages) & 1u, drain_ctl);
       }
       if (kind == 0) {
         for (uint32_t b = 0; b < static_cast<uint32_t>(C::kQBufs); ++b) {
           if (itl <= b) continue;
           const uint32_t last = ((itl - 1 - b) / C::kQBufs) * C::kQBufs + b;  // last Q fill of buffer b
-          wait_one(bar(kQFull0 + b), (last / C::kQBufs) & 1u, WaitCtl{abort_flag, p.err});
+          wait_one(bar(kQFull0 + b), (last / C::kQBufs) & 1u, drain_ctl);
         }
       }
     }
@@ -556,6 +561,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       const SmemDesc dk = sw128_desc_split(sK, 16, 1024);
       uint32_t n = 0, itl = 0;
       bool ok = true;
+      // failure-detection self-test (one-CTA kernels): the first CTA's QK thread
+      // first waits for a phase that nothing completes before the drain below,
+      // so the wait runs out and every role of the CTA takes its abort path
+      if (!kPair && p.selftest_abort && blockIdx.x == 0 && n_items > 0) ok = wait_one(bar(kDrain), 0, ctl);
       int4 iv_next = cid < n_items ? p.items[cid] : make_int4(0, 0, 0, 0);
       for (int kq = 0, idx = cid; idx < n_items && ok;
          idx = cta_item(++kq, cid, ncl), ++itl) {
@@ -610,7 +619,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       // Drain: all UMMAs issued by this thread complete before TMEM is freed.
       if constexpr (kPair) umma_commit_pair(bar(kDrain));
       else umma_commit(bar(kDrain));
-      wait_one(bar(kDrain), 0, ctl);
+      wait_one(bar(kDrain), 0, drain_ctl);
     }
     __syncwarp();
   } else if (warp == 2) {
@@ -716,7 +725,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     if (lane == 0 && (!kPair || rank == 0)) {
       if constexpr (kPair) umma_commit_pair(bar(kDrainPV));
       else umma_commit(bar(kDrainPV));
-      wait_one(bar(kDrainPV), 0, ctl);
+      wait_one(bar(kDrainPV), 0, drain_ctl);
     }
     __syncwarp();
   } else if (warp >= 4) {

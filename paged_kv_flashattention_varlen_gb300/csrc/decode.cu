@@ -255,6 +255,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   uint8_t* misc = smem + C::kOffMisc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 16);
+  // drains wait on their own control word, which nothing sets: after an abort
+  // they still wait (bounded) for every copy and MMA in flight to complete
+  volatile int* never_abort = reinterpret_cast<volatile int*>(misc + 20);
   auto bar = [&](int i) { return sBar + 8u * static_cast<uint32_t>(i); };
   auto ring_full = [&](uint32_t s) { return bar(kDRingFull0 + static_cast<int>(s)); };
   auto ring_ready = [&](uint32_t s) { return bar(kDRingFull0 + R + static_cast<int>(s)); };
@@ -263,9 +266,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtl ctl{abort_flag, p.err};
+  const WaitCtl drain_ctl{never_abort, p.err};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    *never_abort = 0;
     mbar_init(bar(kDQFull), 1);
     mbar_init(bar(kDQEmpty), 1);
     for (int s = 0; s < 2; ++s) {
@@ -309,7 +314,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
 
   if (warp == 0) {
     // ------------------------------------------------------------ load warp (all lanes)
-    uint32_t f = 0, itl = 0;  // ring fills, items
+    uint32_t f = 0, itl = 0, qf = 0;  // ring fills, items, Q fills
     bool ok = true;
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
@@ -326,6 +331,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           mbar_arrive_expect_tx(bar(kDQFull), static_cast<uint32_t>(C::kDBlocks * 128 * G * Tq));
           for (int c = 0; c < C::kDBlocks; ++c)
             tma_load_4d(sQ + c * (kNQ * 128), &tmap_q, bar(kDQFull), c * 64, 0, hk, q0, pol_q);
+          ++qf;
         }
       }
       ok = __shfl_sync(full, ok, 0);
@@ -378,13 +384,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         }
       }
     }
-    // drain: the last fill of every stage has landed
+    // drain: the last fill of every stage, and the last Q fill, have landed
     if (lane == 0) {
       for (uint32_t s = 0; s < static_cast<uint32_t>(R); ++s) {
         if (f <= s) continue;
         const uint32_t last = ((f - 1 - s) / R) * R + s;
-        wait_one(ring_full(s), (last / R) & 1u, WaitCtl{abort_flag, p.err});
+        wait_one(ring_full(s), (last / R) & 1u, drain_ctl);
       }
+      if (qf > 0) wait_one(bar(kDQFull), (qf - 1) & 1u, drain_ctl);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -419,6 +426,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         umma_commit(bar(kDPVDone0 + (m & 1u)));
         return true;
       };
+      // failure-detection self-test: the first CTA's MMA thread first waits for a
+      // phase that nothing completes before the drain below, so the wait runs
+      // out and every role of the CTA takes its abort path
+      if (p.selftest_abort && blockIdx.x == 0 && n_items > 0) ok = wait_one(bar(kDDrain), 0, ctl);
       for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
          idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
         const int4 iv = p.items[idx];
@@ -448,7 +459,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         if (!(ok = issue_pv(n - 1, kt1 - 1 == kt0))) break;
       }
       umma_commit(bar(kDDrain));
-      wait_one(bar(kDDrain), 0, WaitCtl{abort_flag, p.err});
+      wait_one(bar(kDDrain), 0, drain_ctl);
     }
     __syncwarp();
   } else if (warp == 2) {

@@ -160,6 +160,10 @@ struct AttnParams {
   int nb_max;
   // fp8 P.V variant: per-channel V scales [num_seqs][n_heads_kv][head_dim]
   const float* v_scale;
+  // failure-detection self-test only (0 otherwise): the first CTA's MMA-issuing
+  // thread waits for a barrier phase that nothing completes, so that its
+  // bounded wait runs out and the CTA takes its abort-and-drain path
+  int selftest_abort;
 };
 
 

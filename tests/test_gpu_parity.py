@@ -321,6 +321,27 @@ def test_bounded_wait_runs_out_into_an_error_status_and_the_context_survives():
     assert _status() == 0
 
 
+@pytest.mark.parametrize("which", ["decode", "prefill"])
+def test_attention_kernel_abort_path_reports_timeout_and_the_context_survives(which):
+    # the first CTA's MMA-issuing thread of the decode kernel (a decode batch)
+    # or of the one-CTA prefill kernel (a causal prefill batch) waits on a
+    # phase that nothing completes: after the wait limit every role of that CTA
+    # leaves its loop, drains its in-flight copies and MMAs and frees its
+    # tensor memory; the host reads the timeout, and the next ordinary call on
+    # the same context passes parity
+    import paged_kv_flashattention_varlen_gb300 as pk
+    wl = workloads.named(2, scale_down=8) if which == "decode" else workloads.named(3, scale_down=16)
+    d = to_device(wl)
+    out = torch.full_like(d["q"], float("nan"))
+    pk.selftest_attention_timeout(out, d["q"], d["kv"], d["bt"], d["sl"], d["cu"], max_q=wl.max_q,
+                                  max_kv=wl.max_kv, n_heads_kv=wl.n_heads_kv, scale=wl.scale,
+                                  causal=wl.causal, num_pages=wl.num_pages)
+    assert pk.device_status() == 6  # PATTN_ERR_DEVICE_TIMEOUT
+    assert pk.device_status() == 0
+    assert_parity(run_gpu(wl, d=d), wl)
+    assert _status() == 0
+
+
 @pytest.mark.parametrize("world", [2, 4])
 def test_head_shards_through_the_library_reassemble_the_output(world):
     # head (tensor) sharding as one process per GPU would run it, one shard
