@@ -52,7 +52,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # the sources each profiled kernel is compiled from (its ncu summary names their hash)
 KERNEL_SOURCES = {"decode": ["decode.cu", "merge.cuh", "ptx.cuh", "kernels.cuh"],
-                  "prefill": ["attn.cu", "merge.cuh", "ptx.cuh", "kernels.cuh"]}
+                  "prefill": ["attn.cu", "prefill.cuh", "merge.cuh", "ptx.cuh", "kernels.cuh"]}
 
 
 def parse():
@@ -249,8 +249,8 @@ def launches_per_step(wl) -> int:
 
 KERNEL_NAMES = {1: "attn_kernel<256,64> (head_dim 256, one CTA; the decode kernel launches empty)",
                 2: "decode_kernel<128> (swap-AB)",
-                3: "attn_kernel<128,128>",
-                4: "attn_kernel<128,128>",
+                3: "attn_kernel<128,128> (one q tile per CTA)",
+                4: "attn2q_kernel (head_dim 128, two q tiles per CTA)",
                 5: "decode_kernel<256> then attn_kernel<256,128,pair> (cta_group::2)"}
 L2_NOTES = {1: "cold L2: a %d MB buffer written before every step, outside its events",
             2: "inputs larger than L2 (KV pool %.2f GB > 129 MB)",

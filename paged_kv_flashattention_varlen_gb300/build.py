@@ -13,8 +13,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpattn.so")
-SOURCES = ["attn.cu", "decode.cu", "plan.cu", "quant.cu", "api.cu"]
-HEADERS = ["kernels.cuh", "ptx.cuh", "merge.cuh"]
+SOURCES = ["attn.cu", "attn2q.cu", "decode.cu", "plan.cu", "quant.cu", "api.cu"]
+HEADERS = ["kernels.cuh", "ptx.cuh", "merge.cuh", "prefill.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-v", "-I", INCLUDE]

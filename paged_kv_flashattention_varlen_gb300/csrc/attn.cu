@@ -59,6 +59,7 @@
 
 #include "kernels.cuh"
 #include "merge.cuh"
+#include "prefill.cuh"
 #include "ptx.cuh"
 
 namespace pattn {
@@ -139,68 +140,12 @@ enum Bar {
   // CTA pairs, in the rank-0 CTA: the peer's Q, K stage and V stage are ready
   kPeerQ, kPeerK0, kPeerK1, kPeerK2, kPeerV0, kPeerV1, kPeerV2,
   // split items: every softmax warp's partials written; the unit counter read
-  kMergeA, kMergeB, kNumBars
+  kMergeA, kMergeB,
+  // head_dim 128 output slices: warpgroup h's rows staged (4 warps); its buffer read by the store
+  kOSlFull0, kOSlFull1, kOSlFree0, kOSlFree1, kNumBars
 };
 static_assert(kNumBars * 8 <= 512, "mbarrier area");
 constexpr int kAttnThreads = 384;  // load K, MMA, V tail, load V; 2 softmax warpgroups
-constexpr int kSoftmaxWarps = 8;
-
-// part: first partial row of this split, -1 if the item is not split; split:
-// the split's index in its unit.
-struct Item {
-  int b, hk, qt, kt0, kt1, part, split;
-};
-
-__device__ __forceinline__ Item decode_item(int4 v) {
-  Item it;
-  it.b = v.x & kSeqMask;
-  it.hk = v.y >> 16;
-  it.qt = v.y & 0xFFFF;
-  it.kt0 = (v.z >> 16) & 0xFFFF;
-  it.kt1 = v.z & 0xFFFF;
-  it.part = v.w;
-  it.split = v.x >> kSeqBits;
-  return it;
-}
-
-// After a split item's partials are written (softmax warps 4-11): count the
-// split in its unit's counter; the CTA that finishes the unit's last split
-// merges the unit's rows (the decode manifest's last-CTA reduction through its
-// counter scratch). Bounded waits only: warp 4 takes the count once all eight
-// warps have fenced their writes, then releases them with the result.
-template <int D>
-__device__ __forceinline__ bool split_done(const AttnParams& p, const Item& it, int4 si, uint32_t bar_a,
-                                           uint32_t bar_b, volatile int* flag, uint32_t& nsp, int warp,
-                                           const WaitCtl& ctl) {
-  const int lane = threadIdx.x & 31;
-  __threadfence();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar_a);
-  bool ok = true;
-  if (warp == 4) {
-    if (lane == 0) {
-      ok = wait_one(bar_a, nsp & 1u, ctl);
-      int last = 0;
-      if (ok) {
-        const int4 sp = p.seq_plan[it.b];
-        last = atomicAdd(&p.unit_cnt[sp.w + it.hk], 1) == sp.z - 1;
-        if (last) __threadfence();
-      }
-      *flag = last;
-      mbar_arrive(bar_b);
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-  }
-  if (!wait_warp(bar_b, nsp & 1u, ctl)) ok = false;
-  ++nsp;
-  if (!ok) return false;
-  if (*flag) {
-    const int4 sp = p.seq_plan[it.b];
-    const int rows = si.y * p.group;
-    merge_unit<D>(p, si.x, it.hk, sp.z, it.part - it.split * rows, rows, warp - 4, kSoftmaxWarps);
-  }
-  return true;
-}
 
 // One row's probabilities for KH keys: p_i = 2^(S_i c - m_ref) as bf16 pairs in
 // pk, returning the fp32 sum of the p_i. With kMasked only the first nv keys
@@ -358,6 +303,10 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     mbar_init(bar(kPeerQ), 1);
     mbar_init(bar(kMergeA), kSoftmaxWarps);
     mbar_init(bar(kMergeB), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar(kOSlFull0 + h), 4);
+      mbar_init(bar(kOSlFree0 + h), 1);
+    }
     mbar_init_fence();
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_kv);
@@ -746,6 +695,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     const float c = p.scale_log2;
     uint32_t n = 0, itl = 0;
     uint32_t n_split = 0;  // split items finished (merge handshakes)
+    uint32_t n_slice = 0;  // output slices staged by this warpgroup
     bool ok = true;
     // The next item's descriptor and sequence are loaded one item ahead.
     int4 iv_next = cid < n_items ? p.items[cid] : make_int4(0, 0, 0, 0);
@@ -973,16 +923,16 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
       // row by row below.
       const bool tma_out = it.part < 0 && (it.qt + 1) * T <= ql;
       if (tma_out) {
+        // (bounded mbarrier hand-offs, not a named barrier: a warp that gave up
+        // elsewhere cannot leave the others of its warpgroup waiting)
         const uint32_t stage = s_base + C::kOffO + static_cast<uint32_t>(h * (kBM * 64));
         const uint32_t row_addr = stage + static_cast<uint32_t>(r * 64);
         const uint32_t sx = static_cast<uint32_t>((r >> 1) & 3);  // 64-byte swizzle of this row
-        const bool issuer = sw == 0 && lane == 0;
 #pragma unroll 1
-        for (int pp = 0; pp < 2; ++pp) {
+        for (int pp = 0; pp < 2 && ok; ++pp, ++n_slice) {
           const int col = h * (D / 2) + pp * 32;
           // the slice buffer is free once the previous store has read it
-          if (issuer) bulk_wait_read_all();
-          named_bar_sync(1 + h, 128);
+          if (!(ok = wait_warp(bar(kOSlFree0 + h), (n_slice & 1u) ^ 1u, ctl))) break;
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const int cc = col + hf * 16;
@@ -1020,12 +970,22 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
                            w[4 * c2 + 1], w[4 * c2 + 2], w[4 * c2 + 3]);
           }
           fence_proxy_async_smem();
-          named_bar_sync(1 + h, 128);
-          if (issuer) {
-            tma_store_4d(&tmap_o, stage, col, 0, it.hk, q0 + it.qt * T);
-            bulk_commit_group();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kOSlFull0 + h));
+          if (sw == 0) {
+            if (lane == 0) {
+              ok = wait_one(bar(kOSlFull0 + h), n_slice & 1u, ctl);
+              if (ok) {
+                tma_store_4d(&tmap_o, stage, col, 0, it.hk, q0 + it.qt * T);
+                bulk_commit_group();
+                bulk_wait_read_all();
+                mbar_arrive(bar(kOSlFree0 + h));
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
           }
         }
+        if (!ok) break;
       } else if (warp_live) {
         const int hq = it.hk * G + g;
 #pragma unroll 1

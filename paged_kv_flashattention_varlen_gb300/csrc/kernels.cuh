@@ -68,7 +68,7 @@ struct PlanParams {
   int tokens_per_tile;  // T = kBM / group
   int block_n;          // keys per KV tile of the prefill kernel
   int block_n_shift;    // log2(block_n)
-  int pair;             // prefill items of two q tiles (CTA-pair kernel)
+  int pair;             // prefill items of two q tiles (CTA-pair kernel, two-q-tile kernel)
   int dec_enabled;      // group <= kDecRows: units of <= kDecRows packed rows go to the decode kernel
   int bt_stride, num_pages;
   int causal;
@@ -238,6 +238,11 @@ cudaError_t launch_attention_fp8(const AttnParams& p, const CUtensorMap& tq8, co
 cudaError_t launch_attention_fp8pv(const AttnParams& p, const CUtensorMap& tq8, const CUtensorMap& tk8,
                                    const CUtensorMap& tv8, const CUtensorMap& to, int grid, cudaStream_t s,
                                    bool dependent);
+// head_dim 128 with two q tiles per CTA (bf16): items of two q tiles from a plan
+// made with PlanParams::pair; `to` as for launch_attention.
+cudaError_t launch_attention_2q(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,
+                                const CUtensorMap& to, int grid, cudaStream_t s, bool dependent);
+cudaError_t attention2q_set_attributes();
 // head_dim 256 with CTA pairs (cta_group::2 MMAs, 128-key tiles): items of two
 // q tiles from a plan made with PlanParams::pair; grid even.
 cudaError_t launch_attention_pair(const AttnParams& p, const CUtensorMap& tq, const CUtensorMap& tkv,

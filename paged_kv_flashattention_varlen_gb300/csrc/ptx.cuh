@@ -270,6 +270,10 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 }
 // The issuing thread's bulk stores are complete (their writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// The source of every bulk group but the newest one has been read.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 
 // Named barrier `id` (1-15) over `n` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int n) {

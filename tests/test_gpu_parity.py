@@ -321,16 +321,19 @@ def test_bounded_wait_runs_out_into_an_error_status_and_the_context_survives():
     assert _status() == 0
 
 
-@pytest.mark.parametrize("which", ["decode", "prefill"])
+@pytest.mark.parametrize("which", ["decode", "prefill", "prefill_two_q"])
 def test_attention_kernel_abort_path_reports_timeout_and_the_context_survives(which):
-    # the first CTA's MMA-issuing thread of the decode kernel (a decode batch)
-    # or of the one-CTA prefill kernel (a causal prefill batch) waits on a
-    # phase that nothing completes: after the wait limit every role of that CTA
-    # leaves its loop, drains its in-flight copies and MMAs and frees its
-    # tensor memory; the host reads the timeout, and the next ordinary call on
-    # the same context passes parity
+    # the first CTA's MMA-issuing thread of the decode kernel (a decode batch),
+    # of the one-q-tile prefill kernel (a causal prefill batch) or of the
+    # two-q-tile prefill kernel (a non-causal batch) waits on a phase that
+    # nothing completes: after the wait limit every role of that CTA leaves its
+    # loop, drains its in-flight copies and MMAs and frees its tensor memory;
+    # the host reads the timeout, and the next ordinary call on the same
+    # context passes parity
     import paged_kv_flashattention_varlen_gb300 as pk
-    wl = workloads.named(2, scale_down=8) if which == "decode" else workloads.named(3, scale_down=16)
+    wl = {"decode": lambda: workloads.named(2, scale_down=8),
+          "prefill": lambda: workloads.named(3, scale_down=16),
+          "prefill_two_q": lambda: workloads.named(4, scale_down=32)}[which]()
     d = to_device(wl)
     out = torch.full_like(d["q"], float("nan"))
     pk.selftest_attention_timeout(out, d["q"], d["kv"], d["bt"], d["sl"], d["cu"], max_q=wl.max_q,

@@ -38,7 +38,8 @@ def expected_units(wl, rejected=()):
     """(list, b, q tile) -> visible KV tiles, for every q tile that makes an item."""
     G = wl.n_heads_q // wl.n_heads_kv
     T = BM // G
-    pair = wl.head_dim == 256 and wl.max_q > T
+    # two q tiles per item: CTA pairs at head_dim 256, two-q-tile CTAs at 128 (non-causal)
+    pair = wl.max_q > T and (wl.head_dim == 256 or not wl.causal)
     bn_pre = 128 if (wl.head_dim == 128 or pair) else 64
     cu = wl.cu_q.numpy().astype(np.int64)
     sl = wl.seq_lens.numpy().astype(np.int64)
