@@ -80,6 +80,8 @@ def parse():
                     help="with --workload: the fp8 Q/K/P/V variant (pattn_forward_fp8)")
     ap.add_argument("--workload-steps", type=int, default=0,
                     help="with --workload: time at most this many steps (profiling runs)")
+    ap.add_argument("--scale-down", type=int, default=1,
+                    help="with --workload: divide the token counts by this (smaller cases for profiling)")
     ap.add_argument("--append", action="store_true",
                     help="with --workload: each step first writes the query tokens' K/V rows into "
                          "their cache slots (pattn_forward_append)")
@@ -618,7 +620,7 @@ def run_workloads(args):
     idxs = [1, 2, 3, 4, 5] if args.workload == "all" else [int(x) for x in args.workload.split(",")]
     dev = torch.device("cuda", 0)
     for i in idxs:
-        wl = workloads.named(i)
+        wl = workloads.named(i, scale_down=args.scale_down)
         q, kv = wl.q.to(dev), wl.kv_pool.to(dev)
         bt = None if wl.block_table is None else wl.block_table.to(dev)
         sl, cu = wl.seq_lens.to(dev), wl.cu_q.to(dev)
@@ -654,7 +656,8 @@ def run_workloads(args):
         st = _stats(meas["plain"])
         ms = st["mean"]
         line = {
-            "workload": workloads.NAMES[i - 1], "steps": st["count"], "ms_per_step": round(ms, 5),
+            "workload": workloads.NAMES[i - 1] + (f"/{args.scale_down}" if args.scale_down > 1 else ""),
+            "steps": st["count"], "ms_per_step": round(ms, 5),
             "kv_gbs_step": round(nbytes / (ms * 1e-3) / 1e9, 1),
             "tflops_step": round(flops / (ms * 1e-3) / 1e12, 1),
             "attention_kernels_ms": round(attn_ms, 5),
