@@ -52,7 +52,10 @@ NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # the sources each profiled kernel is compiled from (its ncu summary names their hash)
 KERNEL_SOURCES = {"decode": ["decode.cu", "merge.cuh", "ptx.cuh", "kernels.cuh"],
-                  "prefill": ["attn.cu", "prefill.cuh", "merge.cuh", "ptx.cuh", "kernels.cuh"]}
+                  "prefill": ["attn.cu", "prefill.cuh", "merge.cuh", "ptx.cuh", "kernels.cuh"],
+                  "prefill_two_q": ["attn2q.cu", "prefill.cuh", "merge.cuh", "ptx.cuh", "kernels.cuh"]}
+# the kernel each named workload's roofline traffic is taken for (its ncu summary)
+TRAFFIC_KIND = {2: "decode", 3: "prefill", 4: "prefill_two_q"}
 
 
 def parse():
@@ -351,8 +354,8 @@ def run_named(pk, workloads, idx, dev, local, seconds, max_steps, pk_peaks, peak
     meas = measure(pk, _forward_step(pk, wl, q, kv, bt, sl, cu, out), seconds, local, flush, max_steps)
     entry = workload_entry(idx, wl, meas, pk_peaks, peak_kind)
     entry["device_status"] = pk.device_status()
-    if idx in (2, 3):
-        entry["roofline"]["traffic"] = ncu_traffic("decode" if idx == 2 else "prefill")
+    if idx in TRAFFIC_KIND:
+        entry["roofline"]["traffic"] = ncu_traffic(TRAFFIC_KIND[idx])
     del q, kv, bt, sl, cu, out
     torch.cuda.empty_cache()
     if oracle_s > 0:

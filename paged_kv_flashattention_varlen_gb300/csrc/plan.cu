@@ -489,44 +489,47 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   const bool item_overflow = s_list_items[0] > ws.max_items || s_list_items[1] > ws.max_items;
   const bool bad_plan = overflow || item_overflow;
 
-  // ---- pass 4: emit items, longest first. Threads take (KV head, q tile)
-  // pairs with the KV head outermost, so that within a cost bucket of the
-  // prefill list the items of one KV head come out together: the persistent
-  // CTAs, which take the list in rounds of one item each, then work on few KV
-  // heads at a time, and those heads' K/V stay in L2 while every q tile of the
-  // head reads them. The decode list, whose units read each page once, keeps
-  // the KV heads of a unit together instead (a page holds all heads' rows).
+  // ---- pass 4: emit items, longest first, one KV head after the other, so
+  // that within a cost bucket of the prefill list the items of one KV head
+  // come out together: the persistent CTAs, which take the list in rounds of
+  // one item each, then work on few KV heads at a time, and those heads' K/V
+  // stay in L2 while every q tile of the head reads them. The decode list,
+  // whose units read each page once, keeps the KV heads of a unit together
+  // instead (a page holds all heads' rows). Positions within a bucket are
+  // taken by atomics, so each head gets a sweep of its own, with a barrier
+  // between sweeps; one sweep when the prefill list is empty.
   if (!bad_plan) {
-    const int pairs = total_qt * p.n_heads_kv;
-    for (int t = threadIdx.x; t < pairs; t += kPlanThreads) {
-      const int hk_t = t / total_qt;
-      const int gq = t - hk_t * total_qt;
-      const int b = seq_of_qtile(gq);
-      const int4 sq = seq_at(b);
-      if (sq.y <= 0) continue;
-      const int list = is_decode(p, sq.y) ? 1 : 0;
-      if (list == 1 && hk_t != 0) continue;  // the thread of head 0 emits the unit's heads
-      const int qt = gq - qtile_first(b);
-      const int tiles = item_tiles(sq.y, sq.z, qt);
-      if (tiles == 0) continue;
-      const int S = sq.w;
-      const int rows = sq.y * G;
-      const int nh = list ? p.n_heads_kv : 1;
-      int4* dst = list ? ws.dec_items : ws.items;
-      const int part0 = S >= 2 ? part_at(b) : 0;
-      for (int s = 0; s < S; ++s) {
-        const int k0 = s * tiles / S;
-        const int k1 = (s + 1) * tiles / S;
-        const int pos = atomicAdd(&hist[list][min(k1 - k0, kHistBuckets - 1)], nh);
-        for (int j = 0; j < nh; ++j) {
-          const int hk = hk_t + j;
-          if (S >= 2)  // split s of the (b, hk) unit (q tile 0)
-            dst[pos + j] = make_int4(b | (s << kSeqBits), hk << 16, (k0 << 16) | k1,
-                                     part0 + (hk * S + s) * rows);
-          else
-            dst[pos + j] = make_int4(b, (hk << 16) | qt, (k0 << 16) | k1, -1);
+    const int sweeps = s_list_items[0] > 0 ? p.n_heads_kv : 1;
+    for (int hk_t = 0; hk_t < sweeps; ++hk_t) {
+      for (int gq = threadIdx.x; gq < total_qt; gq += kPlanThreads) {
+        const int b = seq_of_qtile(gq);
+        const int4 sq = seq_at(b);
+        if (sq.y <= 0) continue;
+        const int list = is_decode(p, sq.y) ? 1 : 0;
+        if (list == 1 && hk_t != 0) continue;  // the sweep of head 0 emits a decode unit's heads
+        const int qt = gq - qtile_first(b);
+        const int tiles = item_tiles(sq.y, sq.z, qt);
+        if (tiles == 0) continue;
+        const int S = sq.w;
+        const int rows = sq.y * G;
+        const int nh = list ? p.n_heads_kv : 1;
+        int4* dst = list ? ws.dec_items : ws.items;
+        const int part0 = S >= 2 ? part_at(b) : 0;
+        for (int s = 0; s < S; ++s) {
+          const int k0 = s * tiles / S;
+          const int k1 = (s + 1) * tiles / S;
+          const int pos = atomicAdd(&hist[list][min(k1 - k0, kHistBuckets - 1)], nh);
+          for (int j = 0; j < nh; ++j) {
+            const int hk = hk_t + j;
+            if (S >= 2)  // split s of the (b, hk) unit (q tile 0)
+              dst[pos + j] = make_int4(b | (s << kSeqBits), hk << 16, (k0 << 16) | k1,
+                                       part0 + (hk * S + s) * rows);
+            else
+              dst[pos + j] = make_int4(b, (hk << 16) | qt, (k0 << 16) | k1, -1);
+          }
         }
       }
+      __syncthreads();
     }
   }
 
