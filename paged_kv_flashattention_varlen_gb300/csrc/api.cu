@@ -118,8 +118,10 @@ struct WsLayout {
   int max_items, max_units, max_part_rows;
 };
 
-// Items per list the planner aims at on a device with `sms` SMs.
-inline int plan_target(int sms) { return std::min(kTargetHalfItemsPerSm * sms / 2, kTargetItemsCap); }
+// Items per list the planner aims at on a device with `sms` SMs; the decode
+// list may take up to a quarter more (the planner chooses per call).
+inline int plan_target(int sms) { return std::min(kTargetHalfItemsPerSm * sms / 2, kTargetItemsCap * 4 / 5); }
+inline int plan_target_max(int sms) { return plan_target(sms) + plan_target(sms) / 4; }
 
 // Workspace layout for these bounds. `target` is the planner's item target per
 // list (kTargetItemsCap when the device is not known). The planner sizes the
@@ -414,6 +416,7 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   pp.dec_enabled = dec_enabled ? 1 : 0;
   pp.target_items = plan_target(st.sms);
   pp.min_chunk = kMinChunk;
+  pp.ctas = st.sms;
   if (k_new && mode != Mode::kPlanOnly) {
     // the new tokens' K and V rows go into their cache slots from the plan
     // grid's extra CTAs (a warp per token, at most two CTAs per SM), before any
@@ -813,7 +816,7 @@ pattn_status pattn_forward_noalloc(void* out, const void* q, const void* kv_pool
   DeviceState* stp = nullptr;
   if ((s = device_state(&stp)) != PATTN_OK) return s;
   const WsLayout L = ws_layout(num_seqs, total_q, max_q, n_heads_q, n_heads_kv, head_dim, max_kv,
-                              plan_target(stp->sms));
+                              plan_target_max(stp->sms));
   if (L.total > static_cast<size_t>(PATTN_NOALLOC_SCRATCH_BYTES)) return PATTN_ERR_NO_MEMORY;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PATTN_ERR_CUDA;

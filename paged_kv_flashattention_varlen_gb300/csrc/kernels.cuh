@@ -72,8 +72,10 @@ struct PlanParams {
   int dec_enabled;      // group <= kDecRows: units of <= kDecRows packed rows go to the decode kernel
   int bt_stride, num_pages;
   int causal;
-  int target_items;     // items the split heuristic aims at (a multiple of the SM count)
+  int target_items;     // items per list the split heuristic aims at (a multiple of the SM count);
+                        // the decode list may take target_items + target_items / 4 instead
   int min_chunk;        // fewest KV tiles per split
+  int ctas;             // persistent CTAs of the decode kernel (its grid)
   // cache write of the new tokens (pattn_forward_append): CTAs 1..write_ctas of
   // the plan grid copy k_new / v_new [total_q][n_heads_kv][head_dim] into the
   // pool while CTA 0 plans; write_ctas = 0 and null pointers otherwise

@@ -14,7 +14,13 @@
 //      after the other) has about `target_items` items of at least `min_chunk`
 //      tiles of its own work (the
 //      decode manifest's "MultiCtasKv": several CTAs per sequence and KV
-//      head, with partial O and (max, sum) statistics in scratch);
+//      head, with partial O and (max, sum) statistics in scratch). When the
+//      decode units' lengths are skewed (the longest more than 2.5 times the
+//      mean), the decode list's target is chosen per call between
+//      target_items and 1.25 x target_items: the one whose items give the
+//      smaller largest CTA load under the decode kernel's item order (a
+//      counting sort of the item costs and the alternating round robin,
+//      simulated per CTA);
 //   4. orders the items longest first (counting sort on the number of KV
 //      tiles) so that round-robin assignment to persistent CTAs balances;
 //   5. zero-fills the output rows of q tiles that see no key at all, and
@@ -245,6 +251,15 @@ __device__ void write_new_rows(const PlanParams& p) {
   }
 }
 
+// Balance model of the decode list's split target: each item costs its KV
+// tiles plus kItemCost tiles (pipeline fill and drain, epilogue, split
+// merge). The choice is simulated only for skewed lengths (longest unit more
+// than 2.5 times the mean; equal-length units balance at the base target) and
+// for at most kBalanceUnitsPerCta units per CTA (the simulation walks every
+// CTA's items).
+constexpr int kItemCost = 2;
+constexpr int kBalanceUnitsPerCta = 4;
+
 constexpr int kSmemSeqs = 4096;   // sequences whose q-tile prefix is kept in shared memory
 constexpr int kCacheSeqs = 1024;  // sequences whose plan is kept in shared memory
 
@@ -259,6 +274,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   __shared__ int s_chunk[2];
   __shared__ int s_list_items[2];
   __shared__ int s_need_zero;     // some sequence is rejected or has q tiles that see no key
+  __shared__ int s_dec_units;     // decode sequences
+  __shared__ int s_dec_max;       // KV tiles of the longest decode unit
+  __shared__ int s_load[2];       // largest CTA load under each candidate target
   const Workspace& ws = p.ws;
   const int B = p.num_seqs;
   const int G = p.group;
@@ -285,12 +303,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     s_tiles[0] = s_tiles[1] = 0ull;
     s_carry[0] = s_carry[1] = s_carry[2] = s_carry[3] = 0;
     s_need_zero = 0;
+    s_dec_units = s_dec_max = 0;
+    s_load[0] = s_load[1] = 0;
   }
   for (int i = threadIdx.x; i < 2 * kHistBuckets; i += kPlanThreads) (&hist[0][0])[i] = 0;
   __syncthreads();
 
   // ---- pass 1: lengths, KV prefix (contiguous cache), q tile prefix, total work
   unsigned long long my_tiles[2] = {0ull, 0ull};
+  unsigned my_dec_units = 0, my_dec_max = 0;
   for (int base = 0; base < B; base += kPlanThreads) {
     const int b = base + threadIdx.x;
     int q0 = 0, ql = 0, L = 0, nqt = 0;
@@ -313,6 +334,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
         const bool dec = is_decode(p, ql);
         my_tiles[0] += dec ? 0ull : w;
         my_tiles[1] += dec ? w : 0ull;
+        if (dec) {
+          ++my_dec_units;
+          my_dec_max = max(my_dec_max, static_cast<unsigned>(qtile_kv_tiles(p, ql, L, 0)));
+        }
       }
     }
     int kv_excl, qt_excl;
@@ -345,6 +370,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     if (lane == 0 && my_tiles[k] != 0)
       atomicAdd(&s_tiles[k], my_tiles[k] * static_cast<unsigned long long>(p.n_heads_kv));
   }
+  my_dec_units = __reduce_add_sync(0xffffffffu, my_dec_units);
+  my_dec_max = __reduce_max_sync(0xffffffffu, my_dec_max);
+  if (lane == 0 && my_dec_units != 0) {
+    atomicAdd(&s_dec_units, static_cast<int>(my_dec_units));
+    atomicMax(&s_dec_max, static_cast<int>(my_dec_max));
+  }
 
   // ---- pass 1b: every live block-table entry must name a pool page (a warp per
   // sequence, eight independent loads per lane in flight)
@@ -375,14 +406,91 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   }
   __syncthreads();
   const int total_qt = s_carry[1];
-  if (threadIdx.x == 0) {
-    // the two kernels run one after the other, each over all SMs: each list's
-    // split size comes from its own work
-    const unsigned long long want = static_cast<unsigned long long>(max(p.target_items, 1));
-    for (int k = 0; k < 2; ++k) {
-      const int chunk = static_cast<int>((s_tiles[k] + want - 1) / want);
-      s_chunk[k] = max(chunk, max(p.min_chunk, 1));
+  // the two kernels run one after the other, each over all SMs: each list's
+  // split size comes from its own work and target
+  auto chunk_for = [&](int k, int target) {
+    const unsigned long long want = static_cast<unsigned long long>(max(target, 1));
+    return max(static_cast<int>((s_tiles[k] + want - 1) / want), max(p.min_chunk, 1));
+  };
+  int dec_target = p.target_items;
+  const int P = max(p.ctas, 1);
+  const int dec_min_split_tiles = max(1, cdiv(p.min_chunk, kDecBlockN / kPage));
+  const long long dec_units = static_cast<long long>(s_dec_units) * p.n_heads_kv;
+  // skewed: longest unit > 2.5 x the mean unit. s_tiles[1] counts 64-key blocks (two per
+  // decode tile) over all decode units, so mean = s_tiles[1] / (2 units) and the test is
+  // max * units * 2 > 2.5 * s_tiles[1], i.e. 4 * max * units > 5 * s_tiles[1]
+  const bool skewed = 4ull * static_cast<unsigned long long>(s_dec_max) * static_cast<unsigned long long>(dec_units) >
+                      5ull * s_tiles[1];
+  if (skewed && s_dec_max > dec_min_split_tiles && dec_units <= static_cast<long long>(kBalanceUnitsPerCta) * P) {
+    // ---- the decode list's target, per call: counting sorts of its item costs
+    // under both candidates (hist[0] and hist[1], still zero), then the largest
+    // CTA load of each under the decode kernel's alternating round robin
+    const int cand[2] = {p.target_items, p.target_items + p.target_items / 4};
+    if (threadIdx.x == 0) {
+      s_chunk[0] = chunk_for(1, cand[0]);
+      s_chunk[1] = chunk_for(1, cand[1]);
     }
+    __syncthreads();
+    const int ct0 = max(1, cdiv(s_chunk[0], kDecBlockN / kPage));
+    const int ct1 = max(1, cdiv(s_chunk[1], kDecBlockN / kPage));
+    for (int b = threadIdx.x; b < B; b += kPlanThreads) {
+      const int4 sq = seq_at(b);
+      if (sq.y <= 0 || !is_decode(p, sq.y)) continue;
+      const int tiles = qtile_kv_tiles(p, sq.y, sq.z, 0);
+      if (tiles == 0) continue;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int ct = j ? ct1 : ct0;
+        const int S = tiles >= 2 ? min(min(cdiv(tiles, ct), kMaxSplits), tiles) : 1;
+        for (int q = 0; q < S; ++q)
+          atomicAdd(&hist[j][min((q + 1) * tiles / S - q * tiles / S, kHistBuckets - 1)], p.n_heads_kv);
+      }
+    }
+    __syncthreads();
+    int n_items[2];
+    {
+      // exclusive starts from the most expensive bucket down
+      const int c = kHistBuckets - 1 - threadIdx.x;
+      int e0, e1;
+      const int2 tot = block_exclusive_scan2(hist[0][c], hist[1][c], &e0, &e1, warp_sums);
+      hist[0][c] = e0;
+      hist[1][c] = e1;
+      n_items[0] = tot.x;
+      n_items[1] = tot.y;
+      __syncthreads();
+    }
+    for (int t0 = 0; t0 < 2 * P; t0 += kPlanThreads) {
+      const int t = t0 + threadIdx.x;
+      int load = 0, j = 0;
+      if (t < 2 * P) {
+        j = t / P;
+        const int c = t - j * P;
+        const int* start = hist[j];
+        for (int k = 0, pos = c; pos < n_items[j]; pos = cta_item(++k, c, P)) {
+          // the cost of item `pos`: the largest bucket whose items begin at or before it
+          int lo = 0, hi = kHistBuckets - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (start[mid - 1] > pos) lo = mid; else hi = mid - 1;
+          }
+          load += lo + kItemCost;
+        }
+      }
+      // (P threads per candidate: a warp may straddle the two; reduce per candidate)
+      const int l0 = __reduce_max_sync(0xffffffffu, (t < 2 * P && j == 0) ? load : 0);
+      const int l1 = __reduce_max_sync(0xffffffffu, (t < 2 * P && j == 1) ? load : 0);
+      if (lane == 0) {
+        if (l0) atomicMax(&s_load[0], l0);
+        if (l1) atomicMax(&s_load[1], l1);
+      }
+    }
+    __syncthreads();
+    if (s_load[1] < s_load[0]) dec_target = cand[1];
+    for (int i = threadIdx.x; i < 2 * kHistBuckets; i += kPlanThreads) (&hist[0][0])[i] = 0;
+  }
+  if (threadIdx.x == 0) {
+    s_chunk[0] = chunk_for(0, p.target_items);
+    s_chunk[1] = chunk_for(1, dec_target);
     s_carry[2] = s_carry[3] = 0;
   }
   __syncthreads();

@@ -163,3 +163,81 @@ def test_rejected_sequence_makes_no_item():
 def test_contiguous_cache_plan():
     check_plan(workloads.make_contiguous("plan_c", 73, [40, 1, 7, 300], [300, 129, 64, 300], 8, 2, 128,
                                          causal=True))
+
+
+def host_decode_target_items(wl, sms):
+    """The decode list's item count under the planner's split rule, written
+    out on the host. Base target: 2 items per SM (at most 409). When the
+    decode units' lengths are skewed (longest unit more than 2.5 times the
+    mean), some unit exceeds the smallest split (8 tiles) and there are at
+    most 4 units per CTA, the target is chosen between the base and a quarter
+    more: each unit of T KV tiles split into min(ceil(T / chunk_tiles), 64, T)
+    parts, item costs counting-sorted longest first (clamped at 1023), the
+    decode kernel's alternating round robin over `sms` CTAs, each item costing
+    its tiles + 2; the candidate with the smaller largest CTA load wins (ties:
+    the base)."""
+    G = wl.n_heads_q // wl.n_heads_kv
+    hkv = wl.n_heads_kv
+    cu = wl.cu_q.numpy().astype(np.int64)
+    sl = wl.seq_lens.numpy().astype(np.int64)
+    base = min(4 * sms // 2, 512 * 4 // 5)
+    cands = [base, base + base // 4]
+    tiles = []
+    for b in range(wl.num_seqs):
+        ql, L = int(cu[b + 1] - cu[b]), int(sl[b])
+        if G <= DEC_ROWS and 1 <= ql and ql * G <= DEC_ROWS:
+            tiles.append(cdiv(L, DEC_BN) if L > 0 else 0)
+    work = sum(2 * t for t in tiles) * hkv
+    units = len(tiles) * hkv
+
+    def splits(t, target):
+        chunk = max(cdiv(work, max(target, 1)), 16)
+        ct = max(1, cdiv(chunk, 2))
+        return min(cdiv(t, ct), MAX_SPLITS, t) if t >= 2 else 1
+
+    def items(target):
+        out = []
+        for t in tiles:
+            if t == 0:
+                continue
+            S = splits(t, target)
+            out += [min((s + 1) * t // S - s * t // S, 1023) for s in range(S)] * hkv
+        return sorted(out, reverse=True)
+
+    def max_load(its):
+        best = 0
+        for c in range(sms):
+            load, k, pos = 0, 0, c
+            while pos < len(its):
+                load += its[pos] + 2
+                k += 1
+                pos = (k + 1) * sms - 1 - c if k & 1 else k * sms + c
+            best = max(best, load)
+        return best
+
+    tmax = max(tiles) if tiles else 0
+    skewed = 4 * tmax * units > 5 * work
+    choose = skewed and tmax > 8 and units <= 4 * sms
+    target = base
+    if choose and max_load(items(cands[1])) < max_load(items(cands[0])):
+        target = cands[1]
+    return len(items(target)), choose, target
+
+
+def _random_decode_mix(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(8, 76))
+    kv = np.exp(rng.uniform(np.log(64), np.log(40000), size=n)).astype(int).tolist()
+    return workloads.make_paged("plan_dec_mix", 800 + seed, [1] * n, kv, 32, 8, 128, 64, causal=True,
+                                nan_fill=False)
+
+
+@pytest.mark.parametrize("case", ["decode_batch", "mixed", "mix0", "mix1", "mix2", "mix3"])
+def test_decode_split_target_follows_the_balance_model(case):
+    wl = {"decode_batch": lambda: workloads.named(2), "mixed": lambda: workloads.named(5),
+          "mix0": lambda: _random_decode_mix(0), "mix1": lambda: _random_decode_mix(1),
+          "mix2": lambda: _random_decode_mix(2), "mix3": lambda: _random_decode_mix(3)}[case]()
+    counts = check_plan(wl)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_items, _, _ = host_decode_target_items(wl, sms)
+    assert counts[1] == n_items
