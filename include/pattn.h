@@ -85,6 +85,12 @@ typedef enum pattn_status {
  *
  * All pointers 16-byte aligned. The first call on a device allocates the
  * library workspace (grow-only) unless pattn_set_workspace gave one.
+ *
+ * CUDA graphs: once the workspace is large enough for the bounds (a first
+ * call outside the capture, or pattn_set_workspace), a call only launches
+ * kernels on `stream` and can be captured. The plan is made on the device at
+ * every replay, from whatever the length, offset and table buffers hold then,
+ * within the bounds given at capture.
  */
 pattn_status pattn_forward(void *out, const void *q, const void *kv_pool,
                            const int32_t *block_table, const int32_t *seq_lens,
@@ -236,8 +242,8 @@ pattn_status pattn_selftest_wait_timeout(pattn_stream_t stream);
  * pattn_selftest_attention_timeout -- failure-detection self-test of the
  * attention kernels' own abort path. Runs pattn_forward on the given batch
  * (same arguments and rules) with one change: in each attention kernel the
- * batch launches that has work (the swap-AB decode kernel, the one-CTA
- * prefill kernel), the first CTA's MMA-issuing thread first waits for a
+ * batch launches that has work (the swap-AB decode kernel, the one-q-tile and
+ * two-q-tile prefill kernels), the first CTA's MMA-issuing thread first waits for a
  * barrier phase that nothing completes before that thread's own drain. After
  * the wait limit (about 2 s) the wait gives up: it sets the timeout bit of the
  * device error word and the CTA's abort flag; every role of the CTA then
@@ -272,7 +278,8 @@ pattn_status pattn_selftest_attention_timeout(void *out, const void *q, const vo
  * split units, partial rows}.
  *
  * Item record {x, y, z, w}: x = sequence | split << 24; y = kv_head << 16 |
- * q tile (the first q tile of a CTA pair's two at head_dim 256); z = first KV
+ * q tile (the first of an item's two q tiles: CTA pairs at head_dim 256, the
+ * two-q-tile kernel for non-causal head_dim 128); z = first KV
  * tile << 16 | end KV tile (tiles of 128 keys, or 64 for the one-CTA
  * head_dim-256 prefill kernel); w = first partial row of a split item, -1
  * otherwise. Returns PATTN_ERR_NO_MEMORY if the plan did not fit the
