@@ -244,15 +244,17 @@ def measure(pk, step, seconds, device_index, flush=None, max_steps=0):
 
 def launches_per_step(wl) -> int:
     """Kernels pattn_forward launches for this batch: the plan, the decode kernel
-    when the GQA group fits its 16 rows, the prefill kernel when some unit may
-    hold more than 16 packed rows."""
+    when some unit may hold at most 16 packed rows (the GQA group fits and the
+    bounds leave room for a sequence of at most 16 / G queries: every sequence
+    holds at least total_q - (B - 1) * max_q), the prefill kernel when some unit
+    may hold more than 16 packed rows."""
     g = wl.n_heads_q // wl.n_heads_kv
-    dec = g <= 16
+    dec = g <= 16 and (wl.total_q - (wl.num_seqs - 1) * max(wl.max_q, 0)) * g <= 16
     pre = (not dec) or wl.max_q * g > 16
     return 1 + int(dec) + int(pre)
 
 
-KERNEL_NAMES = {1: "attn_kernel<256,64> (head_dim 256, one CTA; the decode kernel launches empty)",
+KERNEL_NAMES = {1: "attn_kernel<256,64> (head_dim 256, one CTA)",
                 2: "decode_kernel<128> (swap-AB)",
                 3: "attn_kernel<128,128> (one q tile per CTA)",
                 4: "attn2q_kernel (head_dim 128, two q tiles per CTA)",

@@ -336,7 +336,14 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
 
   // ---- tensor maps (bf16, 128-byte swizzle, 64-element inner boxes)
   const int g = sh.group, T = sh.tokens_per_tile;
-  const bool dec_enabled = g <= kDecRows;
+  // Units of at most kDecRows packed rows go to the decode kernel, unless the
+  // bounds leave no room for one: every sequence holds at least
+  // total_q - (num_seqs - 1) * max_q queries. Then the decode kernel is not
+  // launched, and the plan sends every unit to the prefill kernel (which serves
+  // any unit; a caller whose cu_q ends short of total_q only loses speed).
+  const long long min_ql =
+      static_cast<long long>(total_q) - static_cast<long long>(num_seqs - 1) * std::max(max_q, 0);
+  const bool dec_enabled = g <= kDecRows && min_ql * g <= kDecRows;
   const bool run_prefill = !dec_enabled || static_cast<long long>(max_q) * g > kDecRows;
   CUtensorMap tq{}, tq_dec{}, tkv{}, to{};
   if (mode != Mode::kPlanOnly && dec_enabled) {

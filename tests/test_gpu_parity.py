@@ -240,6 +240,28 @@ def test_lengths_beyond_host_bounds_are_rejected_on_device():
     assert_parity(out, wl, rows=[2])
 
 
+@pytest.mark.parametrize("d,hq,hkv", [(256, 24, 4), (128, 8, 2)])
+def test_decode_sized_sequence_that_the_bounds_rule_out_runs_on_the_prefill_kernel(d, hq, hkv):
+    # The decode kernel is not launched when every sequence must hold more than
+    # 16 / G queries (total_q - (B - 1) * max_q of them). A caller whose cu_q
+    # ends short of total_q can still pass a sequence of one query: the plan
+    # then gives its unit to the prefill kernel, which serves it exactly.
+    wl = workloads.make_paged("short_seq", 15, [1, 8, 3], [300, 650, 129], hq, hkv, d, 64, causal=True)
+    d_in = to_device(wl)
+    pad = 40  # rows past cu_q[B]: total_q - 2 * max_q > 16 / G
+    d_in["q"] = torch.cat([d_in["q"], torch.randn(pad, hq, d, device="cuda").to(torch.bfloat16)])
+    import paged_kv_flashattention_varlen_gb300 as pk
+    pre, dec, _ = pk.plan_items(d_in["bt"], d_in["sl"], d_in["cu"], total_q=wl.total_q + pad,
+                                max_q=wl.max_q, max_kv=wl.max_kv, n_heads_q=hq, n_heads_kv=hkv,
+                                head_dim=d, causal=True, num_pages=wl.num_pages)
+    assert dec.shape[0] == 0 and (pre[:, 0] & 0xFFFFFF == 0).any()  # sequence 0 on the prefill list
+    out = torch.full_like(d_in["q"], float("nan"))
+    run_gpu(wl, d=d_in, out=out)
+    assert_parity(out[:wl.total_q], wl)
+    assert torch.isnan(out[wl.total_q:].float()).all()  # rows of no sequence are not written
+    assert _status() == 0
+
+
 # --------------------------------------------------------------- invariants on the GPU
 def test_repeatable_and_page_permutation_bitwise():
     wl = workloads.named(2, scale_down=4)

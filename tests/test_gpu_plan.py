@@ -34,6 +34,14 @@ def cdiv(a, b):
     return -(-a // b)
 
 
+def dec_possible(wl):
+    """The decode kernel serves units of <= 16 packed rows, unless the bounds
+    rule them out: every sequence holds >= total_q - (B - 1) * max_q queries."""
+    G = wl.n_heads_q // wl.n_heads_kv
+    min_ql = wl.total_q - (wl.num_seqs - 1) * max(wl.max_q, 0)
+    return G <= DEC_ROWS and min_ql * G <= DEC_ROWS
+
+
 def expected_units(wl, rejected=()):
     """(list, b, q tile) -> visible KV tiles, for every q tile that makes an item."""
     G = wl.n_heads_q // wl.n_heads_kv
@@ -48,7 +56,7 @@ def expected_units(wl, rejected=()):
         ql, L = int(cu[b + 1] - cu[b]), int(sl[b])
         if ql <= 0 or b in rejected:
             continue
-        dec = G <= DEC_ROWS and ql * G <= DEC_ROWS
+        dec = dec_possible(wl) and ql * G <= DEC_ROWS
         bn = DEC_BN if dec else bn_pre
         nqt = cdiv(ql, T)
 
@@ -185,7 +193,7 @@ def host_decode_target_items(wl, sms):
     tiles = []
     for b in range(wl.num_seqs):
         ql, L = int(cu[b + 1] - cu[b]), int(sl[b])
-        if G <= DEC_ROWS and 1 <= ql and ql * G <= DEC_ROWS:
+        if dec_possible(wl) and 1 <= ql and ql * G <= DEC_ROWS:
             tiles.append(cdiv(L, DEC_BN) if L > 0 else 0)
     work = sum(2 * t for t in tiles) * hkv
     units = len(tiles) * hkv
