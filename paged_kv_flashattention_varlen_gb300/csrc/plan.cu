@@ -33,13 +33,19 @@
 // before `attend` in the GB10 model graph. The attention kernels wait for the
 // whole plan grid, so they read the updated cache, and no launch of its own
 // is spent on the write.
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 
 namespace pattn {
 namespace {
 
+// Threads of the planning CTA: 1024 for large batches; small batches (few
+// sequences and q tiles) plan faster on 128, since every phase of the plan is
+// a block-wide step whose cost grows with the warps that take part.
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreadsSmall = 128;
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -83,8 +89,10 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
   return v;
 }
 
-// Block-wide exclusive scan of two ints per thread; returns both block totals.
+// Block-wide exclusive scan of two ints per thread (NT threads); returns both block totals.
+template <int NT>
 __device__ int2 block_exclusive_scan2(int v0, int v1, int* e0, int* e1, int2* warp_sums) {
+  constexpr int kWarps = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x0 = v0, x1 = v1;
 #pragma unroll
@@ -99,7 +107,7 @@ __device__ int2 block_exclusive_scan2(int v0, int v1, int* e0, int* e1, int2* wa
   if (lane == 31) warp_sums[warp] = make_int2(x0, x1);
   __syncthreads();
   if (warp == 0) {
-    int2 w = warp_sums[lane];
+    int2 w = lane < kWarps ? warp_sums[lane] : make_int2(0, 0);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y0 = __shfl_up_sync(0xffffffffu, w.x, o);
@@ -115,9 +123,37 @@ __device__ int2 block_exclusive_scan2(int v0, int v1, int* e0, int* e1, int2* wa
   const int2 before = warp ? warp_sums[warp - 1] : make_int2(0, 0);
   *e0 = before.x + x0 - v0;
   *e1 = before.y + x1 - v1;
-  const int2 total = warp_sums[31];
+  const int2 total = warp_sums[kWarps - 1];
   __syncthreads();
   return total;
+}
+
+// Exclusive starts of both item lists' histograms, from the most expensive
+// bucket down (a counting sort, longest first); returns the list totals. Each
+// thread takes kHistBuckets / NT consecutive buckets.
+template <int NT>
+__device__ int2 scan_hist_desc(int (*hist)[kHistBuckets], int2* warp_sums) {
+  static_assert(kHistBuckets % NT == 0, "whole buckets per thread");
+  constexpr int R = kHistBuckets / NT;
+  const int c0 = kHistBuckets - 1 - static_cast<int>(threadIdx.x) * R;  // buckets c0, c0 - 1, ..
+  int v0[R], v1[R], s0 = 0, s1 = 0;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    v0[i] = hist[0][c0 - i];
+    v1[i] = hist[1][c0 - i];
+    s0 += v0[i];
+    s1 += v1[i];
+  }
+  int e0, e1;
+  const int2 tot = block_exclusive_scan2<NT>(s0, s1, &e0, &e1, warp_sums);
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    hist[0][c0 - i] = e0;
+    hist[1][c0 - i] = e1;
+    e0 += v0[i];
+    e1 += v1[i];
+  }
+  return tot;
 }
 
 // Work of all q tiles of a sequence in 64-key blocks, for the split heuristic
@@ -191,8 +227,9 @@ __device__ SeqCheck warp_check_seq(const PlanParams& p, int b) {
 // streaming loads, all loads of a chunk issued before its stores.
 __device__ void write_new_rows(const PlanParams& p) {
   const int lane = threadIdx.x & 31;
-  const int warps = (static_cast<int>(gridDim.x) - 1) * (kPlanThreads / 32);
-  const int w = (static_cast<int>(blockIdx.x) - 1) * (kPlanThreads / 32) + (threadIdx.x >> 5);
+  const int per_cta = static_cast<int>(blockDim.x) >> 5;
+  const int warps = (static_cast<int>(gridDim.x) - 1) * per_cta;
+  const int w = (static_cast<int>(blockIdx.x) - 1) * per_cta + (threadIdx.x >> 5);
   const int per = cdiv(p.total_q, warps);
   const int t0 = w * per, t1 = min(p.total_q, t0 + per);
   if (t0 >= t1) return;
@@ -263,7 +300,8 @@ constexpr int kBalanceUnitsPerCta = 4;
 constexpr int kSmemSeqs = 4096;   // sequences whose q-tile prefix is kept in shared memory
 constexpr int kCacheSeqs = 1024;  // sequences whose plan is kept in shared memory
 
-__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams p) {
+template <int NT>
+__global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   __shared__ int2 warp_sums[32];
   __shared__ int hist[2][kHistBuckets];  // [0] prefill items, [1] decode items
   __shared__ int s_qt_prefix[kSmemSeqs];
@@ -271,7 +309,6 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   __shared__ int s_part[kCacheSeqs];     // first partial row of the sequence's split units
   __shared__ int s_carry[4];
   __shared__ unsigned long long s_tiles[2];  // work of the prefill [0] and decode [1] kernels
-  __shared__ int s_chunk[2];
   __shared__ int s_list_items[2];
   __shared__ int s_need_zero;     // some sequence is rejected or has q tiles that see no key
   __shared__ int s_dec_units;     // decode sequences
@@ -291,6 +328,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   // The attention kernels launched after this one may set themselves up now;
   // they read nothing of the plan (nor the cache) before the plan grid has completed.
   grid_dep_launch();
+  // The lines of this thread's sequence lengths and of the start of its block
+  // table row go into L2 while the previous grid finishes (prefetches read no
+  // value: the loads below see any write the previous grid made).
+  if (blockIdx.x == 0 && threadIdx.x < B) {
+    prefetch_l2(p.cu_q + threadIdx.x);
+    prefetch_l2(p.seq_lens + threadIdx.x);
+    if (p.block_table) prefetch_l2(p.block_table + static_cast<size_t>(threadIdx.x) * p.bt_stride);
+  }
   // This grid is itself a dependent launch: it may have become resident while
   // the kernel before it (the previous call's attention, or any other) still
   // ran, and it reads and writes nothing before that grid has completed.
@@ -306,13 +351,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     s_dec_units = s_dec_max = 0;
     s_load[0] = s_load[1] = 0;
   }
-  for (int i = threadIdx.x; i < 2 * kHistBuckets; i += kPlanThreads) (&hist[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < 2 * kHistBuckets; i += NT) (&hist[0][0])[i] = 0;
   __syncthreads();
 
   // ---- pass 1: lengths, KV prefix (contiguous cache), q tile prefix, total work
   unsigned long long my_tiles[2] = {0ull, 0ull};
   unsigned my_dec_units = 0, my_dec_max = 0;
-  for (int base = 0; base < B; base += kPlanThreads) {
+  for (int base = 0; base < B; base += NT) {
     const int b = base + threadIdx.x;
     int q0 = 0, ql = 0, L = 0, nqt = 0;
     bool ok = false;
@@ -341,7 +386,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       }
     }
     int kv_excl, qt_excl;
-    const int2 tot = block_exclusive_scan2(b < B ? max(L, 0) : 0, nqt, &kv_excl, &qt_excl, warp_sums);
+    const int2 tot = block_exclusive_scan2<NT>(b < B ? max(L, 0) : 0, nqt, &kv_excl, &qt_excl, warp_sums);
     if (b < B) {
       // contiguous cache: the sequence's rows must lie inside the K/V planes
       if (ok && !p.block_table &&
@@ -380,7 +425,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   // ---- pass 1b: every live block-table entry must name a pool page (a warp per
   // sequence, eight independent loads per lane in flight)
   if (p.block_table) {
-    for (int b = warp; b < B; b += kPlanThreads / 32) {
+    for (int b = warp; b < B; b += NT / 32) {
       const int4 sq = seq_at(b);
       if (sq.y < 0) continue;
       const int np = cdiv(sq.z, kPage);
@@ -426,14 +471,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     // under both candidates (hist[0] and hist[1], still zero), then the largest
     // CTA load of each under the decode kernel's alternating round robin
     const int cand[2] = {p.target_items, p.target_items + p.target_items / 4};
-    if (threadIdx.x == 0) {
-      s_chunk[0] = chunk_for(1, cand[0]);
-      s_chunk[1] = chunk_for(1, cand[1]);
-    }
-    __syncthreads();
-    const int ct0 = max(1, cdiv(s_chunk[0], kDecBlockN / kPage));
-    const int ct1 = max(1, cdiv(s_chunk[1], kDecBlockN / kPage));
-    for (int b = threadIdx.x; b < B; b += kPlanThreads) {
+    const int ct0 = max(1, cdiv(chunk_for(1, cand[0]), kDecBlockN / kPage));
+    const int ct1 = max(1, cdiv(chunk_for(1, cand[1]), kDecBlockN / kPage));
+    for (int b = threadIdx.x; b < B; b += NT) {
       const int4 sq = seq_at(b);
       if (sq.y <= 0 || !is_decode(p, sq.y)) continue;
       const int tiles = qtile_kv_tiles(p, sq.y, sq.z, 0);
@@ -447,26 +487,22 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
       }
     }
     __syncthreads();
-    int n_items[2];
+    int n_items0, n_items1;
     {
-      // exclusive starts from the most expensive bucket down
-      const int c = kHistBuckets - 1 - threadIdx.x;
-      int e0, e1;
-      const int2 tot = block_exclusive_scan2(hist[0][c], hist[1][c], &e0, &e1, warp_sums);
-      hist[0][c] = e0;
-      hist[1][c] = e1;
-      n_items[0] = tot.x;
-      n_items[1] = tot.y;
+      const int2 tot = scan_hist_desc<NT>(hist, warp_sums);
+      n_items0 = tot.x;
+      n_items1 = tot.y;
       __syncthreads();
     }
-    for (int t0 = 0; t0 < 2 * P; t0 += kPlanThreads) {
+    for (int t0 = 0; t0 < 2 * P; t0 += NT) {
       const int t = t0 + threadIdx.x;
       int load = 0, j = 0;
       if (t < 2 * P) {
         j = t / P;
         const int c = t - j * P;
         const int* start = hist[j];
-        for (int k = 0, pos = c; pos < n_items[j]; pos = cta_item(++k, c, P)) {
+        const int n_j = j ? n_items1 : n_items0;
+        for (int k = 0, pos = c; pos < n_j; pos = cta_item(++k, c, P)) {
           // the cost of item `pos`: the largest bucket whose items begin at or before it
           int lo = 0, hi = kHistBuckets - 1;
           while (lo < hi) {
@@ -486,17 +522,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     }
     __syncthreads();
     if (s_load[1] < s_load[0]) dec_target = cand[1];
-    for (int i = threadIdx.x; i < 2 * kHistBuckets; i += kPlanThreads) (&hist[0][0])[i] = 0;
+    for (int i = threadIdx.x; i < 2 * kHistBuckets; i += NT) (&hist[0][0])[i] = 0;
   }
-  if (threadIdx.x == 0) {
-    s_chunk[0] = chunk_for(0, p.target_items);
-    s_chunk[1] = chunk_for(1, dec_target);
-    s_carry[2] = s_carry[3] = 0;
-  }
-  __syncthreads();
+  // (every thread sizes the chunks itself: no barrier)
+  const int chunk_pre = chunk_for(0, p.target_items), chunk_dec = chunk_for(1, dec_target);
 
   // ---- pass 2: splits of single-q-tile units, partial rows and unit slots
-  for (int base = 0; base < B; base += kPlanThreads) {
+  for (int base = 0; base < B; base += NT) {
     const int b = base + threadIdx.x;
     int S = 1, rows = 0;
     if (b < B) {
@@ -505,7 +537,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
         const int tiles = qtile_kv_tiles(p, sq.y, sq.z, 0);
         const bool dec = is_decode(p, sq.y);
         const int per_tile_shift = (dec ? kDecBlockNShift : p.block_n_shift) - kPageShift;
-        const int chunk_tiles = max(1, (s_chunk[dec ? 1 : 0] + (1 << per_tile_shift) - 1) >> per_tile_shift);
+        const int chunk_tiles = max(1, ((dec ? chunk_dec : chunk_pre) + (1 << per_tile_shift) - 1) >> per_tile_shift);
         if (tiles >= 2) S = min(min(cdiv(tiles, chunk_tiles), kMaxSplits), tiles);
         rows = sq.y * G;
       }
@@ -513,7 +545,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
     const int part_rows = S >= 2 ? p.n_heads_kv * S * rows : 0;
     const int units = S >= 2 ? p.n_heads_kv : 0;
     int part_excl, unit_excl;
-    const int2 tot = block_exclusive_scan2(part_rows, units, &part_excl, &unit_excl, warp_sums);
+    const int2 tot = block_exclusive_scan2<NT>(part_rows, units, &part_excl, &unit_excl, warp_sums);
     if (b < B) {
       // (z, w) of the sequence's plan, stored without reading back its (x, y)
       const int2 sp = make_int2(S, s_carry[3] + unit_excl);
@@ -564,7 +596,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
 
   // ---- pass 3: histogram of item costs (KV tiles per item), one per kernel
   if (!overflow) {
-    for (int gq = threadIdx.x; gq < total_qt; gq += kPlanThreads) {
+    for (int gq = threadIdx.x; gq < total_qt; gq += NT) {
       const int b = seq_of_qtile(gq);
       const int4 sq = seq_at(b);
       if (sq.y <= 0) continue;
@@ -582,12 +614,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   __syncthreads();
   // exclusive scan of each list from the most expensive bucket down
   {
-    static_assert(kHistBuckets == kPlanThreads, "one bucket per thread");
-    const int c = kHistBuckets - 1 - threadIdx.x;
-    int e0, e1;
-    const int2 tot = block_exclusive_scan2(hist[0][c], hist[1][c], &e0, &e1, warp_sums);
-    hist[0][c] = e0;
-    hist[1][c] = e1;
+    const int2 tot = scan_hist_desc<NT>(hist, warp_sums);
     if (threadIdx.x == 0) {
       s_list_items[0] = tot.x;
       s_list_items[1] = tot.y;
@@ -605,22 +632,26 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   // whose units read each page once, keeps the KV heads of a unit together
   // instead (a page holds all heads' rows). Positions within a bucket are
   // taken by atomics, so each head gets a sweep of its own, with a barrier
-  // between sweeps; one sweep when the prefill list is empty.
+  // between sweeps. A prefill list of at most P / 2 items runs in one round on
+  // any prefill kernel (all its items at once), where the order within a
+  // bucket does not matter: it is emitted like the decode list, in one sweep.
   if (!bad_plan) {
-    const int sweeps = s_list_items[0] > 0 ? p.n_heads_kv : 1;
+    const bool one_round = s_list_items[0] <= P / 2;
+    const int sweeps = one_round ? 1 : p.n_heads_kv;
     for (int hk_t = 0; hk_t < sweeps; ++hk_t) {
-      for (int gq = threadIdx.x; gq < total_qt; gq += kPlanThreads) {
+      for (int gq = threadIdx.x; gq < total_qt; gq += NT) {
         const int b = seq_of_qtile(gq);
         const int4 sq = seq_at(b);
         if (sq.y <= 0) continue;
         const int list = is_decode(p, sq.y) ? 1 : 0;
-        if (list == 1 && hk_t != 0) continue;  // the sweep of head 0 emits a decode unit's heads
+        const bool all_heads = list == 1 || one_round;  // the unit's heads together, in one sweep
         const int qt = gq - qtile_first(b);
         const int tiles = item_tiles(sq.y, sq.z, qt);
         if (tiles == 0) continue;
         const int S = sq.w;
         const int rows = sq.y * G;
-        const int nh = list ? p.n_heads_kv : 1;
+        const int nh = all_heads ? p.n_heads_kv : 1;
+        if (all_heads && hk_t != 0) continue;  // (emitted by the sweep of head 0)
         int4* dst = list ? ws.dec_items : ws.items;
         const int part0 = S >= 2 ? part_at(b) : 0;
         for (int s = 0; s < S; ++s) {
@@ -645,7 +676,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(const PlanParams 
   // every sequence if the workspace could not hold the plan). Each thread takes
   // whole sequences; only degenerate inputs reach the stores, and the walk is
   // skipped when pass 1 saw none.
-  for (int b = threadIdx.x; (s_need_zero || bad_plan) && b < B; b += kPlanThreads) {
+  for (int b = threadIdx.x; (s_need_zero || bad_plan) && b < B; b += NT) {
     // the query range of a live sequence from the cached plan; a rejected one's
     // from cu_q (it may be out of range)
     const int4 sq = seq_at(b);
@@ -701,7 +732,19 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(int* err) {
 
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s, bool dependent) {
-  return launch_kernel(plan_kernel, dim3(1 + p.write_ctas), dim3(kPlanThreads), 0, s, dependent, p);
+  // small batches: at most 128 sequences and 256 q tiles (each loop of the
+  // plan then takes one or two rounds of 128 threads)
+  const long long qtiles_bound =
+      (static_cast<long long>(p.total_q) + p.tokens_per_tile - 1) / std::max(p.tokens_per_tile, 1) + p.num_seqs;
+  if (p.num_seqs <= kPlanThreadsSmall && qtiles_bound <= 2 * kPlanThreadsSmall) {
+    // the cache-write CTAs keep a warp per 32 tokens at most, as with the large CTA
+    constexpr int kWarpsSmall = kPlanThreadsSmall / 32;
+    const int write =
+        p.write_ctas > 0 ? std::min((p.total_q + kWarpsSmall - 1) / kWarpsSmall, 8 * p.write_ctas) : 0;
+    return launch_kernel(plan_kernel<kPlanThreadsSmall>, dim3(1 + write), dim3(kPlanThreadsSmall), 0, s,
+                         dependent, p);
+  }
+  return launch_kernel(plan_kernel<kPlanThreads>, dim3(1 + p.write_ctas), dim3(kPlanThreads), 0, s, dependent, p);
 }
 
 cudaError_t launch_wait_selftest(int* err, cudaStream_t s) {
