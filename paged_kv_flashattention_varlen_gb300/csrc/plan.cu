@@ -46,8 +46,15 @@ namespace {
 // a block-wide step whose cost grows with the warps that take part.
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanThreadsSmall = 128;
+constexpr int kPlanSmallSeqs = 32;  // batches of at most this many sequences take the small CTA
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Hint: bring the 128-byte line holding `ptr` into L2 (no value is read; a
+// later load sees whatever was written there meanwhile).
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));
+}
 
 // Units of at most kDecRows packed rows run on the swap-AB decode kernel.
 __device__ __forceinline__ bool is_decode(const PlanParams& p, int ql) {
@@ -732,11 +739,11 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(int* err) {
 
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s, bool dependent) {
-  // small batches: at most 128 sequences and 256 q tiles (each loop of the
-  // plan then takes one or two rounds of 128 threads)
+  // small batches: at most 32 sequences (the block-table check, a warp per
+  // sequence, then takes at most 8 rounds of its four warps) and 256 q tiles
   const long long qtiles_bound =
       (static_cast<long long>(p.total_q) + p.tokens_per_tile - 1) / std::max(p.tokens_per_tile, 1) + p.num_seqs;
-  if (p.num_seqs <= kPlanThreadsSmall && qtiles_bound <= 2 * kPlanThreadsSmall) {
+  if (p.num_seqs <= kPlanSmallSeqs && qtiles_bound <= 2 * kPlanThreadsSmall) {
     // the cache-write CTAs keep a warp per 32 tokens at most, as with the large CTA
     constexpr int kWarpsSmall = kPlanThreadsSmall / 32;
     const int write =

@@ -212,12 +212,6 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const W
 }
 
 // ---------------------------------------------------------------- TMA
-// Hint: bring the 128-byte line holding `ptr` into L2 (no value is read; a
-// later load sees whatever was written there meanwhile).
-__device__ __forceinline__ void prefetch_l2(const void* ptr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));
-}
-
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
