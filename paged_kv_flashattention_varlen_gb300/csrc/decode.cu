@@ -515,7 +515,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       if (last) {
         const int4 si = p.seq_info[iv.x & kSeqMask];
         const int rows = si.y * G;
-        merge_unit<D>(p, si.x, iv.y >> 16, sp.z, iv.w - (iv.x >> kSeqBits) * rows, rows, 0, 1);
+        merge_unit<D, D == 256 ? 2 : 4>(p, si.x, iv.y >> 16, sp.z, iv.w - (iv.x >> kSeqBits) * rows, rows, 0, 1);
       }
     }
   } else if (warp >= 4) {

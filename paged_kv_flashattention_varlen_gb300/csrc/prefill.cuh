@@ -63,7 +63,7 @@ __device__ __forceinline__ bool split_done(const AttnParams& p, const Item& it, 
   if (*flag) {
     const int4 sp = p.seq_plan[it.b];
     const int rows = si.y * p.group;
-    merge_unit<D>(p, si.x, it.hk, sp.z, it.part - it.split * rows, rows, warp - 4, kSoftmaxWarps);
+    merge_unit<D, 1>(p, si.x, it.hk, sp.z, it.part - it.split * rows, rows, warp - 4, kSoftmaxWarps);
   }
   return true;
 }
