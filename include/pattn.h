@@ -81,7 +81,11 @@ typedef enum pattn_status {
  *   num_pages   pages in the pool (bounds every block-table entry).
  *   scale       softmax scale, finite and >= 0.
  *   causal      0: every key of the sequence; 1: keys up to the query position.
- *   stream      stream the launches (plan, decode and/or prefill attention) go on.
+ *   stream      stream the launches go on: the plan, then the decode kernel (units
+ *               of at most 16 packed query rows; not launched when the bounds rule
+ *               such units out, i.e. every sequence holds at least
+ *               total_q - (num_seqs - 1) * max_q > 16 / group queries) and/or the
+ *               prefill kernel (every other unit).
  *
  * All pointers 16-byte aligned. The first call on a device allocates the
  * library workspace (grow-only) unless pattn_set_workspace gave one.
