@@ -445,6 +445,11 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   ap.part_o = ws.part_o;
   ap.part_ml = ws.part_ml;
   ap.err = ws.hdr + kHdrErr;
+  ap.go = ws.hdr + kHdrGo;
+  // bf16 calls that launch both attention kernels: the prefill kernel starts on
+  // the decode kernel's go word (the quantised modes' prefill kernel also reads
+  // what the quantisation kernels write, so it keeps its grid wait)
+  ap.early_start = (mode == Mode::kBf16 && dec_enabled && run_prefill) ? 1 : 0;
   ap.bt_stride = pp.bt_stride;
   ap.num_pages = num_pages;
   ap.n_heads_q = hq;

@@ -328,8 +328,8 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
   if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_dep_wait();    // the plan (and whatever ran before) is complete from here on
-  grid_dep_launch();  // a dependent launch after this grid may take SMs as its CTAs leave
+  prefill_start(p, ctl);  // the plan (and whatever ran before it) is complete from here on
+  grid_dep_launch();      // a dependent launch after this grid may take SMs as its CTAs leave
 
   const int n_items = p.hdr[kHdrItems];
   const int G = p.group;
@@ -1251,6 +1251,7 @@ attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ 
     if constexpr (kPair) tmem_dealloc_pair(tmem, kTmemCols);
     else tmem_dealloc(tmem, kTmemCols);
   }
+  prefill_end(p);
 }
 
 }  // namespace

@@ -187,8 +187,8 @@ attn2q_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  grid_dep_wait();    // the plan (and whatever ran before) is complete from here on
-  grid_dep_launch();  // a dependent launch after this grid may take SMs as its CTAs leave
+  prefill_start(p, ctl);  // the plan (and whatever ran before it) is complete from here on
+  grid_dep_launch();      // a dependent launch after this grid may take SMs as its CTAs leave
 
   const int n_items = p.hdr[kHdrItems];
   const int G = p.group;
@@ -635,6 +635,7 @@ attn2q_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  prefill_end(p);
 }
 
 }  // namespace

@@ -305,6 +305,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   grid_dep_wait();    // the plan is complete from here on
+  // tell the prefill kernel so (it may start on this rather than on this grid)
+  if (p.go && blockIdx.x == 0 && threadIdx.x == 0) st_release_gpu(p.go, 1);
   grid_dep_launch();  // the prefill kernel may take SMs as this grid's CTAs leave
 
   const int n_items = p.hdr[kHdrDecItems];

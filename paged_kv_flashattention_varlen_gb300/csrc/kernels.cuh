@@ -27,8 +27,10 @@ constexpr int kErrBadInput = 1;
 constexpr int kErrTimeout = 2;
 
 // Device workspace header (int words).
+// kHdrGo: the plan grid has completed (reset by the plan, set by the decode
+// kernel's first CTA once past its own grid wait); see AttnParams::early_start.
 enum HdrWord { kHdrErr = 0, kHdrItems = 1, kHdrUnits = 2, kHdrPartRows = 3, kHdrOverflow = 4,
-               kHdrDecItems = 5, kHdrWords = 64 };
+               kHdrDecItems = 5, kHdrGo = 6, kHdrWords = 64 };
 
 // Work item, 16 bytes:
 //   x = sequence b (bits 0-23) | split index << 24 (split items)
@@ -166,6 +168,14 @@ struct AttnParams {
   // thread waits for a barrier phase that nothing completes, so that its
   // bounded wait runs out and the CTA takes its abort-and-drain path
   int selftest_abort;
+  // the workspace's kHdrGo word: the decode kernel sets it once past its grid
+  // wait. With early_start (both attention kernels launched), the prefill kernel
+  // starts on it rather than on the decode grid, so that its CTAs work as soon
+  // as they hold an SM (the decode kernel's last CTAs may still run); each of
+  // its CTAs waits for the decode grid before it exits, so the prefill grid
+  // still completes after it, as stream order requires.
+  int* go;
+  int early_start;
 };
 
 

@@ -714,6 +714,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
     ws.hdr[kHdrUnits] = bad_plan ? 0 : total_units;
     ws.hdr[kHdrPartRows] = total_part_rows;
     ws.hdr[kHdrOverflow] = bad_plan ? 1 : 0;
+    ws.hdr[kHdrGo] = 0;  // set by the decode kernel once this grid has completed
     if (bad_plan) atomicOr(ws.hdr + kHdrErr, kErrBadInput);
   }
 }

@@ -11,6 +11,38 @@ namespace pattn {
 
 constexpr int kSoftmaxWarps = 8;  // warps 4-11 of a prefill CTA
 
+// The start of a prefill CTA: the plan grid must be complete. With
+// p.early_start that is the go word (set by the decode kernel past its own
+// grid wait: thread 0 waits for it, bounded; then every thread reads it with
+// acquire ordering), else the grid before this one. Returns false when the
+// wait ran out (the abort flag and the timeout bit are set).
+__device__ __forceinline__ bool prefill_start(const AttnParams& p, const WaitCtl& ctl) {
+  if (!p.early_start) {
+    grid_dep_wait();
+    return true;
+  }
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t n = 0; ld_acquire_gpu(p.go) == 0; ++n) {
+      if ((n & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) {
+        *ctl.abort = 1;
+        atomicOr(ctl.err, kErrTimeout);
+        break;
+      }
+      __nanosleep(100);
+    }
+  }
+  __syncthreads();
+  (void)ld_acquire_gpu(p.go);
+  return *ctl.abort == 0;
+}
+
+// The end of a prefill CTA: with p.early_start, wait for the grid before
+// this one (the decode kernel), so that this grid completes after it.
+__device__ __forceinline__ void prefill_end(const AttnParams& p) {
+  if (p.early_start) grid_dep_wait();
+}
+
 // part: first partial row of this split, -1 if the item is not split; split:
 // the split's index in its unit.
 struct Item {

@@ -212,6 +212,17 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const W
 }
 
 // ---------------------------------------------------------------- TMA
+// A 32-bit global load with acquire ordering at GPU scope, and a 32-bit global
+// store with release ordering at GPU scope (a flag between grids).
+__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* ptr, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
