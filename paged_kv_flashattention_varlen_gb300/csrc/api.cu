@@ -114,7 +114,7 @@ pattn_status check_args(const void* out, const void* q, const void* kv, const in
 }
 
 struct WsLayout {
-  size_t hdr, seq_info, seq_plan, seq_part, items, dec_items, dec_off, unit_cnt, part_ml, part_o, total;
+  size_t hdr, seq_info, seq_plan, seq_part, items, dec_items, unit_cnt, part_ml, part_o, total;
   int max_items, max_units, max_part_rows;
 };
 
@@ -162,8 +162,6 @@ WsLayout ws_layout(int num_seqs, int total_q, int max_q, int hq, int hkv, int d,
   off += sizeof(int4) * static_cast<size_t>(w.max_items);
   w.dec_items = off = align_up(off, 256);
   off += sizeof(int4) * static_cast<size_t>(w.max_items);
-  w.dec_off = off = align_up(off, 256);
-  off += sizeof(int) * static_cast<size_t>(2 * (kMaxDecCtas + 1));  // CTA runs, group parts
   w.unit_cnt = off = align_up(off, 256);
   off += sizeof(int) * static_cast<size_t>(w.max_units);
   w.part_ml = off = align_up(off, 256);
@@ -329,7 +327,6 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   ws.seq_part = reinterpret_cast<int*>(wsb + L.seq_part);
   ws.items = reinterpret_cast<int4*>(wsb + L.items);
   ws.dec_items = reinterpret_cast<int4*>(wsb + L.dec_items);
-  ws.dec_off = reinterpret_cast<int*>(wsb + L.dec_off);
   ws.unit_cnt = reinterpret_cast<int*>(wsb + L.unit_cnt);
   ws.part_ml = reinterpret_cast<float2*>(wsb + L.part_ml);
   ws.part_o = reinterpret_cast<float*>(wsb + L.part_o);
@@ -427,7 +424,6 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   pp.target_items = plan_target(st.sms);
   pp.min_chunk = kMinChunk;
   pp.ctas = st.sms;
-  pp.streamk = 1;
   if (k_new && mode != Mode::kPlanOnly) {
     // the new tokens' K and V rows go into their cache slots from the plan
     // grid's extra CTAs (a warp per token, at most two CTAs per SM), before any
@@ -450,7 +446,6 @@ pattn_status launch_all(DeviceState& st, uint8_t* wsb, const WsLayout& L, void* 
   ap.part_ml = ws.part_ml;
   ap.err = ws.hdr + kHdrErr;
   ap.go = ws.hdr + kHdrGo;
-  ap.dec_off = ws.dec_off;
   // bf16 calls that launch both attention kernels: the prefill kernel starts on
   // the decode kernel's go word (the quantised modes' prefill kernel also reads
   // what the quantisation kernels write, so it keeps its grid wait)

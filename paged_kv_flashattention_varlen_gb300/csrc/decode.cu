@@ -310,14 +310,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
   grid_dep_launch();  // the prefill kernel may take SMs as this grid's CTAs leave
 
   const int n_items = p.hdr[kHdrDecItems];
-  // this CTA's items: a contiguous run of a stream-K list, else the alternating
-  // rounds of the longest-first list (an index past the list ends a walk)
-  const bool streamk = p.hdr[kHdrDecStreamK] != 0;
-  const int sk0 = streamk ? p.dec_off[blockIdx.x] : 0;
-  const int sk1 = streamk ? p.dec_off[blockIdx.x + 1] : 0;
-  auto item_at = [&](int k) {
-    return streamk ? (sk0 + k < sk1 ? sk0 + k : n_items) : cta_item(k, blockIdx.x, gridDim.x);
-  };
   const int G = p.group;
   const int Tq = p.tokens_per_tile;  // query tokens per decode item (kNQ / G)
   const unsigned full = 0xffffffffu;
@@ -328,8 +320,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     bool ok = true;
     const uint64_t pol_kv = l2_policy_evict_first();
     const uint64_t pol_q = l2_policy_evict_last();
-    for (int kq = 0, idx = item_at(0); idx < n_items && ok;
-         idx = item_at(++kq), ++itl) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
+         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
       const int4 iv = p.items[idx];
       const int b = iv.x & kSeqMask, hk = iv.y >> 16;
       const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
@@ -440,8 +432,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       // phase that nothing completes before the drain below, so the wait runs
       // out and every role of the CTA takes its abort path
       if (p.selftest_abort && blockIdx.x == 0 && n_items > 0) ok = wait_one(bar(kDDrain), 0, ctl);
-      for (int kq = 0, idx = item_at(0); idx < n_items && ok;
-         idx = item_at(++kq), ++itl) {
+      for (int kq = 0, idx = blockIdx.x; idx < n_items && ok;
+         idx = cta_item(++kq, blockIdx.x, gridDim.x), ++itl) {
         const int4 iv = p.items[idx];
         const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
         if (!(ok = wait_one(bar(kDQFull), itl & 1u, ctl))) break;
@@ -476,7 +468,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     // ------------------------------------------------------------ ring forwarder / V tail fix
     uint32_t n = 0;
     bool ok = true;
-    for (int kq = 0, idx = item_at(0); idx < n_items && ok; idx = item_at(++kq)) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok; idx = cta_item(++kq, blockIdx.x, gridDim.x)) {
       const int4 iv = p.items[idx];
       const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
       const int L = p.seq_info[iv.x & kSeqMask].z;
@@ -507,15 +499,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     // warps' path.
     uint32_t nsp = 0;
     bool ok = true;
-    for (int kq = 0, idx = item_at(0); idx < n_items && ok; idx = item_at(++kq)) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok; idx = cta_item(++kq, blockIdx.x, gridDim.x)) {
       const int4 iv = p.items[idx];
       if (iv.w < 0) continue;
       if (!(ok = wait_warp(bar(kDMerge0), nsp & 1u, ctl))) break;
-      const int S = iv.y & 0xFFFF;  // the unit's splits (decode items carry them)
+      const int4 sp = p.seq_plan[iv.x & kSeqMask];
       int last = 0;
       if (lane == 0) {
         __threadfence();
-        last = atomicAdd(&p.unit_cnt[(iv.x & kSeqMask) * p.n_heads_kv + (iv.y >> 16)], 1) == S - 1;
+        last = atomicAdd(&p.unit_cnt[sp.w + (iv.y >> 16)], 1) == sp.z - 1;
         if (last) __threadfence();
       }
       last = __shfl_sync(0xffffffffu, last, 0);
@@ -525,7 +517,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       if (last) {
         const int4 si = p.seq_info[iv.x & kSeqMask];
         const int rows = si.y * G;
-        merge_unit<D, D == 256 ? 2 : 4>(p, si.x, iv.y >> 16, S, iv.w - (iv.x >> kSeqBits) * rows, rows, 0, 1);
+        merge_unit<D, D == 256 ? 2 : 4>(p, si.x, iv.y >> 16, sp.z, iv.w - (iv.x >> kSeqBits) * rows, rows, 0, 1);
       }
     }
   } else if (warp >= 4) {
@@ -542,7 +534,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     x.merge_flag = reinterpret_cast<volatile int*>(misc + 32);
     uint32_t n = 0, itl = 0, nsp = 0;
     bool ok = true;
-    for (int kq = 0, idx = item_at(0); idx < n_items && ok; idx = item_at(++kq)) {
+    for (int kq = 0, idx = blockIdx.x; idx < n_items && ok; idx = cta_item(++kq, blockIdx.x, gridDim.x)) {
       const int4 iv = p.items[idx];
       const int4 si = p.seq_info[iv.x & kSeqMask];
       const int rows = si.y * G;

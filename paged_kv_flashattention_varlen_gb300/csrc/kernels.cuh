@@ -29,10 +29,8 @@ constexpr int kErrTimeout = 2;
 // Device workspace header (int words).
 // kHdrGo: the plan grid has completed (reset by the plan, set by the decode
 // kernel's first CTA once past its own grid wait); see AttnParams::early_start.
-// kHdrDecStreamK: the decode list is a stream-K partition (Workspace::dec_off).
 enum HdrWord { kHdrErr = 0, kHdrItems = 1, kHdrUnits = 2, kHdrPartRows = 3, kHdrOverflow = 4,
-               kHdrDecItems = 5, kHdrGo = 6, kHdrDecStreamK = 7, kHdrWords = 64 };
-constexpr int kMaxDecCtas = 1024;  // decode grids a stream-K list can describe
+               kHdrDecItems = 5, kHdrGo = 6, kHdrWords = 64 };
 
 // Work item, 16 bytes:
 //   x = sequence b (bits 0-23) | split index << 24 (split items)
@@ -49,15 +47,11 @@ constexpr int kSeqMask = (1 << kSeqBits) - 1;
 struct Workspace {
   int* hdr;
   int4* seq_info;
-  int4* seq_plan;   // x = first global q tile, y = q tiles, z = splits (per sequence; not
-                    // used by stream-K decode units), w = the sequence's first decode tile
-                    // on the stream-K axis (its units' tiles, KV heads innermost)
-  int* unit_cnt;    // finished splits of unit (b, hk) at b * n_heads_kv + hk (zeroed by the
-                    // plan for the units it splits)
+  int4* seq_plan;   // x = first global q tile, y = q tiles, z = splits, w = first split unit
+  int* unit_cnt;    // finished splits per split unit (zeroed by the plan)
   int* seq_part;    // first partial row of the sequence's split units
   int4* items;      // prefill kernel items
   int4* dec_items;  // swap-AB decode kernel items
-  int* dec_off;     // stream-K decode list: CTA c takes items [dec_off[c], dec_off[c + 1])
   float* part_o;    // [rows][D] split-normalised partial O
   float2* part_ml;  // [rows] (running max in log2 units, sum of exp2)
   int max_items;
@@ -84,7 +78,6 @@ struct PlanParams {
                         // the decode list may take target_items + target_items / 4 instead
   int min_chunk;        // fewest KV tiles per split
   int ctas;             // persistent CTAs of the decode kernel (its grid)
-  int streamk;          // the decode list may be a stream-K partition (see plan.cu)
   // cache write of the new tokens (pattn_forward_append): CTAs 1..write_ctas of
   // the plan grid copy k_new / v_new [total_q][n_heads_kv][head_dim] into the
   // pool while CTA 0 plans; write_ctas = 0 and null pointers otherwise
@@ -183,9 +176,6 @@ struct AttnParams {
   // still completes after it, as stream order requires.
   int* go;
   int early_start;
-  // stream-K decode list (the header's kHdrDecStreamK): CTA c of the decode
-  // kernel takes items [dec_off[c], dec_off[c + 1])
-  const int* dec_off;
 };
 
 

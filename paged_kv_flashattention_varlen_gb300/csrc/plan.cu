@@ -135,36 +135,6 @@ __device__ int2 block_exclusive_scan2(int v0, int v1, int* e0, int* e1, int2* wa
   return total;
 }
 
-// Block-wide exclusive scan of a third int alongside block_exclusive_scan2's two
-// (its own warp-sum slots); returns the block total.
-template <int NT>
-__device__ int block_exclusive_scan1(int v, int* e, int* wsum) {
-  constexpr int kWarps = NT / 32;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) wsum[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kWarps ? wsum[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    wsum[lane] = w;  // inclusive
-  }
-  __syncthreads();
-  *e = (warp ? wsum[warp - 1] : 0) + x - v;
-  const int total = wsum[kWarps - 1];
-  __syncthreads();
-  return total;
-}
-
 // Exclusive starts of both item lists' histograms, from the most expensive
 // bucket down (a counting sort, longest first); returns the list totals. Each
 // thread takes kHistBuckets / NT consecutive buckets.
@@ -344,10 +314,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   __shared__ int s_qt_prefix[kSmemSeqs];
   __shared__ int4 s_seq[kCacheSeqs];     // x = first token, y = query length (-1 rejected), z = L, w = splits
   __shared__ int s_part[kCacheSeqs];     // first partial row of the sequence's split units
-  __shared__ int s_carry[5];       // KV rows, q tiles, partial rows, segments/units, decode tiles
-  __shared__ int s_wsum1[32];
-  __shared__ int s_split_units;
-  __shared__ int s_rejected;      // some sequence is rejected (its units would leave holes on the stream-K axis)
+  __shared__ int s_carry[4];
   __shared__ unsigned long long s_tiles[2];  // work of the prefill [0] and decode [1] kernels
   __shared__ int s_list_items[2];
   __shared__ int s_need_zero;     // some sequence is rejected or has q tiles that see no key
@@ -386,9 +353,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   }
   if (threadIdx.x == 0) {
     s_tiles[0] = s_tiles[1] = 0ull;
-    s_carry[0] = s_carry[1] = s_carry[2] = s_carry[3] = s_carry[4] = 0;
-    s_split_units = 0;
-    s_rejected = 0;
+    s_carry[0] = s_carry[1] = s_carry[2] = s_carry[3] = 0;
     s_need_zero = 0;
     s_dec_units = s_dec_max = 0;
     s_load[0] = s_load[1] = 0;
@@ -409,10 +374,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
       L = p.seq_lens[b];
       ql = q1 - q0;
       ok = q0 >= 0 && q1 >= q0 && q1 <= p.total_q && ql <= p.max_q && L >= 0 && L <= p.max_kv;
-      if (!ok) {
-        atomicOr(ws.hdr + kHdrErr, kErrBadInput);
-        s_rejected = 1;
-      }
+      if (!ok) atomicOr(ws.hdr + kHdrErr, kErrBadInput);
       // rows to zero: a rejected sequence's, or a first q tile that sees no key
       if (!ok || (ql > 0 && (L == 0 || (p.causal && L - ql + min(ql, p.tokens_per_tile) <= 0))))
         s_need_zero = 1;
@@ -439,7 +401,6 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
         ok = false;
         atomicOr(ws.hdr + kHdrErr, kErrBadInput);
         s_need_zero = 1;
-        s_rejected = 1;
       }
       const int4 si = make_int4(q0, ok ? ql : -1, L, s_carry[0] + kv_excl);
       ws.seq_info[b] = si;
@@ -492,7 +453,6 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
         if (b < kCacheSeqs) s_seq[b].y = -1;
         atomicOr(ws.hdr + kHdrErr, kErrBadInput);
         s_need_zero = 1;
-        s_rejected = 1;
       }
     }
   }
@@ -513,51 +473,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   // max * units * 2 > 2.5 * s_tiles[1], i.e. 4 * max * units > 5 * s_tiles[1]
   const bool skewed = 4ull * static_cast<unsigned long long>(s_dec_max) * static_cast<unsigned long long>(dec_units) >
                       5ull * s_tiles[1];
-  // ---- stream-K decode list: lay every decode sequence's KV tiles (one head's
-  // worth; sequences in order, T tiles in all) on one axis and cut it into
-  // PG = P / Hkv equal group ranges [floor(j T / PG), floor((j + 1) T / PG));
-  // CTA j Hkv + h of the decode kernel takes head h of every sequence part in
-  // range j. Every CTA gets the same tiles to one, whatever the length mix, and
-  // the Hkv CTAs of a group read each page at the same time (a page holds every
-  // head's rows). A sequence that a group boundary cuts is split (every head
-  // alike), and each unit is merged by the CTA that finishes its last part.
-  // Taken for skewed lengths (as above) when no sequence is rejected, each CTA
-  // gets at least two smallest splits' worth of tiles and no sequence exceeds
-  // kMaxSplits parts; otherwise the longest-first list with per-sequence splits
-  // below. (Measured on one GB300: the mixed batch's head_dim-256 decode part
-  // 0.267 -> 0.262 ms; the decode batch, uniform lengths, 0.1758 -> 0.1792 ms,
-  // its ~20 % more items and a merge at every CTA's end costing more than the
-  // 3.4 % imbalance of the longest-first list.)
-  const int PG = P / max(p.n_heads_kv, 1);
-  // (the decode list's work counts 2 blocks of 64 keys per tile, for every KV head)
-  const long long dec_T = static_cast<long long>(s_tiles[1] / (2ull * max(p.n_heads_kv, 1)));
-  bool streamk = p.streamk && skewed && !s_rejected && PG >= 1 && P <= kMaxDecCtas &&
-                       dec_T >= 2ll * PG * dec_min_split_tiles &&
-                       static_cast<long long>(s_dec_max) * PG < static_cast<long long>(kMaxSplits - 2) * dec_T;
-  // group of axis tile g: the largest j with floor(j T / PG) <= g
-  auto sk_grp = [&](long long g) { return static_cast<int>(((g + 1) * PG - 1) / dec_T); };
-  auto sk_start = [&](int j) { return static_cast<long long>(j) * dec_T / PG; };
-  int* grp_first = ws.dec_off + (kMaxDecCtas + 1);  // first axis part of each group (scratch)
-  if (streamk) {
-    // ---- pass 2a: each decode sequence's first tile on the axis (seq_plan.w)
-    for (int base = 0; base < B; base += NT) {
-      const int b = base + threadIdx.x;
-      int t = 0;
-      if (b < B) {
-        const int4 sq = seq_at(b);
-        if (sq.y > 0 && is_decode(p, sq.y)) t = qtile_kv_tiles(p, sq.y, sq.z, 0);
-      }
-      int excl;
-      const int tot = block_exclusive_scan1<NT>(t, &excl, s_wsum1);
-      if (b < B) ws.seq_plan[b].w = s_carry[4] + excl;
-      __syncthreads();
-      if (threadIdx.x == 0) s_carry[4] += tot;
-      __syncthreads();
-    }
-    streamk = s_carry[4] == dec_T;  // (the same tiles as the work total: a check)
-  }
-  if (!streamk && skewed && s_dec_max > dec_min_split_tiles &&
-      dec_units <= static_cast<long long>(kBalanceUnitsPerCta) * P) {
+  if (skewed && s_dec_max > dec_min_split_tiles && dec_units <= static_cast<long long>(kBalanceUnitsPerCta) * P) {
     // ---- the decode list's target, per call: counting sorts of its item costs
     // under both candidates (hist[0] and hist[1], still zero), then the largest
     // CTA load of each under the decode kernel's alternating round robin
@@ -618,60 +534,39 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
   // (every thread sizes the chunks itself: no barrier)
   const int chunk_pre = chunk_for(0, p.target_items), chunk_dec = chunk_for(1, dec_target);
 
-  // ---- pass 2: splits of single-q-tile units and their partial rows (on the
-  // stream-K axis, a decode sequence's parts)
+  // ---- pass 2: splits of single-q-tile units, partial rows and unit slots
   for (int base = 0; base < B; base += NT) {
     const int b = base + threadIdx.x;
-    int S = 1, rows = 0, part_rows = 0, segs = 0, split_units = 0;
-    bool sk = false;
-    long long g_seq = 0;
-    int j0 = 0;
+    int S = 1, rows = 0;
     if (b < B) {
       const int4 sq = seq_at(b);
       if (sq.y > 0 && sq.y <= p.tokens_per_tile) {  // one q tile
         const int tiles = qtile_kv_tiles(p, sq.y, sq.z, 0);
         const bool dec = is_decode(p, sq.y);
+        const int per_tile_shift = (dec ? kDecBlockNShift : p.block_n_shift) - kPageShift;
+        const int chunk_tiles = max(1, ((dec ? chunk_dec : chunk_pre) + (1 << per_tile_shift) - 1) >> per_tile_shift);
+        if (tiles >= 2) S = min(min(cdiv(tiles, chunk_tiles), kMaxSplits), tiles);
         rows = sq.y * G;
-        if (streamk && dec) {
-          sk = tiles > 0;
-          if (sk) {
-            g_seq = ws.seq_plan[b].w;
-            j0 = sk_grp(g_seq);
-            S = sk_grp(g_seq + tiles - 1) - j0 + 1;
-            segs = S;
-          }
-        } else {
-          const int per_tile_shift = (dec ? kDecBlockNShift : p.block_n_shift) - kPageShift;
-          const int chunk_tiles = max(1, ((dec ? chunk_dec : chunk_pre) + (1 << per_tile_shift) - 1) >> per_tile_shift);
-          if (tiles >= 2) S = min(min(cdiv(tiles, chunk_tiles), kMaxSplits), tiles);
-        }
-        if (S >= 2) {
-          part_rows = p.n_heads_kv * S * rows;
-          split_units = p.n_heads_kv;
-        }
       }
     }
-    int part_excl, seg_excl;
-    const int2 tot = block_exclusive_scan2<NT>(part_rows, segs, &part_excl, &seg_excl, warp_sums);
+    const int part_rows = S >= 2 ? p.n_heads_kv * S * rows : 0;
+    const int units = S >= 2 ? p.n_heads_kv : 0;
+    int part_excl, unit_excl;
+    const int2 tot = block_exclusive_scan2<NT>(part_rows, units, &part_excl, &unit_excl, warp_sums);
     if (b < B) {
-      const int part0 = s_carry[2] + part_excl;
-      // (z, and for a stream-K sequence y = its first part on the axis)
-      if (sk) ws.seq_plan[b].y = s_carry[3] + seg_excl;
-      ws.seq_plan[b].z = S;
-      ws.seq_part[b] = part0;
+      // (z, w) of the sequence's plan, stored without reading back its (x, y)
+      const int2 sp = make_int2(S, s_carry[3] + unit_excl);
+      *reinterpret_cast<int2*>(&ws.seq_plan[b].z) = sp;
+      ws.seq_part[b] = s_carry[2] + part_excl;
       if (b < kCacheSeqs) {
         s_seq[b].w = S;
-        s_part[b] = part0;
+        s_part[b] = s_carry[2] + part_excl;
       }
-      // the finished-split counters of the sequence's units start at zero
-      if (S >= 2)
-        for (int hk = 0; hk < p.n_heads_kv; ++hk) ws.unit_cnt[b * p.n_heads_kv + hk] = 0;
-      // the part that opens a group range records where the group's parts begin
-      for (int sp = 0; sk && sp < S; ++sp)
-        if (max(g_seq, sk_start(j0 + sp)) == sk_start(j0 + sp)) grp_first[j0 + sp] = s_carry[3] + seg_excl + sp;
+      // the finished-split counters of the unit's KV heads start at zero (a plan
+      // with more units than the workspace holds is rejected below)
+      if (S >= 2 && sp.y + p.n_heads_kv <= ws.max_units)
+        for (int hk = 0; hk < p.n_heads_kv; ++hk) ws.unit_cnt[sp.y + hk] = 0;
     }
-    const int su = __reduce_add_sync(0xffffffffu, split_units);
-    if (lane == 0 && su != 0) atomicAdd(&s_split_units, su);
     __syncthreads();
     if (threadIdx.x == 0) {
       s_carry[2] += tot.x;
@@ -679,40 +574,8 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
     }
     __syncthreads();
   }
-  if (streamk) {
-    // ---- the stream-K decode list, CTA-major: CTA j Hkv + h takes head h of
-    // group j's parts, n_j = grp_first[j + 1] - grp_first[j] of them
-    if (threadIdx.x == 0) grp_first[PG] = s_carry[3];
-    __syncthreads();
-    const int hkv = p.n_heads_kv;
-    for (int b = threadIdx.x; b < B; b += NT) {
-      const int4 sq = seq_at(b);
-      if (sq.y <= 0 || !is_decode(p, sq.y)) continue;
-      const int tiles = qtile_kv_tiles(p, sq.y, sq.z, 0);
-      if (tiles == 0) continue;
-      const long long g0 = ws.seq_plan[b].w, g1 = g0 + tiles;
-      const int gi0 = ws.seq_plan[b].y, S = sq.w, rows = sq.y * G, part0 = part_at(b);
-      const int j0 = sk_grp(g0);
-      for (int sp = 0; sp < S; ++sp) {
-        const int j = j0 + sp, first = grp_first[j], n_j = grp_first[j + 1] - first;
-        const long long a = max(g0, sk_start(j)), e = min(g1, sk_start(j + 1));
-        const int z = (static_cast<int>(a - g0) << 16) | static_cast<int>(e - g0);
-        for (int hk = 0; hk < hkv; ++hk) {
-          const int pos = first * hkv + hk * n_j + (gi0 + sp - first);
-          if (pos < ws.max_items)
-            ws.dec_items[pos] = make_int4(b | (sp << kSeqBits), (hk << 16) | S, z,
-                                          S >= 2 ? part0 + (hk * S + sp) * rows : -1);
-        }
-      }
-    }
-    for (int c = threadIdx.x; c <= P; c += NT) {
-      const int j = c / hkv, h = c - j * hkv;
-      ws.dec_off[c] = j < PG ? grp_first[j] * hkv + h * (grp_first[j + 1] - grp_first[j]) : grp_first[PG] * hkv;
-    }
-  }
   const int total_part_rows = s_carry[2];
-  const int total_units = s_split_units;
-  const int sk_items = s_carry[3] * p.n_heads_kv;  // stream-K decode items
+  const int total_units = s_carry[3];
   const bool overflow = total_part_rows > ws.max_part_rows || total_units > ws.max_units;
 
   // global q tile -> (sequence, q tile): the last sequence whose first q tile is <= gq
@@ -747,7 +610,6 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
       const int tiles = item_tiles(sq.y, sq.z, gq - qtile_first(b));
       if (tiles == 0) continue;
       const int list = is_decode(p, sq.y) ? 1 : 0;
-      if (list == 1 && streamk) continue;  // (emitted in pass 2)
       for (int s = 0; s < sq.w; ++s) {
         // (s <= 64 and tiles < 2^16: 32-bit products)
         const int k0 = s * tiles / sq.w;
@@ -762,7 +624,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
     const int2 tot = scan_hist_desc<NT>(hist, warp_sums);
     if (threadIdx.x == 0) {
       s_list_items[0] = tot.x;
-      s_list_items[1] = streamk ? sk_items : tot.y;
+      s_list_items[1] = tot.y;
     }
     __syncthreads();
   }
@@ -789,7 +651,6 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
         const int4 sq = seq_at(b);
         if (sq.y <= 0) continue;
         const int list = is_decode(p, sq.y) ? 1 : 0;
-        if (list == 1 && streamk) continue;  // (emitted in pass 2)
         const bool all_heads = list == 1 || one_round;  // the unit's heads together, in one sweep
         const int qt = gq - qtile_first(b);
         const int tiles = item_tiles(sq.y, sq.z, qt);
@@ -806,13 +667,11 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
           const int pos = atomicAdd(&hist[list][min(k1 - k0, kHistBuckets - 1)], nh);
           for (int j = 0; j < nh; ++j) {
             const int hk = hk_t + j;
-            // decode items carry their unit's splits where prefill items carry the q tile
-            const int y_lo = list ? S : qt;
             if (S >= 2)  // split s of the (b, hk) unit (q tile 0)
-              dst[pos + j] = make_int4(b | (s << kSeqBits), (hk << 16) | y_lo, (k0 << 16) | k1,
+              dst[pos + j] = make_int4(b | (s << kSeqBits), hk << 16, (k0 << 16) | k1,
                                        part0 + (hk * S + s) * rows);
             else
-              dst[pos + j] = make_int4(b, (hk << 16) | y_lo, (k0 << 16) | k1, -1);
+              dst[pos + j] = make_int4(b, (hk << 16) | qt, (k0 << 16) | k1, -1);
           }
         }
       }
@@ -856,7 +715,6 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(const PlanParams p) {
     ws.hdr[kHdrPartRows] = total_part_rows;
     ws.hdr[kHdrOverflow] = bad_plan ? 1 : 0;
     ws.hdr[kHdrGo] = 0;  // set by the decode kernel once this grid has completed
-    ws.hdr[kHdrDecStreamK] = (streamk && !bad_plan) ? 1 : 0;
     if (bad_plan) atomicOr(ws.hdr + kHdrErr, kErrBadInput);
   }
 }

@@ -81,7 +81,7 @@ __device__ __forceinline__ bool split_done(const AttnParams& p, const Item& it, 
       int last = 0;
       if (ok) {
         const int4 sp = p.seq_plan[it.b];
-        last = atomicAdd(&p.unit_cnt[it.b * p.n_heads_kv + it.hk], 1) == sp.z - 1;
+        last = atomicAdd(&p.unit_cnt[sp.w + it.hk], 1) == sp.z - 1;
         if (last) __threadfence();
       }
       *flag = last;

@@ -262,20 +262,6 @@ def test_decode_sized_sequence_that_the_bounds_rule_out_runs_on_the_prefill_kern
     assert _status() == 0
 
 
-@pytest.mark.parametrize("d,hq,hkv,ql", [(128, 32, 8, 1), (128, 16, 4, 4), (256, 16, 2, 1), (256, 16, 2, 2)])
-def test_skewed_decode_batch_on_the_stream_k_list(d, hq, hkv, ql):
-    # log-uniform KV lengths (64 to 40,000) over 48 sequences: skewed enough, and
-    # with enough tiles, for the planner's stream-K decode list (sequences cut
-    # at group boundaries into split units, merged in the kernel); every row
-    # against the oracle
-    rng = np.random.default_rng(77 + d + ql)
-    kv = np.exp(rng.uniform(np.log(64), np.log(40000), size=48)).astype(int).tolist()
-    kv[3] = 40000
-    wl = workloads.make_paged("streamk", 90 + d + ql, [ql] * 48, kv, hq, hkv, d, 64, causal=True, extra_pages=2)
-    assert_parity(run_gpu(wl), wl)
-    assert _status() == 0
-
-
 # --------------------------------------------------------------- invariants on the GPU
 def test_repeatable_and_page_permutation_bitwise():
     wl = workloads.named(2, scale_down=4)

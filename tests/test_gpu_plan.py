@@ -42,51 +42,6 @@ def dec_possible(wl):
     return G <= DEC_ROWS and min_ql * G <= DEC_ROWS
 
 
-def host_streamk(wl, sms, rejected=()):
-    """The stream-K decode list, written out on the host, or None when the
-    planner keeps the longest-first list. Taken for skewed lengths (longest
-    unit > 2.5 x the mean decode unit). Every decode sequence's KV tiles (128
-    keys, one head's worth) on one axis, sequences in order, T tiles in all; PG =
-    sms // Hkv group ranges [j T // PG, (j + 1) T // PG); CTA j * Hkv + h takes
-    head h of group j's sequence parts. Taken when no sequence is rejected,
-    T >= 2 * PG * 8 and the longest sequence times PG < 62 * T. Items (b, hk,
-    part index, parts, first tile, end tile) in list order: CTA-major."""
-    if rejected or not dec_possible(wl):
-        return None
-    G = wl.n_heads_q // wl.n_heads_kv
-    hkv = wl.n_heads_kv
-    cu = wl.cu_q.numpy().astype(np.int64)
-    sl = wl.seq_lens.numpy().astype(np.int64)
-    seqs, n_dec = [], 0
-    for b in range(wl.num_seqs):
-        ql, L = int(cu[b + 1] - cu[b]), int(sl[b])
-        if 1 <= ql and ql * G <= DEC_ROWS:
-            n_dec += 1
-            if L > 0:
-                seqs.append((b, cdiv(L, DEC_BN)))  # a decode unit's one q tile sees keys [0, L)
-    PG = sms // hkv
-    T = sum(t for _, t in seqs)
-    tmax = max([t for _, t in seqs] or [0])
-    skewed = 4 * tmax * n_dec > 10 * T  # longest > 2.5 x the mean (over units with no key too)
-    if not (skewed and PG >= 1 and T >= 2 * PG * 8 and tmax * PG < (MAX_SPLITS - 2) * T):
-        return None
-    groups = [[] for _ in range(PG)]  # per group: (b, part, parts, first tile, end tile)
-    g = 0
-    for b, t in seqs:
-        j0, j1 = ((g + 1) * PG - 1) // T, ((g + t) * PG - 1) // T
-        S = j1 - j0 + 1
-        for sp in range(S):
-            j = j0 + sp
-            a, e = max(g, j * T // PG), min(g + t, (j + 1) * T // PG)
-            groups[j].append((b, sp, S, a - g, e - g))
-        g += t
-    items = []
-    for j in range(PG):
-        for hk in range(hkv):
-            items += [(b, hk, sp, S, k0, k1) for b, sp, S, k0, k1 in groups[j]]
-    return items
-
-
 def expected_units(wl, rejected=()):
     """(list, b, q tile) -> visible KV tiles, for every q tile that makes an item."""
     G = wl.n_heads_q // wl.n_heads_kv
@@ -132,27 +87,16 @@ def check_plan(wl, rejected=()):
     assert counts[0] == len(pre) and counts[1] == len(dec)
     units = expected_units(wl, rejected)
     hkv = wl.n_heads_kv
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    sk = host_streamk(wl, sms, rejected)
-    if sk is not None:
-        # the stream-K decode list, exactly and in order
-        got_sk = [(x & ((1 << SEQ_BITS) - 1), y >> 16, x >> SEQ_BITS, y & 0xFFFF, z >> 16, z & 0xFFFF)
-                  for x, y, z, w in dec.tolist()]
-        assert got_sk == sk, "stream-K decode list differs from the host partition"
     got = collections.defaultdict(list)  # (list, b, hk, qt) -> [(k0, k1, split, w)]
     for lst, items in ((0, pre), (1, dec)):
         cost = (items[:, 2] & 0xFFFF) - ((items[:, 2] >> 16) & 0xFFFF)
         assert np.all(cost > 0)
-        if not (lst == 1 and sk is not None):
-            assert np.all(np.diff(np.minimum(cost, 1023)) <= 0), "list not longest first"
+        assert np.all(np.diff(np.minimum(cost, 1023)) <= 0), "list not longest first"
         for x, y, z, w in items.tolist():
             b, s = x & ((1 << SEQ_BITS) - 1), x >> SEQ_BITS
-            # decode items carry their unit's parts where prefill items carry the q tile
-            hk, qt = y >> 16, (0 if lst == 1 else y & 0xFFFF)
+            hk, qt = y >> 16, y & 0xFFFF
             assert 0 <= hk < hkv
-            if lst == 1:
-                assert (y & 0xFFFF) >= 1
-            got[(lst, b, hk, qt)].append((z >> 16, z & 0xFFFF, s, w, y & 0xFFFF))
+            got[(lst, b, hk, qt)].append((z >> 16, z & 0xFFFF, s, w))
     want_keys = {(lst, b, hk, qt) for (lst, b, qt) in units for hk in range(hkv)}
     assert set(got) == want_keys, (sorted(set(got) ^ want_keys)[:8])
     split_units, part_ranges = 0, []
@@ -163,21 +107,18 @@ def check_plan(wl, rejected=()):
         assert its[0][0] == 0 and its[-1][1] == n, "KV range not covered"
         for a, c in zip(its, its[1:]):
             assert a[1] == c[0], "gap or overlap between splits"
-        if lst == 1:
-            assert all(i[4] == S for i in its), "decode item's part count"
         if S == 1:
             assert its[0][2] == 0 and its[0][3] == -1
             continue
         assert nqt == 1 and S <= MAX_SPLITS, "only single-q-tile units split"
-        if not (lst == 1 and sk is not None):
-            for k0, k1, s, w, _ in its:
-                assert (k0, k1) == (s * n // S, (s + 1) * n // S), "unbalanced split"
+        for k0, k1, s, w in its:
+            assert (k0, k1) == (s * n // S, (s + 1) * n // S), "unbalanced split"
         ss = sorted(i[2] for i in its)
         assert ss == list(range(S))
-        base = {w - s * rows for _, _, s, w, _ in its}
-        assert len(base) == 1, "partial rows of one unit not in its slots"
-        b0 = base.pop()
-        part_ranges.append((b0, b0 + S * rows))
+        part0 = {w - (hk * S + s) * rows for _, _, s, w in its}
+        assert len(part0) == 1, "partial rows of one unit not in its slots"
+        p0 = part0.pop()
+        part_ranges.append((p0 + hk * S * rows, p0 + (hk + 1) * S * rows))
         split_units += 1
     assert split_units == counts[2]
     part_ranges.sort()
@@ -282,9 +223,6 @@ def host_decode_target_items(wl, sms):
             best = max(best, load)
         return best
 
-    sk = host_streamk(wl, sms)
-    if sk is not None:
-        return len(sk), False, base
     tmax = max(tiles) if tiles else 0
     skewed = 4 * tmax * units > 5 * work
     choose = skewed and tmax > 8 and units <= 4 * sms
@@ -302,22 +240,11 @@ def _random_decode_mix(seed):
                                 nan_fill=False)
 
 
-def _small_skewed_mix(seed):
-    # skewed lengths but too few tiles for the stream-K list: the per-call split
-    # target of the longest-first list decides
-    rng = np.random.default_rng(seed)
-    kv = np.exp(rng.uniform(np.log(64), np.log(6000), size=12)).astype(int).tolist()
-    kv[0] = 6000
-    return workloads.make_paged("plan_dec_small", 850 + seed, [1] * 12, kv, 32, 8, 128, 64, causal=True,
-                                nan_fill=False)
-
-
-@pytest.mark.parametrize("case", ["decode_batch", "mixed", "mix0", "mix1", "mix2", "mix3", "small0", "small1"])
+@pytest.mark.parametrize("case", ["decode_batch", "mixed", "mix0", "mix1", "mix2", "mix3"])
 def test_decode_split_target_follows_the_balance_model(case):
     wl = {"decode_batch": lambda: workloads.named(2), "mixed": lambda: workloads.named(5),
           "mix0": lambda: _random_decode_mix(0), "mix1": lambda: _random_decode_mix(1),
-          "mix2": lambda: _random_decode_mix(2), "mix3": lambda: _random_decode_mix(3),
-          "small0": lambda: _small_skewed_mix(0), "small1": lambda: _small_skewed_mix(1)}[case]()
+          "mix2": lambda: _random_decode_mix(2), "mix3": lambda: _random_decode_mix(3)}[case]()
     counts = check_plan(wl)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     n_items, _, _ = host_decode_target_items(wl, sms)
