@@ -50,3 +50,16 @@ def test_reference_line_matches_the_gpu_arm(ref_line):
     assert ref_line["unit"] == "GB/s" and ref_line["higher_is_better"] is True
     assert ref_line["scaling"] == "weak" and ref_line["vs_baseline"] is None
     assert ref_line["config"] == bench.headline_config(workloads, wl, 1)
+
+
+@pytest.mark.parametrize("index,launches", [(1, 2), (2, 2), (3, 2), (4, 2), (5, 3)])
+def test_launch_count_claim_follows_the_launch_rules(index, launches):
+    # the line's gpu_launches claim: the plan, then the decode kernel only when
+    # some unit may hold <= 16 packed rows (not when every sequence must hold
+    # more than 16 / G queries: the tiny decode's 8-query sequences at G 6, the
+    # prefill batches), and the prefill kernel only when some unit may hold more
+    # (not the decode batch's 1-query sequences at G 4)
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    assert bench.launches_per_step(workloads.named(index, scale_down=1 if index < 3 else 16)) == launches
