@@ -54,7 +54,8 @@ struct DCfg {
 // P is double-buffered: p_full[b] / pv_done[b] complete once per use of P buffer b.
 enum DBar { kDQFull = 0, kDQEmpty, kDSFull0, kDSFull1, kDSFree0, kDSFree1, kDPFull0, kDPFull1,
             kDPVDone0, kDPVDone1, kDDrain, kDRedMax0, kDRedMax1, kDRedSum, kDMerge0, kDMerge1,
-            kDRingFull0 = 16 };  // then ring full [R], ring ready [R], ring empty [R]
+            kDRingFull0 = 16,    // then ring full [R], ring ready [R], ring empty [R]
+            kDDrainPV = 40 };    // the PV warp's drain (after the ring's 3 R <= 18)
 
 struct SoftCtx {
   uint8_t* smem;
@@ -282,6 +283,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
       mbar_init(bar(kDPVDone0 + s), 1);
     }
     mbar_init(bar(kDDrain), 1);
+    mbar_init(bar(kDDrainPV), 1);
     mbar_init(bar(kDRedMax0), 4);
     mbar_init(bar(kDRedMax1), 4);
     mbar_init(bar(kDRedSum), 4);
@@ -397,37 +399,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA warp
+    // ------------------------------------------------------------ QK MMA warp
+    // S^T = K Q^T for every tile, issued by one thread; the PV MMAs come from
+    // warp 8, so that a PV waiting for its P never holds up the next QK (and
+    // each V stage is released as soon as its PV is done)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kNQ, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kNQ, true, false);
       const SmemDesc dring_k = sw128_desc_split(sRing, 16, 1024);          // K tiles, K-major
-      const SmemDesc dring_v = sw128_desc_split(sRing, kDBN * 128, 1024);  // V tiles, MN-major
       const SmemDesc dq = sw128_desc_split(sQ, 16, 1024);
-      const SmemDesc dp = sw128_desc_split(sP, 16, 1024);
       uint32_t n = 0, itl = 0;
       bool ok = true;
-      auto issue_pv = [&](uint32_t m, bool first) -> bool {
-        const uint32_t fv = 2 * m + 1, s = fv % R, ph = (fv / R) & 1u;
-        if (!wait_one(bar(kDPFull0 + (m & 1u)), (m >> 1) & 1u, ctl)) return false;
-        if (!wait_one(ring_ready(s), ph, ctl)) return false;
-        tc_fence_after();
-        const uint32_t v_lo = desc_lo_at(dring_v, s * C::kStage);
-        const uint32_t p_lo = desc_lo_at(dp, (m & 1u) * C::kPBytes);
-#pragma unroll
-        for (int kk = 0; kk < kDBN / 16; ++kk) {
-          const uint32_t b_lo = p_lo + (((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4);
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) {
-            const uint32_t a_lo = v_lo + (((2 * h) * (kDBN * 128) + kk * (16 * 128)) >> 4);
-            umma_f16_ss(tmem + C::kColO + h * kNQ, a_lo, dring_v.hi, b_lo, dp.hi, idesc_pv,
-                        (first && kk == 0) ? 0u : 1u);
-          }
-        }
-        umma_commit(ring_empty(s));
-        umma_commit(bar(kDPVDone0 + (m & 1u)));
-        return true;
-      };
       // failure-detection self-test: the first CTA's MMA thread first waits for a
       // phase that nothing completes before the drain below, so the wait runs
       // out and every role of the CTA takes its abort path
@@ -454,11 +435,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
           }
           umma_commit(ring_empty(s));
           umma_commit(bar(kDSFull0 + sb));
-          if (kt > kt0 && !(ok = issue_pv(n - 1, kt - 1 == kt0))) break;
         }
         if (!ok) break;
-        umma_commit(bar(kDQEmpty));
-        if (!(ok = issue_pv(n - 1, kt1 - 1 == kt0))) break;
+        umma_commit(bar(kDQEmpty));  // the item's last QK has read Q
       }
       umma_commit(bar(kDDrain));
       wait_one(bar(kDDrain), 0, drain_ctl);
@@ -520,6 +499,45 @@ decode_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant_
         merge_unit<D, D == 256 ? 2 : 4>(p, si.x, iv.y >> 16, sp.z, iv.w - (iv.x >> kSeqBits) * rows, rows, 0, 1);
       }
     }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ PV MMA warp
+    // O^T += V^T P^T for every tile, one thread, as soon as the tile's P is
+    // written and its V stage forwarded; the commit releases that V stage
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, kNQ, true, false);
+      const SmemDesc dring_v = sw128_desc_split(sRing, kDBN * 128, 1024);  // V tiles, MN-major
+      const SmemDesc dp = sw128_desc_split(sP, 16, 1024);
+      uint32_t n = 0;
+      bool ok = true;
+      for (int kq = 0, idx = blockIdx.x; idx < n_items && ok; idx = cta_item(++kq, blockIdx.x, gridDim.x)) {
+        const int4 iv = p.items[idx];
+        const int kt0 = (iv.z >> 16) & 0xFFFF, kt1 = iv.z & 0xFFFF;
+        for (int kt = kt0; kt < kt1; ++kt, ++n) {
+          const uint32_t fv = 2 * n + 1, s = fv % R, ph = (fv / R) & 1u;
+          if (!(ok = wait_one(bar(kDPFull0 + (n & 1u)), (n >> 1) & 1u, ctl))) break;
+          if (!(ok = wait_one(ring_ready(s), ph, ctl))) break;
+          tc_fence_after();
+          const uint32_t v_lo = desc_lo_at(dring_v, s * C::kStage);
+          const uint32_t p_lo = desc_lo_at(dp, (n & 1u) * C::kPBytes);
+          const bool first = kt == kt0;
+#pragma unroll
+          for (int kk = 0; kk < kDBN / 16; ++kk) {
+            const uint32_t b_lo = p_lo + (((kk >> 2) * (kNQ * 128) + (kk & 3) * 32) >> 4);
+#pragma unroll
+            for (int h = 0; h < C::kHalves; ++h) {
+              const uint32_t a_lo = v_lo + (((2 * h) * (kDBN * 128) + kk * (16 * 128)) >> 4);
+              umma_f16_ss(tmem + C::kColO + h * kNQ, a_lo, dring_v.hi, b_lo, dp.hi, idesc_pv,
+                          (first && kk == 0) ? 0u : 1u);
+            }
+          }
+          umma_commit(ring_empty(s));
+          umma_commit(bar(kDPVDone0 + (n & 1u)));
+        }
+      }
+      umma_commit(bar(kDDrainPV));
+      wait_one(bar(kDDrainPV), 0, drain_ctl);
+    }
+    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax: one key per thread
     SoftCtx x;

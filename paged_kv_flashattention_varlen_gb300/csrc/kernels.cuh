@@ -12,7 +12,7 @@ namespace pattn {
 
 constexpr int kBM = 128;            // packed query rows per tile (tokens x GQA group)
 constexpr int kPage = 64;           // page size handled by the gather (rows per TMA box)
-constexpr int kThreads = 256;       // decode kernel: load, MMA, V tail fix, split merge, 4 x softmax
+constexpr int kThreads = 288;       // decode kernel: load, QK MMA, V tail fix, split merge, 4 x softmax, PV MMA
 constexpr int kTmemCols = 512;
 constexpr int kHistBuckets = 1024;  // cost buckets of the longest-first order, per item list
 constexpr int kDecRows = 16;        // packed query rows a swap-AB decode item holds
